@@ -1,0 +1,137 @@
+"""CPU oracle for the KDA forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+Python binding) never imports, links or calls anything here.
+
+Contents:
+  * ``kda_oracle.c``  -- plain fp64 token-by-token recurrence (the definition),
+    threaded over (sequence, head) pairs; built with gcc by ``build()``.
+  * ``token_np.py``   -- a NumPy twin of the same definition for tiny inputs.
+  * ``chunked_np.py`` -- the 16-token chunked (WY/UT) form of the method in
+    NumPy fp64, used to pin the token form and to study rounding.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (portable flags, no -march) and return its path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            fn = lib.kda_oracle_fwd
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            fn.argtypes = [i64, i64, i64, i64, i64, i64, p, p, p, p, p, ctypes.c_double, p, p,
+                           ctypes.c_double, p, p, p, p, p, ctypes.c_int]
+            fn.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 tensor/array -> contiguous uint16 bit patterns."""
+    import torch  # local: the oracle itself needs only numpy
+
+    if isinstance(x, torch.Tensor):
+        assert x.dtype == torch.bfloat16
+        return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy()
+                                    .view(np.uint16))
+    x = np.asarray(x)
+    assert x.dtype == np.uint16
+    return np.ascontiguousarray(x)
+
+
+def _f64(x) -> Optional[np.ndarray]:
+    import torch
+
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return np.ascontiguousarray(x.detach().cpu().to(torch.float64).numpy())
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _f32(x) -> np.ndarray:
+    import torch
+
+    if isinstance(x, torch.Tensor):
+        return np.ascontiguousarray(x.detach().cpu().to(torch.float32).numpy())
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def kda_forward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None,
+                cu_seqlens=None, out_rows=None, want_out=True, want_final_state=True,
+                nthreads: Optional[int] = None):
+    """Run the fp64 token recurrence.
+
+    q, k, g: [B,T,H,K] bf16; v: [B,T,H,V] bf16; beta: [B,T,H] bf16 (torch
+    tensors or uint16 bit arrays); A_log [H] and dt_bias [H,K] fp32; scale and
+    lower_bound are rounded to fp32 first, as they cross the C ABI as floats.
+    initial_state: [N,H,V,K] of any float dtype (converted exactly) or None.
+    out_rows: optional sorted token-row indices (over B*T) whose outputs are
+    wanted; default all rows.  Returns (out [rows,H,V] fp64 or None,
+    final_state [N,H,V,K] fp64 or None).
+    """
+    qb, kb, vb, gb, bb = (_bits(x) for x in (q, k, v, g, beta))
+    B, T, H, K = qb.shape
+    V = vb.shape[-1]
+    cu = None
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+            dtype=np.int64))
+        N = cu.shape[0] - 1
+    else:
+        N = B
+    A = _f32(A_log)
+    D = _f32(dt_bias)
+    s0 = _f64(initial_state)
+    out = row_map = None
+    if want_out:
+        if out_rows is None:
+            out = np.zeros((B * T, H, V), dtype=np.float64)
+        else:
+            rows = np.asarray(out_rows, dtype=np.int64)
+            row_map = np.full(B * T, -1, dtype=np.int64)
+            row_map[rows] = np.arange(rows.shape[0], dtype=np.int64)
+            out = np.zeros((rows.shape[0], H, V), dtype=np.float64)
+    fin = np.zeros((N, H, V, K), dtype=np.float64) if want_final_state else None
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _load().kda_oracle_fwd(B, T, H, K, V, N, _ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb),
+                                _ptr(bb), float(np.float32(scale)), _ptr(A), _ptr(D),
+                                float(np.float32(lower_bound)), _ptr(s0), _ptr(out),
+                                _ptr(row_map), _ptr(fin), _ptr(cu), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_fwd failed with code {rc}")
+    return out, fin

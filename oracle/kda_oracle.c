@@ -1,0 +1,194 @@
+/*
+ * kda_oracle.c -- plain fp64 CPU oracle for the Kimi Delta Attention (KDA)
+ * forward pass.  TEST INFRASTRUCTURE ONLY: the product path never links,
+ * loads or calls this file; only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark do.
+ *
+ * What it computes (FlashKDA README, "Kernel API" table; KDA recurrence):
+ *   for every sequence n and head h, token by token, starting from the
+ *   initial state S (K x V; zeros when no initial state is given):
+ *     ghat_t[c] = lower_bound * sigmoid(exp(A_log[h]) * (g_t[c] + dt_bias[h,c]))
+ *     alpha_t   = exp(ghat_t)                       (per channel c < K)
+ *     beta_t    = sigmoid(beta_logit_t)            ("sigmoid applied internally")
+ *     qh = q_t / sqrt(|q_t|^2 + 1e-6),  kh = k_t / sqrt(|k_t|^2 + 1e-6)
+ *     S   <- Diag(alpha_t) S                        (decay first)
+ *     S   <- S + beta_t * kh (v_t - S^T kh)^T        (delta-rule update)
+ *     o_t  = scale * S^T qh                         (output from updated S)
+ *   and the final S is written transposed, final[n,h,v,c] = S[c][v]
+ *   (README: state shape [B,H,V,K] / [N,H,V,K], FLA transpose_state_layout).
+ *
+ * Readings where the pages are silent: the gate is a sigmoid scaled by the
+ * lower bound (README "safe_gate", "Gate lower bound (range from -5.0 to 0)");
+ * the L2-norm epsilon is 1e-6 inside the square root; scale is applied after
+ * normalisation.  Parity of these readings against the original library is
+ * unpinned (no printed values exist); everything else is pinned by the tests.
+ *
+ * Everything is fp64.  Inputs arrive as raw bf16 bit patterns (converted
+ * exactly), fp32 parameters (exact in fp64) and an fp64 initial state.
+ * Outputs are written as fp64 (out may be restricted to sampled token rows).
+ * Work is split over (sequence, head) pairs with POSIX threads; each pair is a
+ * plain sequential loop over its tokens.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double bf16_to_double(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+typedef struct {
+    int64_t B, T, H, K, V, N;
+    const uint16_t *q, *k, *v, *g, *beta;
+    double scale, lower_bound;
+    const float *A_log, *dt_bias;
+    const double *initial_state;
+    double *out;                 /* [n_rows_out, H, V] */
+    const int64_t *out_row_map;  /* token row -> output row, or -1; NULL = identity */
+    double *final_state;
+    const int64_t *cu_seqlens;
+    int64_t next_pair;           /* shared work counter */
+    pthread_mutex_t lock;
+} oracle_job;
+
+/* One (sequence, head) pair: the plain token recurrence. */
+static void run_pair(oracle_job *J, int64_t n, int64_t h, double *S, double *qh, double *kh,
+                     double *alpha, double *pred) {
+    const int64_t H = J->H, K = J->K, V = J->V;
+    int64_t t0, t1;
+    if (J->cu_seqlens) {
+        t0 = J->cu_seqlens[n];
+        t1 = J->cu_seqlens[n + 1];
+    } else {
+        t0 = n * J->T;
+        t1 = t0 + J->T;
+    }
+    /* initial state: state[n,h,v,c] = S[c][v] */
+    if (J->initial_state) {
+        const double *s0 = J->initial_state + (n * H + h) * V * K;
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) S[c * V + j] = s0[j * K + c];
+    } else {
+        memset(S, 0, sizeof(double) * (size_t)(K * V));
+    }
+    const double rate = exp((double)J->A_log[h]);
+    for (int64_t t = t0; t < t1; ++t) {
+        const uint16_t *qt = J->q + (t * H + h) * K;
+        const uint16_t *kt = J->k + (t * H + h) * K;
+        const uint16_t *gt = J->g + (t * H + h) * K;
+        const uint16_t *vt = J->v + (t * H + h) * V;
+        double qq = 0.0, kk = 0.0;
+        for (int64_t c = 0; c < K; ++c) {
+            qh[c] = bf16_to_double(qt[c]);
+            kh[c] = bf16_to_double(kt[c]);
+            qq += qh[c] * qh[c];
+            kk += kh[c] * kh[c];
+        }
+        const double qinv = 1.0 / sqrt(qq + 1e-6), kinv = 1.0 / sqrt(kk + 1e-6);
+        for (int64_t c = 0; c < K; ++c) {
+            qh[c] *= qinv;
+            kh[c] *= kinv;
+            double x = rate * (bf16_to_double(gt[c]) + (double)J->dt_bias[h * K + c]);
+            alpha[c] = exp(J->lower_bound * sigmoid(x));
+        }
+        const double b = sigmoid(bf16_to_double(J->beta[t * H + h]));
+        /* decay */
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) S[c * V + j] *= alpha[c];
+        /* prediction S^T kh */
+        for (int64_t j = 0; j < V; ++j) pred[j] = 0.0;
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) pred[j] += S[c * V + j] * kh[c];
+        /* delta-rule correction */
+        for (int64_t j = 0; j < V; ++j) pred[j] = b * (bf16_to_double(vt[j]) - pred[j]);
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) S[c * V + j] += kh[c] * pred[j];
+        /* output from the updated state */
+        int64_t row = J->out_row_map ? J->out_row_map[t] : t;
+        if (J->out && row >= 0) {
+            double *o = J->out + (row * H + h) * V;
+            for (int64_t j = 0; j < V; ++j) o[j] = 0.0;
+            for (int64_t c = 0; c < K; ++c)
+                for (int64_t j = 0; j < V; ++j) o[j] += S[c * V + j] * qh[c];
+            for (int64_t j = 0; j < V; ++j) o[j] *= J->scale;
+        }
+    }
+    if (J->final_state) {
+        double *sf = J->final_state + (n * H + h) * V * K;
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) sf[j * K + c] = S[c * V + j];
+    }
+}
+
+static void *worker(void *arg) {
+    oracle_job *J = (oracle_job *)arg;
+    const int64_t K = J->K, V = J->V;
+    double *S = (double *)malloc(sizeof(double) * (size_t)(K * V));
+    double *buf = (double *)malloc(sizeof(double) * (size_t)(3 * K + V));
+    if (!S || !buf) {
+        free(S);
+        free(buf);
+        return (void *)1;
+    }
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int64_t p = J->next_pair++;
+        pthread_mutex_unlock(&J->lock);
+        if (p >= J->N * J->H) break;
+        run_pair(J, p / J->H, p % J->H, S, buf, buf + K, buf + 2 * K, buf + 3 * K);
+    }
+    free(S);
+    free(buf);
+    return NULL;
+}
+
+/*
+ * Returns 0 on success, -1 on a bad argument, -2 on allocation failure.
+ * N is the number of sequences: N = B when cu_seqlens is NULL, else
+ * cu_seqlens has N+1 entries and B must be 1.  out_row_map (optional, length
+ * B*T) maps each token row to a row of `out` (or -1 to skip it).
+ */
+int kda_oracle_fwd(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, int64_t N,
+                   const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *g,
+                   const uint16_t *beta, double scale, const float *A_log, const float *dt_bias,
+                   double lower_bound, const double *initial_state, double *out,
+                   const int64_t *out_row_map, double *final_state, const int64_t *cu_seqlens,
+                   int nthreads) {
+    if (B < 0 || T < 0 || H <= 0 || K <= 0 || V <= 0 || N < 0) return -1;
+    if (!cu_seqlens && N != B) return -1;
+    if (cu_seqlens && B != 1) return -1;
+    if (nthreads < 1) nthreads = 1;
+    oracle_job J;
+    J.B = B; J.T = T; J.H = H; J.K = K; J.V = V; J.N = N;
+    J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta;
+    J.scale = scale; J.lower_bound = lower_bound;
+    J.A_log = A_log; J.dt_bias = dt_bias;
+    J.initial_state = initial_state; J.out = out; J.out_row_map = out_row_map;
+    J.final_state = final_state; J.cu_seqlens = cu_seqlens;
+    J.next_pair = 0;
+    pthread_mutex_init(&J.lock, NULL);
+    int64_t pairs = N * H;
+    if (nthreads > pairs) nthreads = (int)(pairs > 0 ? pairs : 1);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th) return -2;
+    int started = 0, rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, worker, &J) == 0) ++started;
+    }
+    if (started == 0) rc = (worker(&J) == NULL) ? 0 : -2;
+    for (int i = 0; i < started; ++i) {
+        void *r = NULL;
+        pthread_join(th[i], &r);
+        if (r != NULL) rc = -2;
+    }
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return rc;
+}
