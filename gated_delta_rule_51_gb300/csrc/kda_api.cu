@@ -1,0 +1,304 @@
+// kda_api.cu -- the C ABI (include/kda.h): argument checks, workspace layout,
+// TMA descriptors and the launch sequence of the KDA forward pass.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/kda.h"
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+using namespace kda;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kSlotBytes = 128 * 128 * sizeof(float);
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct DeviceInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+kda_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  DeviceInfo d;
+  if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KDA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return KDA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return KDA_ERR_CUDA;
+  *out = d;
+  return KDA_OK;
+}
+
+// Tokens per segment.  A (sequence, head) chain is sequential over its chunks;
+// when there are too few chains to fill the GPU, long sequences are cut into
+// segments so that about one wave of forward work items exists.  Segments are
+// at least 512 tokens; the value is a multiple of 16.
+int64_t choose_seg_tokens(const kda_shape& s, int sms) {
+  const int64_t rows = s.B * s.T;
+  const char* env = std::getenv("KDA_SEG_TOKENS");
+  if (env != nullptr) {
+    const long long v = std::atoll(env);
+    if (v >= 16) return std::max<int64_t>(16, (v + 15) / 16 * 16);
+  }
+  const int64_t resident = 2 * (int64_t)std::max(sms, 1);   // CTAs resident at once
+  const int64_t chains = s.N * s.H;
+  const int64_t no_split = std::max<int64_t>(16, (rows + 15) / 16 * 16);
+  if (chains >= 2 * resident || rows == 0) return no_split;
+  int64_t L = (rows * s.H + resident - 1) / resident;
+  L = std::max<int64_t>(512, (L + 15) / 16 * 16);
+  return std::min(L, no_split);
+}
+
+struct Layout {
+  int64_t seg_tokens = 0;
+  int64_t cap_forward = 0, cap_phase1 = 0, cap_compose = 0, cap_slots = 0;
+  size_t off_hdr = 0, off_forward = 0, off_phase1 = 0, off_compose = 0, off_slots = 0, total = 0;
+};
+
+Layout make_layout(const kda_shape& s, int sms) {
+  Layout L;
+  const int64_t rows = s.B * s.T;
+  L.seg_tokens = choose_seg_tokens(s, sms);
+  const int64_t splits = rows / L.seg_tokens;   // bound on sum over sequences of (nseg - 1)
+  L.cap_forward = s.H * (splits + s.N);
+  const int64_t qcap = s.H * splits;
+  L.cap_slots = 2 * qcap;
+  L.cap_phase1 = 2 * qcap;
+  L.cap_compose = s.H * std::min<int64_t>(s.N, splits);
+  size_t off = 0;
+  L.off_hdr = off;
+  off = align_up(off + sizeof(WorkHeader));
+  L.off_forward = off;
+  off = align_up(off + (size_t)L.cap_forward * sizeof(WorkItem));
+  L.off_phase1 = off;
+  off = align_up(off + (size_t)L.cap_phase1 * sizeof(WorkItem));
+  L.off_compose = off;
+  off = align_up(off + (size_t)L.cap_compose * sizeof(ComposeItem));
+  L.off_slots = off;
+  off = align_up(off + (size_t)L.cap_slots * kSlotBytes);
+  L.total = off;
+  return L;
+}
+
+kda_status check_shape(const kda_shape* s) {
+  if (s == nullptr) return KDA_ERR_INVALID_ARGUMENT;
+  if (s->K != 128 || s->V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (s->B < 0 || s->T < 0 || s->H <= 0 || s->N < 0) return KDA_ERR_INVALID_ARGUMENT;
+  if (s->B > 0 && s->T > (int64_t)0x7fffffff / std::max<int64_t>(s->B, 1)) return KDA_ERR_INVALID_ARGUMENT;
+  if (s->H > 65535 || s->N > (int64_t)0x7fffffff / s->H) return KDA_ERR_INVALID_ARGUMENT;
+  return KDA_OK;
+}
+
+cudaEvent_t g_profile_events[4] = {nullptr, nullptr, nullptr, nullptr};
+bool g_profile = false;
+
+void mark(int i, cudaStream_t s) {
+  if (g_profile && g_profile_events[i] != nullptr) cudaEventRecord(g_profile_events[i], s);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [rows, H, 128] bf16 viewed as a 3-D tensor {128, H, rows}; box {64, 1, 16}, 128-byte swizzle.
+bool encode_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)std::max<int64_t>(rows, 1)};
+  cuuint64_t strides[2] = {256, (cuuint64_t)(H * 256)};
+  cuuint32_t box[3] = {64, 1, 16};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K and V must be 128)";
+    case KDA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case KDA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3, sm_103a)";
+    case KDA_ERR_CUDA: return "CUDA error";
+    case KDA_ERR_TIMEOUT: return "a device-side wait timed out";
+    case KDA_ERR_BAD_SEQLENS: return "malformed cu_seqlens";
+  }
+  return "unknown status";
+}
+
+kda_status kda_workspace_size(const kda_shape* shape, size_t* bytes) {
+  if (bytes == nullptr) return KDA_ERR_INVALID_ARGUMENT;
+  kda_status st = check_shape(shape);
+  if (st != KDA_OK) return st;
+  DeviceInfo d;
+  if (device_info(&d) != KDA_OK) d.sms = 152;   // sizing only; kda_fwd checks the device
+  *bytes = make_layout(*shape, d.sms).total;
+  return KDA_OK;
+}
+
+kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const void* v, const void* g,
+                   const void* beta, float scale, void* out, const float* A_log, const float* dt_bias,
+                   float lower_bound, const void* initial_state, kda_state_dtype init_dtype, void* final_state,
+                   kda_state_dtype final_dtype, const int64_t* cu_seqlens, void* workspace,
+                   size_t workspace_bytes, kda_stream_t stream_) {
+  kda_status st = check_shape(shape);
+  if (st != KDA_OK) return st;
+  const kda_shape s = *shape;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // README: "When cu_seqlens is provided, B must be 1"; otherwise N = B.
+  if (cu_seqlens != nullptr) {
+    if (s.B != 1 || s.N < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (s.N == 0 && s.T != 0) return KDA_ERR_INVALID_ARGUMENT;
+  } else if (s.N != s.B) {
+    return KDA_ERR_INVALID_ARGUMENT;
+  }
+  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
+  const int64_t rows = s.B * s.T;
+  // q, k, g, v are read by TMA (16-byte aligned base); beta and out are accessed
+  // element-wise (2-byte alignment); the gate parameters as fp32 (4 bytes).
+  auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  if (rows > 0) {
+    const void* tma[] = {q, k, v, g};
+    for (const void* p : tma)
+      if (p == nullptr || !aligned16(p)) return KDA_ERR_INVALID_ARGUMENT;
+    if (beta == nullptr || out == nullptr || !aligned(beta, 2) || !aligned(out, 2)) return KDA_ERR_INVALID_ARGUMENT;
+  }
+  if (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned(dt_bias, 4))
+    return KDA_ERR_INVALID_ARGUMENT;
+  // states: README "accept None (stateless), bf16, or fp32 ... When both are provided, their dtypes must match"
+  auto dtype_ok = [](kda_state_dtype d) { return d == KDA_STATE_BF16 || d == KDA_STATE_FP32; };
+  if (initial_state != nullptr && (!dtype_ok(init_dtype) || !aligned16(initial_state))) return KDA_ERR_INVALID_ARGUMENT;
+  if (final_state != nullptr && (!dtype_ok(final_dtype) || !aligned16(final_state))) return KDA_ERR_INVALID_ARGUMENT;
+  if (initial_state == nullptr && init_dtype != KDA_STATE_NONE) return KDA_ERR_INVALID_ARGUMENT;
+  if (final_state == nullptr && final_dtype != KDA_STATE_NONE) return KDA_ERR_INVALID_ARGUMENT;
+  if (initial_state != nullptr && final_state != nullptr) {
+    if (init_dtype != final_dtype) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t bytes = (size_t)s.N * s.H * 128 * 128 * (init_dtype == KDA_STATE_FP32 ? 4 : 2);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(initial_state), b = reinterpret_cast<uintptr_t>(final_state);
+    if (a != b && a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARGUMENT;   // partial overlap
+  }
+  DeviceInfo d;
+  if (device_info(&d) != KDA_OK) return KDA_ERR_CUDA;
+  if (d.major != 10 || d.minor != 3) return KDA_ERR_UNSUPPORTED_DEVICE;
+  const Layout L = make_layout(s, d.sms);
+  if (workspace == nullptr || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return KDA_ERR_WORKSPACE_TOO_SMALL;
+  if (s.N == 0) return KDA_OK;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WorkHeader* hdr = reinterpret_cast<WorkHeader*>(ws + L.off_hdr);
+
+  ScheduleParams sp;
+  sp.cu_seqlens = cu_seqlens;
+  sp.B = s.B;
+  sp.T = s.T;
+  sp.H = s.H;
+  sp.N = s.N;
+  sp.seg_tokens = (int)L.seg_tokens;
+  sp.has_init = initial_state != nullptr;
+  sp.has_final = final_state != nullptr;
+  sp.hdr = hdr;
+  sp.phase1 = reinterpret_cast<WorkItem*>(ws + L.off_phase1);
+  sp.forward = reinterpret_cast<WorkItem*>(ws + L.off_forward);
+  sp.compose = reinterpret_cast<ComposeItem*>(ws + L.off_compose);
+  sp.cap_phase1 = L.cap_phase1;
+  sp.cap_forward = L.cap_forward;
+  sp.cap_compose = L.cap_compose;
+  sp.cap_slots = L.cap_slots;
+  if (launch_schedule(sp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  mark(0, stream);
+
+  ChainParams cp;
+  std::memset(&cp, 0, sizeof(cp));
+  if (rows > 0) {
+    if (!encode_tile_map(&cp.tm_q, q, rows, s.H) || !encode_tile_map(&cp.tm_k, k, rows, s.H) ||
+        !encode_tile_map(&cp.tm_g, g, rows, s.H) || !encode_tile_map(&cp.tm_v, v, rows, s.H))
+      return KDA_ERR_CUDA;
+  }
+  cp.beta = static_cast<const uint16_t*>(beta);
+  cp.A_log = A_log;
+  cp.dt_bias = dt_bias;
+  cp.out = static_cast<uint16_t*>(out);
+  cp.init_state = initial_state;
+  cp.final_state = final_state;
+  cp.ws_states = reinterpret_cast<float*>(ws + L.off_slots);
+  cp.err = &hdr->err;
+  cp.H = (int)s.H;
+  cp.init_dtype = (int)init_dtype;
+  cp.final_dtype = (int)final_dtype;
+  cp.scale = scale;
+  cp.lower_bound = lower_bound;
+
+  if (L.cap_phase1 > 0) {
+    cp.items = sp.phase1;
+    cp.item_count = &hdr->n_phase1;
+    if (launch_chain(cp, (int)L.cap_phase1, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    ComposeParams cmp;
+    cmp.ws_states = cp.ws_states;
+    cmp.items = sp.compose;
+    cmp.item_count = &hdr->n_compose;
+    mark(1, stream);
+    if (launch_compose(cmp, (int)L.cap_compose, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    mark(2, stream);
+  } else {
+    mark(1, stream);
+    mark(2, stream);
+  }
+  cp.items = sp.forward;
+  cp.item_count = &hdr->n_forward;
+  if (launch_chain(cp, (int)L.cap_forward, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  mark(3, stream);
+  return KDA_OK;
+}
+
+kda_status kda_set_profile_events(void* const* events, int n_events) {
+  if (events == nullptr) {
+    g_profile = false;
+    return KDA_OK;
+  }
+  if (n_events != 4) return KDA_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < 4; ++i) g_profile_events[i] = static_cast<cudaEvent_t>(events[i]);
+  g_profile = true;
+  return KDA_OK;
+}
+
+kda_status kda_check_device_error(const void* workspace, kda_stream_t stream_, int* flags) {
+  if (workspace == nullptr || flags == nullptr) return KDA_ERR_INVALID_ARGUMENT;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_CUDA;
+  int err = 0;
+  if (cudaMemcpy(&err, &static_cast<const WorkHeader*>(workspace)->err, sizeof(int), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return KDA_ERR_CUDA;
+  *flags = err;
+  if (err & kErrTimeout) return KDA_ERR_TIMEOUT;
+  if (err & kErrBadSeqlens) return KDA_ERR_BAD_SEQLENS;
+  return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,212 @@
+// kda_aux.cu -- device-side work scheduling and the segment-carry composition.
+//
+// Long sequences are cut into segments of at most `seg_tokens` tokens so that
+// the sequential chunk recurrence of one (sequence, head) can run on several
+// SMs at once.  Because one chunk maps the state affinely, S_out = P S_in + Q,
+// a segment s >= 1 is first run twice from a known start -- once from the
+// identity with zero values (its transition P_s) and once from zero (its
+// local carry Q_s) -- segment 0 is run from the true initial state (which
+// gives S_1 directly), the carries are then composed in order,
+// S_{s+1} = P_s S_s + Q_s, and finally every segment runs its forward pass
+// from its true initial state.  All of this is derived from the recurrence;
+// the pages describe state carry across calls but not a segment scan.
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+// ------------------------------------------------------------------ schedule
+// One CTA.  Reads cu_seqlens (or the fixed batch layout), validates it, and
+// writes the three work lists and their counts into the workspace.
+//
+// Slots (128 x 128 fp32 each) for a sequence with nseg >= 2 segments, head h:
+//   q slot (s) = qbase + h (nseg-1) + s,  s = 0 .. nseg-2   local carry Q_s
+//                (Q_0 is the true state after segment 0; the composition
+//                overwrites Q_s with the true state after segment s)
+//   p slot (s) = q slot (s) + q_total H                     transition P_s;
+//                p slot (0) keeps a copy of the initial state instead.
+// The first-phase list has one entry per slot (entry i writes slot i); the
+// entries of the unused transitions P_0 are no-ops (len = -1).
+constexpr int kSchedThreads = 1024;
+
+__device__ __forceinline__ WorkItem make_item(long long row0, long long len, long long h, int mode, long long n,
+                                              long long in_slot, long long out_slot, long long aux_slot) {
+  WorkItem w;
+  w.row0 = (int)row0;
+  w.len = (int)len;
+  w.head = (int)h;
+  w.mode = mode;
+  w.seq = (int)n;
+  w.in_slot = (int)in_slot;
+  w.out_slot = (int)out_slot;
+  w.aux_slot = (int)aux_slot;
+  return w;
+}
+
+// inclusive scan of one value per thread across the block
+__device__ long long block_scan(long long x, long long* buf) {
+  const int tid = threadIdx.x;
+  buf[tid] = x;
+  __syncthreads();
+  for (int off = 1; off < kSchedThreads; off <<= 1) {
+    const long long a = tid >= off ? buf[tid - off] : 0;
+    __syncthreads();
+    buf[tid] += a;
+    __syncthreads();
+  }
+  const long long r = buf[tid];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const ScheduleParams p) {
+  __shared__ long long s_buf[kSchedThreads];
+  __shared__ long long s_tot[3];   // segments, q slots, compose chains (running)
+  __shared__ int s_err;
+  const int tid = threadIdx.x;
+  const long long H = p.H;
+  const long long L = p.seg_tokens;
+  const long long total_rows = p.B * p.T;
+  if (tid == 0) s_err = 0;
+  long long q_total = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    if (tid == 0) s_tot[0] = s_tot[1] = s_tot[2] = 0;
+    __syncthreads();
+    for (long long base = 0; base < p.N; base += kSchedThreads) {
+      const long long n = base + tid;
+      long long start = 0, len = 0, nseg = 0;
+      if (n < p.N) {
+        if (p.cu_seqlens) {
+          long long a = p.cu_seqlens[n], b = p.cu_seqlens[n + 1];
+          if ((n == 0 && a != 0) || b < a || (n == p.N - 1 && b != total_rows)) s_err = 1;
+          a = a < 0 ? 0 : (a > total_rows ? total_rows : a);
+          b = b < a ? a : (b > total_rows ? total_rows : b);
+          start = a;
+          len = b - a;
+        } else {
+          start = n * p.T;
+          len = p.T;
+        }
+        nseg = len <= 0 ? 1 : (len + L - 1) / L;
+      }
+      const long long nq = nseg >= 2 ? nseg - 1 : 0;
+      const long long nc = nseg >= 3 ? 1 : 0;
+      const long long seg0 = s_tot[0] + block_scan(nseg, s_buf) - nseg;
+      const long long q0 = s_tot[1] + block_scan(nq, s_buf) - nq;
+      const long long c0 = s_tot[2] + block_scan(nc, s_buf) - nc;
+      if (pass == 1 && n < p.N) {
+        const long long in_user = p.has_init ? kInUser : kInZero;
+        for (long long h = 0; h < H; ++h) {
+          const long long qb = q0 * H + h * nq;          // q slot of segment 0
+          const long long pb = qb + q_total * H;          // p slot of segment 0
+          for (long long s = 0; s < nseg; ++s) {
+            const long long fi = (seg0 + s) * H + h;
+            const long long flen = len <= 0 ? 0 : (len - s * L < L ? len - s * L : L);
+            long long in_slot;
+            if (s == 0) in_slot = (nseg >= 2 && p.has_init) ? pb : in_user;
+            else in_slot = qb + s - 1;
+            const long long out_slot = (s == nseg - 1 && p.has_final) ? kOutUser : kOutNone;
+            if (fi < p.cap_forward)
+              p.forward[fi] = make_item(start + s * L, flen, h, kModeForward, n, in_slot, out_slot, -1);
+            if (s <= nseg - 2) {
+              const long long qs = qb + s, ps = pb + s;
+              if (ps < p.cap_phase1 && ps < p.cap_slots) {
+                p.phase1[qs] = make_item(start + s * L, L, h, kModeLocal, n, s == 0 ? in_user : kInZero, qs,
+                                         (s == 0 && p.has_init) ? ps : -1);
+                p.phase1[ps] = s >= 1 ? make_item(start + s * L, L, h, kModeTransition, n, kInIdentity, ps, -1)
+                                      : make_item(0, -1, h, kModeTransition, n, kInZero, kOutNone, -1);
+              }
+            }
+          }
+          if (nseg >= 3) {
+            const long long ci = c0 * H + h;
+            if (ci < p.cap_compose) {
+              ComposeItem it;
+              it.head = (int)h;
+              it.first_q_slot = (int)qb;
+              it.first_p_slot = (int)(pb + 1);
+              it.n_steps = (int)(nseg - 2);
+              p.compose[ci] = it;
+            }
+          }
+        }
+      }
+      __syncthreads();
+      if (tid == kSchedThreads - 1) {
+        s_tot[0] = seg0 + nseg;
+        s_tot[1] = q0 + nq;
+        s_tot[2] = c0 + nc;
+      }
+      __syncthreads();
+    }
+    q_total = s_tot[1];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const long long nf = s_tot[0] * H;
+    const long long n1 = 2 * s_tot[1] * H;
+    const long long ncm = s_tot[2] * H;
+    p.hdr->n_forward = (int)(nf < p.cap_forward ? nf : p.cap_forward);
+    p.hdr->n_phase1 = (int)(n1 < p.cap_phase1 ? n1 : p.cap_phase1);
+    p.hdr->n_compose = (int)(ncm < p.cap_compose ? ncm : p.cap_compose);
+    p.hdr->err = s_err ? kErrBadSeqlens : 0;
+  }
+}
+
+cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s) {
+  kda_schedule_kernel<<<1, kSchedThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ compose
+// S^T_{s+1} = S^T_s P^T_s + Q^T_s, all 128 x 128 fp32 in the [V, K] layout:
+// out[v][k] = sum_m in[v][m] * Pst[m][k] + Qst[v][k] where Pst is the stored
+// transition slot (row m = column m of P).  Rows of S^T are independent, so
+// each CTA owns 16 rows of one (sequence, head) chain and walks its segments.
+constexpr int kComposeRows = 16;
+constexpr int kComposeThreads = 256;
+
+__global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const ComposeParams p) {
+  const int item = blockIdx.x / (128 / kComposeRows);
+  const int part = blockIdx.x % (128 / kComposeRows);
+  if (item >= *p.item_count) return;
+  const ComposeItem ci = p.items[item];
+  __shared__ float s_in[kComposeRows][128];
+  const int tid = threadIdx.x;
+  const int k = tid & 127;
+  const int vh = tid >> 7;   // rows vh*8 .. vh*8+7 of this CTA's 16
+  const int v0 = part * kComposeRows;
+  float* slots = p.ws_states;
+  // S_1 = Q slot 0 (already the true state after segment 0)
+  for (int i = tid; i < kComposeRows * 128; i += kComposeThreads)
+    s_in[i / 128][i % 128] = slots[(size_t)ci.first_q_slot * 16384 + (size_t)(v0 + i / 128) * 128 + i % 128];
+  __syncthreads();
+  for (int s = 1; s <= ci.n_steps; ++s) {
+    const float* P = slots + (size_t)(ci.first_p_slot + s - 1) * 16384;
+    float* Q = slots + (size_t)(ci.first_q_slot + s) * 16384;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = Q[(size_t)(v0 + vh * 8 + i) * 128 + k];
+#pragma unroll 4
+    for (int m = 0; m < 128; ++m) {
+      const float pm = P[(size_t)m * 128 + k];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(s_in[vh * 8 + i][m], pm, acc[i]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s_in[vh * 8 + i][k] = acc[i];
+      Q[(size_t)(v0 + vh * 8 + i) * 128 + k] = acc[i];
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_compose(const ComposeParams& p, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  kda_compose_kernel<<<grid * (128 / kComposeRows), kComposeThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,94 @@
+// kda_internal.h -- shared definitions between the host launcher and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kChunk = 16;   // tokens per chunk
+constexpr int kDimK = 128;
+constexpr int kDimV = 128;
+
+// One unit of sequential work: a run of chunks of one (sequence, head).
+enum : int { kModeForward = 0, kModeLocal = 1, kModeTransition = 2 };
+// in_slot values below zero:
+enum : int { kInZero = -1, kInIdentity = -2, kInUser = -3 };
+// out_slot values below zero:
+enum : int { kOutNone = -1, kOutUser = -3 };
+
+struct WorkItem {
+  int row0;      // first token row in the flattened [B*T] token index
+  int len;       // tokens in this run (may be 0)
+  int head;
+  int mode;      // kModeForward / kModeLocal / kModeTransition
+  int seq;       // sequence index n (user state row)
+  int in_slot;   // initial state source
+  int out_slot;  // final state target
+  int aux_slot;  // >= 0: also store the (undecayed) initial state there
+};
+
+// Device-side work list built by the scheduling kernel inside the workspace.
+struct WorkHeader {
+  int err;             // error word (bit flags, see kda_device.cuh)
+  int n_phase1;        // number of segment items of the first phase
+  int n_forward;       // number of forward items
+  int n_compose;       // number of (sequence, head) carry chains to compose
+  int pad[4];
+};
+
+struct ComposeItem {
+  int head;
+  int first_q_slot;   // workspace slot holding the true state after segment 0
+  int first_p_slot;   // slot of the transition of segment 1 (P_1)
+  int n_steps;        // number of compositions (segments 1 .. n_seg-2)
+  // step s (1 <= s <= n_steps) uses P slot first_p_slot + (s-1) and Q slots
+  // first_q_slot + s - 1 (input) and first_q_slot + s (carry, overwritten)
+};
+
+struct ChainParams {
+  CUtensorMap tm_q, tm_k, tm_g, tm_v;  // 3-D maps over [B*T, H, 128] bf16, box {64, 1, 16}
+  const uint16_t* beta;                // [B*T, H] bf16 logits
+  const float* A_log;                  // [H]
+  const float* dt_bias;                // [H, 128]
+  uint16_t* out;                       // [B*T, H, 128] bf16
+  const void* init_state;              // [N, H, 128, 128] or null
+  void* final_state;                   // [N, H, 128, 128] or null
+  float* ws_states;                    // workspace state slots, 128*128 fp32 each
+  const WorkItem* items;
+  const int* item_count;
+  int* err;
+  int H;
+  int init_dtype;                      // kda_state_dtype
+  int final_dtype;
+  float scale;
+  float lower_bound;
+};
+
+struct ComposeParams {
+  float* ws_states;
+  const ComposeItem* items;
+  const int* item_count;
+};
+
+struct ScheduleParams {
+  const int64_t* cu_seqlens;  // null: fixed-length rows of T tokens
+  int64_t B, T, H, N;
+  int seg_tokens;             // maximum tokens per segment (multiple of 16)
+  int has_init;
+  int has_final;
+  WorkHeader* hdr;
+  WorkItem* phase1;
+  WorkItem* forward;
+  ComposeItem* compose;
+  long long cap_phase1, cap_forward, cap_compose, cap_slots;
+};
+
+// Host-side launchers (defined in the .cu files).
+cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
+cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s);
+cudaError_t launch_compose(const ComposeParams& p, int grid, cudaStream_t s);
+size_t chain_smem_bytes();
+
+}  // namespace kda

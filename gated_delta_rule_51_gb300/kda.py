@@ -1,0 +1,193 @@
+"""Python binding of the KDA forward library (``include/kda.h``).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels of ``libkda.so``; PyTorch provides device memory and the stream.  There
+is no CPU or framework fallback -- if the library cannot be loaded, or the GPU
+is not an sm_103 part, the calls raise.
+
+``fwd`` mirrors FlashKDA's ``flash_kda.fwd(q, k, v, g, beta, scale, out,
+A_log, dt_bias, lower_bound, initial_state=None, final_state=None,
+cu_seqlens=None)`` (README "Kernel API").
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from typing import Dict, Optional, Tuple
+
+import torch
+
+from . import _build
+
+KDA_OK = 0
+KDA_STATE_NONE, KDA_STATE_BF16, KDA_STATE_FP32 = 0, 1, 2
+STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
+                3: "KDA_ERR_WORKSPACE_TOO_SMALL", 4: "KDA_ERR_UNSUPPORTED_DEVICE", 5: "KDA_ERR_CUDA",
+                6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_BAD_SEQLENS"}
+EXPORTED_SYMBOLS = ("kda_status_string", "kda_workspace_size", "kda_fwd", "kda_check_device_error",
+                    "kda_set_profile_events")
+
+
+class kda_shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("B", "T", "H", "K", "V", "N")]
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the in-tree libkda.so and declare its C ABI."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_missing else _build.LIB
+        lib = ctypes.CDLL(path)
+        p, i64 = ctypes.c_void_p, ctypes.c_int64
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_workspace_size.argtypes = [ctypes.POINTER(kda_shape), ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_workspace_size.restype = ctypes.c_int
+        lib.kda_fwd.argtypes = [ctypes.POINTER(kda_shape), p, p, p, p, p, ctypes.c_float, p, p, p,
+                                ctypes.c_float, p, ctypes.c_int, p, ctypes.c_int, p, p, ctypes.c_size_t, p]
+        lib.kda_fwd.restype = ctypes.c_int
+        lib.kda_check_device_error.argtypes = [p, p, ctypes.POINTER(ctypes.c_int)]
+        lib.kda_check_device_error.restype = ctypes.c_int
+        lib.kda_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+        lib.kda_set_profile_events.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def make_shape(B: int, T: int, H: int, N: int, K: int = 128, V: int = 128) -> kda_shape:
+    return kda_shape(B, T, H, K, V, N)
+
+
+def workspace_size(shape: kda_shape) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    st = lib.kda_workspace_size(ctypes.byref(shape), ctypes.byref(n))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_workspace_size")
+    return int(n.value)
+
+
+_workspaces: Dict[Tuple[int, int], torch.Tensor] = {}
+
+
+def _workspace(device: torch.device, stream: int, nbytes: int) -> torch.Tensor:
+    key = (device.index, stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _state_code(t: Optional[torch.Tensor]) -> int:
+    if t is None:
+        return KDA_STATE_NONE
+    if t.dtype == torch.bfloat16:
+        return KDA_STATE_BF16
+    if t.dtype == torch.float32:
+        return KDA_STATE_FP32
+    raise TypeError(f"state dtype must be bf16 or fp32, got {t.dtype}")
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, shape: Tuple[int, ...], device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+        final_state=None, cu_seqlens=None, workspace: Optional[torch.Tensor] = None,
+        stream: Optional[torch.cuda.Stream] = None):
+    """KDA forward on the GPU; writes ``out`` (and ``final_state``) and returns them.
+
+    q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,128] bf16; beta: [B,T,H] bf16 logits;
+    A_log: [H] fp32; dt_bias: [H,128] fp32; states: [N,H,128,128] bf16/fp32 or None;
+    cu_seqlens: int64 [N+1] on the device (then B must be 1).
+    """
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda.fwd runs on CUDA tensors only")
+    V = v.shape[-1]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    for name, t, dt, shp in (("q", q, torch.bfloat16, (B, T, H, K)), ("k", k, torch.bfloat16, (B, T, H, K)),
+                             ("g", g, torch.bfloat16, (B, T, H, K)), ("v", v, torch.bfloat16, (B, T, H, V)),
+                             ("out", out, torch.bfloat16, (B, T, H, V)),
+                             ("beta", beta, torch.bfloat16, (B, T, H)),
+                             ("A_log", A_log, torch.float32, (H,)), ("dt_bias", dt_bias, torch.float32, (H, K))):
+        _check(t, name, dt, shp, dev)
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        if t is not None:
+            _check(t, name, t.dtype, (N, H, V, K), dev)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int64, (N + 1,), dev)
+    lib = load_library()
+    shape = make_shape(B, T, H, N, K, V)
+    need = workspace_size(shape)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = _workspace(dev, s.cuda_stream, need)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    st = lib.kda_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                     ctypes.c_float(scale), _ptr(out), _ptr(A_log), _ptr(dt_bias),
+                     ctypes.c_float(lower_bound), _ptr(initial_state), _state_code(initial_state),
+                     _ptr(final_state), _state_code(final_state), _ptr(cu_seqlens), _ptr(workspace),
+                     ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                     ctypes.c_void_p(s.cuda_stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_fwd")
+    return out, final_state
+
+
+def check_device_error(workspace: Optional[torch.Tensor] = None, device=None) -> int:
+    """Synchronise and return the device error flags left by the last fwd on this workspace."""
+    lib = load_library()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    s = torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = _workspaces.get((dev.index, s.cuda_stream))
+        if workspace is None:
+            return 0
+    flags = ctypes.c_int(0)
+    lib.kda_check_device_error(_ptr(workspace), ctypes.c_void_p(s.cuda_stream), ctypes.byref(flags))
+    return int(flags.value)
+
+
+def set_profile_events(events) -> None:
+    """Record the given 4 torch.cuda.Events after each launch phase of fwd (None to stop)."""
+    lib = load_library()
+    if events is None:
+        lib.kda_set_profile_events(None, 0)
+        return
+    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    st = lib.kda_set_profile_events(arr, 4)
+    if st != KDA_OK:
+        raise KDAError(st, "kda_set_profile_events")

@@ -1,0 +1,141 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library.
+ *
+ * The operation is the chunked forward pass of Kimi Delta Attention (KDA), as
+ * stated by the FlashKDA README ("Kernel API", flash_kda.fwd parameter table)
+ * together with the KDA recurrence, per sequence n and head h, K = V = 128:
+ *
+ *   ghat_t  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h,:]))  (per channel)
+ *   S_t     = (I - beta_t k_t k_t^T) Diag(exp(ghat_t)) S_{t-1} + beta_t k_t v_t^T
+ *   o_t     = scale * S_t^T q_t
+ *
+ * with beta_t = sigmoid(beta logit) ("sigmoid applied internally"), q_t and
+ * k_t L2-normalised per token and head (x / sqrt(|x|^2 + 1e-6)), and the state
+ * S (K x V) stored transposed as [.., V, K] (FLA transpose_state_layout=True).
+ * The device computes it in 16-token chunks ("processes 16-token chunks"); the
+ * chunk's unit lower-triangular system is inverted in fp32 by forward
+ * substitution (the pages use a Neumann-series product; both give the exact
+ * inverse of a 16 x 16 unit lower-triangular matrix).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major tensors.
+ *    q, k, v, g and the states must be 16-byte aligned, beta and out 2-byte,
+ *    A_log and dt_bias 4-byte.  The caller owns all memory; the library allocates none
+ *    and never synchronises the host (except kda_check_device_error).
+ *  - Work is stream-ordered on `stream` (0 = legacy default stream).
+ *  - Inputs are never modified; `out` and `final_state` are fully overwritten.
+ *  - Errors in the arguments are reported by the return code before anything
+ *    is launched.  Errors found on the device (malformed cu_seqlens, a wait
+ *    that ran out of time) are recorded in the workspace's error word and read
+ *    back with kda_check_device_error; kernels never trap.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kda_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, bad size, lower_bound out of range */
+    KDA_ERR_UNSUPPORTED_SHAPE = 2,  /* K or V other than 128 ("Currently requires K = V = 128") */
+    KDA_ERR_WORKSPACE_TOO_SMALL = 3,
+    KDA_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+    KDA_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+    KDA_ERR_TIMEOUT = 6,            /* a device-side wait ran out of time (error word) */
+    KDA_ERR_BAD_SEQLENS = 7         /* cu_seqlens not monotone or not ending at T (error word) */
+} kda_status;
+
+/* State dtype for initial_state / final_state (README: "bf16/fp32/None"). */
+typedef enum { KDA_STATE_NONE = 0, KDA_STATE_BF16 = 1, KDA_STATE_FP32 = 2 } kda_state_dtype;
+
+/*
+ * Problem shape (README parameter table):
+ *   q, k, g : [B, T, H, K] bf16      v, out : [B, T, H, V] bf16
+ *   beta    : [B, T, H]    bf16 (logits)
+ *   A_log   : [H] fp32               dt_bias : [H, K] fp32
+ *   states  : [N, H, V, K]           cu_seqlens : int64 [N + 1]
+ * N is the number of sequences: N = B without cu_seqlens ("each batch element
+ * is treated as an independent sequence"); with cu_seqlens B must be 1 and T
+ * is the total length across all sequences.
+ */
+typedef struct {
+    int64_t B, T, H, K, V, N;
+} kda_shape;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+KDA_API const char *kda_status_string(kda_status s);
+
+/*
+ * Bytes of device workspace kda_fwd needs for this shape.  The size is linear
+ * in the number of heads and of sequence tiles ("workspace size ... linear
+ * scaling with attention heads and sequence tiles"): it holds the device-side
+ * work list and, for sequences split into segments, one pair of 128 x 128
+ * fp32 segment transition/carry matrices per (segment, head).
+ * Returns KDA_ERR_INVALID_ARGUMENT / KDA_ERR_UNSUPPORTED_SHAPE for bad shapes.
+ */
+KDA_API kda_status kda_workspace_size(const kda_shape *shape, size_t *bytes);
+
+/*
+ * The forward pass (README flash_kda.fwd).
+ *   q, k, v, g, beta : bf16 inputs as above.
+ *   scale            : output scale (README "scaling factor").
+ *   out              : bf16 [B, T, H, V], written for every token.
+ *   A_log, dt_bias   : fp32 gate parameters.
+ *   lower_bound      : gate lower bound, must lie in [-5, 0] (README range).
+ *   initial_state    : NULL (zeros) or [N, H, V, K] of init_dtype.
+ *   final_state      : NULL (not written) or [N, H, V, K] of final_dtype;
+ *                      when both states are given their dtypes must match
+ *                      (README), and final_state may be exactly the same
+ *                      buffer as initial_state (in-place update); partial
+ *                      overlap is not allowed.
+ *   cu_seqlens       : NULL or int64 [N + 1] device array, cu[0] = 0,
+ *                      non-decreasing, cu[N] = T (zero-length sequences allowed:
+ *                      their final state equals their initial state).
+ *   workspace        : device scratch of at least kda_workspace_size bytes,
+ *                      256-byte aligned; its contents are undefined afterwards,
+ *                      except the error word read by kda_check_device_error.
+ * Returns KDA_OK once the kernels are enqueued.
+ */
+KDA_API kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k, const void *v,
+                   const void *g, const void *beta, float scale, void *out, const float *A_log,
+                   const float *dt_bias, float lower_bound, const void *initial_state,
+                   kda_state_dtype init_dtype, void *final_state, kda_state_dtype final_dtype,
+                   const int64_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                   kda_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the error word that the last kda_fwd on this
+ * workspace left behind, stores it in *flags (0 = none; bit 0 = a device wait
+ * timed out; bit 1 = malformed cu_seqlens) and returns KDA_OK, KDA_ERR_TIMEOUT
+ * or KDA_ERR_BAD_SEQLENS accordingly.
+ */
+KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t stream, int *flags);
+
+/*
+ * Measurement aid (no counterpart on the pages): while `events` is non-NULL,
+ * every kda_fwd records events[i] (cudaEvent_t handles owned by the caller) on
+ * its stream right after its i-th launch -- 0: work-list scheduling, 1: the
+ * segment carry/transition runs, 2: carry composition, 3: the forward runs --
+ * so each phase can be timed with cudaEventElapsedTime.  n_events must be 4.
+ * Pass NULL to stop.  The setting is process-wide and not thread-safe.
+ */
+KDA_API kda_status kda_set_profile_events(void *const *events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every
+symbol include/kda.h declares, and rejects bad arguments on the host before any
+CUDA call (fake device addresses are never dereferenced)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_51_gb300 import kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000000   # 16-byte aligned fake device address, never dereferenced
+
+
+def declared_symbols():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = kda.load_library()
+    syms = declared_symbols()
+    assert set(kda.EXPORTED_SYMBOLS) <= set(syms)
+    for s in syms:
+        assert hasattr(lib, s), f"{s} not exported"
+
+
+def test_status_strings():
+    lib = kda.load_library()
+    for code in range(8):
+        s = lib.kda_status_string(code)
+        assert s and isinstance(s, bytes)
+    assert lib.kda_status_string(0) == b"ok"
+
+
+def test_workspace_size_linear_in_heads_and_tiles():
+    sh = kda.make_shape(1, 1 << 20, 8, 1)
+    n8 = kda.workspace_size(sh)
+    assert n8 > 0
+    lib = kda.load_library()
+    n = ctypes.c_size_t(0)
+    bad = kda.make_shape(1, 64, 1, 1, K=64)
+    assert lib.kda_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
+    assert lib.kda_workspace_size(None, ctypes.byref(n)) == 1
+
+
+def _call(shape, q=FAKE, beta=FAKE, out=FAKE, A_log=FAKE, dt_bias=FAKE, lb=-1.0, scale=0.1,
+          init=None, init_dt=0, fin=None, fin_dt=0, cu=None, ws=FAKE, ws_bytes=1 << 30):
+    lib = kda.load_library()
+    p = ctypes.c_void_p
+    return lib.kda_fwd(ctypes.byref(shape), p(q), p(FAKE), p(FAKE), p(FAKE), p(beta),
+                       ctypes.c_float(scale), p(out), p(A_log), p(dt_bias), ctypes.c_float(lb),
+                       p(init) if init else None, init_dt, p(fin) if fin else None, fin_dt,
+                       p(cu) if cu else None, p(ws), ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("case,expected", [
+    (dict(shape=kda.make_shape(1, 64, 1, 1, K=64)), 2),
+    (dict(shape=kda.make_shape(1, 64, 1, 1, V=256)), 2),
+    (dict(shape=kda.make_shape(2, 64, 1, 2), cu=FAKE), 1),          # cu_seqlens needs B = 1
+    (dict(shape=kda.make_shape(2, 64, 1, 3)), 1),                   # N must equal B
+    (dict(shape=kda.make_shape(1, 64, 1, 1), lb=0.5), 1),           # lower_bound in [-5, 0]
+    (dict(shape=kda.make_shape(1, 64, 1, 1), lb=-5.5), 1),
+    (dict(shape=kda.make_shape(1, 64, 1, 1), lb=float("nan")), 1),
+    (dict(shape=kda.make_shape(1, 64, 1, 1), q=0), 1),              # null input
+    (dict(shape=kda.make_shape(1, 64, 1, 1), q=FAKE + 2), 1),       # misaligned input
+    (dict(shape=kda.make_shape(1, 64, 1, 1), out=0), 1),
+    (dict(shape=kda.make_shape(1, 64, 1, 1), A_log=0), 1),
+    (dict(shape=kda.make_shape(1, 64, 1, 1), init=FAKE, init_dt=1, fin=FAKE + (1 << 24), fin_dt=2), 1),
+    (dict(shape=kda.make_shape(1, 64, 1, 1), init=FAKE, init_dt=0), 1),   # dtype missing
+    (dict(shape=kda.make_shape(1, 64, 2, 1), init=FAKE, init_dt=2, fin=FAKE + 4096, fin_dt=2), 1),  # overlap
+    (dict(shape=kda.make_shape(-1, 64, 1, -1)), 1),
+    (dict(shape=kda.make_shape(1, 64, 0, 1)), 1),
+])
+def test_host_side_argument_errors(case, expected):
+    shape = case.pop("shape")
+    assert _call(shape, **case) == expected
+
+
+def test_element_aligned_beta_and_out_pass_the_argument_checks():
+    # 2-byte aligned beta/out are valid; without a GPU the call then stops at the
+    # device query (KDA_ERR_CUDA or KDA_ERR_UNSUPPORTED_DEVICE), not at the checks
+    assert _call(kda.make_shape(1, 64, 1, 1), beta=FAKE + 2, out=FAKE + 6) in (4, 5)
+
+
+def test_python_binding_requires_cuda_tensors():
+    import torch
+
+    q = torch.zeros(1, 16, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda.fwd(q, q, q, q, torch.zeros(1, 16, 1, dtype=torch.bfloat16), 0.1, q.clone(),
+                torch.zeros(1), torch.zeros(1, 128), -1.0)

@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Every case draws seeded synthetic inputs, runs ``kda_fwd`` on the GPU and the
+token-by-token oracle on the CPU, and compares element by element with the
+bounds in ``tests/gpu_helpers.py``.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_51_gb300 import inputs as I
+from tests.gpu_helpers import (check_out, check_state, random_case, run_gpu, run_oracle, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_51_gb300 import kda
+
+    kda.load_library()
+
+
+@pytest.fixture
+def seg_tokens(monkeypatch):
+    """Force the segment length (exercises the segment scan on small inputs)."""
+    def set_(n):
+        if n is None:
+            monkeypatch.delenv("KDA_SEG_TOKENS", raising=False)
+        else:
+            monkeypatch.setenv("KDA_SEG_TOKENS", str(n))
+    return set_
+
+
+def _compare(x, final_dtype=torch.float32, label="", seg=None):
+    out, fin = run_gpu(x, final_dtype=final_dtype)
+    ref_out, ref_fin = run_oracle(x)
+    B, T, H, _ = x["q"].shape
+    m, r = check_out(out, ref_out.reshape(B * T, H, 128), label=label)
+    s = check_state(fin, ref_fin, label=label) if fin is not None else None
+    return m, r, s
+
+
+def test_tiny_workload():
+    w = I.tiny_workload()
+    x = I.make_inputs(w, device="cuda")
+    _compare(x, torch.float32, "tiny")
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 15, 16, 17, 31, 32, 33, 48, 127, 129])
+def test_partial_chunks_single_sequence(T):
+    x = random_case(1, T, 2, seed=100 + T)
+    _compare(x, torch.float32, f"T={T}")
+
+
+def test_partial_chunk_sweep_varlen():
+    lens = list(range(1, 34)) + [127, 129]
+    x = random_case(1, sum(lens), 2, seed=7, lens=lens)
+    _compare(x, torch.float32, "sweep varlen")
+
+
+def test_varlen_with_empty_sequences_bf16_state():
+    lens = [0, 5, 0, 40, 16, 0]
+    x = random_case(1, sum(lens), 3, seed=8, lens=lens, init_dtype=torch.bfloat16)
+    _compare(x, torch.bfloat16, "empty seqs")
+
+
+@pytest.mark.parametrize("lb", [0.0, -1.0, -5.0])
+def test_lower_bound_range(lb):
+    x = random_case(2, 100, 2, seed=9, lb=lb)
+    _compare(x, torch.float32, f"lb={lb}")
+
+
+def test_no_initial_state_no_final_state():
+    x = random_case(1, 50, 2, seed=10, init_dtype=None)
+    out, fin = run_gpu(x, final_dtype=None)
+    assert fin is None
+    ref_out, _ = run_oracle(x)
+    check_out(out, ref_out.reshape(50, 2, 128), label="no states")
+
+
+@pytest.mark.parametrize("seg", [16, 48, 64, 512])
+def test_segment_scan_matches_oracle(seg_tokens, seg):
+    """Short segments force the three-phase segment scan (carry + composition)."""
+    seg_tokens(seg)
+    lens = [300, 17, 1000, 64, 129]
+    x = random_case(1, sum(lens), 2, seed=11 + seg, lens=lens)
+    _compare(x, torch.float32, f"seg={seg}")
+    x2 = random_case(1, sum(lens), 2, seed=12 + seg, lens=lens, init_dtype=torch.bfloat16)
+    _compare(x2, torch.bfloat16, f"seg={seg} bf16")
+
+
+def test_segment_scan_without_initial_state(seg_tokens):
+    seg_tokens(32)
+    x = random_case(2, 200, 2, seed=13, init_dtype=None)
+    _compare(x, torch.float32, "seg no init")
+
+
+def test_fixed_batch_workload():
+    w = I.fixed_batch_workload()
+    x = I.make_inputs(w, device="cuda")
+    _compare(x, torch.float32, w.name)
+
+
+def test_varlen_workload():
+    w = I.varlen_workload()
+    x = I.make_inputs(w, device="cuda")
+    _compare(x, torch.bfloat16, w.name)
+
+
+@pytest.mark.parametrize("total,H", [(8192, 32), (8192, 64), (32768, 32)])
+def test_sweep_workloads_small_cells(total, H):
+    w = I.sweep_workload(total, H)
+    x = I.make_inputs(w, device="cuda")
+    _compare(x, torch.float32, w.name)
+
+
+def test_determinism_bitwise():
+    x = random_case(1, 3000, 4, seed=14, lens=[1000, 2000])
+    o1, f1 = run_gpu(x)
+    o2, f2 = run_gpu(x)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(f1, f2)
+
+
+def test_in_place_state_update(seg_tokens):
+    for seg in (None, 64):
+        seg_tokens(seg)
+        x = random_case(1, 400, 2, seed=15, lens=[150, 250])
+        ref_out, ref_fin = run_oracle(x)
+        state = x["initial_state"].clone()
+        y = dict(x)
+        y["initial_state"] = state
+        out, fin = run_gpu(y, final_state=state)
+        assert fin.data_ptr() == state.data_ptr()
+        check_out(out, ref_out, label="in place")
+        check_state(state, ref_fin, label="in place")
+
+
+def test_split_and_carry_on_gpu():
+    x = random_case(1, 300, 2, seed=16)
+    out, fin = run_gpu(x)
+    a = dict(x)
+    b = dict(x)
+    for n in ("q", "k", "v", "g", "beta"):
+        a[n] = x[n][:, :137].contiguous()
+        b[n] = x[n][:, 137:].contiguous()
+    oa, fa = run_gpu(a)
+    b["initial_state"] = fa
+    ob, fb = run_gpu(b)
+    ref_out, ref_fin = run_oracle(x)
+    check_out(torch.cat([oa, ob], 1), ref_out, label="carry")
+    check_state(fb, ref_fin, label="carry")
+
+
+def test_batch_rows_equal_varlen_equal_lengths():
+    x = random_case(3, 80, 2, seed=17)
+    o1, f1 = run_gpu(x)
+    y = dict(x)
+    for n in ("q", "k", "v", "g", "beta"):
+        y[n] = x[n].reshape(1, 240, *x[n].shape[2:]).contiguous()
+    y["cu_seqlens"] = torch.tensor([0, 80, 160, 240], dtype=torch.int64, device="cuda")
+    o2, f2 = run_gpu(y)
+    assert torch.equal(o1.reshape(-1).view(torch.int16), o2.reshape(-1).view(torch.int16))
+    assert torch.equal(f1, f2)
+
+
+def test_malformed_cu_seqlens_is_flagged_not_trapped():
+    from gated_delta_rule_51_gb300 import kda
+
+    x = random_case(1, 64, 1, seed=18, lens=[32, 32])
+    x["cu_seqlens"] = torch.tensor([0, 40, 32], dtype=torch.int64, device="cuda")   # decreasing
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    run_gpu(x, workspace=ws)
+    flags = kda.check_device_error(ws)
+    assert flags & 2
+    # a well-formed call on the same workspace clears the word
+    x["cu_seqlens"] = torch.tensor([0, 32, 64], dtype=torch.int64, device="cuda")
+    run_gpu(x, workspace=ws)
+    assert kda.check_device_error(ws) == 0
+
+
+def test_long_workload_sampled():
+    """T = 1,048,576, H = 8: final state in full, outputs on sampled rows."""
+    w = I.long_workload()
+    x = I.make_inputs(w, device="cuda")
+    out, fin = run_gpu(x)
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(0, 64), rng.integers(0, w.T, 2048),
+                                     np.arange(w.T - 64, w.T)]))
+    ref_out, ref_fin = run_oracle(x, out_rows=rows)
+    check_out(out, ref_out, rows=rows, label=w.name)
+    check_state(fin, ref_fin, label=w.name)
