@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Throughput of the KDA chunked forward pass on GB300 (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one full forward pass (every kernel of kda_fwd) over one batch of
+seeded synthetic inputs shaped like the workload (gated_delta_rule_51_gb300/
+inputs.py).  `value` is whole-job tokens/s with the inputs already resident in
+HBM; `e2e` repeats the measurement through the public API with pinned host
+buffers, the host->device input copies and the device->host result copies
+inside the timed region.  The roofline object reports the forward kernel's
+compulsory HBM bytes (1282 B per token-head plus states and gate parameters)
+over its CUDA-event duration against the measured copy bandwidth.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload (the pages ship no code to run).
+Under torchrun every rank runs its own replica of the workload (weak scaling,
+no data-path collective); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd tokens/s and % of roofline (TFLOP/s, HBM GB/s) on 1xGB300"
+DEFAULT_CONFIG = "varlen_T32768_N8_H32"
+BYTES_PER_TOKEN_HEAD = 4 * 128 * 2 + 2 + 128 * 2      # q, k, v, g + beta + out (bf16)
+FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 6 * 16 * 128 + 4 * 16 * 128   # 16-token chunked form
+L2_BYTES = 126 * 1024 * 1024
+ALIASES = {"tiny": "tiny_B1_T64_H1", "fixed": "fixed_B2_T4096_H16",
+           "varlen": "varlen_T32768_N8_H32", "long": "long_T1048576_H8"}
+
+
+def workload(name):
+    from gated_delta_rule_51_gb300 import inputs as I
+
+    ws = I.named_workloads()
+    name = ALIASES.get(name, name)
+    if name not in ws:
+        raise SystemExit(f"unknown config {name}; choose from {sorted(ws)}")
+    return ws[name]
+
+
+def compulsory_bytes(w) -> int:
+    """Bytes the method must move: inputs, outputs, states, gate parameters."""
+    import torch
+
+    sb = 0
+    if w.state_dtype is not None:
+        per = 128 * 128 * (4 if w.state_dtype == torch.float32 else 2)
+        sb = w.N * w.H * per * (int(w.has_initial_state) + int(w.has_final_state))
+    params = w.H * 4 + w.H * 128 * 4
+    cu = 8 * (w.N + 1) if w.seq_lens is not None else 0
+    return w.token_heads * BYTES_PER_TOKEN_HEAD + sb + params + cu
+
+
+def config_dict(w, extra=None):
+    d = {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": 128, "V": 128, "N": w.N,
+         "state": str(w.state_dtype).replace("torch.", "") if w.state_dtype is not None else None,
+         "initial_state": w.has_initial_state, "lower_bound": w.lower_bound, "seed": w.seed,
+         "token_heads": w.token_heads}
+    if w.seq_lens is not None:
+        d["seq_lens"] = w.seq_lens if len(w.seq_lens) <= 16 else f"{len(w.seq_lens)} lengths"
+    if extra:
+        d.update(extra)
+    return d
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_51_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_name: str):
+    """DRAM bytes per forward-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload_name)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, x_cpu, budget_s: float = 15.0):
+    """Time the fp64 oracle, as it stands, on a bounded sample of the workload.
+
+    The sample is the first sequences (whole, or a prefix of the first one) of
+    the first heads, sized to about `budget_s` of CPU time; tokens/s is scaled
+    by the fraction of the workload's token-heads covered."""
+    import torch
+
+    import oracle
+
+    threads = os.cpu_count() or 1
+    lens = w.seq_lens if w.seq_lens is not None else [w.T] * w.B
+    budget_th = int(budget_s * 20000 * threads)    # ~20k token-heads/s per thread
+    heads = min(w.H, max(1, threads))
+    nseq, tok = 0, 0
+    for L in lens:
+        if (tok + L) * heads > budget_th and nseq > 0:
+            break
+        nseq += 1
+        tok += L
+    if tok * heads > budget_th:                    # one sequence too long: take a prefix
+        tok = max(16, budget_th // heads)
+    if w.seq_lens is not None:
+        q, k, v, g, beta = (x_cpu[n][:, :tok, :heads].contiguous() for n in ("q", "k", "v", "g", "beta"))
+        bounds = [0]
+        for L in lens[:nseq]:
+            bounds.append(min(tok, bounds[-1] + L))
+        cu = torch.tensor(bounds, dtype=torch.int64)
+        init = x_cpu["initial_state"][:nseq, :heads].contiguous() if x_cpu["initial_state"] is not None else None
+    else:
+        rows = max(1, min(nseq, w.B))
+        t_len = min(tok, w.T)
+        q, k, v, g, beta = (x_cpu[n][:rows, :t_len, :heads].contiguous() for n in ("q", "k", "v", "g", "beta"))
+        cu = None
+        init = x_cpu["initial_state"][:rows, :heads].contiguous() if x_cpu["initial_state"] is not None else None
+    th = q.shape[0] * q.shape[1] * heads
+    t0 = time.perf_counter()
+    oracle.kda_forward(q, k, v, g, beta, x_cpu["scale"], x_cpu["A_log"][:heads].contiguous(),
+                       x_cpu["dt_bias"][:heads].contiguous(), x_cpu["lower_bound"], init, cu,
+                       nthreads=threads)
+    dt = time.perf_counter() - t0
+    tokens_per_s = (th / w.H) / dt
+    desc = (f"{th} token-heads ({q.shape[0]}x{q.shape[1]} tokens x {heads} of {w.H} heads"
+            f"{', ' + str(len(cu) - 1) + ' sequences' if cu is not None else ''}); tokens/s scaled by "
+            f"covered token-heads / H")
+    return tokens_per_s, threads, desc, dt
+
+
+def run_reference(args, w):
+    """--impl reference: the fp64 oracle on the host cores, timed per step on a bounded sample."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from gated_delta_rule_51_gb300 import inputs as I
+    import oracle
+
+    oracle.build()
+    x = I.make_inputs(w, device="cpu")
+    budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, x, budget)
+    vals, times = [], []
+    desc, threads = "", 1
+    for _ in range(args.steps):
+        v, threads, desc, dt = cpu_oracle_sample(w, x, budget)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * statistics.mean(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, {"parallelism": "cpu threads"}),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from gated_delta_rule_51_gb300 import inputs as I
+    from gated_delta_rule_51_gb300 import kda
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    kda.load_library()
+    x = I.make_inputs(w, device=dev)          # replicas: every rank runs its own copy
+    out = torch.empty((w.B, w.T, w.H, 128), dtype=torch.bfloat16, device=dev)
+    fin = (torch.empty((w.N, w.H, 128, 128), dtype=w.state_dtype, device=dev)
+           if w.has_final_state else None)
+    ws = torch.empty(kda.workspace_size(kda.make_shape(w.B, w.T, w.H, w.N)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], out, x["A_log"], x["dt_bias"],
+                x["lower_bound"], initial_state=x["initial_state"], final_state=fin,
+                cu_seqlens=x["cu_seqlens"], workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if kda.check_device_error(ws, dev):
+        raise SystemExit("device error flags set during warm-up")
+    launches_per_step = kda.last_launch_count()
+
+    # timed region: per step an L2 flush, then start event, kernels (phase events)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e in ev:
+        for t in e:
+            t.record(stream)        # creates the events before their handles are handed out
+    torch.cuda.synchronize(dev)
+    barrier()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            kda.set_profile_events(ev[i][1:])
+            step()
+        kda.set_profile_events(None)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    barrier()
+    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    fwd_ms = [e[3].elapsed_time(e[4]) for e in ev]
+    ph1_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    cmp_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    sch_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = w.B * w.T
+    value = tokens * world * args.steps / (total_ms / 1000.0)
+    ms_per_step = total_ms / args.steps
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        names = [n for n in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens") if x[n] is not None]
+        host = {n: x[n].cpu().pin_memory() for n in names}
+        dev_in = {n: torch.empty_like(x[n]) for n in names}
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h_fin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True) if fin is not None else None
+        h_A, h_dt = x["A_log"].cpu().pin_memory(), x["dt_bias"].cpu().pin_memory()
+        d_A, d_dt = torch.empty_like(x["A_log"]), torch.empty_like(x["dt_bias"])
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names) + h_A.numel() * 4 + h_dt.numel() * 4
+        d2h = h_out.numel() * 2 + (h_fin.numel() * h_fin.element_size() if h_fin is not None else 0)
+
+        def e2e_step():
+            for n in names:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            d_A.copy_(h_A, non_blocking=True)
+            d_dt.copy_(h_dt, non_blocking=True)
+            kda.fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], x["scale"], out,
+                    d_A, d_dt, x["lower_bound"], initial_state=dev_in.get("initial_state"),
+                    final_state=fin, cu_seqlens=dev_in.get("cu_seqlens"), workspace=ws)
+            h_out.copy_(out, non_blocking=True)
+            if h_fin is not None:
+                h_fin.copy_(fin, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": tokens * world * args.steps / (e2e_ms / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        del host, dev_in
+    if kda.check_device_error(ws, dev):
+        raise SystemExit("device error flags set during the timed steps")
+
+    hbm_gbs, bf16_tf, peak_kind = load_peaks()
+    nbytes = compulsory_bytes(w)
+    flops = w.token_heads * FLOPS_PER_TOKEN_HEAD
+    fwd_mean = statistics.mean(fwd_ms)
+    achieved = nbytes / (fwd_mean / 1000.0) / 1e9
+    step_s = ms_per_step / 1000.0
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "traffic": measured_traffic(w.name),
+                "kernel": "kda_chain_kernel (forward runs)",
+                "peak_source": "measured, MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": nbytes,
+                "step_frac": (nbytes / step_s / 1e9) / hbm_gbs,
+                "step_tflops": flops / step_s / 1e12,
+                "step_tflops_frac_of_bf16_peak": flops / step_s / 1e12 / bf16_tf,
+                "phase_ms": {"schedule": statistics.mean(sch_ms), "segment_runs": statistics.mean(ph1_ms),
+                             "compose": statistics.mean(cmp_ms), "forward": fwd_mean}}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x_cpu = {n: (t.cpu() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+        v, threads, desc, _ = cpu_oracle_sample(w, x_cpu, budget_s=15.0)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config_dict(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                          "l2": "flushed between timed steps (252 MB write)"}),
+                "roofline": roofline, "cpu_baseline": cpu,
+                "clocks": clocks.summary(), "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps,
+                "tflops": flops / step_s / 1e12, "hbm_gbs": nbytes / step_s / 1e9,
+                "wall_s": t_wall}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = workload(args.config)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -98,6 +98,7 @@ kda_status check_shape(const kda_shape* s) {
 
 cudaEvent_t g_profile_events[4] = {nullptr, nullptr, nullptr, nullptr};
 bool g_profile = false;
+thread_local int t_last_launches = 0;
 
 void mark(int i, cudaStream_t s) {
   if (g_profile && g_profile_events[i] != nullptr) cudaEventRecord(g_profile_events[i], s);
@@ -230,7 +231,9 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
   sp.cap_forward = L.cap_forward;
   sp.cap_compose = L.cap_compose;
   sp.cap_slots = L.cap_slots;
+  int launches = 0;
   if (launch_schedule(sp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  ++launches;
   mark(0, stream);
 
   ChainParams cp;
@@ -258,12 +261,14 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
     cp.items = sp.phase1;
     cp.item_count = &hdr->n_phase1;
     if (launch_chain(cp, (int)L.cap_phase1, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    ++launches;
     ComposeParams cmp;
     cmp.ws_states = cp.ws_states;
     cmp.items = sp.compose;
     cmp.item_count = &hdr->n_compose;
     mark(1, stream);
     if (launch_compose(cmp, (int)L.cap_compose, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (L.cap_compose > 0) ++launches;
     mark(2, stream);
   } else {
     mark(1, stream);
@@ -272,9 +277,13 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
   cp.items = sp.forward;
   cp.item_count = &hdr->n_forward;
   if (launch_chain(cp, (int)L.cap_forward, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  ++launches;
   mark(3, stream);
+  t_last_launches = launches;
   return KDA_OK;
 }
+
+int kda_last_launch_count(void) { return t_last_launches; }
 
 kda_status kda_set_profile_events(void* const* events, int n_events) {
   if (events == nullptr) {

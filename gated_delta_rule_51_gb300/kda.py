@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPOR
                 3: "KDA_ERR_WORKSPACE_TOO_SMALL", 4: "KDA_ERR_UNSUPPORTED_DEVICE", 5: "KDA_ERR_CUDA",
                 6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_BAD_SEQLENS"}
 EXPORTED_SYMBOLS = ("kda_status_string", "kda_workspace_size", "kda_fwd", "kda_check_device_error",
-                    "kda_set_profile_events")
+                    "kda_set_profile_events", "kda_last_launch_count")
 
 
 class kda_shape(ctypes.Structure):
@@ -66,6 +66,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_check_device_error.restype = ctypes.c_int
         lib.kda_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
         lib.kda_set_profile_events.restype = ctypes.c_int
+        lib.kda_last_launch_count.argtypes = []
+        lib.kda_last_launch_count.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -191,3 +193,8 @@ def set_profile_events(events) -> None:
     st = lib.kda_set_profile_events(arr, 4)
     if st != KDA_OK:
         raise KDAError(st, "kda_set_profile_events")
+
+
+def last_launch_count() -> int:
+    """Kernels enqueued by this thread's most recent fwd call."""
+    return int(load_library().kda_last_launch_count())

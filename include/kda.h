@@ -134,6 +134,13 @@ KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t st
  */
 KDA_API kda_status kda_set_profile_events(void *const *events, int n_events);
 
+/*
+ * Measurement aid (no counterpart on the pages): the number of kernels the
+ * calling thread's most recent successful kda_fwd enqueued (2 to 4: work-list
+ * scheduling, segment runs, carry composition, forward runs).
+ */
+KDA_API int kda_last_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif
