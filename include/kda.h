@@ -141,6 +141,35 @@ KDA_API kda_status kda_set_profile_events(void *const *events, int n_events);
  */
 KDA_API int kda_last_launch_count(void);
 
+/*
+ * kda_fwd for callers that cannot allocate device memory (no counterpart on
+ * the pages).  Some callers have no way to hand over scratch memory: code that
+ * runs where cudaMalloc is not allowed (a framework that owns every device
+ * allocation through its own pool, a runtime that must not grow its footprint
+ * after start-up, a plugin without access to the application's allocator).
+ * This entry point takes the same arguments as kda_fwd except the workspace,
+ * which it takes from a fixed 64 MiB array built into the library; every GPU
+ * that loads the library holds that array until the process exits.  The
+ * caller still passes all inputs and outputs.
+ *   - Problems whose kda_workspace_size exceeds 64 MiB are rejected with
+ *     KDA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - It allocates nothing and calls no allocating routine.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (different streams, different threads, without ordering between them)
+ *     race on it and give undefined results.  Nothing in it needs clearing
+ *     between calls.  Its device error word cannot be read back through
+ *     kda_check_device_error, which needs a workspace address.
+ */
+KDA_API kda_status kda_fwd_static_workspace(const kda_shape *shape, const void *q, const void *k,
+                                            const void *v, const void *g, const void *beta, float scale,
+                                            void *out, const float *A_log, const float *dt_bias,
+                                            float lower_bound, const void *initial_state,
+                                            kda_state_dtype init_dtype, void *final_state,
+                                            kda_state_dtype final_dtype, const int64_t *cu_seqlens,
+                                            kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
