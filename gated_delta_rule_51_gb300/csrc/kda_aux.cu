@@ -61,7 +61,10 @@ __device__ long long block_scan(long long x, long long* buf) {
 
 __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const ScheduleParams p) {
   __shared__ long long s_buf[kSchedThreads];
-  __shared__ long long s_tot[3];   // segments, q slots, compose chains (running)
+  __shared__ long long s_tot[3];   // segments, q slots, compose chains (running totals)
+  __shared__ int s_start[kSchedThreads], s_len[kSchedThreads], s_nseg[kSchedThreads], s_incl[kSchedThreads];
+  __shared__ long long s_seg0[kSchedThreads], s_q0[kSchedThreads];
+  __shared__ int s_c0[kSchedThreads];
   __shared__ int s_err;
   const int tid = threadIdx.x;
   const long long H = p.H;
@@ -91,41 +94,64 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
       }
       const long long nq = nseg >= 2 ? nseg - 1 : 0;
       const long long nc = nseg >= 3 ? 1 : 0;
-      const long long seg0 = s_tot[0] + block_scan(nseg, s_buf) - nseg;
+      const long long incl = block_scan(nseg, s_buf);
+      const long long seg0 = s_tot[0] + incl - nseg;
       const long long q0 = s_tot[1] + block_scan(nq, s_buf) - nq;
       const long long c0 = s_tot[2] + block_scan(nc, s_buf) - nc;
-      if (pass == 1 && n < p.N) {
+      const int count = (int)(p.N - base < kSchedThreads ? p.N - base : kSchedThreads);
+      if (pass == 1) {
+        s_start[tid] = (int)start;
+        s_len[tid] = (int)len;
+        s_nseg[tid] = (int)nseg;
+        s_incl[tid] = (int)incl;
+        s_seg0[tid] = seg0;
+        s_q0[tid] = q0;
+        s_c0[tid] = (int)c0;
+        __syncthreads();
+        // every (head, segment) of this tile's sequences, spread over all threads
+        const long long tile_segs = s_incl[count - 1];
         const long long in_user = p.has_init ? kInUser : kInZero;
-        for (long long h = 0; h < H; ++h) {
-          const long long qb = q0 * H + h * nq;          // q slot of segment 0
+        for (long long idx = tid; idx < tile_segs * H; idx += kSchedThreads) {
+          const long long h = idx / tile_segs;
+          const int sl = (int)(idx - h * tile_segs);
+          int lo = 0, hi = count - 1;                 // first sequence with s_incl > sl
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_incl[mid] > sl) hi = mid; else lo = mid + 1;
+          }
+          const int nl = lo;
+          const long long ns = s_nseg[nl];
+          const long long s = sl - (s_incl[nl] - ns);
+          const long long st0 = s_start[nl], ln = s_len[nl];
+          const long long nq_ = ns >= 2 ? ns - 1 : 0;
+          const long long qb = s_q0[nl] * H + h * nq_;    // q slot of segment 0
           const long long pb = qb + q_total * H;          // p slot of segment 0
-          for (long long s = 0; s < nseg; ++s) {
-            const long long fi = (seg0 + s) * H + h;
-            const long long flen = len <= 0 ? 0 : (len - s * L < L ? len - s * L : L);
-            long long in_slot;
-            if (s == 0) in_slot = (nseg >= 2 && p.has_init) ? pb : in_user;
-            else in_slot = qb + s - 1;
-            const long long out_slot = (s == nseg - 1 && p.has_final) ? kOutUser : kOutNone;
-            if (fi < p.cap_forward)
-              p.forward[fi] = make_item(start + s * L, flen, h, kModeForward, n, in_slot, out_slot, -1);
-            if (s <= nseg - 2) {
-              const long long qs = qb + s, ps = pb + s;
-              if (ps < p.cap_phase1 && ps < p.cap_slots) {
-                p.phase1[qs] = make_item(start + s * L, L, h, kModeLocal, n, s == 0 ? in_user : kInZero, qs,
-                                         (s == 0 && p.has_init) ? ps : -1);
-                p.phase1[ps] = s >= 1 ? make_item(start + s * L, L, h, kModeTransition, n, kInIdentity, ps, -1)
-                                      : make_item(0, -1, h, kModeTransition, n, kInZero, kOutNone, -1);
-              }
+          const long long nn = base + nl;
+          const long long fi = (s_seg0[nl] + s) * H + h;
+          const long long flen = ln <= 0 ? 0 : (ln - s * L < L ? ln - s * L : L);
+          long long in_slot;
+          if (s == 0) in_slot = (ns >= 2 && p.has_init) ? pb : in_user;
+          else in_slot = qb + s - 1;
+          const long long out_slot = (s == ns - 1 && p.has_final) ? kOutUser : kOutNone;
+          if (fi < p.cap_forward)
+            p.forward[fi] = make_item(st0 + s * L, flen, h, kModeForward, nn, in_slot, out_slot, -1);
+          if (s <= ns - 2) {
+            const long long qs = qb + s, ps = pb + s;
+            if (ps < p.cap_phase1 && ps < p.cap_slots) {
+              p.phase1[qs] = make_item(st0 + s * L, L, h, kModeLocal, nn, s == 0 ? in_user : kInZero, qs,
+                                       (s == 0 && p.has_init) ? ps : -1);
+              p.phase1[ps] = s >= 1 ? make_item(st0 + s * L, L, h, kModeTransition, nn, kInIdentity, ps, -1)
+                                    : make_item(0, -1, h, kModeTransition, nn, kInZero, kOutNone, -1);
             }
           }
-          if (nseg >= 3) {
-            const long long ci = c0 * H + h;
+          if (s == 0 && ns >= 3) {
+            const long long ci = s_c0[nl] * H + h;
             if (ci < p.cap_compose) {
               ComposeItem it;
               it.head = (int)h;
               it.first_q_slot = (int)qb;
               it.first_p_slot = (int)(pb + 1);
-              it.n_steps = (int)(nseg - 2);
+              it.n_steps = (int)(ns - 2);
               p.compose[ci] = it;
             }
           }

@@ -12,15 +12,19 @@
 //   O    = scale * ((qh*2^G) S + Aqk Vn)
 //   S'   = Diag(2^G_C) S + (kh*2^(G_C-G))^T Vn
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: q, k, g tiles into a ring, v tile into the
-//               operand stage (v is the A operand of U^T = V^T Tm^T as is).
+// Warp roles (256 threads, two CTAs per SM):
+//   warp 0      TMA producer: the q, k, g and v tiles of a chunk into one stage
+//               of a four-stage ring.
 //   warp 1      tcgen05 issuer (one thread).  State GEMMs in the M = V = 128
 //               orientation:  D1 = V^T Tm^T + S^T [-W^T | (qh 2^G)^T]   (N = 32)
 //                             D2 += Vn^T kfac ;  D1[:,16:] += Vn^T Aqk^T
-//   warps 2-5   prologue: gate, cumsum, L2 norms, Gram matrices (warp MMA,
-//               tf32), inverse, W (warp MMA, split bf16), operand tiles.
-//   warps 6-9   epilogue: Vn read-out (split into bf16 hi + lo), outputs,
+//   warps 2-3   prologue: each warp prepares whole chunks on its own (even /
+//               odd chunks): gate, cumsum, L2 norms, Gram matrices (tf32 warp
+//               MMA), inverse, W (bf16 warp MMA).  The tcgen05 operands are
+//               written in place over the tiles they are made from: q -> qh*2^G,
+//               k -> kfac (hi), g -> kfac (lo), and a bf16 copy of kh*2^G next
+//               to q, which the W product then overwrites with -W.
+//   warps 4-7   epilogue: Vn read-out (split into bf16 hi + lo), outputs,
 //               state decay + bf16 copy of S^T for the next chunk's A operand.
 // TMEM (256 columns): [0,128) S^T fp32 accumulator, [128,192) S^T as packed
 // bf16 (A operand read straight from TMEM), [192,256) two 32-column D1 tiles.
@@ -33,64 +37,53 @@
 
 namespace kda {
 
-constexpr int kThreads = 320;
-constexpr int kNRaw = 2;
-constexpr int kNOp = 2;
+constexpr int kThreads = 256;
+constexpr int kStages = 4;
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpProlog0 = 2;
-constexpr int kWarpEpi0 = 6;
+constexpr int kProlog = 2;            // prologue warps
+constexpr int kWarpEpi0 = 4;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColState = 0;
 constexpr uint32_t kColSbf = 128;
 constexpr uint32_t kColD1 = 192;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kBarProlog = 1;   // named barrier id of the prologue warps
 
-struct RawStage {         // q, k, g tiles, each 2 boxes [16 rows x 64 ch] bf16 SW128
-  uint8_t q[4096];
-  uint8_t k[4096];
-  uint8_t g[4096];
-};
-struct OpStage {
-  uint8_t X[8192];        // B of the S-GEMM: rows 0-15 = -W, rows 16-31 = qh*2^G; K-major SW128
-  uint8_t v[4096];        // v tile from TMA (MN-major SW128 A operand)
-  uint8_t KFhi[4096];     // kfac^T [128 ch][16 tok] K-major, no swizzle (hi part)
-  uint8_t KFlo[4096];
+// One chunk's stage.  Offsets of the 128-byte swizzled regions are multiples
+// of 1024 bytes.  X block b (b = 0, 1 for channels 64b .. 64b+63) is the K-major
+// B operand of the S-side GEMM: rows 0-15 = -W (first holds bf16 kh*2^G),
+// rows 16-31 = qh*2^G (first holds the q tile, as the TMA box lands there).
+struct Stage {
+  uint8_t X[2][4096];
+  uint8_t K[4096];        // k tile -> kfac hi   (MN-major B of the state update)
+  uint8_t G[4096];        // g tile -> kfac lo
+  uint8_t V[4096];        // v tile (MN-major A of U^T = V^T Tm^T)
   uint8_t TPhi[1024];     // [Tm ; 0] [32 rows][16] K-major, no swizzle
   uint8_t TPlo[1024];
   uint8_t AQhi[512];      // Aqk [16][16] K-major, no swizzle
   uint8_t AQlo[512];
   float gamC[128];        // 2^G_C per channel
-  uint8_t pad[24576 - 8192 - 4096 - 8192 - 2048 - 1024 - 512];
+  uint8_t pad[512];
 };
-static_assert(sizeof(OpStage) == 24576, "op stage size");
-struct PrologScratch {
-  uint16_t kg[16][136];        // bf16 kh*2^G, row stride 272 B (ldmatrix friendly)
-  float gram[4][2][16][16];    // per-warp partial Grams (kk, qk)
-  float normp[4][16][2];       // per-warp partial |q|^2, |k|^2
-  float beta[16];
-  float pad[12];
+static_assert(sizeof(Stage) == 24576, "stage size (multiple of 1024 for the swizzled regions)");
+struct PrologScratch {    // Gram matrices of one prologue warp (fp32, rows = tokens)
+  float Gk[16][16];
+  float Gq[16][16];
 };
 struct SmemLayout {
-  RawStage raw[kNRaw];
-  OpStage op[kNOp];
-  uint8_t vn_hi[4096];         // Vn^T [128 v][16 tok] K-major, no swizzle
+  Stage st[kStages];
+  uint8_t vn_hi[4096];    // Vn^T [128 v][16 tok] K-major, no swizzle
   uint8_t vn_lo[4096];
-  PrologScratch ps;
+  PrologScratch ps[kProlog];
 };
 
 size_t chain_smem_bytes() { return sizeof(SmemLayout) + 1024; }
 
-// byte offset of element (row r, channel c) in a [16 x 128] bf16 tile stored as
-// two TMA boxes of [16 x 64] with the 128-byte swizzle
-__device__ __forceinline__ uint32_t tile_off(int r, int c) {
-  return (uint32_t)((c >> 6) * 2048 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
-}
-// byte offset of (row n, k) in a K-major SW128 [32 x 128] bf16 operand (two 4 KB k-blocks)
-__device__ __forceinline__ uint32_t xop_off(int n, int c) {
-  return (uint32_t)((c >> 6) * 4096 + (n >> 3) * 1024 + (n & 7) * 128 + ((((c & 63) >> 3) ^ (n & 7)) << 4) +
-                    (c & 7) * 2);
+// byte offset of the 16-byte chunk holding channels [8 j16', 8 j16' + 8) of row r
+// in a [16 x 64] bf16 tile with the 128-byte swizzle (j16 = chunk index 0..7)
+__device__ __forceinline__ uint32_t sw_off(int r, int j16) {
+  return (uint32_t)(r * 128 + ((j16 ^ (r & 7)) << 4));
 }
 // byte offset of (row n, k) in a K-major, unswizzled operand with 16 k per row:
 // 8x16-byte core matrices, LBO = 128 (k direction), SBO = 256 (row direction)
@@ -108,6 +101,271 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) 
   hi = __bfloat16_as_ushort(h);
   lo = __bfloat16_as_ushort(l);
 }
+// split two floats into packed hi and lo bf16x2 words
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+}
+// (a0, a1) * (b0, b1) with one packed fp32x2 multiply
+__device__ __forceinline__ void mul2(uint32_t& x0, uint32_t& x1, float b0, float b1) {
+  uint64_t a, b, c;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "r"(x0), "r"(x1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(a), "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(x0), "=r"(x1) : "l"(c));
+}
+
+// Prepare the tcgen05 operands of one chunk (one warp, 16 tokens x 128 channels).
+// Lane (gid, tig) holds tokens ra = 2 gid and rb = 2 gid + 1 and, in pass p,
+// channels 32 p + 8 tig + j (j < 8).  For the Gram warp MMAs the physical
+// tokens 2 gid / 2 gid + 1 play the fragment rows gid / gid + 8, and the
+// channel pair (8 tig + 2 s, + 1) the k positions (tig, tig + 4) of k-step s.
+__device__ __forceinline__ void prologue_chunk(Stage& st, PrologScratch& sc, int nv, const float nr, const float lbl2,
+                                               const float* __restrict__ dtb, float beta_a, float beta_b,
+                                               int lane, bool v_used) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const int ra = 2 * gid, rb = 2 * gid + 1;
+  const bool va = ra < nv, vb = rb < nv;
+  const bool partial = nv < kChunk;
+
+  // ---- L2 norms of q and k over all 128 channels
+  float sq[2] = {0.f, 0.f}, sk[2] = {0.f, 0.f};
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int j16 = 4 * (p & 1) + tig;
+    const uint8_t* qb = st.X[p >> 1] + 2048;
+    const uint8_t* kb = st.K + 2048 * (p >> 1);
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = ra + hr;
+      const uint4 wq = *reinterpret_cast<const uint4*>(qb + sw_off(r, j16));
+      const uint4 wk = *reinterpret_cast<const uint4*>(kb + sw_off(r, j16));
+      const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float q0 = bf16lo_to_f32(aq[u]), q1 = bf16hi_to_f32(aq[u]);
+        const float k0 = bf16lo_to_f32(ak[u]), k1 = bf16hi_to_f32(ak[u]);
+        sq[hr] = fmaf(q0, q0, fmaf(q1, q1, sq[hr]));
+        sk[hr] = fmaf(k0, k0, fmaf(k1, k1, sk[hr]));
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m <= 2; m <<= 1) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      sq[hr] += __shfl_xor_sync(0xffffffffu, sq[hr], m);
+      sk[hr] += __shfl_xor_sync(0xffffffffu, sk[hr], m);
+    }
+  }
+  const float rq[2] = {va ? rsqrt_approx(sq[0] + 1e-6f) : 0.f, vb ? rsqrt_approx(sq[1] + 1e-6f) : 0.f};
+  const float rk[2] = {va ? rsqrt_approx(sk[0] + 1e-6f) : 0.f, vb ? rsqrt_approx(sk[1] + 1e-6f) : 0.f};
+
+  float ck0[4] = {0, 0, 0, 0}, ck1[4] = {0, 0, 0, 0}, cq0[4] = {0, 0, 0, 0}, cq1[4] = {0, 0, 0, 0};
+#pragma unroll 1
+  for (int p = 0; p < 4; ++p) {
+    const int j16 = 4 * (p & 1) + tig;
+    const int ch0 = 32 * p + 8 * tig;
+    uint8_t* qb = st.X[p >> 1] + 2048;
+    uint8_t* wb = st.X[p >> 1];
+    uint8_t* kb = st.K + 2048 * (p >> 1);
+    uint8_t* gb = st.G + 2048 * (p >> 1);
+    float nrdb[8];
+    {
+      const float4 d0 = *reinterpret_cast<const float4*>(dtb + ch0);
+      const float4 d1 = *reinterpret_cast<const float4*>(dtb + ch0 + 4);
+      nrdb[0] = nr * d0.x; nrdb[1] = nr * d0.y; nrdb[2] = nr * d0.z; nrdb[3] = nr * d0.w;
+      nrdb[4] = nr * d1.x; nrdb[5] = nr * d1.y; nrdb[6] = nr * d1.z; nrdb[7] = nr * d1.w;
+    }
+    float q[2][8], k[2][8], G[2][8];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = ra + hr;
+      const bool valid = hr == 0 ? va : vb;
+      uint4 wq = *reinterpret_cast<const uint4*>(qb + sw_off(r, j16));
+      uint4 wk = *reinterpret_cast<const uint4*>(kb + sw_off(r, j16));
+      const uint4 wg = *reinterpret_cast<const uint4*>(gb + sw_off(r, j16));
+      if (partial && !valid) {
+        wq = make_uint4(0u, 0u, 0u, 0u);
+        wk = make_uint4(0u, 0u, 0u, 0u);
+      }
+      const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
+      const uint32_t ag[4] = {wg.x, wg.y, wg.z, wg.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        q[hr][2 * u] = bf16lo_to_f32(aq[u]);
+        q[hr][2 * u + 1] = bf16hi_to_f32(aq[u]);
+        k[hr][2 * u] = bf16lo_to_f32(ak[u]);
+        k[hr][2 * u + 1] = bf16hi_to_f32(ak[u]);
+        // gate: base-2 log-decay lb * log2(e) * sigmoid(exp(A_log) (g + dt_bias)); 0 past the end
+        const float t0 = ex2_approx(fmaf(nr, bf16lo_to_f32(ag[u]), nrdb[2 * u]));
+        const float t1 = ex2_approx(fmaf(nr, bf16hi_to_f32(ag[u]), nrdb[2 * u + 1]));
+        G[hr][2 * u] = valid ? lbl2 * rcp_approx(1.f + t0) : 0.f;
+        G[hr][2 * u + 1] = valid ? lbl2 * rcp_approx(1.f + t1) : 0.f;
+      }
+    }
+    // ---- within-chunk inclusive cumsum over tokens (pairs in a lane, scan over gid)
+    float gC[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float pair = G[0][j] + G[1][j];
+      float incl = pair;
+#pragma unroll
+      for (int d = 1; d <= 4; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, 4 * d);
+        if (gid >= d) incl += y;
+      }
+      const float excl = incl - pair;
+      G[0][j] = excl + G[0][j];
+      G[1][j] = incl;
+      gC[j] = __shfl_sync(0xffffffffu, incl, 28 + tig);
+    }
+    // ---- decay-scaled operands
+    float kg[2][8], ki[2][8], qg[2][8];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float gam = ex2_approx(G[hr][j]);
+        const float gin = ex2_approx(-G[hr][j]);
+        const float kh = k[hr][j] * rk[hr];
+        kg[hr][j] = kh * gam;
+        ki[hr][j] = kh * gin;
+        qg[hr][j] = q[hr][j] * rq[hr] * gam;
+      }
+    // ---- Gram partials over this pass's 32 channels (tf32 warp MMA)
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int j = 2 * s;
+      const uint32_t ak[4] = {f32_to_tf32(kg[0][j]), f32_to_tf32(kg[1][j]), f32_to_tf32(kg[0][j + 1]),
+                              f32_to_tf32(kg[1][j + 1])};
+      const uint32_t aq[4] = {f32_to_tf32(qg[0][j]), f32_to_tf32(qg[1][j]), f32_to_tf32(qg[0][j + 1]),
+                              f32_to_tf32(qg[1][j + 1])};
+      const uint32_t b0[2] = {f32_to_tf32(ki[0][j]), f32_to_tf32(ki[0][j + 1])};
+      const uint32_t b1[2] = {f32_to_tf32(ki[1][j]), f32_to_tf32(ki[1][j + 1])};
+      mma_tf32_16x8x8(ck0, ak, b0);
+      mma_tf32_16x8x8(ck1, ak, b1);
+      mma_tf32_16x8x8(cq0, aq, b0);
+      mma_tf32_16x8x8(cq1, aq, b1);
+    }
+    // ---- operand tiles, written in place
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const uint32_t o = sw_off(ra + hr, j16);
+      *reinterpret_cast<uint4*>(qb + o) =
+          make_uint4(pack_bf16x2(qg[hr][0], qg[hr][1]), pack_bf16x2(qg[hr][2], qg[hr][3]),
+                     pack_bf16x2(qg[hr][4], qg[hr][5]), pack_bf16x2(qg[hr][6], qg[hr][7]));
+      *reinterpret_cast<uint4*>(wb + o) =
+          make_uint4(pack_bf16x2(kg[hr][0], kg[hr][1]), pack_bf16x2(kg[hr][2], kg[hr][3]),
+                     pack_bf16x2(kg[hr][4], kg[hr][5]), pack_bf16x2(kg[hr][6], kg[hr][7]));
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float gc0 = ex2_approx(gC[2 * u]), gc1 = ex2_approx(gC[2 * u + 1]);
+        split_bf16x2(ki[hr][2 * u] * gc0, ki[hr][2 * u + 1] * gc1, hw[u], lw[u]);
+      }
+      *reinterpret_cast<uint4*>(kb + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(gb + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    if (gid == 0) {
+      float e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) e[j] = ex2_approx(gC[j]);
+      *reinterpret_cast<float4*>(&st.gamC[ch0]) = make_float4(e[0], e[1], e[2], e[3]);
+      *reinterpret_cast<float4*>(&st.gamC[ch0 + 4]) = make_float4(e[4], e[5], e[6], e[7]);
+    }
+  }
+  // ---- Grams -> shared memory in token order (fragment row gid = token 2 gid,
+  //      gid + 8 = token 2 gid + 1; column 2 tig = token 4 tig, 8 + 2 tig = 4 tig + 1)
+  *reinterpret_cast<float4*>(&sc.Gk[ra][4 * tig]) = make_float4(ck0[0], ck1[0], ck0[1], ck1[1]);
+  *reinterpret_cast<float4*>(&sc.Gk[rb][4 * tig]) = make_float4(ck0[2], ck1[2], ck0[3], ck1[3]);
+  *reinterpret_cast<float4*>(&sc.Gq[ra][4 * tig]) = make_float4(cq0[0], cq1[0], cq0[1], cq1[1]);
+  *reinterpret_cast<float4*>(&sc.Gq[rb][4 * tig]) = make_float4(cq0[2], cq1[2], cq0[3], cq1[3]);
+  // beta of every token, from the lanes that hold it
+  const float sa = va ? rcp_approx(1.f + ex2_approx(-beta_a * kLog2e)) : 0.f;
+  const float sb = vb ? rcp_approx(1.f + ex2_approx(-beta_b * kLog2e)) : 0.f;
+  float bet[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bet[i] = __shfl_sync(0xffffffffu, (i & 1) ? sb : sa, 4 * (i >> 1));
+  __syncwarp();
+  if (lane < 16) {
+    // column j of X = (I + Akk)^-1 by forward substitution, Akk[i][m] = beta_i Gk[i][m]
+    const int j = lane;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+    for (int m = 0; m < 15; ++m) {
+#pragma unroll
+      for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-bet[i] * sc.Gk[i][m], x[m], x[i]);
+    }
+    float bj = bet[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) bj = (j == i) ? bet[i] : bj;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint16_t hi, lo;
+      split_bf16(x[i] * bj, hi, lo);
+      const uint32_t o = ns_off(i, j);
+      *reinterpret_cast<uint16_t*>(st.TPhi + o) = hi;
+      *reinterpret_cast<uint16_t*>(st.TPlo + o) = lo;
+    }
+  } else {
+    // Aqk row i = lane - 16, inclusive lower triangle
+    const int i = lane - 16;
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int jj = 0; jj < 16; jj += 2) {
+      const float a = jj <= i ? sc.Gq[i][jj] : 0.f;
+      const float b = jj + 1 <= i ? sc.Gq[i][jj + 1] : 0.f;
+      split_bf16x2(a, b, hw[jj / 2], lw[jj / 2]);
+    }
+    *reinterpret_cast<uint4*>(st.AQhi + ns_off(i, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(st.AQhi + ns_off(i, 8)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    *reinterpret_cast<uint4*>(st.AQlo + ns_off(i, 0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    *reinterpret_cast<uint4*>(st.AQlo + ns_off(i, 8)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+  }
+  __syncwarp();
+  // ---- W = Tm (kh*2^G) per 8-channel tile (bf16 warp MMA, Tm split hi + lo), -W over kh*2^G
+  uint32_t ahi[4], alo[4];
+  {
+    const int mat = lane >> 3, rr = lane & 7;
+    const uint32_t moff = (uint32_t)((mat & 1) * 256 + (mat >> 1) * 128 + rr * 16);
+    ldmatrix_x4(ahi, smem_u32(st.TPhi) + moff);
+    ldmatrix_x4(alo, smem_u32(st.TPlo) + moff);
+  }
+#pragma unroll 2
+  for (int nt = 0; nt < 16; nt += 2) {
+    uint32_t bfr[4];
+    {
+      // matrices: (tokens 0-7, tile nt), (8-15, nt), (0-7, nt+1), (8-15, nt+1)
+      const int mat = lane >> 3, rr = lane & 7;
+      const int row = (mat & 1) * 8 + rr;
+      const int t = nt + (mat >> 1);
+      ldmatrix_x4_trans(bfr, smem_u32(st.X[t >> 3]) + sw_off(row, t & 7));
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int t = nt + u;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t bb[2] = {bfr[2 * u], bfr[2 * u + 1]};
+      mma_bf16_16x8x16(d, ahi, bb);
+      mma_bf16_16x8x16(d, alo, bb);
+      uint8_t* xb = st.X[t >> 3];
+      *reinterpret_cast<uint32_t*>(xb + sw_off(gid, t & 7) + 4 * tig) = pack_bf16x2(-d[0], -d[1]);
+      *reinterpret_cast<uint32_t*>(xb + sw_off(gid + 8, t & 7) + 4 * tig) = pack_bf16x2(-d[2], -d[3]);
+    }
+  }
+  // rows of the v tile past the end of the sequence: zero
+  if (partial && v_used) {
+    for (int idx = lane; idx < (kChunk - nv) * 16; idx += 32) {
+      const int r = nv + idx / 16, c16 = idx % 16;
+      *reinterpret_cast<uint4*>(st.V + (c16 >> 3) * 2048 + r * 128 + (c16 & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
 
 __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_constant__ ChainParams p) {
   if ((int)blockIdx.x >= *p.item_count) return;
@@ -118,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   extern __shared__ uint8_t smem_dyn[];
   SmemLayout& S = *reinterpret_cast<SmemLayout*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                  ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t bar_full[kNRaw], bar_raw_empty[kNRaw], bar_op_full[kNOp],
-      bar_op_empty[kNOp], bar_d1_full[2], bar_vn_ready, bar_d2_full, bar_s_ready, bar_drain;
+  __shared__ __align__(8) uint64_t bar_full[kStages], bar_op_full[kStages], bar_op_empty[kStages],
+      bar_d1_full[2], bar_vn_ready, bar_d2_full, bar_s_ready, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -128,11 +386,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   AbortState ab{&s_abort, p.err};
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNRaw; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar_full[i], 1);
-      mbar_init(&bar_raw_empty[i], 1);
-    }
-    for (int i = 0; i < kNOp; ++i) {
       mbar_init(&bar_op_full[i], 1);
       mbar_init(&bar_op_empty[i], 1);
     }
@@ -147,10 +402,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   }
   if (warp >= kWarpProlog0 && warp < kWarpEpi0) {
     // rows 16..31 of the [Tm ; 0] operands stay zero for the whole run
-    const int t = threadIdx.x - kWarpProlog0 * 32;
-    for (int s = 0; s < kNOp; ++s) {
-      reinterpret_cast<uint32_t*>(S.op[s].TPhi + 512)[t] = 0u;
-      reinterpret_cast<uint32_t*>(S.op[s].TPlo + 512)[t] = 0u;
+    const int t = threadIdx.x - kWarpProlog0 * 32;   // 0..63
+    for (int s = 0; s < kStages; ++s) {
+      reinterpret_cast<uint64_t*>(S.st[s].TPhi + 512)[t] = 0ull;
+      reinterpret_cast<uint64_t*>(S.st[s].TPlo + 512)[t] = 0ull;
     }
     fence_proxy_async_smem();
   }
@@ -171,22 +426,22 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         const bool load_v = it.mode != kModeTransition;
         int issued = 0;
         for (int c = 0; c < nchunks; ++c) {
-          const int rs = c % kNRaw, os = c % kNOp;
-          if (c >= kNRaw && !mbar_wait(&bar_raw_empty[rs], ((c / kNRaw) - 1) & 1, ab)) break;
-          if (c >= kNOp && !mbar_wait(&bar_op_empty[os], ((c / kNOp) - 1) & 1, ab)) break;
+          const int s = c % kStages;
+          if (c >= kStages && !mbar_wait(&bar_op_empty[s], ((c / kStages) - 1) & 1, ab)) break;
           const int row = it.row0 + c * kChunk;
-          mbar_arrive_expect_tx(&bar_full[rs], load_v ? 16384u : 12288u);
+          Stage& st = S.st[s];
+          mbar_arrive_expect_tx(&bar_full[s], load_v ? 16384u : 12288u);
           for (int b = 0; b < 2; ++b) {
-            tma_load_3d(S.raw[rs].q + b * 2048, &p.tm_q, &bar_full[rs], b * 64, it.head, row);
-            tma_load_3d(S.raw[rs].k + b * 2048, &p.tm_k, &bar_full[rs], b * 64, it.head, row);
-            tma_load_3d(S.raw[rs].g + b * 2048, &p.tm_g, &bar_full[rs], b * 64, it.head, row);
-            if (load_v) tma_load_3d(S.op[os].v + b * 2048, &p.tm_v, &bar_full[rs], b * 64, it.head, row);
+            tma_load_3d(st.X[b] + 2048, &p.tm_q, &bar_full[s], b * 64, it.head, row);
+            tma_load_3d(st.K + b * 2048, &p.tm_k, &bar_full[s], b * 64, it.head, row);
+            tma_load_3d(st.G + b * 2048, &p.tm_g, &bar_full[s], b * 64, it.head, row);
+            if (load_v) tma_load_3d(st.V + b * 2048, &p.tm_v, &bar_full[s], b * 64, it.head, row);
           }
           ++issued;
         }
         if (s_abort) {  // let loads in flight land before the CTA exits
-          for (int c = (issued > kNRaw ? issued - kNRaw : 0); c < issued; ++c)
-            mbar_wait_drain(&bar_full[c % kNRaw], (c / kNRaw) & 1);
+          for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
+            mbar_wait_drain(&bar_full[c % kStages], (c / kStages) & 1);
         }
       }
       __syncwarp();
@@ -195,52 +450,51 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       if (lane == 0) {
         const uint32_t id_u = idesc_bf16_f32(128, 32, 1, 0);
         const uint32_t id_x = idesc_bf16_f32(128, 32, 0, 0);
-        const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);
+        const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1);   // kfac is an MN-major B
         const uint32_t id_o = idesc_bf16_f32(128, 16, 0, 0);
         const uint32_t vnh = smem_u32(S.vn_hi), vnl = smem_u32(S.vn_lo);
         const bool with_u = it.mode != kModeTransition;
         const bool with_o = it.mode == kModeForward;
         bool issued_any = false;
         for (int c = 0; c < nchunks; ++c) {
-          const int rs = c % kNRaw, os = c % kNOp, b = c & 1;
+          const int s = c % kStages, b = c & 1;
           const uint32_t d1 = tmem + kColD1 + 32u * b;
-          OpStage& op = S.op[os];
-          if (!mbar_wait(&bar_op_full[os], (c / kNOp) & 1, ab)) break;
-          if (!mbar_wait(&bar_full[rs], (c / kNRaw) & 1, ab)) break;
+          Stage& st = S.st[s];
+          if (!mbar_wait(&bar_op_full[s], (c / kStages) & 1, ab)) break;
+          if (!mbar_wait(&bar_full[s], (c / kStages) & 1, ab)) break;
           tc_fence_after();
           if (with_u) {
-            const uint64_t a_v = smem_desc(smem_u32(op.v), 2048, 1024, kSwizzle128B);
-            mma_ss(d1, a_v, smem_desc(smem_u32(op.TPhi), 128, 256, kSwizzleNone), id_u, 0);
-            mma_ss(d1, a_v, smem_desc(smem_u32(op.TPlo), 128, 256, kSwizzleNone), id_u, 1);
+            const uint64_t a_v = smem_desc(smem_u32(st.V), 2048, 1024, kSwizzle128B);
+            mma_ss(d1, a_v, smem_desc(smem_u32(st.TPhi), 128, 256, kSwizzleNone), id_u, 0);
+            mma_ss(d1, a_v, smem_desc(smem_u32(st.TPlo), 128, 256, kSwizzleNone), id_u, 1);
           }
           issued_any = true;
           if (!mbar_wait(&bar_s_ready, c & 1, ab)) break;
           tc_fence_after();
-          const uint32_t xb = smem_u32(op.X);
 #pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            const uint64_t bd = smem_desc(xb + (s >> 2) * 4096 + (s & 3) * 32, 16, 1024, kSwizzle128B);
-            mma_ts(d1, tmem + kColSbf + 8u * s, bd, id_x, (with_u || s > 0) ? 1u : 0u);
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t bd = smem_desc(smem_u32(st.X[k >> 2]) + (k & 3) * 32, 16, 1024, kSwizzle128B);
+            mma_ts(d1, tmem + kColSbf + 8u * k, bd, id_x, (with_u || k > 0) ? 1u : 0u);
           }
           tc_commit(&bar_d1_full[b]);
           if (!mbar_wait(&bar_vn_ready, c & 1, ab)) break;
           tc_fence_after();
           const uint64_t a_hi = smem_desc(vnh, 128, 256, kSwizzleNone);
           const uint64_t a_lo = smem_desc(vnl, 128, 256, kSwizzleNone);
-          const uint64_t kf_hi = smem_desc(smem_u32(op.KFhi), 128, 256, kSwizzleNone);
-          const uint64_t kf_lo = smem_desc(smem_u32(op.KFlo), 128, 256, kSwizzleNone);
+          const uint64_t kf_hi = smem_desc(smem_u32(st.K), 2048, 1024, kSwizzle128B);
+          const uint64_t kf_lo = smem_desc(smem_u32(st.G), 2048, 1024, kSwizzle128B);
           mma_ss(tmem + kColState, a_hi, kf_hi, id_s, 1);
           mma_ss(tmem + kColState, a_hi, kf_lo, id_s, 1);
           mma_ss(tmem + kColState, a_lo, kf_hi, id_s, 1);
           if (with_o) {
-            const uint64_t aq_hi = smem_desc(smem_u32(op.AQhi), 128, 256, kSwizzleNone);
-            const uint64_t aq_lo = smem_desc(smem_u32(op.AQlo), 128, 256, kSwizzleNone);
+            const uint64_t aq_hi = smem_desc(smem_u32(st.AQhi), 128, 256, kSwizzleNone);
+            const uint64_t aq_lo = smem_desc(smem_u32(st.AQlo), 128, 256, kSwizzleNone);
             mma_ss(d1 + 16, a_hi, aq_hi, id_o, 1);
             mma_ss(d1 + 16, a_lo, aq_hi, id_o, 1);
             mma_ss(d1 + 16, a_hi, aq_lo, id_o, 1);
           }
           tc_commit(&bar_d2_full);
-          tc_commit(&bar_op_empty[os]);
+          tc_commit(&bar_op_empty[s]);
         }
         if (s_abort && issued_any) {  // wait for MMAs in flight before TMEM is released
           tc_commit(&bar_drain);
@@ -250,295 +504,31 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       __syncwarp();
     } else if (warp < kWarpEpi0) {
       // ------------------------------------------------------------ prologue
-      const int pw = warp - kWarpProlog0;        // channels [32 pw, 32 pw + 32)
-      const int ptid = threadIdx.x - kWarpProlog0 * 32;
-      const int gid = lane >> 2, tig = lane & 3;
-      PrologScratch& ps = S.ps;
+      const int pw = warp - kWarpProlog0;
       const int h = it.head;
       const int H = p.H;
-      // per-thread channel constants: ch(pp, e) = 32 pw + 8 pp + 2 tig + e
-      const float rate = expf(p.A_log[h]);
-      const float nr = -rate * kLog2e;
-      float nrdb[4][2];
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) nrdb[pp][e] = nr * p.dt_bias[h * kDimK + 32 * pw + 8 * pp + 2 * tig + e];
+      const float nr = -expf(p.A_log[h]) * kLog2e;
       const float lbl2 = p.lower_bound * kLog2e;
-      // beta logits for rows gid, gid + 8 of the current chunk (prefetched one chunk ahead)
+      const float* dtb = p.dt_bias + (size_t)h * kDimK;
+      const int gid = lane >> 2;
       auto load_beta = [&](int c, float& b0, float& b1) {
         const int base = it.row0 + c * kChunk;
         const int nv = min(kChunk, it.len - c * kChunk);
-        b0 = (c < nchunks && gid < nv) ? bf16_bits_to_f32(p.beta[(size_t)(base + gid) * H + h]) : 0.f;
-        b1 = (c < nchunks && gid + 8 < nv) ? bf16_bits_to_f32(p.beta[(size_t)(base + gid + 8) * H + h]) : 0.f;
+        b0 = (c < nchunks && 2 * gid < nv) ? bf16_bits_to_f32(p.beta[(size_t)(base + 2 * gid) * H + h]) : 0.f;
+        b1 = (c < nchunks && 2 * gid + 1 < nv) ? bf16_bits_to_f32(p.beta[(size_t)(base + 2 * gid + 1) * H + h])
+                                               : 0.f;
       };
       float bl0, bl1;
-      load_beta(0, bl0, bl1);
-      for (int c = 0; c < nchunks; ++c) {
-        const int rs = c % kNRaw, os = c % kNOp;
+      load_beta(pw, bl0, bl1);
+      for (int c = pw; c < nchunks; c += kProlog) {
+        const int s = c % kStages;
         const int nv = min(kChunk, it.len - c * kChunk);
-        OpStage& op = S.op[os];
-        const float cur_b0 = bl0, cur_b1 = bl1;
-        load_beta(c + 1, bl0, bl1);
-        bool ok = mbar_wait(&bar_full[rs], (c / kNRaw) & 1, ab);
-        if (c >= kNOp) ok = mbar_wait(&bar_op_empty[os], ((c / kNOp) - 1) & 1, ab) && ok;
-        ok = __all_sync(0xffffffffu, ok);
-        // ---- load q, k, g for rows gid and gid + 8 (pairs of channels)
-        float q[2][4][2], k[2][4][2], g[2][4][2];
-        if (ok) {
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int r = gid + 8 * hr;
-            const bool valid = r < nv;
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-              const uint32_t off = tile_off(r, 32 * pw + 8 * pp + 2 * tig);
-              const uint32_t wq = *reinterpret_cast<const uint32_t*>(S.raw[rs].q + off);
-              const uint32_t wk = *reinterpret_cast<const uint32_t*>(S.raw[rs].k + off);
-              const uint32_t wg = *reinterpret_cast<const uint32_t*>(S.raw[rs].g + off);
-              q[hr][pp][0] = valid ? bf16lo_to_f32(wq) : 0.f;
-              q[hr][pp][1] = valid ? bf16hi_to_f32(wq) : 0.f;
-              k[hr][pp][0] = valid ? bf16lo_to_f32(wk) : 0.f;
-              k[hr][pp][1] = valid ? bf16hi_to_f32(wk) : 0.f;
-              g[hr][pp][0] = bf16lo_to_f32(wg);
-              g[hr][pp][1] = bf16hi_to_f32(wg);
-            }
-          }
-          // partial squared norms over this thread's 8 channels, then over tig
-          float sq[2], sk[2];
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            sq[hr] = 0.f;
-            sk[hr] = 0.f;
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                sq[hr] = fmaf(q[hr][pp][e], q[hr][pp][e], sq[hr]);
-                sk[hr] = fmaf(k[hr][pp][e], k[hr][pp][e], sk[hr]);
-              }
-#pragma unroll
-            for (int m = 1; m <= 2; m <<= 1) {
-              sq[hr] += __shfl_xor_sync(0xffffffffu, sq[hr], m);
-              sk[hr] += __shfl_xor_sync(0xffffffffu, sk[hr], m);
-            }
-          }
-          if (tig == 0) {
-            ps.normp[pw][gid][0] = sq[0];
-            ps.normp[pw][gid][1] = sk[0];
-            ps.normp[pw][gid + 8][0] = sq[1];
-            ps.normp[pw][gid + 8][1] = sk[1];
-          }
-        }
-        named_bar(kBarProlog, 128);
-        if (ptid == 0 && ok) mbar_arrive(&bar_raw_empty[rs]);   // q, k, g are in registers now
-        float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
-        float gc_l2[4][2];
-        if (ok) {
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int r = gid + 8 * hr;
-            float tq = 0.f, tk = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              tq += ps.normp[w][r][0];
-              tk += ps.normp[w][r][1];
-            }
-            rq[hr] = rsqrt_approx(tq + 1e-6f);
-            rk[hr] = rsqrt_approx(tk + 1e-6f);
-          }
-          // ---- gate: base-2 log-decay per element, then the within-chunk cumsum over rows
-#pragma unroll
-          for (int pp = 0; pp < 4; ++pp)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float a = 0.f, bq = 0.f;
-              {
-                const float t0 = ex2_approx(fmaf(nr, g[0][pp][e], nrdb[pp][e]));
-                const float t1 = ex2_approx(fmaf(nr, g[1][pp][e], nrdb[pp][e]));
-                a = (gid < nv) ? lbl2 * rcp_approx(1.f + t0) : 0.f;
-                bq = (gid + 8 < nv) ? lbl2 * rcp_approx(1.f + t1) : 0.f;
-              }
-#pragma unroll
-              for (int d = 1; d <= 4; d <<= 1) {
-                const float ya = __shfl_up_sync(0xffffffffu, a, 4 * d);
-                const float yb = __shfl_up_sync(0xffffffffu, bq, 4 * d);
-                if (gid >= d) {
-                  a += ya;
-                  bq += yb;
-                }
-              }
-              bq += __shfl_sync(0xffffffffu, a, 28 + tig);
-              gc_l2[pp][e] = __shfl_sync(0xffffffffu, bq, 28 + tig);
-              g[0][pp][e] = a;    // g now holds G (base 2) for rows gid, gid + 8
-              g[1][pp][e] = bq;
-            }
-        }
-        // ---- decay-scaled operands, Gram partials (tf32 warp MMA), operand tiles
-        float kgv[2][4][2], kiv[2][4][2];
-        if (ok) {
-          float ck0[4] = {0, 0, 0, 0}, ck1[4] = {0, 0, 0, 0}, cq0[4] = {0, 0, 0, 0}, cq1[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int pp = 0; pp < 4; ++pp) {
-            float qg[2][2];
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float G = g[hr][pp][e];
-                const float gam = ex2_approx(G);
-                const float ginv = ex2_approx(-G);
-                const float kh = k[hr][pp][e] * rk[hr];
-                kgv[hr][pp][e] = kh * gam;
-                kiv[hr][pp][e] = kh * ginv;
-                qg[hr][e] = q[hr][pp][e] * rq[hr] * gam;
-              }
-            const uint32_t ak[4] = {f32_to_tf32(kgv[0][pp][0]), f32_to_tf32(kgv[1][pp][0]),
-                                    f32_to_tf32(kgv[0][pp][1]), f32_to_tf32(kgv[1][pp][1])};
-            const uint32_t aq[4] = {f32_to_tf32(qg[0][0]), f32_to_tf32(qg[1][0]), f32_to_tf32(qg[0][1]),
-                                    f32_to_tf32(qg[1][1])};
-            const uint32_t b0[2] = {f32_to_tf32(kiv[0][pp][0]), f32_to_tf32(kiv[0][pp][1])};
-            const uint32_t b1[2] = {f32_to_tf32(kiv[1][pp][0]), f32_to_tf32(kiv[1][pp][1])};
-            mma_tf32_16x8x8(ck0, ak, b0);
-            mma_tf32_16x8x8(ck1, ak, b1);
-            mma_tf32_16x8x8(cq0, aq, b0);
-            mma_tf32_16x8x8(cq1, aq, b1);
-            // qh*2^G -> rows 16..31 of X; kh*2^G (bf16) -> scratch for W
-            const int ch = 32 * pw + 8 * pp + 2 * tig;
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-              const int r = gid + 8 * hr;
-              *reinterpret_cast<uint32_t*>(op.X + xop_off(16 + r, ch)) = pack_bf16x2(qg[hr][0], qg[hr][1]);
-              *reinterpret_cast<uint32_t*>(&ps.kg[r][ch]) = pack_bf16x2(kgv[hr][pp][0], kgv[hr][pp][1]);
-            }
-            // kfac = kh * 2^(G_C - G) as split bf16, transposed K-major [ch][tok]
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float gcl = ex2_approx(gc_l2[pp][e]);
-              if (gid == 0) op.gamC[ch + e] = gcl;
-#pragma unroll
-              for (int hr = 0; hr < 2; ++hr) {
-                uint16_t hi, lo;
-                split_bf16(kiv[hr][pp][e] * gcl, hi, lo);
-                const uint32_t o = ns_off(ch + e, gid + 8 * hr);
-                *reinterpret_cast<uint16_t*>(op.KFhi + o) = hi;
-                *reinterpret_cast<uint16_t*>(op.KFlo + o) = lo;
-              }
-            }
-          }
-          // partial Grams -> scratch
-          {
-            float* gk = &ps.gram[pw][0][0][0];
-            float* gq = &ps.gram[pw][1][0][0];
-            const int c0 = 2 * tig;
-            *reinterpret_cast<float2*>(gk + gid * 16 + c0) = make_float2(ck0[0], ck0[1]);
-            *reinterpret_cast<float2*>(gk + (gid + 8) * 16 + c0) = make_float2(ck0[2], ck0[3]);
-            *reinterpret_cast<float2*>(gk + gid * 16 + 8 + c0) = make_float2(ck1[0], ck1[1]);
-            *reinterpret_cast<float2*>(gk + (gid + 8) * 16 + 8 + c0) = make_float2(ck1[2], ck1[3]);
-            *reinterpret_cast<float2*>(gq + gid * 16 + c0) = make_float2(cq0[0], cq0[1]);
-            *reinterpret_cast<float2*>(gq + (gid + 8) * 16 + c0) = make_float2(cq0[2], cq0[3]);
-            *reinterpret_cast<float2*>(gq + gid * 16 + 8 + c0) = make_float2(cq1[0], cq1[1]);
-            *reinterpret_cast<float2*>(gq + (gid + 8) * 16 + 8 + c0) = make_float2(cq1[2], cq1[3]);
-          }
-          if (pw == 0 && tig == 0) {
-            ps.beta[gid] = (gid < nv) ? rcp_approx(1.f + ex2_approx(-cur_b0 * kLog2e)) : 0.f;
-            ps.beta[gid + 8] = (gid + 8 < nv) ? rcp_approx(1.f + ex2_approx(-cur_b1 * kLog2e)) : 0.f;
-          }
-        }
-        named_bar(kBarProlog, 128);
-        // ---- warp 0 of the prologue: reduce Grams, invert, write Tm and Aqk
-        if (ok && pw == 0) {
-          // reduce the four partials in place into gram[0]
-#pragma unroll 4
-          for (int i = 0; i < 16; ++i) {
-            const int e = lane + 32 * i;   // 0..511 over [2][16][16]
-            float* base = &ps.gram[0][0][0][0];
-            const float s = base[e] + base[512 + e] + base[1024 + e] + base[1536 + e];
-            base[e] = s;
-          }
-          __syncwarp();
-          const float* Gk = &ps.gram[0][0][0][0];
-          const float* Gq = &ps.gram[0][1][0][0];
-          if (lane < 16) {
-            // column j = lane of X = (I + Akk)^-1, Akk[i][m] = beta_i Gk[i][m] (m < i)
-            const int j = lane;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < 15; ++m) {
-#pragma unroll
-              for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-ps.beta[i] * Gk[i * 16 + m], x[m], x[i]);
-            }
-            const float bj = ps.beta[j];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              uint16_t hi, lo;
-              split_bf16(x[i] * bj, hi, lo);
-              const uint32_t o = ns_off(i, j);
-              *reinterpret_cast<uint16_t*>(op.TPhi + o) = hi;
-              *reinterpret_cast<uint16_t*>(op.TPlo + o) = lo;
-            }
-          } else {
-            // Aqk row i = lane - 16, inclusive lower triangle
-            const int i = lane - 16;
-            uint32_t hw[8], lw[8];
-#pragma unroll
-            for (int jj = 0; jj < 16; jj += 2) {
-              uint16_t h0, l0, h1, l1;
-              split_bf16(jj <= i ? Gq[i * 16 + jj] : 0.f, h0, l0);
-              split_bf16(jj + 1 <= i ? Gq[i * 16 + jj + 1] : 0.f, h1, l1);
-              hw[jj / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-              lw[jj / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-            }
-            *reinterpret_cast<uint4*>(op.AQhi + ns_off(i, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(op.AQhi + ns_off(i, 8)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-            *reinterpret_cast<uint4*>(op.AQlo + ns_off(i, 0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            *reinterpret_cast<uint4*>(op.AQlo + ns_off(i, 8)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-          }
-        }
-        named_bar(kBarProlog, 128);
-        // ---- W = Tm (kh*2^G) for this warp's 32 channels (bf16 warp MMA, Tm split hi + lo)
-        if (ok) {
-          uint32_t ahi[4], alo[4];
-          {
-            const int mat = lane >> 3, rr = lane & 7;
-            const uint32_t moff = (uint32_t)((mat & 1) * 256 + (mat >> 1) * 128 + rr * 16);
-            ldmatrix_x4(ahi, smem_u32(op.TPhi) + moff);
-            ldmatrix_x4(alo, smem_u32(op.TPlo) + moff);
-          }
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t bfr[4];
-            {
-              const int mat = lane >> 3, rr = lane & 7;
-              const int krow = (mat & 1) * 8 + rr;
-              const int ncol = 32 * pw + 16 * half + 8 * (mat >> 1);
-              ldmatrix_x4_trans(bfr, smem_u32(&ps.kg[krow][ncol]));
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              float d[4] = {0.f, 0.f, 0.f, 0.f};
-              const uint32_t bb[2] = {bfr[2 * nt], bfr[2 * nt + 1]};
-              mma_bf16_16x8x16(d, ahi, bb);
-              mma_bf16_16x8x16(d, alo, bb);
-              const int ch = 32 * pw + 16 * half + 8 * nt + 2 * tig;
-              *reinterpret_cast<uint32_t*>(op.X + xop_off(gid, ch)) = pack_bf16x2(-d[0], -d[1]);
-              *reinterpret_cast<uint32_t*>(op.X + xop_off(gid + 8, ch)) = pack_bf16x2(-d[2], -d[3]);
-            }
-          }
-          // zero the rows of the v tile that lie past the end of the sequence
-          if (nv < kChunk && it.mode != kModeTransition) {
-            for (int idx = ptid; idx < (kChunk - nv) * 16; idx += 128) {
-              const int r = nv + idx / 16, cchunk = idx % 16;
-              *reinterpret_cast<uint4*>(op.v + (cchunk >> 3) * 2048 + r * 128 + (cchunk & 7) * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-          fence_proxy_async_smem();
-        }
-        named_bar(kBarProlog, 128);
-        if (ptid == 0 && ok) mbar_arrive(&bar_op_full[os]);
+        const float cb0 = bl0, cb1 = bl1;
+        load_beta(c + kProlog, bl0, bl1);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_full[s], (c / kStages) & 1, ab));
+        if (!ok) break;
+        prologue_chunk(S.st[s], S.ps[pw], nv, nr, lbl2, dtb, cb0, cb1, lane, it.mode != kModeTransition);
+        if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
     } else {
       // ------------------------------------------------------------ epilogue
@@ -553,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_op_full[0], 0, ab));
       // ---- initial state row v of S^T -> bf16 copy + decayed fp32 accumulator
       if (ok) {
-        const OpStage& op0 = S.op[0];
+        const Stage& st0 = S.st[0];
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
           float s[32];
@@ -605,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
           tmem_st16(tSb + 16u * j, pk);
           uint32_t sv[32];
 #pragma unroll
-          for (int t = 0; t < 32; ++t) sv[t] = __float_as_uint(s[t] * op0.gamC[32 * j + t]);
+          for (int t = 0; t < 32; ++t) sv[t] = __float_as_uint(s[t] * st0.gamC[32 * j + t]);
           tmem_st32(tS + 32u * j, sv);
         }
         tmem_st_wait();
@@ -626,13 +616,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
           tmem_ld_wait();
           uint32_t hw[8], lw[8];
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            uint16_t h0, l0, h1, l1;
-            split_bf16(__uint_as_float(r[2 * t]), h0, l0);
-            split_bf16(__uint_as_float(r[2 * t + 1]), h1, l1);
-            hw[t] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-            lw[t] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-          }
+          for (int t = 0; t < 8; ++t)
+            split_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]), hw[t], lw[t]);
           *reinterpret_cast<uint4*>(S.vn_hi + ns_off(vrow, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(S.vn_hi + ns_off(vrow, 8)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           *reinterpret_cast<uint4*>(S.vn_lo + ns_off(vrow, 0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -661,10 +646,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         }
         const bool last = (c == nchunks - 1);
         if (!last) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_op_full[(c + 1) % kNOp], ((c + 1) / kNOp) & 1, ab));
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bar_op_full[(c + 1) % kStages], ((c + 1) / kStages) & 1, ab));
           if (!ok) break;
         }
-        const OpStage& opn = S.op[(c + 1) % kNOp];
+        const Stage& stn = S.st[(c + 1) % kStages];
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
           uint32_t r[32];
@@ -676,7 +662,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
             for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
             tmem_st16(tSb + 16u * j, pk);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * opn.gamC[32 * j + t]);
+            for (int t = 0; t < 8; ++t) {
+              const float4 gm = *reinterpret_cast<const float4*>(&stn.gamC[32 * j + 4 * t]);
+              mul2(r[4 * t], r[4 * t + 1], gm.x, gm.y);
+              mul2(r[4 * t + 2], r[4 * t + 3], gm.z, gm.w);
+            }
             tmem_st32(tS + 32u * j, r);
           } else if (it.out_slot >= 0) {
             float4* dst = reinterpret_cast<float4*>(p.ws_states + (size_t)it.out_slot * 16384 +
