@@ -37,13 +37,13 @@
 
 namespace kda {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;
 constexpr int kStages = 4;
 constexpr int kWarpProducer = 0;
-constexpr int kWarpMma = 1;
-constexpr int kWarpProlog0 = 2;
-constexpr int kProlog = 2;            // prologue warps
-constexpr int kWarpEpi0 = 4;
+constexpr int kWarpProlog0 = 1;
+constexpr int kProlog = 4;            // prologue warps: two pairs, one pair per chunk
+constexpr int kWarpEpi0 = 5;          // epilogue warps 5-8; lane 0 of warp 5 issues the MMAs
+constexpr uint32_t kBarEpi = 3;       // named barrier of the epilogue warps
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColState = 0;
 constexpr uint32_t kColSbf = 128;
@@ -67,15 +67,18 @@ struct Stage {
   uint8_t pad[512];
 };
 static_assert(sizeof(Stage) == 24576, "stage size (multiple of 1024 for the swizzled regions)");
-struct PrologScratch {    // Gram matrices of one prologue warp (fp32, rows = tokens)
-  float Gk[16][16];
-  float Gq[16][16];
+struct PairScratch {      // exchange area of one prologue pair (fp32, token indices)
+  float normx[2][16][2];  // per-warp partial |q|^2, |k|^2
+  float GkX[16][16];      // warp 1's partial Gk, then -beta_i Gk[i][m] stored at [m][i]
+  float Gq0[16][16];      // warp 0's partial Gq
+  int okf[2][2];          // both warps' wait results, by iteration parity
+  int pad[60];
 };
 struct SmemLayout {
   Stage st[kStages];
   uint8_t vn_hi[4096];    // Vn^T [128 v][16 tok] K-major, no swizzle
   uint8_t vn_lo[4096];
-  PrologScratch ps[kProlog];
+  PairScratch ps[2];
 };
 
 size_t chain_smem_bytes() { return sizeof(SmemLayout) + 1024; }
@@ -106,6 +109,31 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
   hi = pack_bf16x2(a, b);
   lo = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
 }
+// packed fp32x2 arithmetic on pairs of floats
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ void fmul2(float& a0, float& a1, float b0, float b1) {
+  uint64_t c;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(f2pack(a0, a1)), "l"(f2pack(b0, b1)));
+  f2unpack(c, a0, a1);
+}
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2pack(a0, a1)), "l"(f2pack(b0, b1)), "l"(f2pack(c0, c1)));
+  f2unpack(r, d0, d1);
+}
+__device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) {
+  uint64_t c;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(f2pack(a0, a1)), "l"(f2pack(b0, b1)));
+  f2unpack(c, a0, a1);
+}
 // (a0, a1) * (b0, b1) with one packed fp32x2 multiply
 __device__ __forceinline__ void mul2(uint32_t& x0, uint32_t& x1, float b0, float b1) {
   uint64_t a, b, c;
@@ -115,55 +143,77 @@ __device__ __forceinline__ void mul2(uint32_t& x0, uint32_t& x1, float b0, float
   asm("mov.b64 {%0, %1}, %2;" : "=r"(x0), "=r"(x1) : "l"(c));
 }
 
-// Prepare the tcgen05 operands of one chunk (one warp, 16 tokens x 128 channels).
+// Named barrier of one prologue pair (64 threads; ids 1 and 2).
+__device__ __forceinline__ void pair_bar(int pair) { named_bar(1 + pair, 64); }
+
+// Prepare the tcgen05 operands of one chunk with a pair of warps; warp w of the
+// pair handles channels [64 w, 64 w + 64) (passes p = 2 w, 2 w + 1 of 32 channels).
 // Lane (gid, tig) holds tokens ra = 2 gid and rb = 2 gid + 1 and, in pass p,
-// channels 32 p + 8 tig + j (j < 8).  For the Gram warp MMAs the physical
-// tokens 2 gid / 2 gid + 1 play the fragment rows gid / gid + 8, and the
-// channel pair (8 tig + 2 s, + 1) the k positions (tig, tig + 4) of k-step s.
-__device__ __forceinline__ void prologue_chunk(Stage& st, PrologScratch& sc, int nv, const float nr, const float lbl2,
-                                               const float* __restrict__ dtb, float beta_a, float beta_b,
-                                               int lane, bool v_used) {
+// channels 32 p + 8 tig + j (j < 8).  For the Gram warp MMAs the physical tokens
+// 2 gid / 2 gid + 1 play the fragment rows gid / gid + 8, and the channel pair
+// (8 tig + 2 s, + 1) the k positions (tig, tig + 4) of k-step s; the partial
+// Grams of the two warps are summed through shared memory.
+__device__ __forceinline__ void prologue_pair_chunk(Stage& st, PairScratch& sc, int pair, int w, int nv,
+                                                    const float nr, const float lbl2,
+                                                    const float* __restrict__ dtb, float beta_a, float beta_b,
+                                                    int lane, bool v_used) {
   const int gid = lane >> 2, tig = lane & 3;
   const int ra = 2 * gid, rb = 2 * gid + 1;
   const bool va = ra < nv, vb = rb < nv;
   const bool partial = nv < kChunk;
 
-  // ---- L2 norms of q and k over all 128 channels
-  float sq[2] = {0.f, 0.f}, sk[2] = {0.f, 0.f};
+  // ---- L2 norms of q and k: partial sums over this warp's 64 channels
+  {
+    float sq[2] = {0.f, 0.f}, sk[2] = {0.f, 0.f};
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const int j16 = 4 * (p & 1) + tig;
-    const uint8_t* qb = st.X[p >> 1] + 2048;
-    const uint8_t* kb = st.K + 2048 * (p >> 1);
+    for (int pp = 0; pp < 2; ++pp) {
+      const int p = 2 * w + pp;
+      const int j16 = 4 * (p & 1) + tig;
+      const uint8_t* qb = st.X[p >> 1] + 2048;
+      const uint8_t* kb = st.K + 2048 * (p >> 1);
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int r = ra + hr;
-      const uint4 wq = *reinterpret_cast<const uint4*>(qb + sw_off(r, j16));
-      const uint4 wk = *reinterpret_cast<const uint4*>(kb + sw_off(r, j16));
-      const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
+      for (int hr = 0; hr < 2; ++hr) {
+        const int r = ra + hr;
+        const uint4 wq = *reinterpret_cast<const uint4*>(qb + sw_off(r, j16));
+        const uint4 wk = *reinterpret_cast<const uint4*>(kb + sw_off(r, j16));
+        const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float q0 = bf16lo_to_f32(aq[u]), q1 = bf16hi_to_f32(aq[u]);
-        const float k0 = bf16lo_to_f32(ak[u]), k1 = bf16hi_to_f32(ak[u]);
-        sq[hr] = fmaf(q0, q0, fmaf(q1, q1, sq[hr]));
-        sk[hr] = fmaf(k0, k0, fmaf(k1, k1, sk[hr]));
+        for (int u = 0; u < 4; ++u) {
+          const float q0 = bf16lo_to_f32(aq[u]), q1 = bf16hi_to_f32(aq[u]);
+          const float k0 = bf16lo_to_f32(ak[u]), k1 = bf16hi_to_f32(ak[u]);
+          sq[hr] = fmaf(q0, q0, fmaf(q1, q1, sq[hr]));
+          sk[hr] = fmaf(k0, k0, fmaf(k1, k1, sk[hr]));
+        }
       }
     }
-  }
 #pragma unroll
-  for (int m = 1; m <= 2; m <<= 1) {
+    for (int m = 1; m <= 2; m <<= 1) {
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      sq[hr] += __shfl_xor_sync(0xffffffffu, sq[hr], m);
-      sk[hr] += __shfl_xor_sync(0xffffffffu, sk[hr], m);
+      for (int hr = 0; hr < 2; ++hr) {
+        sq[hr] += __shfl_xor_sync(0xffffffffu, sq[hr], m);
+        sk[hr] += __shfl_xor_sync(0xffffffffu, sk[hr], m);
+      }
+    }
+    if (tig == 0) {
+      *reinterpret_cast<float2*>(&sc.normx[w][ra][0]) = make_float2(sq[0], sk[0]);
+      *reinterpret_cast<float2*>(&sc.normx[w][rb][0]) = make_float2(sq[1], sk[1]);
     }
   }
-  const float rq[2] = {va ? rsqrt_approx(sq[0] + 1e-6f) : 0.f, vb ? rsqrt_approx(sq[1] + 1e-6f) : 0.f};
-  const float rk[2] = {va ? rsqrt_approx(sk[0] + 1e-6f) : 0.f, vb ? rsqrt_approx(sk[1] + 1e-6f) : 0.f};
+  pair_bar(pair);
+  float rq[2], rk[2];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const float2 a = *reinterpret_cast<const float2*>(&sc.normx[0][ra + hr][0]);
+    const float2 b = *reinterpret_cast<const float2*>(&sc.normx[1][ra + hr][0]);
+    const bool valid = hr == 0 ? va : vb;
+    rq[hr] = valid ? rsqrt_approx(a.x + b.x + 1e-6f) : 0.f;
+    rk[hr] = valid ? rsqrt_approx(a.y + b.y + 1e-6f) : 0.f;
+  }
 
   float ck0[4] = {0, 0, 0, 0}, ck1[4] = {0, 0, 0, 0}, cq0[4] = {0, 0, 0, 0}, cq1[4] = {0, 0, 0, 0};
 #pragma unroll 1
-  for (int p = 0; p < 4; ++p) {
+  for (int pp = 0; pp < 2; ++pp) {
+    const int p = 2 * w + pp;
     const int j16 = 4 * (p & 1) + tig;
     const int ch0 = 32 * p + 8 * tig;
     uint8_t* qb = st.X[p >> 1] + 2048;
@@ -198,51 +248,66 @@ __device__ __forceinline__ void prologue_chunk(Stage& st, PrologScratch& sc, int
         k[hr][2 * u] = bf16lo_to_f32(ak[u]);
         k[hr][2 * u + 1] = bf16hi_to_f32(ak[u]);
         // gate: base-2 log-decay lb * log2(e) * sigmoid(exp(A_log) (g + dt_bias)); 0 past the end
-        const float t0 = ex2_approx(fmaf(nr, bf16lo_to_f32(ag[u]), nrdb[2 * u]));
-        const float t1 = ex2_approx(fmaf(nr, bf16hi_to_f32(ag[u]), nrdb[2 * u + 1]));
-        G[hr][2 * u] = valid ? lbl2 * rcp_approx(1.f + t0) : 0.f;
-        G[hr][2 * u + 1] = valid ? lbl2 * rcp_approx(1.f + t1) : 0.f;
+        float x0, x1;
+        ffma2(x0, x1, nr, nr, bf16lo_to_f32(ag[u]), bf16hi_to_f32(ag[u]), nrdb[2 * u], nrdb[2 * u + 1]);
+        float t0 = ex2_approx(x0), t1 = ex2_approx(x1);
+        fadd2(t0, t1, 1.f, 1.f);
+        float r0 = rcp_approx(t0), r1 = rcp_approx(t1);
+        const float lv = valid ? lbl2 : 0.f;
+        fmul2(r0, r1, lv, lv);
+        G[hr][2 * u] = (partial && !valid) ? 0.f : r0;
+        G[hr][2 * u + 1] = (partial && !valid) ? 0.f : r1;
       }
     }
     // ---- within-chunk inclusive cumsum over tokens (pairs in a lane, scan over gid)
     float gC[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float pair = G[0][j] + G[1][j];
-      float incl = pair;
+      const float pr = G[0][j] + G[1][j];
+      float incl = pr;
 #pragma unroll
       for (int d = 1; d <= 4; d <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, incl, 4 * d);
         if (gid >= d) incl += y;
       }
-      const float excl = incl - pair;
+      const float excl = incl - pr;
       G[0][j] = excl + G[0][j];
       G[1][j] = incl;
       gC[j] = __shfl_sync(0xffffffffu, incl, 28 + tig);
     }
+    float eC[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) eC[j] = ex2_approx(gC[j]);
     // ---- decay-scaled operands
     float kg[2][8], ki[2][8], qg[2][8];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float gam = ex2_approx(G[hr][j]);
-        const float gin = ex2_approx(-G[hr][j]);
-        const float kh = k[hr][j] * rk[hr];
-        kg[hr][j] = kh * gam;
-        ki[hr][j] = kh * gin;
-        qg[hr][j] = q[hr][j] * rq[hr] * gam;
+      for (int j = 0; j < 8; j += 2) {
+        const float gam0 = ex2_approx(G[hr][j]), gam1 = ex2_approx(G[hr][j + 1]);
+        const float gin0 = ex2_approx(-G[hr][j]), gin1 = ex2_approx(-G[hr][j + 1]);
+        float kh0 = k[hr][j], kh1 = k[hr][j + 1];
+        fmul2(kh0, kh1, rk[hr], rk[hr]);
+        float qh0 = q[hr][j], qh1 = q[hr][j + 1];
+        fmul2(qh0, qh1, rq[hr], rq[hr]);
+        kg[hr][j] = kh0; kg[hr][j + 1] = kh1;
+        fmul2(kg[hr][j], kg[hr][j + 1], gam0, gam1);
+        ki[hr][j] = kh0; ki[hr][j + 1] = kh1;
+        fmul2(ki[hr][j], ki[hr][j + 1], gin0, gin1);
+        qg[hr][j] = qh0; qg[hr][j + 1] = qh1;
+        fmul2(qg[hr][j], qg[hr][j + 1], gam0, gam1);
       }
     // ---- Gram partials over this pass's 32 channels (tf32 warp MMA)
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int j = 2 * s;
-      const uint32_t ak[4] = {f32_to_tf32(kg[0][j]), f32_to_tf32(kg[1][j]), f32_to_tf32(kg[0][j + 1]),
-                              f32_to_tf32(kg[1][j + 1])};
-      const uint32_t aq[4] = {f32_to_tf32(qg[0][j]), f32_to_tf32(qg[1][j]), f32_to_tf32(qg[0][j + 1]),
-                              f32_to_tf32(qg[1][j + 1])};
-      const uint32_t b0[2] = {f32_to_tf32(ki[0][j]), f32_to_tf32(ki[0][j + 1])};
-      const uint32_t b1[2] = {f32_to_tf32(ki[1][j]), f32_to_tf32(ki[1][j + 1])};
+    for (int s2 = 0; s2 < 4; ++s2) {
+      const int j = 2 * s2;
+      // fp32 bit patterns; the tf32 MMA uses their top 19 bits
+      const uint32_t ak[4] = {__float_as_uint(kg[0][j]), __float_as_uint(kg[1][j]), __float_as_uint(kg[0][j + 1]),
+                              __float_as_uint(kg[1][j + 1])};
+      const uint32_t aq[4] = {__float_as_uint(qg[0][j]), __float_as_uint(qg[1][j]), __float_as_uint(qg[0][j + 1]),
+                              __float_as_uint(qg[1][j + 1])};
+      const uint32_t b0[2] = {__float_as_uint(ki[0][j]), __float_as_uint(ki[0][j + 1])};
+      const uint32_t b1[2] = {__float_as_uint(ki[1][j]), __float_as_uint(ki[1][j + 1])};
       mma_tf32_16x8x8(ck0, ak, b0);
       mma_tf32_16x8x8(ck1, ak, b1);
       mma_tf32_16x8x8(cq0, aq, b0);
@@ -261,72 +326,108 @@ __device__ __forceinline__ void prologue_chunk(Stage& st, PrologScratch& sc, int
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const float gc0 = ex2_approx(gC[2 * u]), gc1 = ex2_approx(gC[2 * u + 1]);
-        split_bf16x2(ki[hr][2 * u] * gc0, ki[hr][2 * u + 1] * gc1, hw[u], lw[u]);
+        float f0 = ki[hr][2 * u], f1 = ki[hr][2 * u + 1];
+        fmul2(f0, f1, eC[2 * u], eC[2 * u + 1]);
+        split_bf16x2(f0, f1, hw[u], lw[u]);
       }
       *reinterpret_cast<uint4*>(kb + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *reinterpret_cast<uint4*>(gb + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     if (gid == 0) {
-      float e[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) e[j] = ex2_approx(gC[j]);
-      *reinterpret_cast<float4*>(&st.gamC[ch0]) = make_float4(e[0], e[1], e[2], e[3]);
-      *reinterpret_cast<float4*>(&st.gamC[ch0 + 4]) = make_float4(e[4], e[5], e[6], e[7]);
+      *reinterpret_cast<float4*>(&st.gamC[ch0]) = make_float4(eC[0], eC[1], eC[2], eC[3]);
+      *reinterpret_cast<float4*>(&st.gamC[ch0 + 4]) = make_float4(eC[4], eC[5], eC[6], eC[7]);
     }
   }
-  // ---- Grams -> shared memory in token order (fragment row gid = token 2 gid,
-  //      gid + 8 = token 2 gid + 1; column 2 tig = token 4 tig, 8 + 2 tig = 4 tig + 1)
-  *reinterpret_cast<float4*>(&sc.Gk[ra][4 * tig]) = make_float4(ck0[0], ck1[0], ck0[1], ck1[1]);
-  *reinterpret_cast<float4*>(&sc.Gk[rb][4 * tig]) = make_float4(ck0[2], ck1[2], ck0[3], ck1[3]);
-  *reinterpret_cast<float4*>(&sc.Gq[ra][4 * tig]) = make_float4(cq0[0], cq1[0], cq0[1], cq1[1]);
-  *reinterpret_cast<float4*>(&sc.Gq[rb][4 * tig]) = make_float4(cq0[2], cq1[2], cq0[3], cq1[3]);
-  // beta of every token, from the lanes that hold it
+  // ---- Gram exchange: warp 1 hands its Gk partial to warp 0, warp 0 its Gq partial
+  //      to warp 1 (fragment row gid = token 2 gid, gid + 8 = 2 gid + 1; columns 2 tig,
+  //      2 tig + 1, 8 + 2 tig, 9 + 2 tig = tokens 4 tig, 4 tig + 2, 4 tig + 1, 4 tig + 3)
+  {
+    float* dst = w == 0 ? &sc.Gq0[0][0] : &sc.GkX[0][0];
+    const float* c0 = w == 0 ? cq0 : ck0;
+    const float* c1 = w == 0 ? cq1 : ck1;
+    *reinterpret_cast<float4*>(dst + ra * 16 + 4 * tig) = make_float4(c0[0], c1[0], c0[1], c1[1]);
+    *reinterpret_cast<float4*>(dst + rb * 16 + 4 * tig) = make_float4(c0[2], c1[2], c0[3], c1[3]);
+  }
+  pair_bar(pair);
+  // beta of the lane's tokens
   const float sa = va ? rcp_approx(1.f + ex2_approx(-beta_a * kLog2e)) : 0.f;
   const float sb = vb ? rcp_approx(1.f + ex2_approx(-beta_b * kLog2e)) : 0.f;
-  float bet[16];
+  if (w == 0) {
+    // full Gk = own partial + warp 1's; store column m of -Akk contiguous: AT[m][i] = -beta_i Gk[i][m]
+    const float4 xa = *reinterpret_cast<const float4*>(&sc.GkX[ra][4 * tig]);
+    const float4 xb = *reinterpret_cast<const float4*>(&sc.GkX[rb][4 * tig]);
+    const float ka[4] = {ck0[0] + xa.x, ck1[0] + xa.y, ck0[1] + xa.z, ck1[1] + xa.w};
+    const float kb[4] = {ck0[2] + xb.x, ck1[2] + xb.y, ck0[3] + xb.z, ck1[3] + xb.w};
+    __syncwarp();
 #pragma unroll
-  for (int i = 0; i < 16; ++i) bet[i] = __shfl_sync(0xffffffffu, (i & 1) ? sb : sa, 4 * (i >> 1));
-  __syncwarp();
-  if (lane < 16) {
-    // column j of X = (I + Akk)^-1 by forward substitution, Akk[i][m] = beta_i Gk[i][m]
-    const int j = lane;
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
-#pragma unroll
-    for (int m = 0; m < 15; ++m) {
-#pragma unroll
-      for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-bet[i] * sc.Gk[i][m], x[m], x[i]);
+    for (int u = 0; u < 4; ++u) {
+      sc.GkX[4 * tig + u][ra] = -sa * ka[u];
+      sc.GkX[4 * tig + u][rb] = -sb * kb[u];
     }
-    float bj = bet[0];
+    float bet[16];
 #pragma unroll
-    for (int i = 1; i < 16; ++i) bj = (j == i) ? bet[i] : bj;
+    for (int i = 0; i < 16; ++i) bet[i] = __shfl_sync(0xffffffffu, (i & 1) ? sb : sa, 4 * (i >> 1));
+    __syncwarp();
+    if (lane < 16) {
+      // column j of X = (I + Akk)^-1 by forward substitution
+      const int j = lane;
+      float x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      uint16_t hi, lo;
-      split_bf16(x[i] * bj, hi, lo);
-      const uint32_t o = ns_off(i, j);
-      *reinterpret_cast<uint16_t*>(st.TPhi + o) = hi;
-      *reinterpret_cast<uint16_t*>(st.TPlo + o) = lo;
+      for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < 15; ++m) {
+        float a[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 t = *reinterpret_cast<const float4*>(&sc.GkX[m][4 * q4]);
+          a[4 * q4] = t.x; a[4 * q4 + 1] = t.y; a[4 * q4 + 2] = t.z; a[4 * q4 + 3] = t.w;
+        }
+#pragma unroll
+        for (int i = m + 1; i < 16; ++i) x[i] = fmaf(a[i], x[m], x[i]);
+      }
+      float bj = bet[0];
+#pragma unroll
+      for (int i = 1; i < 16; ++i) bj = (j == i) ? bet[i] : bj;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint16_t hi, lo;
+        split_bf16(x[i] * bj, hi, lo);
+        const uint32_t o = ns_off(i, j);
+        *reinterpret_cast<uint16_t*>(st.TPhi + o) = hi;
+        *reinterpret_cast<uint16_t*>(st.TPlo + o) = lo;
+      }
     }
   } else {
-    // Aqk row i = lane - 16, inclusive lower triangle
-    const int i = lane - 16;
-    uint32_t hw[8], lw[8];
+    // Aqk = own Gq partial + warp 0's, inclusive lower triangle, split bf16 (4 tokens per store)
+    const float4 xa = *reinterpret_cast<const float4*>(&sc.Gq0[ra][4 * tig]);
+    const float4 xb = *reinterpret_cast<const float4*>(&sc.Gq0[rb][4 * tig]);
+    const float qa[4] = {cq0[0] + xa.x, cq1[0] + xa.y, cq0[1] + xa.z, cq1[1] + xa.w};
+    const float qb[4] = {cq0[2] + xb.x, cq1[2] + xb.y, cq0[3] + xb.z, cq1[3] + xb.w};
 #pragma unroll
-    for (int jj = 0; jj < 16; jj += 2) {
-      const float a = jj <= i ? sc.Gq[i][jj] : 0.f;
-      const float b = jj + 1 <= i ? sc.Gq[i][jj + 1] : 0.f;
-      split_bf16x2(a, b, hw[jj / 2], lw[jj / 2]);
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = ra + hr;
+      const float* v = hr == 0 ? qa : qb;
+      float m4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) m4[u] = (4 * tig + u <= i) ? v[u] : 0.f;
+      uint32_t h0, l0, h1, l1;
+      split_bf16x2(m4[0], m4[1], h0, l0);
+      split_bf16x2(m4[2], m4[3], h1, l1);
+      const uint32_t o = ns_off(i, 4 * tig);
+      *reinterpret_cast<uint2*>(st.AQhi + o) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(st.AQlo + o) = make_uint2(l0, l1);
     }
-    *reinterpret_cast<uint4*>(st.AQhi + ns_off(i, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(st.AQhi + ns_off(i, 8)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-    *reinterpret_cast<uint4*>(st.AQlo + ns_off(i, 0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    *reinterpret_cast<uint4*>(st.AQlo + ns_off(i, 8)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+    // rows of the v tile past the end of the sequence: zero
+    if (partial && v_used) {
+      for (int idx = lane; idx < (kChunk - nv) * 16; idx += 32) {
+        const int r = nv + idx / 16, c16 = idx % 16;
+        *reinterpret_cast<uint4*>(st.V + (c16 >> 3) * 2048 + r * 128 + (c16 & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
   }
-  __syncwarp();
-  // ---- W = Tm (kh*2^G) per 8-channel tile (bf16 warp MMA, Tm split hi + lo), -W over kh*2^G
+  pair_bar(pair);
+  // ---- W = Tm (kh*2^G) for this warp's 64 channels (bf16 warp MMA, Tm split hi + lo), -W over kh*2^G
   uint32_t ahi[4], alo[4];
   {
     const int mat = lane >> 3, rr = lane & 7;
@@ -335,7 +436,7 @@ __device__ __forceinline__ void prologue_chunk(Stage& st, PrologScratch& sc, int
     ldmatrix_x4(alo, smem_u32(st.TPlo) + moff);
   }
 #pragma unroll 2
-  for (int nt = 0; nt < 16; nt += 2) {
+  for (int nt = 8 * w; nt < 8 * w + 8; nt += 2) {
     uint32_t bfr[4];
     {
       // matrices: (tokens 0-7, tile nt), (8-15, nt), (0-7, nt+1), (8-15, nt+1)
@@ -356,13 +457,6 @@ __device__ __forceinline__ void prologue_chunk(Stage& st, PrologScratch& sc, int
       *reinterpret_cast<uint32_t*>(xb + sw_off(gid + 8, t & 7) + 4 * tig) = pack_bf16x2(-d[2], -d[3]);
     }
   }
-  // rows of the v tile past the end of the sequence: zero
-  if (partial && v_used) {
-    for (int idx = lane; idx < (kChunk - nv) * 16; idx += 32) {
-      const int r = nv + idx / 16, c16 = idx % 16;
-      *reinterpret_cast<uint4*>(st.V + (c16 >> 3) * 2048 + r * 128 + (c16 & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
   fence_proxy_async_smem();
   __syncwarp();
 }
@@ -377,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   SmemLayout& S = *reinterpret_cast<SmemLayout*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                  ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t bar_full[kStages], bar_op_full[kStages], bar_op_empty[kStages],
-      bar_d1_full[2], bar_vn_ready, bar_d2_full, bar_s_ready, bar_drain;
+      bar_d1_full[2], bar_d2_full, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -388,24 +482,24 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar_full[i], 1);
-      mbar_init(&bar_op_full[i], 1);
+      mbar_init(&bar_op_full[i], 2);   // both warps of a prologue pair
       mbar_init(&bar_op_empty[i], 1);
     }
     mbar_init(&bar_d1_full[0], 1);
     mbar_init(&bar_d1_full[1], 1);
-    mbar_init(&bar_vn_ready, 4);
     mbar_init(&bar_d2_full, 1);
-    mbar_init(&bar_s_ready, 4);
     mbar_init(&bar_drain, 1);
     s_abort = 0;
     mbar_fence_init();
   }
   if (warp >= kWarpProlog0 && warp < kWarpEpi0) {
     // rows 16..31 of the [Tm ; 0] operands stay zero for the whole run
-    const int t = threadIdx.x - kWarpProlog0 * 32;   // 0..63
-    for (int s = 0; s < kStages; ++s) {
-      reinterpret_cast<uint64_t*>(S.st[s].TPhi + 512)[t] = 0ull;
-      reinterpret_cast<uint64_t*>(S.st[s].TPlo + 512)[t] = 0ull;
+    const int t = threadIdx.x - kWarpProlog0 * 32;   // 0..127
+    if (t < 64) {
+      for (int s = 0; s < kStages; ++s) {
+        reinterpret_cast<uint64_t*>(S.st[s].TPhi + 512)[t] = 0ull;
+        reinterpret_cast<uint64_t*>(S.st[s].TPlo + 512)[t] = 0ull;
+      }
     }
     fence_proxy_async_smem();
   }
@@ -445,66 +539,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         }
       }
       __syncwarp();
-    } else if (warp == kWarpMma) {
-      // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        const uint32_t id_u = idesc_bf16_f32(128, 32, 1, 0);
-        const uint32_t id_x = idesc_bf16_f32(128, 32, 0, 0);
-        const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1);   // kfac is an MN-major B
-        const uint32_t id_o = idesc_bf16_f32(128, 16, 0, 0);
-        const uint32_t vnh = smem_u32(S.vn_hi), vnl = smem_u32(S.vn_lo);
-        const bool with_u = it.mode != kModeTransition;
-        const bool with_o = it.mode == kModeForward;
-        bool issued_any = false;
-        for (int c = 0; c < nchunks; ++c) {
-          const int s = c % kStages, b = c & 1;
-          const uint32_t d1 = tmem + kColD1 + 32u * b;
-          Stage& st = S.st[s];
-          if (!mbar_wait(&bar_op_full[s], (c / kStages) & 1, ab)) break;
-          if (!mbar_wait(&bar_full[s], (c / kStages) & 1, ab)) break;
-          tc_fence_after();
-          if (with_u) {
-            const uint64_t a_v = smem_desc(smem_u32(st.V), 2048, 1024, kSwizzle128B);
-            mma_ss(d1, a_v, smem_desc(smem_u32(st.TPhi), 128, 256, kSwizzleNone), id_u, 0);
-            mma_ss(d1, a_v, smem_desc(smem_u32(st.TPlo), 128, 256, kSwizzleNone), id_u, 1);
-          }
-          issued_any = true;
-          if (!mbar_wait(&bar_s_ready, c & 1, ab)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t bd = smem_desc(smem_u32(st.X[k >> 2]) + (k & 3) * 32, 16, 1024, kSwizzle128B);
-            mma_ts(d1, tmem + kColSbf + 8u * k, bd, id_x, (with_u || k > 0) ? 1u : 0u);
-          }
-          tc_commit(&bar_d1_full[b]);
-          if (!mbar_wait(&bar_vn_ready, c & 1, ab)) break;
-          tc_fence_after();
-          const uint64_t a_hi = smem_desc(vnh, 128, 256, kSwizzleNone);
-          const uint64_t a_lo = smem_desc(vnl, 128, 256, kSwizzleNone);
-          const uint64_t kf_hi = smem_desc(smem_u32(st.K), 2048, 1024, kSwizzle128B);
-          const uint64_t kf_lo = smem_desc(smem_u32(st.G), 2048, 1024, kSwizzle128B);
-          mma_ss(tmem + kColState, a_hi, kf_hi, id_s, 1);
-          mma_ss(tmem + kColState, a_hi, kf_lo, id_s, 1);
-          mma_ss(tmem + kColState, a_lo, kf_hi, id_s, 1);
-          if (with_o) {
-            const uint64_t aq_hi = smem_desc(smem_u32(st.AQhi), 128, 256, kSwizzleNone);
-            const uint64_t aq_lo = smem_desc(smem_u32(st.AQlo), 128, 256, kSwizzleNone);
-            mma_ss(d1 + 16, a_hi, aq_hi, id_o, 1);
-            mma_ss(d1 + 16, a_lo, aq_hi, id_o, 1);
-            mma_ss(d1 + 16, a_hi, aq_lo, id_o, 1);
-          }
-          tc_commit(&bar_d2_full);
-          tc_commit(&bar_op_empty[s]);
-        }
-        if (s_abort && issued_any) {  // wait for MMAs in flight before TMEM is released
-          tc_commit(&bar_drain);
-          mbar_wait_drain(&bar_drain, 0);
-        }
-      }
-      __syncwarp();
     } else if (warp < kWarpEpi0) {
       // ------------------------------------------------------------ prologue
       const int pw = warp - kWarpProlog0;
+      const int pair = pw >> 1, w = pw & 1;      // pair 0: even chunks, pair 1: odd chunks
+      PairScratch& sc = S.ps[pair];
       const int h = it.head;
       const int H = p.H;
       const float nr = -expf(p.A_log[h]) * kLog2e;
@@ -519,27 +558,85 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
                                                : 0.f;
       };
       float bl0, bl1;
-      load_beta(pw, bl0, bl1);
-      for (int c = pw; c < nchunks; c += kProlog) {
+      load_beta(pair, bl0, bl1);
+      int iter = 0;
+      for (int c = pair; c < nchunks; c += 2, ++iter) {
         const int s = c % kStages;
         const int nv = min(kChunk, it.len - c * kChunk);
         const float cb0 = bl0, cb1 = bl1;
-        load_beta(c + kProlog, bl0, bl1);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_full[s], (c / kStages) & 1, ab));
-        if (!ok) break;
-        prologue_chunk(S.st[s], S.ps[pw], nv, nr, lbl2, dtb, cb0, cb1, lane, it.mode != kModeTransition);
+        load_beta(c + 2, bl0, bl1);
+        // both warps of the pair agree on going on (the pair shares named barriers)
+        const bool okw = __all_sync(0xffffffffu, mbar_wait(&bar_full[s], (c / kStages) & 1, ab));
+        if (lane == 0) sc.okf[iter & 1][w] = okw ? 1 : 0;
+        pair_bar(pair);
+        if (!(sc.okf[iter & 1][0] && sc.okf[iter & 1][1])) break;
+        prologue_pair_chunk(S.st[s], sc, pair, w, nv, nr, lbl2, dtb, cb0, cb1, lane, it.mode != kModeTransition);
         if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
     } else {
       // ------------------------------------------------------------ epilogue
+      // Four warps, one TMEM lane quarter each (row v of S^T per thread).  Lane 0
+      // of warp kWarpEpi0 issues every tcgen05 MMA right after a named barrier of
+      // the four warps; the other roles never wait on the tensor core.
       const int q4 = warp & 3;
       const int vrow = q4 * 32 + lane;
+      const bool leader = (warp == kWarpEpi0) && (lane == 0);
       const uint32_t loff = static_cast<uint32_t>(q4 * 32) << 16;
       const uint32_t tS = tmem + kColState + loff;
       const uint32_t tSb = tmem + kColSbf + loff;
       const uint32_t tD1 = tmem + kColD1 + loff;
       const int h = it.head;
       const size_t srow = ((size_t)it.seq * p.H + h) * kDimV + vrow;   // user state row (n, h, v)
+      const bool with_u = it.mode != kModeTransition;
+      const bool with_o = it.mode == kModeForward;
+      // instruction and shared-memory descriptors (stage s adds s * sizeof(Stage))
+      const uint32_t id_u = idesc_bf16_f32(128, 32, 1, 0);
+      const uint32_t id_x = idesc_bf16_f32(128, 32, 0, 0);
+      const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1);   // kfac is an MN-major B
+      const uint32_t id_o = idesc_bf16_f32(128, 16, 0, 0);
+      constexpr uint64_t kStageStep = sizeof(Stage) >> 4;
+      const Stage& s0 = S.st[0];
+      // U and the S-side GEMM of chunk c into D1[c & 1] (the leader thread only)
+      auto issue_gemm1 = [&](int c) {
+        const uint64_t so = (uint64_t)(c % kStages) * kStageStep;
+        const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
+        if (with_u) {
+          const uint64_t d_v = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
+          mma_ss(d1, d_v, smem_desc(smem_u32(s0.TPhi), 128, 256, kSwizzleNone) + so, id_u, 0);
+          mma_ss(d1, d_v, smem_desc(smem_u32(s0.TPlo), 128, 256, kSwizzleNone) + so, id_u, 1);
+        }
+        const uint64_t d_x0 = smem_desc(smem_u32(s0.X[0]), 16, 1024, kSwizzle128B) + so;
+        const uint64_t d_x1 = smem_desc(smem_u32(s0.X[1]), 16, 1024, kSwizzle128B) + so;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(d1, tmem + kColSbf + 8u * k, (k < 4 ? d_x0 : d_x1) + (uint64_t)((k & 3) * 2), id_x,
+                 (with_u || k > 0) ? 1u : 0u);
+        tc_commit(&bar_d1_full[c & 1]);
+      };
+      // rank-16 state update and the intra-chunk output term of chunk c
+      auto issue_update = [&](int c) {
+        const uint64_t so = (uint64_t)(c % kStages) * kStageStep;
+        const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
+        const uint64_t a_hi = smem_desc(smem_u32(S.vn_hi), 128, 256, kSwizzleNone);
+        const uint64_t a_lo = smem_desc(smem_u32(S.vn_lo), 128, 256, kSwizzleNone);
+        const uint64_t kf_hi = smem_desc(smem_u32(s0.K), 2048, 1024, kSwizzle128B) + so;
+        const uint64_t kf_lo = smem_desc(smem_u32(s0.G), 2048, 1024, kSwizzle128B) + so;
+        mma_ss(tmem + kColState, a_hi, kf_hi, id_s, 1);
+        mma_ss(tmem + kColState, a_hi, kf_lo, id_s, 1);
+        mma_ss(tmem + kColState, a_lo, kf_hi, id_s, 1);
+        if (with_o) {
+          const uint64_t aq_hi = smem_desc(smem_u32(s0.AQhi), 128, 256, kSwizzleNone) + so;
+          const uint64_t aq_lo = smem_desc(smem_u32(s0.AQlo), 128, 256, kSwizzleNone) + so;
+          mma_ss(d1 + 16, a_hi, aq_hi, id_o, 1);
+          mma_ss(d1 + 16, a_lo, aq_hi, id_o, 1);
+          mma_ss(d1 + 16, a_hi, aq_lo, id_o, 1);
+        }
+        tc_commit(&bar_d2_full);
+        tc_commit(&bar_op_empty[c % kStages]);
+      };
+      bool issued_any = false;
+      // every epilogue warp runs every named barrier below, also after an abort,
+      // so that the group never waits on a warp that left early
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_op_full[0], 0, ab));
       // ---- initial state row v of S^T -> bf16 copy + decayed fp32 accumulator
       if (ok) {
@@ -601,16 +698,23 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         tmem_st_wait();
       }
       tc_fence_before();
+      named_bar(kBarEpi, 128);
+      if (leader && !s_abort) {
+        tc_fence_after();
+        if (mbar_wait(&bar_full[0], 0, ab)) {
+          issue_gemm1(0);
+          issued_any = true;
+        }
+      }
       __syncwarp();
-      if (lane == 0 && ok) mbar_arrive(&bar_s_ready);
-      for (int c = 0; c < nchunks && ok; ++c) {
+      for (int c = 0; c < nchunks; ++c) {
         const int b = c & 1;
         const int nv = min(kChunk, it.len - c * kChunk);
-        // ---- E1: Vn^T row v (16 tokens) -> split bf16 operand
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_d1_full[b], (c >> 1) & 1, ab));
-        if (!ok) break;
-        tc_fence_after();
-        {
+        const bool last = (c == nchunks - 1);
+        // ---- E1: Vn^T row v (16 tokens) -> split bf16 operand; then the update MMAs
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar_d1_full[b], (c >> 1) & 1, ab));
+        if (ok) {
+          tc_fence_after();
           uint32_t r[16];
           tmem_ld16(tD1 + 32u * b, r);
           tmem_ld_wait();
@@ -622,16 +726,79 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
           *reinterpret_cast<uint4*>(S.vn_hi + ns_off(vrow, 8)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           *reinterpret_cast<uint4*>(S.vn_lo + ns_off(vrow, 0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           *reinterpret_cast<uint4*>(S.vn_lo + ns_off(vrow, 8)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
+        named_bar(kBarEpi, 128);
+        if (leader && !s_abort) {
+          tc_fence_after();
+          issue_update(c);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_vn_ready);
-        // ---- E2: outputs and the state for the next chunk
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_d2_full, c & 1, ab));
-        if (!ok) break;
-        tc_fence_after();
-        if (it.mode == kModeForward) {
+        // ---- E2: the new state S' -> bf16 copy (A operand of the next S-side GEMM) and,
+        //      in the same pass, the fp32 accumulator decayed by the next chunk's 2^G_C
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar_d2_full, c & 1, ab));
+        if (!last)
+          ok = ok && __all_sync(0xffffffffu,
+                                mbar_wait(&bar_op_full[(c + 1) % kStages], ((c + 1) / kStages) & 1, ab));
+        if (ok) {
+          tc_fence_after();
+          const Stage& stn = S.st[(c + 1) % kStages];
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            tmem_ld32(tS + 32u * j, r);
+            tmem_ld_wait();
+            if (!last) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int t = 0; t < 16; ++t)
+                pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
+              tmem_st16(tSb + 16u * j, pk);
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                const float4 gm = *reinterpret_cast<const float4*>(&stn.gamC[32 * j + 4 * t]);
+                r[4 * t] = __float_as_uint(__uint_as_float(r[4 * t]) * gm.x);
+                r[4 * t + 1] = __float_as_uint(__uint_as_float(r[4 * t + 1]) * gm.y);
+                r[4 * t + 2] = __float_as_uint(__uint_as_float(r[4 * t + 2]) * gm.z);
+                r[4 * t + 3] = __float_as_uint(__uint_as_float(r[4 * t + 3]) * gm.w);
+              }
+              tmem_st32(tS + 32u * j, r);
+            } else if (it.out_slot >= 0) {
+              float4* dst = reinterpret_cast<float4*>(p.ws_states + (size_t)it.out_slot * 16384 +
+                                                      (size_t)vrow * 128 + 32 * j);
+#pragma unroll
+              for (int t = 0; t < 8; ++t)
+                dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
+                                     __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
+            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * 128 + 32 * j);
+#pragma unroll
+              for (int t = 0; t < 8; ++t)
+                dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
+                                     __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
+            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * 128 + 32 * j);
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+                dst[t] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * t]), __uint_as_float(r[8 * t + 1])),
+                                    pack_bf16x2(__uint_as_float(r[8 * t + 2]), __uint_as_float(r[8 * t + 3])),
+                                    pack_bf16x2(__uint_as_float(r[8 * t + 4]), __uint_as_float(r[8 * t + 5])),
+                                    pack_bf16x2(__uint_as_float(r[8 * t + 6]), __uint_as_float(r[8 * t + 7])));
+            }
+          }
+          if (!last) tmem_st_wait();
+        }
+        tc_fence_before();
+        named_bar(kBarEpi, 128);
+        if (!last && leader && !s_abort) {
+          tc_fence_after();
+          const int c1 = c + 1;
+          if (mbar_wait(&bar_full[c1 % kStages], (c1 / kStages) & 1, ab)) issue_gemm1(c1);
+        }
+        __syncwarp();
+        // ---- outputs of this chunk (overlaps the next S-side GEMM)
+        if (ok && with_o) {
           uint32_t r[16];
           tmem_ld16(tD1 + 32u * b + 16u, r);
           tmem_ld_wait();
@@ -644,60 +811,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
             }
           }
         }
-        const bool last = (c == nchunks - 1);
-        if (!last) {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(&bar_op_full[(c + 1) % kStages], ((c + 1) / kStages) & 1, ab));
-          if (!ok) break;
-        }
-        const Stage& stn = S.st[(c + 1) % kStages];
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-          uint32_t r[32];
-          tmem_ld32(tS + 32u * j, r);
-          tmem_ld_wait();
-          if (!last) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
-            tmem_st16(tSb + 16u * j, pk);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const float4 gm = *reinterpret_cast<const float4*>(&stn.gamC[32 * j + 4 * t]);
-              mul2(r[4 * t], r[4 * t + 1], gm.x, gm.y);
-              mul2(r[4 * t + 2], r[4 * t + 3], gm.z, gm.w);
-            }
-            tmem_st32(tS + 32u * j, r);
-          } else if (it.out_slot >= 0) {
-            float4* dst = reinterpret_cast<float4*>(p.ws_states + (size_t)it.out_slot * 16384 +
-                                                    (size_t)vrow * 128 + 32 * j);
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-              dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
-                                   __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-          } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * 128 + 32 * j);
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-              dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
-                                   __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-          } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * 128 + 32 * j);
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              dst[t] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * t]), __uint_as_float(r[8 * t + 1])),
-                                  pack_bf16x2(__uint_as_float(r[8 * t + 2]), __uint_as_float(r[8 * t + 3])),
-                                  pack_bf16x2(__uint_as_float(r[8 * t + 4]), __uint_as_float(r[8 * t + 5])),
-                                  pack_bf16x2(__uint_as_float(r[8 * t + 6]), __uint_as_float(r[8 * t + 7])));
-          }
-        }
-        if (!last) {
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_s_ready);
-        }
       }
+      if (leader && s_abort && issued_any) {  // wait for MMAs in flight before TMEM is released
+        tc_commit(&bar_drain);
+        mbar_wait_drain(&bar_drain, 0);
+      }
+      __syncwarp();
     }
   } else if (warp >= kWarpEpi0) {
     // zero-length run: the final state equals the initial state

@@ -60,6 +60,16 @@ def run_oracle(x: dict, out_rows=None, want_out=True):
                               nthreads=os.cpu_count())
 
 
+def _report(label: str, what: str, value: float) -> None:
+    """With KDA_TEST_REPORT set, append the measured error to gpurun_out/parity_report.txt."""
+    if not os.environ.get("KDA_TEST_REPORT"):
+        return
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    os.makedirs(os.path.join(root, "gpurun_out"), exist_ok=True)
+    with open(os.path.join(root, "gpurun_out", "parity_report.txt"), "a") as f:
+        f.write(f"{label}\t{what}\t{value:.3e}\n")
+
+
 def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
     d = np.linalg.norm((np.asarray(a, np.float64) - np.asarray(b, np.float64)).ravel())
     n = np.linalg.norm(np.asarray(b, np.float64).ravel())
@@ -73,6 +83,8 @@ def check_out(gpu_out: torch.Tensor, ref: np.ndarray, rows=None, label=""):
     assert np.all(np.isfinite(g)), f"{label}: non-finite output"
     max_abs = float(np.abs(g - ref).max()) if ref.size else 0.0
     rf = rel_fro(g, ref) if ref.size else 0.0
+    _report(label, "out_max_abs", max_abs)
+    _report(label, "out_rel_fro", rf)
     assert max_abs <= OUT_MAX_ABS, f"{label}: out max-abs {max_abs:.3e} > {OUT_MAX_ABS}"
     assert rf <= OUT_REL_FRO, f"{label}: out rel-Fro {rf:.3e} > {OUT_REL_FRO}"
     return max_abs, rf
@@ -83,6 +95,7 @@ def check_state(gpu_state: torch.Tensor, ref: np.ndarray, label=""):
     assert np.all(np.isfinite(g)), f"{label}: non-finite state"
     rf = rel_fro(g, ref)
     bound = STATE_REL_FRO_BF16 if gpu_state.dtype == torch.bfloat16 else STATE_REL_FRO_FP32
+    _report(label, f"state_rel_fro_{str(gpu_state.dtype).replace('torch.', '')}", rf)
     assert rf <= bound, f"{label}: state rel-Fro {rf:.3e} > {bound}"
     return rf
 
