@@ -59,25 +59,28 @@ struct Stage {
   uint8_t K[4096];        // k tile -> kfac hi   (MN-major B of the state update)
   uint8_t G[4096];        // g tile -> kfac lo
   uint8_t V[4096];        // v tile (MN-major A of U^T = V^T Tm^T)
+};
+static_assert(sizeof(Stage) == 20480, "stage size (multiple of 1024 for the swizzled regions)");
+struct StageSmall {       // the unswizzled operands of the same chunk
   uint8_t TPhi[1024];     // [Tm ; 0] [32 rows][16] K-major, no swizzle
   uint8_t TPlo[1024];
   uint8_t AQhi[512];      // Aqk [16][16] K-major, no swizzle
   uint8_t AQlo[512];
   float gamC[128];        // 2^G_C per channel
-  uint8_t pad[512];
 };
-static_assert(sizeof(Stage) == 24576, "stage size (multiple of 1024 for the swizzled regions)");
+static_assert(sizeof(StageSmall) == 3584, "small stage size");
 struct PairScratch {      // exchange area of one prologue pair (fp32, token indices)
   float normx[2][16][2];  // per-warp partial |q|^2, |k|^2
   float GkX[16][16];      // warp 1's partial Gk, then -beta_i Gk[i][m] stored at [m][i]
   float Gq0[16][16];      // warp 0's partial Gq
   int okf[2][2];          // both warps' wait results, by iteration parity
-  int pad[60];
 };
 struct SmemLayout {
   Stage st[kStages];
+  StageSmall sm[kStages];
   uint8_t vn_hi[4096];    // Vn^T [128 v][16 tok] K-major, no swizzle
   uint8_t vn_lo[4096];
+  uint8_t ostage[16][256];  // one chunk's bf16 outputs [token][v], for coalesced stores
   PairScratch ps[2];
 };
 
@@ -153,7 +156,7 @@ __device__ __forceinline__ void pair_bar(int pair) { named_bar(1 + pair, 64); }
 // 2 gid / 2 gid + 1 play the fragment rows gid / gid + 8, and the channel pair
 // (8 tig + 2 s, + 1) the k positions (tig, tig + 4) of k-step s; the partial
 // Grams of the two warps are summed through shared memory.
-__device__ __forceinline__ void prologue_pair_chunk(Stage& st, PairScratch& sc, int pair, int w, int nv,
+__device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, PairScratch& sc, int pair, int w, int nv,
                                                     const float nr, const float lbl2,
                                                     const float* __restrict__ dtb, float beta_a, float beta_b,
                                                     int lane, bool v_used) {
@@ -334,8 +337,8 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, PairScratch& sc, 
       *reinterpret_cast<uint4*>(gb + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     if (gid == 0) {
-      *reinterpret_cast<float4*>(&st.gamC[ch0]) = make_float4(eC[0], eC[1], eC[2], eC[3]);
-      *reinterpret_cast<float4*>(&st.gamC[ch0 + 4]) = make_float4(eC[4], eC[5], eC[6], eC[7]);
+      *reinterpret_cast<float4*>(&sm.gamC[ch0]) = make_float4(eC[0], eC[1], eC[2], eC[3]);
+      *reinterpret_cast<float4*>(&sm.gamC[ch0 + 4]) = make_float4(eC[4], eC[5], eC[6], eC[7]);
     }
   }
   // ---- Gram exchange: warp 1 hands its Gk partial to warp 0, warp 0 its Gq partial
@@ -393,8 +396,8 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, PairScratch& sc, 
         uint16_t hi, lo;
         split_bf16(x[i] * bj, hi, lo);
         const uint32_t o = ns_off(i, j);
-        *reinterpret_cast<uint16_t*>(st.TPhi + o) = hi;
-        *reinterpret_cast<uint16_t*>(st.TPlo + o) = lo;
+        *reinterpret_cast<uint16_t*>(sm.TPhi + o) = hi;
+        *reinterpret_cast<uint16_t*>(sm.TPlo + o) = lo;
       }
     }
   } else {
@@ -414,8 +417,8 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, PairScratch& sc, 
       split_bf16x2(m4[0], m4[1], h0, l0);
       split_bf16x2(m4[2], m4[3], h1, l1);
       const uint32_t o = ns_off(i, 4 * tig);
-      *reinterpret_cast<uint2*>(st.AQhi + o) = make_uint2(h0, h1);
-      *reinterpret_cast<uint2*>(st.AQlo + o) = make_uint2(l0, l1);
+      *reinterpret_cast<uint2*>(sm.AQhi + o) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(sm.AQlo + o) = make_uint2(l0, l1);
     }
     // rows of the v tile past the end of the sequence: zero
     if (partial && v_used) {
@@ -432,8 +435,8 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, PairScratch& sc, 
   {
     const int mat = lane >> 3, rr = lane & 7;
     const uint32_t moff = (uint32_t)((mat & 1) * 256 + (mat >> 1) * 128 + rr * 16);
-    ldmatrix_x4(ahi, smem_u32(st.TPhi) + moff);
-    ldmatrix_x4(alo, smem_u32(st.TPlo) + moff);
+    ldmatrix_x4(ahi, smem_u32(sm.TPhi) + moff);
+    ldmatrix_x4(alo, smem_u32(sm.TPlo) + moff);
   }
 #pragma unroll 2
   for (int nt = 8 * w; nt < 8 * w + 8; nt += 2) {
@@ -497,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
     const int t = threadIdx.x - kWarpProlog0 * 32;   // 0..127
     if (t < 64) {
       for (int s = 0; s < kStages; ++s) {
-        reinterpret_cast<uint64_t*>(S.st[s].TPhi + 512)[t] = 0ull;
-        reinterpret_cast<uint64_t*>(S.st[s].TPlo + 512)[t] = 0ull;
+        reinterpret_cast<uint64_t*>(S.sm[s].TPhi + 512)[t] = 0ull;
+        reinterpret_cast<uint64_t*>(S.sm[s].TPlo + 512)[t] = 0ull;
       }
     }
     fence_proxy_async_smem();
@@ -570,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         if (lane == 0) sc.okf[iter & 1][w] = okw ? 1 : 0;
         pair_bar(pair);
         if (!(sc.okf[iter & 1][0] && sc.okf[iter & 1][1])) break;
-        prologue_pair_chunk(S.st[s], sc, pair, w, nv, nr, lbl2, dtb, cb0, cb1, lane, it.mode != kModeTransition);
+        prologue_pair_chunk(S.st[s], S.sm[s], sc, pair, w, nv, nr, lbl2, dtb, cb0, cb1, lane, it.mode != kModeTransition);
         if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
     } else {
@@ -595,15 +598,18 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1);   // kfac is an MN-major B
       const uint32_t id_o = idesc_bf16_f32(128, 16, 0, 0);
       constexpr uint64_t kStageStep = sizeof(Stage) >> 4;
+      constexpr uint64_t kSmallStep = sizeof(StageSmall) >> 4;
       const Stage& s0 = S.st[0];
+      const StageSmall& m0 = S.sm[0];
       // U and the S-side GEMM of chunk c into D1[c & 1] (the leader thread only)
       auto issue_gemm1 = [&](int c) {
         const uint64_t so = (uint64_t)(c % kStages) * kStageStep;
+        const uint64_t sso = (uint64_t)(c % kStages) * kSmallStep;
         const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
         if (with_u) {
           const uint64_t d_v = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
-          mma_ss(d1, d_v, smem_desc(smem_u32(s0.TPhi), 128, 256, kSwizzleNone) + so, id_u, 0);
-          mma_ss(d1, d_v, smem_desc(smem_u32(s0.TPlo), 128, 256, kSwizzleNone) + so, id_u, 1);
+          mma_ss(d1, d_v, smem_desc(smem_u32(m0.TPhi), 128, 256, kSwizzleNone) + sso, id_u, 0);
+          mma_ss(d1, d_v, smem_desc(smem_u32(m0.TPlo), 128, 256, kSwizzleNone) + sso, id_u, 1);
         }
         const uint64_t d_x0 = smem_desc(smem_u32(s0.X[0]), 16, 1024, kSwizzle128B) + so;
         const uint64_t d_x1 = smem_desc(smem_u32(s0.X[1]), 16, 1024, kSwizzle128B) + so;
@@ -616,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       // rank-16 state update and the intra-chunk output term of chunk c
       auto issue_update = [&](int c) {
         const uint64_t so = (uint64_t)(c % kStages) * kStageStep;
+        const uint64_t sso = (uint64_t)(c % kStages) * kSmallStep;
         const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
         const uint64_t a_hi = smem_desc(smem_u32(S.vn_hi), 128, 256, kSwizzleNone);
         const uint64_t a_lo = smem_desc(smem_u32(S.vn_lo), 128, 256, kSwizzleNone);
@@ -625,8 +632,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         mma_ss(tmem + kColState, a_hi, kf_lo, id_s, 1);
         mma_ss(tmem + kColState, a_lo, kf_hi, id_s, 1);
         if (with_o) {
-          const uint64_t aq_hi = smem_desc(smem_u32(s0.AQhi), 128, 256, kSwizzleNone) + so;
-          const uint64_t aq_lo = smem_desc(smem_u32(s0.AQlo), 128, 256, kSwizzleNone) + so;
+          const uint64_t aq_hi = smem_desc(smem_u32(m0.AQhi), 128, 256, kSwizzleNone) + sso;
+          const uint64_t aq_lo = smem_desc(smem_u32(m0.AQlo), 128, 256, kSwizzleNone) + sso;
           mma_ss(d1 + 16, a_hi, aq_hi, id_o, 1);
           mma_ss(d1 + 16, a_lo, aq_hi, id_o, 1);
           mma_ss(d1 + 16, a_hi, aq_lo, id_o, 1);
@@ -640,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_op_full[0], 0, ab));
       // ---- initial state row v of S^T -> bf16 copy + decayed fp32 accumulator
       if (ok) {
-        const Stage& st0 = S.st[0];
+        const StageSmall& st0 = S.sm[0];
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
           float s[32];
@@ -743,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
                                 mbar_wait(&bar_op_full[(c + 1) % kStages], ((c + 1) / kStages) & 1, ab));
         if (ok) {
           tc_fence_after();
-          const Stage& stn = S.st[(c + 1) % kStages];
+          const StageSmall& stn = S.sm[(c + 1) % kStages];
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
             uint32_t r[32];
@@ -797,17 +804,33 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
           if (mbar_wait(&bar_full[c1 % kStages], (c1 / kStages) & 1, ab)) issue_gemm1(c1);
         }
         __syncwarp();
-        // ---- outputs of this chunk (overlaps the next S-side GEMM)
-        if (ok && with_o) {
-          uint32_t r[16];
-          tmem_ld16(tD1 + 32u * b + 16u, r);
-          tmem_ld_wait();
-          const size_t base = ((size_t)(it.row0 + c * kChunk) * p.H + h) * kDimV + vrow;
+        // ---- outputs of this chunk (overlaps the next S-side GEMM): through shared
+        //      memory, then 16-byte stores of whole token rows
+        if (with_o) {
+          if (ok) {
+            uint32_t r[16];
+            tmem_ld16(tD1 + 32u * b + 16u, r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if (i < nv) {
-              const __nv_bfloat16 o = __float2bfloat16_rn(p.scale * __uint_as_float(r[i]));
-              p.out[base + (size_t)i * p.H * kDimV] = __bfloat16_as_ushort(o);
+            for (int i = 0; i < 16; ++i)
+              *reinterpret_cast<uint16_t*>(&S.ostage[i][2 * vrow]) =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * __uint_as_float(r[i])));
+          }
+          named_bar(kBarEpi, 128);
+          if (ok) {
+            const int et = threadIdx.x - kWarpEpi0 * 32;     // 0..127
+            const size_t row_elems = (size_t)p.H * kDimV;
+            uint16_t* obase = p.out + ((size_t)(it.row0 + c * kChunk) * p.H + h) * kDimV;
+            if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0) {
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                const int q = et + 128 * rr, i = q >> 4, c16 = q & 15;
+                if (i < nv)
+                  *reinterpret_cast<uint4*>(obase + (size_t)i * row_elems + 8 * c16) =
+                      *reinterpret_cast<const uint4*>(&S.ostage[i][16 * c16]);
+              }
+            } else {
+              for (int i = 0; i < nv; ++i) obase[(size_t)i * row_elems + et] = *reinterpret_cast<const uint16_t*>(&S.ostage[i][2 * et]);
             }
           }
         }
