@@ -37,12 +37,11 @@
 
 namespace kda {
 
-constexpr int kThreads = 288;
+// Eight warps, two CTAs per SM: sixteen warps per SM leave 128 registers a thread.
+constexpr int kThreads = 256;
 constexpr int kStages = 4;
-constexpr int kWarpProducer = 0;
-constexpr int kWarpProlog0 = 1;
-constexpr int kProlog = 4;            // prologue warps: two pairs, one pair per chunk
-constexpr int kWarpEpi0 = 5;          // epilogue warps 5-8; lane 0 of warp 5 issues the MMAs
+constexpr int kWarpProlog0 = 0;       // prologue warps 0-3: two pairs, one pair per chunk
+constexpr int kWarpEpi0 = 4;          // epilogue warps 4-7; lane 0 of warp 4 issues the MMAs and TMA loads
 constexpr uint32_t kBarEpi = 3;       // named barrier of the epilogue warps
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColState = 0;
@@ -506,43 +505,14 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
     }
     fence_proxy_async_smem();
   }
-  if (warp == kWarpProducer) tmem_alloc(&s_tmem, kTmemCols);
+  if (warp == kWarpEpi0) tmem_alloc(&s_tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
   if (nchunks > 0) {
-    if (warp == kWarpProducer) {
-      // ------------------------------------------------------------ producer
-      if (lane == 0) {
-        tma_prefetch_desc(&p.tm_q);
-        tma_prefetch_desc(&p.tm_k);
-        tma_prefetch_desc(&p.tm_g);
-        tma_prefetch_desc(&p.tm_v);
-        const bool load_v = it.mode != kModeTransition;
-        int issued = 0;
-        for (int c = 0; c < nchunks; ++c) {
-          const int s = c % kStages;
-          if (c >= kStages && !mbar_wait(&bar_op_empty[s], ((c / kStages) - 1) & 1, ab)) break;
-          const int row = it.row0 + c * kChunk;
-          Stage& st = S.st[s];
-          mbar_arrive_expect_tx(&bar_full[s], load_v ? 16384u : 12288u);
-          for (int b = 0; b < 2; ++b) {
-            tma_load_3d(st.X[b] + 2048, &p.tm_q, &bar_full[s], b * 64, it.head, row);
-            tma_load_3d(st.K + b * 2048, &p.tm_k, &bar_full[s], b * 64, it.head, row);
-            tma_load_3d(st.G + b * 2048, &p.tm_g, &bar_full[s], b * 64, it.head, row);
-            if (load_v) tma_load_3d(st.V + b * 2048, &p.tm_v, &bar_full[s], b * 64, it.head, row);
-          }
-          ++issued;
-        }
-        if (s_abort) {  // let loads in flight land before the CTA exits
-          for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
-            mbar_wait_drain(&bar_full[c % kStages], (c / kStages) & 1);
-        }
-      }
-      __syncwarp();
-    } else if (warp < kWarpEpi0) {
+    if (warp < kWarpEpi0) {
       // ------------------------------------------------------------ prologue
       const int pw = warp - kWarpProlog0;
       const int pair = pw >> 1, w = pw & 1;      // pair 0: even chunks, pair 1: odd chunks
@@ -580,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       // ------------------------------------------------------------ epilogue
       // Four warps, one TMEM lane quarter each (row v of S^T per thread).  Lane 0
       // of warp kWarpEpi0 issues every tcgen05 MMA right after a named barrier of
-      // the four warps; the other roles never wait on the tensor core.
+      // the four warps, and the TMA loads of each stage once the MMAs that read the
+      // stage's previous chunk have completed; the prologue never waits on the tensor core.
       const int q4 = warp & 3;
       const int vrow = q4 * 32 + lane;
       const bool leader = (warp == kWarpEpi0) && (lane == 0);
@@ -641,6 +612,30 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         tc_commit(&bar_d2_full);
         tc_commit(&bar_op_empty[c % kStages]);
       };
+      // TMA loads of chunk c into stage c % kStages (the leader thread only)
+      const bool load_v = it.mode != kModeTransition;
+      int tma_issued = 0;
+      auto issue_tma = [&](int c) {
+        const int s = c % kStages;
+        const int row = it.row0 + c * kChunk;
+        Stage& st = S.st[s];
+        mbar_arrive_expect_tx(&bar_full[s], load_v ? 16384u : 12288u);
+        for (int b = 0; b < 2; ++b) {
+          tma_load_3d(st.X[b] + 2048, &p.tm_q, &bar_full[s], b * 64, it.head, row);
+          tma_load_3d(st.K + b * 2048, &p.tm_k, &bar_full[s], b * 64, it.head, row);
+          tma_load_3d(st.G + b * 2048, &p.tm_g, &bar_full[s], b * 64, it.head, row);
+          if (load_v) tma_load_3d(st.V + b * 2048, &p.tm_v, &bar_full[s], b * 64, it.head, row);
+        }
+        ++tma_issued;
+      };
+      if (leader) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_g);
+        tma_prefetch_desc(&p.tm_v);
+        for (int c = 0; c < kStages && c < nchunks; ++c) issue_tma(c);
+      }
+      __syncwarp();
       bool issued_any = false;
       // every epilogue warp runs every named barrier below, also after an abort,
       // so that the group never waits on a warp that left early
@@ -802,6 +797,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
           tc_fence_after();
           const int c1 = c + 1;
           if (mbar_wait(&bar_full[c1 % kStages], (c1 / kStages) & 1, ab)) issue_gemm1(c1);
+          // stage c % kStages is free once the MMAs of chunk c are done (long since, by now)
+          if (c + kStages < nchunks && mbar_wait(&bar_op_empty[c % kStages], (c / kStages) & 1, ab))
+            issue_tma(c + kStages);
         }
         __syncwarp();
         // ---- outputs of this chunk (overlaps the next S-side GEMM): through shared
@@ -839,6 +837,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         tc_commit(&bar_drain);
         mbar_wait_drain(&bar_drain, 0);
       }
+      if (leader && s_abort) {  // let loads in flight land before the CTA exits
+        for (int c = (tma_issued > kStages ? tma_issued - kStages : 0); c < tma_issued; ++c)
+          mbar_wait_drain(&bar_full[c % kStages], (c / kStages) & 1);
+      }
       __syncwarp();
     }
   } else if (warp >= kWarpEpi0) {
@@ -865,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kWarpProducer) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpEpi0) tmem_dealloc(tmem, kTmemCols);
 }
 
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
