@@ -133,6 +133,21 @@ bool encode_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H) 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same tensor seen as 4-D {64, H, rows, 2}: the two 64-channel halves of a row
+// become the outermost dimension, so box {64, 1, 16, 2} lands in shared memory as
+// [half][16 rows][64 channels] -- two consecutive swizzled tiles -- in one copy.
+bool encode_halves_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)H, (cuuint64_t)std::max<int64_t>(rows, 1), 2};
+  cuuint64_t strides[3] = {256, (cuuint64_t)(H * 256), 128};
+  cuuint32_t box[4] = {64, 1, 16, 2};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -239,8 +254,8 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
   ChainParams cp;
   std::memset(&cp, 0, sizeof(cp));
   if (rows > 0) {
-    if (!encode_tile_map(&cp.tm_q, q, rows, s.H) || !encode_tile_map(&cp.tm_k, k, rows, s.H) ||
-        !encode_tile_map(&cp.tm_g, g, rows, s.H) || !encode_tile_map(&cp.tm_v, v, rows, s.H))
+    if (!encode_tile_map(&cp.tm_q, q, rows, s.H) || !encode_halves_map(&cp.tm_k, k, rows, s.H) ||
+        !encode_halves_map(&cp.tm_g, g, rows, s.H) || !encode_halves_map(&cp.tm_v, v, rows, s.H))
       return KDA_ERR_CUDA;
   }
   cp.beta = static_cast<const uint16_t*>(beta);

@@ -41,7 +41,8 @@ namespace kda {
 constexpr int kThreads = 256;
 constexpr int kStages = 4;
 constexpr int kWarpProlog0 = 0;       // prologue warps 0-3: two pairs, one pair per chunk
-constexpr int kWarpEpi0 = 4;          // epilogue warps 4-7; lane 0 of warp 4 issues the MMAs and TMA loads
+constexpr int kWarpEpi0 = 4;          // epilogue warps 4-7; lane 0 of warp 4 issues the MMAs
+constexpr int kWarpTma = 5;           // lane 0 of epilogue warp 5 issues the TMA loads
 constexpr uint32_t kBarEpi = 3;       // named barrier of the epilogue warps
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColState = 0;
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   extern __shared__ uint8_t smem_dyn[];
   SmemLayout& S = *reinterpret_cast<SmemLayout*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                  ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t bar_full[kStages], bar_op_full[kStages], bar_op_empty[kStages],
+  __shared__ __align__(8) uint64_t bar_full[kStages], bar_op_full[kStages],
       bar_d1_full[2], bar_d2_full, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
@@ -485,7 +486,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_op_full[i], 2);   // both warps of a prologue pair
-      mbar_init(&bar_op_empty[i], 1);
     }
     mbar_init(&bar_d1_full[0], 1);
     mbar_init(&bar_d1_full[1], 1);
@@ -609,10 +609,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
           mma_ss(d1 + 16, a_lo, aq_hi, id_o, 1);
           mma_ss(d1 + 16, a_hi, aq_lo, id_o, 1);
         }
-        tc_commit(&bar_d2_full);
-        tc_commit(&bar_op_empty[c % kStages]);
+        tc_commit(&bar_d2_full);   // every MMA of chunk c: its stage may be refilled after this
       };
-      // TMA loads of chunk c into stage c % kStages (the leader thread only)
+      // TMA loads of chunk c into stage c % kStages (lane 0 of warp kWarpTma only)
+      const bool tma_thread = (warp == kWarpTma) && (lane == 0);
       const bool load_v = it.mode != kModeTransition;
       int tma_issued = 0;
       auto issue_tma = [&](int c) {
@@ -620,15 +620,15 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         const int row = it.row0 + c * kChunk;
         Stage& st = S.st[s];
         mbar_arrive_expect_tx(&bar_full[s], load_v ? 16384u : 12288u);
-        for (int b = 0; b < 2; ++b) {
-          tma_load_3d(st.X[b] + 2048, &p.tm_q, &bar_full[s], b * 64, it.head, row);
-          tma_load_3d(st.K + b * 2048, &p.tm_k, &bar_full[s], b * 64, it.head, row);
-          tma_load_3d(st.G + b * 2048, &p.tm_g, &bar_full[s], b * 64, it.head, row);
-          if (load_v) tma_load_3d(st.V + b * 2048, &p.tm_v, &bar_full[s], b * 64, it.head, row);
-        }
+        // q: one 64-channel half into each S-side operand tile; k, g, v: both halves at once
+        tma_load_3d(st.X[0] + 2048, &p.tm_q, &bar_full[s], 0, it.head, row);
+        tma_load_3d(st.X[1] + 2048, &p.tm_q, &bar_full[s], 64, it.head, row);
+        tma_load_4d(st.K, &p.tm_k, &bar_full[s], 0, it.head, row, 0);
+        tma_load_4d(st.G, &p.tm_g, &bar_full[s], 0, it.head, row, 0);
+        if (load_v) tma_load_4d(st.V, &p.tm_v, &bar_full[s], 0, it.head, row, 0);
         ++tma_issued;
       };
-      if (leader) {
+      if (tma_thread) {
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_g);
@@ -797,47 +797,44 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
           tc_fence_after();
           const int c1 = c + 1;
           if (mbar_wait(&bar_full[c1 % kStages], (c1 / kStages) & 1, ab)) issue_gemm1(c1);
-          // stage c % kStages is free once the MMAs of chunk c are done (long since, by now)
-          if (c + kStages < nchunks && mbar_wait(&bar_op_empty[c % kStages], (c / kStages) & 1, ab))
-            issue_tma(c + kStages);
         }
+        // stage c % kStages is free: this warp saw every MMA of chunk c complete (bar_d2_full)
+        if (tma_thread && ok && !s_abort && c + kStages < nchunks) issue_tma(c + kStages);
         __syncwarp();
-        // ---- outputs of this chunk (overlaps the next S-side GEMM): through shared
-        //      memory, then 16-byte stores of whole token rows
-        if (with_o) {
-          if (ok) {
-            uint32_t r[16];
-            tmem_ld16(tD1 + 32u * b + 16u, r);
-            tmem_ld_wait();
+        // ---- outputs of this chunk (overlaps the next S-side GEMM): each warp stages its
+        //      32 output columns of the 16 token rows in shared memory, then writes them as
+        //      16-byte pieces, four per row (64 contiguous bytes)
+        if (with_o && ok) {
+          uint32_t r[16];
+          tmem_ld16(tD1 + 32u * b + 16u, r);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              *reinterpret_cast<uint16_t*>(&S.ostage[i][2 * vrow]) =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * __uint_as_float(r[i])));
-          }
-          named_bar(kBarEpi, 128);
-          if (ok) {
-            const int et = threadIdx.x - kWarpEpi0 * 32;     // 0..127
-            const size_t row_elems = (size_t)p.H * kDimV;
-            uint16_t* obase = p.out + ((size_t)(it.row0 + c * kChunk) * p.H + h) * kDimV;
-            if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0) {
+          for (int i = 0; i < 16; ++i)
+            *reinterpret_cast<uint16_t*>(&S.ostage[i][2 * vrow]) =
+                __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * __uint_as_float(r[i])));
+          __syncwarp();
+          const size_t row_elems = (size_t)p.H * kDimV;
+          uint16_t* obase = p.out + ((size_t)(it.row0 + c * kChunk) * p.H + h) * kDimV;
+          if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0) {
 #pragma unroll
-              for (int rr = 0; rr < 2; ++rr) {
-                const int q = et + 128 * rr, i = q >> 4, c16 = q & 15;
-                if (i < nv)
-                  *reinterpret_cast<uint4*>(obase + (size_t)i * row_elems + 8 * c16) =
-                      *reinterpret_cast<const uint4*>(&S.ostage[i][16 * c16]);
-              }
-            } else {
-              for (int i = 0; i < nv; ++i) obase[(size_t)i * row_elems + et] = *reinterpret_cast<const uint16_t*>(&S.ostage[i][2 * et]);
+            for (int rr = 0; rr < 2; ++rr) {
+              const int q = lane + 32 * rr, i = q >> 2, seg = q & 3;
+              if (i < nv)
+                *reinterpret_cast<uint4*>(obase + (size_t)i * row_elems + 32 * q4 + 8 * seg) =
+                    *reinterpret_cast<const uint4*>(&S.ostage[i][64 * q4 + 16 * seg]);
             }
+          } else {
+            for (int i = 0; i < nv; ++i)
+              obase[(size_t)i * row_elems + vrow] = *reinterpret_cast<const uint16_t*>(&S.ostage[i][2 * vrow]);
           }
+          __syncwarp();   // the staging rows are rewritten by the next chunk
         }
       }
       if (leader && s_abort && issued_any) {  // wait for MMAs in flight before TMEM is released
         tc_commit(&bar_drain);
         mbar_wait_drain(&bar_drain, 0);
       }
-      if (leader && s_abort) {  // let loads in flight land before the CTA exits
+      if (tma_thread && s_abort) {  // let loads in flight land before the CTA exits
         for (int c = (tma_issued > kStages ? tma_issued - kStages : 0); c < tma_issued; ++c)
           mbar_wait_drain(&bar_full[c % kStages], (c / kStages) & 1);
       }

@@ -48,7 +48,8 @@ struct ComposeItem {
 };
 
 struct ChainParams {
-  CUtensorMap tm_q, tm_k, tm_g, tm_v;  // 3-D maps over [B*T, H, 128] bf16, box {64, 1, 16}
+  CUtensorMap tm_q;                  // 3-D map over [B*T, H, 128] bf16, box {64, 1, 16}
+  CUtensorMap tm_k, tm_g, tm_v;      // 4-D maps {64, H, B*T, 2 halves}, box {64, 1, 16, 2}
   const uint16_t* beta;                // [B*T, H] bf16 logits
   const float* A_log;                  // [H]
   const float* dt_bias;                // [H, 128]
