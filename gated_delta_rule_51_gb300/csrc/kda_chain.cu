@@ -219,10 +219,6 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
     const int p = 2 * w + pp;
     const int j16 = 4 * (p & 1) + tig;
     const int ch0 = 32 * p + 8 * tig;
-    uint8_t* qb = st.X[p >> 1] + 2048;
-    uint8_t* wb = st.X[p >> 1];
-    uint8_t* kb = st.K + 2048 * (p >> 1);
-    uint8_t* gb = st.G + 2048 * (p >> 1);
     float nrdb[8];
     {
       const float4 d0 = *reinterpret_cast<const float4*>(dtb + ch0);
@@ -230,6 +226,10 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
       nrdb[0] = nr * d0.x; nrdb[1] = nr * d0.y; nrdb[2] = nr * d0.z; nrdb[3] = nr * d0.w;
       nrdb[4] = nr * d1.x; nrdb[5] = nr * d1.y; nrdb[6] = nr * d1.z; nrdb[7] = nr * d1.w;
     }
+    uint8_t* qb = st.X[p >> 1] + 2048;
+    uint8_t* wb = st.X[p >> 1];
+    uint8_t* kb = st.K + 2048 * (p >> 1);
+    uint8_t* gb = st.G + 2048 * (p >> 1);
     float q[2][8], k[2][8], G[2][8];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
@@ -520,8 +520,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       const int h = it.head;
       const int H = p.H;
       const float nr = -expf(p.A_log[h]) * kLog2e;
-      const float lbl2 = p.lower_bound * kLog2e;
       const float* dtb = p.dt_bias + (size_t)h * kDimK;
+      const float lbl2 = p.lower_bound * kLog2e;
       const int gid = lane >> 2;
       auto load_beta = [&](int c, float& b0, float& b1) {
         const int base = it.row0 + c * kChunk;
@@ -572,16 +572,20 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       constexpr uint64_t kSmallStep = sizeof(StageSmall) >> 4;
       const Stage& s0 = S.st[0];
       const StageSmall& m0 = S.sm[0];
-      // U and the S-side GEMM of chunk c into D1[c & 1] (the leader thread only)
-      auto issue_gemm1 = [&](int c) {
+      // U = V^T Tm^T of chunk c into D1[c & 1] (the leader thread only)
+      auto issue_u = [&](int c) {
         const uint64_t so = (uint64_t)(c % kStages) * kStageStep;
         const uint64_t sso = (uint64_t)(c % kStages) * kSmallStep;
         const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
-        if (with_u) {
-          const uint64_t d_v = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
-          mma_ss(d1, d_v, smem_desc(smem_u32(m0.TPhi), 128, 256, kSwizzleNone) + sso, id_u, 0);
-          mma_ss(d1, d_v, smem_desc(smem_u32(m0.TPlo), 128, 256, kSwizzleNone) + sso, id_u, 1);
-        }
+        const uint64_t d_v = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
+        mma_ss(d1, d_v, smem_desc(smem_u32(m0.TPhi), 128, 256, kSwizzleNone) + sso, id_u, 0);
+        mma_ss(d1, d_v, smem_desc(smem_u32(m0.TPlo), 128, 256, kSwizzleNone) + sso, id_u, 1);
+      };
+      // U, then the S-side GEMM of chunk c into D1[c & 1]
+      auto issue_gemm1 = [&](int c) {
+        const uint64_t so = (uint64_t)(c % kStages) * kStageStep;
+        const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
+        if (with_u) issue_u(c);
         const uint64_t d_x0 = smem_desc(smem_u32(s0.X[0]), 16, 1024, kSwizzle128B) + so;
         const uint64_t d_x1 = smem_desc(smem_u32(s0.X[1]), 16, 1024, kSwizzle128B) + so;
 #pragma unroll
@@ -760,10 +764,14 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
 #pragma unroll
               for (int t = 0; t < 8; ++t) {
                 const float4 gm = *reinterpret_cast<const float4*>(&stn.gamC[32 * j + 4 * t]);
-                r[4 * t] = __float_as_uint(__uint_as_float(r[4 * t]) * gm.x);
-                r[4 * t + 1] = __float_as_uint(__uint_as_float(r[4 * t + 1]) * gm.y);
-                r[4 * t + 2] = __float_as_uint(__uint_as_float(r[4 * t + 2]) * gm.z);
-                r[4 * t + 3] = __float_as_uint(__uint_as_float(r[4 * t + 3]) * gm.w);
+                float a0 = __uint_as_float(r[4 * t]), a1 = __uint_as_float(r[4 * t + 1]);
+                float a2 = __uint_as_float(r[4 * t + 2]), a3 = __uint_as_float(r[4 * t + 3]);
+                fmul2(a0, a1, gm.x, gm.y);
+                fmul2(a2, a3, gm.z, gm.w);
+                r[4 * t] = __float_as_uint(a0);
+                r[4 * t + 1] = __float_as_uint(a1);
+                r[4 * t + 2] = __float_as_uint(a2);
+                r[4 * t + 3] = __float_as_uint(a3);
               }
               tmem_st32(tS + 32u * j, r);
             } else if (it.out_slot >= 0) {
