@@ -40,13 +40,19 @@ kda_status device_info(DeviceInfo* out) {
 // when there are too few chains to fill the GPU, long sequences are cut into
 // segments so that about one wave of forward work items exists.  Segments are
 // at least 512 tokens; the value is a multiple of 16.
+// Segment length set through the environment (tests and tuning), else 0.
+int64_t forced_seg_tokens() {
+  const char* env = std::getenv("KDA_SEG_TOKENS");
+  if (env == nullptr) return 0;
+  const long long v = std::atoll(env);
+  return v >= 16 ? (v + 15) / 16 * 16 : 0;
+}
+
+// Upper bound on the segment length the schedule kernel uses (it never cuts
+// shorter, so the work-list capacities sized from this bound always suffice).
 int64_t choose_seg_tokens(const kda_shape& s, int sms) {
   const int64_t rows = s.B * s.T;
-  const char* env = std::getenv("KDA_SEG_TOKENS");
-  if (env != nullptr) {
-    const long long v = std::atoll(env);
-    if (v >= 16) return std::max<int64_t>(16, (v + 15) / 16 * 16);
-  }
+  if (const int64_t f = forced_seg_tokens()) return f;
   const int64_t resident = 2 * (int64_t)std::max(sms, 1);   // CTAs resident at once
   const int64_t chains = s.N * s.H;
   const int64_t no_split = std::max<int64_t>(16, (rows + 15) / 16 * 16);
@@ -236,6 +242,8 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
   sp.H = s.H;
   sp.N = s.N;
   sp.seg_tokens = (int)L.seg_tokens;
+  sp.seg_forced = forced_seg_tokens() != 0;
+  sp.resident = 2 * (long long)std::max(d.sms, 1);
   sp.has_init = initial_state != nullptr;
   sp.has_final = final_state != nullptr;
   sp.hdr = hdr;

@@ -66,11 +66,49 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
   __shared__ long long s_seg0[kSchedThreads], s_q0[kSchedThreads];
   __shared__ int s_c0[kSchedThreads];
   __shared__ int s_err;
+  __shared__ unsigned long long s_max_chunks, s_sum_chunks;
+  __shared__ long long s_L;
   const int tid = threadIdx.x;
   const long long H = p.H;
-  const long long L = p.seg_tokens;
   const long long total_rows = p.B * p.T;
-  if (tid == 0) s_err = 0;
+  if (tid == 0) {
+    s_err = 0;
+    s_max_chunks = 0;
+    s_sum_chunks = 0;
+  }
+  __syncthreads();
+  // Split long sequences only when one of them would outlast the rest of the
+  // work by a wide margin: a split run costs a second pass over its tokens
+  // (local state, transition), so with the longest sequence within 3x the mean
+  // load of a resident CTA the unsplit chains finish first.
+  if (!p.seg_forced && p.seg_tokens < total_rows) {
+    unsigned long long mx = 0, sum = 0;
+    for (long long n = tid; n < p.N; n += kSchedThreads) {
+      long long len = p.T;
+      if (p.cu_seqlens) {
+        long long a = p.cu_seqlens[n], b = p.cu_seqlens[n + 1];
+        a = a < 0 ? 0 : (a > total_rows ? total_rows : a);
+        b = b < a ? a : (b > total_rows ? total_rows : b);
+        len = b - a;
+      }
+      const unsigned long long c = (unsigned long long)((len + 15) / 16);
+      mx = c > mx ? c : mx;
+      sum += c;
+    }
+    atomicMax(&s_max_chunks, mx);
+    atomicAdd(&s_sum_chunks, sum);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    long long Lx = p.seg_tokens;
+    if (!p.seg_forced && p.seg_tokens < total_rows) {
+      const long long per_cta = ((long long)s_sum_chunks * H + p.resident - 1) / p.resident;
+      if ((long long)s_max_chunks <= 3 * per_cta) Lx = (total_rows + 15) / 16 * 16;   // no split
+    }
+    s_L = Lx;
+  }
+  __syncthreads();
+  const long long L = s_L;
   long long q_total = 0;
   for (int pass = 0; pass < 2; ++pass) {
     if (tid == 0) s_tot[0] = s_tot[1] = s_tot[2] = 0;

@@ -77,6 +77,8 @@ struct ScheduleParams {
   const int64_t* cu_seqlens;  // null: fixed-length rows of T tokens
   int64_t B, T, H, N;
   int seg_tokens;             // maximum tokens per segment (multiple of 16)
+  int seg_forced;             // seg_tokens was set by the caller: split at it, whatever the lengths
+  long long resident;         // chain CTAs resident on the device at once
   int has_init;
   int has_final;
   WorkHeader* hdr;
