@@ -209,6 +209,24 @@ def cpu_oracle_sample(w, x_cpu, budget_s: float = 15.0):
     return tokens_per_s, threads, desc, dt
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's value (timings: the job ends with its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: int, world: int, steps: int, max_ms: float) -> float:
+    """Units per second of the whole job: every rank runs its own replica of the workload
+    (weak scaling), so the job processes world x steps x units in the slowest rank's time."""
+    return units_per_rank_step * world * steps / (max_ms / 1000.0)
+
+
 def run_reference(args, w):
     """--impl reference: the fp64 oracle on the host cores, timed per step on a bounded sample."""
     if int(os.environ.get("RANK", "0")) != 0:
@@ -303,13 +321,9 @@ def run_ours(args, w):
     ph1_ms = [e[1].elapsed_time(e[2]) for e in ev]
     cmp_ms = [e[2].elapsed_time(e[3]) for e in ev]
     sch_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     tokens = w.B * w.T
-    value = tokens * world * args.steps / (total_ms / 1000.0)
+    value = whole_job_rate(tokens, world, args.steps, total_ms)
     ms_per_step = total_ms / args.steps
 
     # end to end through the public API with pinned host buffers
@@ -346,12 +360,8 @@ def run_ours(args, w):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": tokens * world * args.steps / (e2e_ms / 1000.0), "unit": "tokens/s",
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": whole_job_rate(tokens, world, args.steps, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
         del host, dev_in
     if kda.check_device_error(ws, dev):
