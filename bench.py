@@ -37,7 +37,8 @@ BYTES_PER_TOKEN_HEAD = 4 * 128 * 2 + 2 + 128 * 2      # q, k, v, g + beta + out 
 FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 6 * 16 * 128 + 4 * 16 * 128   # 16-token chunked form
 L2_BYTES = 126 * 1024 * 1024
 ALIASES = {"tiny": "tiny_B1_T64_H1", "fixed": "fixed_B2_T4096_H16",
-           "varlen": "varlen_T32768_N8_H32", "long": "long_T1048576_H8"}
+           "varlen": "varlen_T32768_N8_H32", "long": "long_T1048576_H8", "decode": "decode_B256_T1_H32"}
+DECODE_METRIC = "KDA decode tokens/s and % of HBM roofline on 1xGB300"
 
 
 def workload(name):
@@ -407,6 +408,101 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_decode(args, w):
+    """The recurrent decode step (kda_decode): every call reads and writes each
+    (sequence, head) state once; timed per call with CUDA events."""
+    import torch
+
+    from gated_delta_rule_51_gb300 import inputs as I
+    from gated_delta_rule_51_gb300 import kda
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    kda.load_library()
+    x = I.make_inputs(w, device=dev)
+    state = x["initial_state"].clone()
+    out = torch.empty_like(x["v"])
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(xx):
+        kda.decode(xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], xx["scale"], out, xx["A_log"],
+                   xx["dt_bias"], xx["lower_bound"], state)
+
+    for _ in range(args.warmup):
+        step(x)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            step(x)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world, dev)
+    tokens = w.B * w.T
+    value = whole_job_rate(tokens, world, args.steps, total_ms)
+    ms = total_ms / args.steps
+    state_bytes = w.B * w.H * 128 * 128 * (4 if w.state_dtype == torch.float32 else 2) * 2
+    nbytes = state_bytes + w.token_heads * BYTES_PER_TOKEN_HEAD + w.H * (4 + 128 * 4)
+    hbm_gbs, _, peak_kind = load_peaks()
+    achieved = nbytes / (ms / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+                "traffic": None, "kernel": "kda_decode_kernel",
+                "peak_source": "measured, MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": nbytes}
+
+    e2e = None
+    if not args.no_e2e:
+        names = ("q", "k", "v", "g", "beta")
+        host = {n: x[n].cpu().pin_memory() for n in names}
+        dev_in = dict(x)
+        dev_in.update({n: torch.empty_like(x[n]) for n in names})
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = h_out.numel() * h_out.element_size()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for n in names:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            step(dev_in)
+            h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": whole_job_rate(tokens, world, args.steps, e2e_ms), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "note": "states stay resident on the device between steps"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x_cpu = {n: (t.cpu() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+        v, threads, desc, _ = cpu_oracle_sample(w, x_cpu, budget_s=15.0)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        line = {"metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": config_dict(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                          "l2": "flushed between timed steps (252 MB write); states 4x L2"}),
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks.summary(), "e2e": e2e,
+                "gpu_launches": args.steps}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,6 +516,8 @@ def main():
     w = workload(args.config)
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.name.startswith("decode"):
+        run_decode(args, w)
     else:
         run_ours(args, w)
 

@@ -36,10 +36,6 @@ kda_status device_info(DeviceInfo* out) {
   return KDA_OK;
 }
 
-// Tokens per segment.  A (sequence, head) chain is sequential over its chunks;
-// when there are too few chains to fill the GPU, long sequences are cut into
-// segments so that about one wave of forward work items exists.  Segments are
-// at least 512 tokens; the value is a multiple of 16.
 // Segment length set through the environment (tests and tuning), else 0.
 int64_t forced_seg_tokens() {
   const char* env = std::getenv("KDA_SEG_TOKENS");
@@ -48,8 +44,12 @@ int64_t forced_seg_tokens() {
   return v >= 16 ? (v + 15) / 16 * 16 : 0;
 }
 
-// Upper bound on the segment length the schedule kernel uses (it never cuts
-// shorter, so the work-list capacities sized from this bound always suffice).
+// Tokens per segment.  A (sequence, head) chain is sequential over its chunks;
+// when there are too few chains to fill the GPU, long sequences are cut into
+// segments so that about one wave of forward work items exists.  Segments are
+// at least 512 tokens; the value is a multiple of 16.  This is an upper bound on
+// the length the schedule kernel uses (it never cuts shorter, so the work-list
+// capacities sized from it always suffice).
 int64_t choose_seg_tokens(const kda_shape& s, int sms) {
   const int64_t rows = s.B * s.T;
   if (const int64_t f = forced_seg_tokens()) return f;
@@ -179,6 +179,49 @@ kda_status kda_workspace_size(const kda_shape* shape, size_t* bytes) {
   DeviceInfo d;
   if (device_info(&d) != KDA_OK) d.sms = 152;   // sizing only; kda_fwd checks the device
   *bytes = make_layout(*shape, d.sms).total;
+  return KDA_OK;
+}
+
+kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, const void* v, const void* g,
+                      const void* beta, float scale, void* out, const float* A_log, const float* dt_bias,
+                      float lower_bound, void* state, kda_state_dtype state_dtype, kda_stream_t stream_) {
+  kda_status st = check_shape(shape);
+  if (st != KDA_OK) return st;
+  const kda_shape s = *shape;
+  if (s.N != s.B) return KDA_ERR_INVALID_ARGUMENT;
+  if ((long long)s.B * s.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
+  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
+  auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  if (s.B * s.T > 0) {
+    const void* tok[] = {q, k, v, g, beta, out};
+    for (const void* p : tok)
+      if (p == nullptr || !aligned(p, 2)) return KDA_ERR_INVALID_ARGUMENT;
+  }
+  if (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned(dt_bias, 4))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32) return KDA_ERR_INVALID_ARGUMENT;
+  if (s.B > 0 && (state == nullptr || !aligned16(state))) return KDA_ERR_INVALID_ARGUMENT;
+  DeviceInfo d;
+  if (device_info(&d) != KDA_OK) return KDA_ERR_CUDA;
+  if (d.major != 10 || d.minor != 3) return KDA_ERR_UNSUPPORTED_DEVICE;
+  DecodeParams dp;
+  dp.q = static_cast<const uint16_t*>(q);
+  dp.k = static_cast<const uint16_t*>(k);
+  dp.v = static_cast<const uint16_t*>(v);
+  dp.g = static_cast<const uint16_t*>(g);
+  dp.beta = static_cast<const uint16_t*>(beta);
+  dp.out = static_cast<uint16_t*>(out);
+  dp.A_log = A_log;
+  dp.dt_bias = dt_bias;
+  dp.state = state;
+  dp.state_dtype = state_dtype == KDA_STATE_FP32 ? 2 : 1;
+  dp.B = (int)s.B;
+  dp.T = (int)s.T;
+  dp.H = (int)s.H;
+  dp.scale = scale;
+  dp.lower_bound = lower_bound;
+  if (launch_decode(dp, reinterpret_cast<cudaStream_t>(stream_)) != cudaSuccess) return KDA_ERR_CUDA;
   return KDA_OK;
 }
 

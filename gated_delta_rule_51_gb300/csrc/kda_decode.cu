@@ -1,0 +1,147 @@
+// kda_decode.cu -- the recurrent step of KDA for decoding: a few tokens per
+// sequence, the state read from and written back to HBM once per call.
+//
+// Per (sequence n, head h) and token t, with K = V = 128 and the state kept as
+// S^T (row v holds S[:, v] over the 128 key channels k), the step is the KDA
+// recurrence itself (FlashKDA README "Kernel API" parameter table for the
+// inputs, gate and layout):
+//   ghat  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h, :]))
+//   beta  = sigmoid(beta logit);   qh, kh = x / sqrt(|x|^2 + 1e-6)
+//   row v of S^T:  s <- s * exp(ghat);  s <- s + beta (v_v - s . kh) kh
+//   o_v   = scale * s . qh        (from the updated row)
+// Rows are independent, so the work is bandwidth-bound: one CTA per (n, h),
+// eight warps with sixteen rows each, every lane holding four key channels of
+// each of its rows in registers for all the call's tokens.  The state is read
+// once (64 KiB fp32 or 32 KiB bf16) and written once.
+#include <cuda_bf16.h>
+
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kDecThreads = 256;
+constexpr int kRowsPerWarp = 16;
+
+__device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  return x;
+}
+
+// every lane ends with the full sums of all sixteen rows
+__device__ __forceinline__ void warp_sum16(float (&x)[kRowsPerWarp]) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) x[r] += __shfl_xor_sync(0xffffffffu, x[r], m);
+}
+
+__device__ __forceinline__ float sigmoidf(float x) { return 1.f / (1.f + expf(-x)); }
+
+__global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeParams p) {
+  const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ __align__(16) float s_alpha[128], s_kh[128], s_qh[128], s_v[128];
+  __shared__ float s_norm[2][4];
+  __shared__ float s_beta;
+
+  // ---- the state rows of this warp, four key channels per lane
+  const size_t head = (size_t)n * p.H + h;
+  float4 st[kRowsPerWarp];
+  if (p.state_dtype == 2) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.state) + head * 16384);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) st[r] = src[(kRowsPerWarp * warp + r) * 32 + lane];
+  } else {
+    const uint2* src = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.state) + head * 16384);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const uint2 w = src[(kRowsPerWarp * warp + r) * 32 + lane];
+      st[r] = make_float4(bf(w.x & 0xffffu), bf(w.x >> 16), bf(w.y & 0xffffu), bf(w.y >> 16));
+    }
+  }
+  const float rate = expf(p.A_log[h]);
+
+#pragma unroll 1
+  for (int t = 0; t < p.T; ++t) {
+    const size_t tok = ((size_t)n * p.T + t) * p.H + h;   // row of [B*T, H]
+    // ---- per-channel vectors of this token (threads 0-127, channel = tid)
+    float kk = 0.f, qq = 0.f;
+    if (tid < 128) {
+      const float gt = bf(p.g[tok * 128 + tid]);
+      const float ghat = p.lower_bound * sigmoidf(rate * (gt + p.dt_bias[(size_t)h * 128 + tid]));
+      s_alpha[tid] = expf(ghat);
+      kk = bf(p.k[tok * 128 + tid]);
+      qq = bf(p.q[tok * 128 + tid]);
+      s_v[tid] = bf(p.v[tok * 128 + tid]);
+      const float sk = warp_sum(kk * kk), sq = warp_sum(qq * qq);
+      if (lane == 0) {
+        s_norm[0][warp] = sk;
+        s_norm[1][warp] = sq;
+      }
+    }
+    if (tid == 0) s_beta = sigmoidf(bf(p.beta[tok]));
+    __syncthreads();
+    if (tid < 128) {
+      const float nk = s_norm[0][0] + s_norm[0][1] + s_norm[0][2] + s_norm[0][3];
+      const float nq = s_norm[1][0] + s_norm[1][1] + s_norm[1][2] + s_norm[1][3];
+      s_kh[tid] = kk / sqrtf(nk + 1e-6f);
+      s_qh[tid] = qq / sqrtf(nq + 1e-6f);
+    }
+    __syncthreads();
+    // ---- the rows: decay, delta update, output from the updated row
+    const float4 al = reinterpret_cast<const float4*>(s_alpha)[lane];
+    const float4 kh = reinterpret_cast<const float4*>(s_kh)[lane];
+    const float4 qh = reinterpret_cast<const float4*>(s_qh)[lane];
+    const float beta = s_beta;
+    float d[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      st[r].x *= al.x; st[r].y *= al.y; st[r].z *= al.z; st[r].w *= al.w;
+      d[r] = st[r].x * kh.x + st[r].y * kh.y + st[r].z * kh.z + st[r].w * kh.w;
+    }
+    warp_sum16(d);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const float c = beta * (s_v[kRowsPerWarp * warp + r] - d[r]);
+      st[r].x = fmaf(c, kh.x, st[r].x); st[r].y = fmaf(c, kh.y, st[r].y);
+      st[r].z = fmaf(c, kh.z, st[r].z); st[r].w = fmaf(c, kh.w, st[r].w);
+      d[r] = st[r].x * qh.x + st[r].y * qh.y + st[r].z * qh.z + st[r].w * qh.w;
+    }
+    warp_sum16(d);
+    if (lane < kRowsPerWarp) {
+      float o = d[0];
+#pragma unroll
+      for (int r = 1; r < kRowsPerWarp; ++r) o = lane == r ? d[r] : o;
+      p.out[tok * 128 + kRowsPerWarp * warp + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * o));
+    }
+    __syncthreads();   // the per-channel vectors are rewritten by the next token
+  }
+
+  // ---- write the rows back
+  if (p.state_dtype == 2) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.state) + head * 16384);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) dst[(kRowsPerWarp * warp + r) * 32 + lane] = st[r];
+  } else {
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.state) + head * 16384);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r)
+      dst[(kRowsPerWarp * warp + r) * 32 + lane] = make_uint2(pack_bf16x2(st[r].x, st[r].y), pack_bf16x2(st[r].z, st[r].w));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+  const long long grid = (long long)p.B * p.H;
+  if (grid <= 0 || p.T <= 0) return cudaSuccess;
+  kda_decode_kernel<<<(unsigned)grid, kDecThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -88,10 +88,22 @@ struct ScheduleParams {
   long long cap_phase1, cap_forward, cap_compose, cap_slots;
 };
 
+struct DecodeParams {
+  const uint16_t *q, *k, *v, *g, *beta;  // bf16 [B, T, H, 128] (beta [B, T, H], logits)
+  uint16_t* out;                          // bf16 [B, T, H, 128]
+  const float* A_log;                     // [H]
+  const float* dt_bias;                   // [H, 128]
+  void* state;                            // [B, H, 128 (v), 128 (k)], read and written in place
+  int state_dtype;                        // 1 bf16, 2 fp32
+  int B, T, H;
+  float scale, lower_bound;
+};
+
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_compose(const ComposeParams& p, int grid, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 size_t chain_smem_bytes();
 
 }  // namespace kda

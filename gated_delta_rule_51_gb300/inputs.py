@@ -97,6 +97,12 @@ def long_workload() -> Workload:
     return Workload("long_T1048576_H8", 1, 1 << 20, 8, None, torch.float32, False, True, -1.0, 3)
 
 
+def decode_workload() -> Workload:
+    """One decoding step of a serving batch: B=256 sequences x T=1 token, H=32, fp32 states
+    read and written in place (512 MiB, four times L2); lower_bound -5."""
+    return Workload("decode_B256_T1_H32", 256, 1, 32, None, torch.float32, True, True, -5.0, 5)
+
+
 SWEEP_TOTALS = (8192, 32768, 131072, 262144)
 SWEEP_HEADS = (32, 64)
 
@@ -119,7 +125,7 @@ def custom_workload(name: str, B: int, T: int, H: int, seq_lens=None, state_dtyp
 
 def named_workloads() -> Dict[str, Workload]:
     out = {w.name: w for w in (tiny_workload(), fixed_batch_workload(), varlen_workload(),
-                               long_workload())}
+                               long_workload(), decode_workload())}
     for total in SWEEP_TOTALS:
         for H in SWEEP_HEADS:
             w = sweep_workload(total, H)

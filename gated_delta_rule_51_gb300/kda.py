@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPOR
                 3: "KDA_ERR_WORKSPACE_TOO_SMALL", 4: "KDA_ERR_UNSUPPORTED_DEVICE", 5: "KDA_ERR_CUDA",
                 6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_BAD_SEQLENS"}
 EXPORTED_SYMBOLS = ("kda_status_string", "kda_workspace_size", "kda_fwd", "kda_check_device_error",
-                    "kda_set_profile_events", "kda_last_launch_count")
+                    "kda_set_profile_events", "kda_last_launch_count", "kda_fwd_static_workspace",
+                    "kda_decode")
 
 
 class kda_shape(ctypes.Structure):
@@ -68,6 +69,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_set_profile_events.restype = ctypes.c_int
         lib.kda_last_launch_count.argtypes = []
         lib.kda_last_launch_count.restype = ctypes.c_int
+        lib.kda_decode.argtypes = [ctypes.POINTER(kda_shape), p, p, p, p, p, ctypes.c_float, p, p, p,
+                                   ctypes.c_float, p, ctypes.c_int, p]
+        lib.kda_decode.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -167,6 +171,38 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
     if st != KDA_OK:
         raise KDAError(st, "kda_fwd")
     return out, final_state
+
+
+def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
+           stream: Optional[torch.cuda.Stream] = None):
+    """Recurrent KDA step(s) for decoding; updates ``state`` in place, writes ``out``.
+
+    q, k, g, v, out: [B,T,H,128] bf16 (T new tokens per sequence, usually 1);
+    beta: [B,T,H] bf16 logits; A_log: [H] fp32; dt_bias: [H,128] fp32;
+    state: [B,H,128,128] bf16 or fp32, read before the first token and overwritten.
+    """
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda.decode runs on CUDA tensors only")
+    for name, t, dt, shp in (("q", q, torch.bfloat16, (B, T, H, K)), ("k", k, torch.bfloat16, (B, T, H, K)),
+                             ("g", g, torch.bfloat16, (B, T, H, K)), ("v", v, torch.bfloat16, (B, T, H, K)),
+                             ("out", out, torch.bfloat16, (B, T, H, K)),
+                             ("beta", beta, torch.bfloat16, (B, T, H)),
+                             ("A_log", A_log, torch.float32, (H,)), ("dt_bias", dt_bias, torch.float32, (H, K))):
+        _check(t, name, dt, shp, dev)
+    _check(state, "state", state.dtype, (B, H, K, K), dev)
+    lib = load_library()
+    shape = make_shape(B, T, H, B, K, K)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = lib.kda_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                        ctypes.c_float(scale), _ptr(out), _ptr(A_log), _ptr(dt_bias), ctypes.c_float(lower_bound),
+                        _ptr(state), _state_code(state), ctypes.c_void_p(s.cuda_stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode")
+    return out, state
 
 
 def check_device_error(workspace: Optional[torch.Tensor] = None, device=None) -> int:

@@ -170,6 +170,27 @@ KDA_API kda_status kda_fwd_static_workspace(const kda_shape *shape, const void *
                                             kda_state_dtype final_dtype, const int64_t *cu_seqlens,
                                             kda_stream_t stream);
 
+/*
+ * The recurrent step for decoding (no counterpart in flash_kda.fwd): the same
+ * recurrence as kda_fwd, token by token, for B sequences of T tokens each
+ * (T = 1 for one decoding step), with the state updated IN PLACE.  Every
+ * (sequence, head) state is read from HBM once and written back once per call,
+ * whatever T is; no workspace is needed.
+ *   shape            : B sequences, T >= 0 tokens each, H heads, K = V = 128, N = B.
+ *   q, k, v, g, beta : bf16 [B, T, H, 128] (beta [B, T, H], logits), 2-byte aligned.
+ *   out              : bf16 [B, T, H, V], written for every token, 2-byte aligned.
+ *   A_log, dt_bias, lower_bound, scale : as for kda_fwd.
+ *   state            : [B, H, V, K] of state_dtype (bf16 or fp32), 16-byte aligned;
+ *                      read as the state before the first token and overwritten with
+ *                      the state after the last (a bf16 state is rounded once, at the
+ *                      end of the call).  T = 0 leaves it untouched.
+ * Returns KDA_OK once the kernel is enqueued; argument errors as for kda_fwd.
+ */
+KDA_API kda_status kda_decode(const kda_shape *shape, const void *q, const void *k, const void *v,
+                              const void *g, const void *beta, float scale, void *out, const float *A_log,
+                              const float *dt_bias, float lower_bound, void *state,
+                              kda_state_dtype state_dtype, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

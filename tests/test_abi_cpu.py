@@ -97,3 +97,30 @@ def test_python_binding_requires_cuda_tensors():
     with pytest.raises(ValueError):
         kda.fwd(q, q, q, q, torch.zeros(1, 16, 1, dtype=torch.bfloat16), 0.1, q.clone(),
                 torch.zeros(1), torch.zeros(1, 128), -1.0)
+
+
+def _decode_call(shape, q=FAKE, out=FAKE, A_log=FAKE, state=FAKE, dtype=2, lb=-1.0):
+    lib = kda.load_library()
+    p = lambda a: ctypes.c_void_p(a) if a else None
+    return lib.kda_decode(ctypes.byref(shape), p(q), p(FAKE), p(FAKE), p(FAKE), p(FAKE), ctypes.c_float(0.1),
+                          p(out), p(A_log), p(FAKE), ctypes.c_float(lb), p(state), dtype, None)
+
+
+@pytest.mark.parametrize("case,expected", [
+    (dict(shape=kda.make_shape(4, 1, 2, 4, K=64)), 2),
+    (dict(shape=kda.make_shape(4, 1, 2, 3)), 1),                     # N must equal B
+    (dict(shape=kda.make_shape(4, 1, 2, 4), lb=0.25), 1),            # lower_bound in [-5, 0]
+    (dict(shape=kda.make_shape(4, 1, 2, 4), state=0), 1),            # the state is required
+    (dict(shape=kda.make_shape(4, 1, 2, 4), state=FAKE + 8), 1),     # and 16-byte aligned
+    (dict(shape=kda.make_shape(4, 1, 2, 4), dtype=0), 1),            # with a dtype
+    (dict(shape=kda.make_shape(4, 1, 2, 4), q=0), 1),
+    (dict(shape=kda.make_shape(4, 1, 2, 4), out=FAKE + 1), 1),       # 2-byte aligned tokens
+    (dict(shape=kda.make_shape(4, 1, 2, 4), A_log=FAKE + 2), 1),
+])
+def test_decode_host_side_argument_errors(case, expected):
+    shape = case.pop("shape")
+    assert _decode_call(shape, **case) == expected
+
+
+def test_decode_valid_arguments_reach_the_device_query():
+    assert _decode_call(kda.make_shape(4, 1, 2, 4), q=FAKE + 2, out=FAKE + 6) in (4, 5)
