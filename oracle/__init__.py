@@ -47,7 +47,7 @@ def _load():
             lib = ctypes.CDLL(build())
             fn = lib.kda_oracle_fwd
             i64, p = ctypes.c_int64, ctypes.c_void_p
-            fn.argtypes = [i64, i64, i64, i64, i64, i64, p, p, p, p, p, ctypes.c_double, p, p,
+            fn.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.c_int, p, p, p, p, p, ctypes.c_double, p, p,
                            ctypes.c_double, p, p, p, p, p, ctypes.c_int]
             fn.restype = ctypes.c_int
             _lib = lib
@@ -91,7 +91,8 @@ def _ptr(a: Optional[np.ndarray]):
 
 def kda_forward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None,
                 cu_seqlens=None, out_rows=None, want_out=True, want_final_state=True,
-                nthreads: Optional[int] = None):
+                nthreads: Optional[int] = None, use_gate_in_kernel: bool = True,
+                use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True):
     """Run the fp64 token recurrence.
 
     q, k, g: [B,T,H,K] bf16; v: [B,T,H,V] bf16; beta: [B,T,H] bf16 (torch
@@ -101,6 +102,9 @@ def kda_forward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_st
     out_rows: optional sorted token-row indices (over B*T) whose outputs are
     wanted; default all rows.  Returns (out [rows,H,V] fp64 or None,
     final_state [N,H,V,K] fp64 or None).
+    The three use_* switches mirror the reference call's flags: when False, g
+    already holds the natural-log decay (A_log, dt_bias and lower_bound are then
+    unused), beta already holds beta, or q and k are used without L2 norms.
     """
     qb, kb, vb, gb, bb = (_bits(x) for x in (q, k, v, g, beta))
     B, T, H, K = qb.shape
@@ -128,7 +132,9 @@ def kda_forward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_st
     fin = np.zeros((N, H, V, K), dtype=np.float64) if want_final_state else None
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    rc = _load().kda_oracle_fwd(B, T, H, K, V, N, _ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb),
+    flags = ((0 if use_gate_in_kernel else 1) | (0 if use_beta_sigmoid_in_kernel else 2)
+             | (0 if use_qk_l2norm_in_kernel else 4))
+    rc = _load().kda_oracle_fwd(B, T, H, K, V, N, flags, _ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb),
                                 _ptr(bb), float(np.float32(scale)), _ptr(A), _ptr(D),
                                 float(np.float32(lower_bound)), _ptr(s0), _ptr(out),
                                 _ptr(row_map), _ptr(fin), _ptr(cu), int(nthreads))

@@ -17,6 +17,14 @@
  *   and the final S is written transposed, final[n,h,v,c] = S[c][v]
  *   (README: state shape [B,H,V,K] / [N,H,V,K], FLA transpose_state_layout).
  *
+ * Three switches follow the flags of the pages' reference call (chunk_kda's
+ * use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel), each
+ * set in `flags` when the step is NOT done here:
+ *   ORACLE_GATE_PREACTIVATED (1): g already holds ghat (natural-log decay), so
+ *       alpha_t = exp(g_t); A_log, dt_bias and lower_bound are not used;
+ *   ORACLE_BETA_PREACTIVATED (2): beta already holds beta_t (no sigmoid);
+ *   ORACLE_NO_QK_L2NORM      (4): qh = q_t and kh = k_t as given.
+ *
  * Readings where the pages are silent: the gate is a sigmoid scaled by the
  * lower bound (README "safe_gate", "Gate lower bound (range from -5.0 to 0)");
  * the L2-norm epsilon is 1e-6 inside the square root; scale is applied after
@@ -44,8 +52,11 @@ static double bf16_to_double(uint16_t bits) {
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
+enum { ORACLE_GATE_PREACTIVATED = 1, ORACLE_BETA_PREACTIVATED = 2, ORACLE_NO_QK_L2NORM = 4 };
+
 typedef struct {
     int64_t B, T, H, K, V, N;
+    int flags;
     const uint16_t *q, *k, *v, *g, *beta;
     double scale, lower_bound;
     const float *A_log, *dt_bias;
@@ -78,7 +89,8 @@ static void run_pair(oracle_job *J, int64_t n, int64_t h, double *S, double *qh,
     } else {
         memset(S, 0, sizeof(double) * (size_t)(K * V));
     }
-    const double rate = exp((double)J->A_log[h]);
+    const int gate_pre = J->flags & ORACLE_GATE_PREACTIVATED;
+    const double rate = gate_pre ? 0.0 : exp((double)J->A_log[h]);
     for (int64_t t = t0; t < t1; ++t) {
         const uint16_t *qt = J->q + (t * H + h) * K;
         const uint16_t *kt = J->k + (t * H + h) * K;
@@ -91,14 +103,20 @@ static void run_pair(oracle_job *J, int64_t n, int64_t h, double *S, double *qh,
             qq += qh[c] * qh[c];
             kk += kh[c] * kh[c];
         }
-        const double qinv = 1.0 / sqrt(qq + 1e-6), kinv = 1.0 / sqrt(kk + 1e-6);
+        const int norm = !(J->flags & ORACLE_NO_QK_L2NORM);
+        const double qinv = norm ? 1.0 / sqrt(qq + 1e-6) : 1.0, kinv = norm ? 1.0 / sqrt(kk + 1e-6) : 1.0;
         for (int64_t c = 0; c < K; ++c) {
             qh[c] *= qinv;
             kh[c] *= kinv;
-            double x = rate * (bf16_to_double(gt[c]) + (double)J->dt_bias[h * K + c]);
-            alpha[c] = exp(J->lower_bound * sigmoid(x));
+            if (gate_pre) {
+                alpha[c] = exp(bf16_to_double(gt[c]));
+            } else {
+                double x = rate * (bf16_to_double(gt[c]) + (double)J->dt_bias[h * K + c]);
+                alpha[c] = exp(J->lower_bound * sigmoid(x));
+            }
         }
-        const double b = sigmoid(bf16_to_double(J->beta[t * H + h]));
+        const double braw = bf16_to_double(J->beta[t * H + h]);
+        const double b = (J->flags & ORACLE_BETA_PREACTIVATED) ? braw : sigmoid(braw);
         /* decay */
         for (int64_t c = 0; c < K; ++c)
             for (int64_t j = 0; j < V; ++j) S[c * V + j] *= alpha[c];
@@ -153,9 +171,10 @@ static void *worker(void *arg) {
  * Returns 0 on success, -1 on a bad argument, -2 on allocation failure.
  * N is the number of sequences: N = B when cu_seqlens is NULL, else
  * cu_seqlens has N+1 entries and B must be 1.  out_row_map (optional, length
- * B*T) maps each token row to a row of `out` (or -1 to skip it).
+ * B*T) maps each token row to a row of `out` (or -1 to skip it).  `flags` as
+ * above (0: the gate, the beta sigmoid and the L2 norms are all applied here).
  */
-int kda_oracle_fwd(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, int64_t N,
+int kda_oracle_fwd(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, int64_t N, int flags,
                    const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *g,
                    const uint16_t *beta, double scale, const float *A_log, const float *dt_bias,
                    double lower_bound, const double *initial_state, double *out,
@@ -166,7 +185,7 @@ int kda_oracle_fwd(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, int64_
     if (cu_seqlens && B != 1) return -1;
     if (nthreads < 1) nthreads = 1;
     oracle_job J;
-    J.B = B; J.T = T; J.H = H; J.K = K; J.V = V; J.N = N;
+    J.B = B; J.T = T; J.H = H; J.K = K; J.V = V; J.N = N; J.flags = flags;
     J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta;
     J.scale = scale; J.lower_bound = lower_bound;
     J.A_log = A_log; J.dt_bias = dt_bias;
