@@ -184,13 +184,16 @@ kda_status kda_workspace_size(const kda_shape* shape, size_t* bytes) {
 
 kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, const void* v, const void* g,
                       const void* beta, float scale, void* out, const float* A_log, const float* dt_bias,
-                      float lower_bound, void* state, kda_state_dtype state_dtype, kda_stream_t stream_) {
+                      float lower_bound, void* state, kda_state_dtype state_dtype, unsigned flags,
+                      kda_stream_t stream_) {
   kda_status st = check_shape(shape);
   if (st != KDA_OK) return st;
   const kda_shape s = *shape;
   if (s.N != s.B) return KDA_ERR_INVALID_ARGUMENT;
   if ((long long)s.B * s.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
-  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
+  if (flags & ~7u) return KDA_ERR_INVALID_ARGUMENT;
+  const bool gate_here = !(flags & KDA_GATE_PREACTIVATED);
+  if (gate_here && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
   auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
   if (s.B * s.T > 0) {
@@ -198,7 +201,7 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
     for (const void* p : tok)
       if (p == nullptr || !aligned(p, 2)) return KDA_ERR_INVALID_ARGUMENT;
   }
-  if (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned(dt_bias, 4))
+  if (gate_here && (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned(dt_bias, 4)))
     return KDA_ERR_INVALID_ARGUMENT;
   if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32) return KDA_ERR_INVALID_ARGUMENT;
   if (s.B > 0 && (state == nullptr || !aligned16(state))) return KDA_ERR_INVALID_ARGUMENT;
@@ -221,6 +224,7 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
   dp.H = (int)s.H;
   dp.scale = scale;
   dp.lower_bound = lower_bound;
+  dp.flags = (int)flags;
   if (launch_decode(dp, reinterpret_cast<cudaStream_t>(stream_)) != cudaSuccess) return KDA_ERR_CUDA;
   return KDA_OK;
 }
@@ -229,7 +233,16 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
                    const void* beta, float scale, void* out, const float* A_log, const float* dt_bias,
                    float lower_bound, const void* initial_state, kda_state_dtype init_dtype, void* final_state,
                    kda_state_dtype final_dtype, const int64_t* cu_seqlens, void* workspace,
-                   size_t workspace_bytes, kda_stream_t stream_) {
+                   size_t workspace_bytes, kda_stream_t stream) {
+  return kda_fwd_ex(shape, q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, init_dtype,
+                    final_state, final_dtype, cu_seqlens, 0u, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, const void* v, const void* g,
+                      const void* beta, float scale, void* out, const float* A_log, const float* dt_bias,
+                      float lower_bound, const void* initial_state, kda_state_dtype init_dtype, void* final_state,
+                      kda_state_dtype final_dtype, const int64_t* cu_seqlens, unsigned flags, void* workspace,
+                      size_t workspace_bytes, kda_stream_t stream_) {
   kda_status st = check_shape(shape);
   if (st != KDA_OK) return st;
   const kda_shape s = *shape;
@@ -241,7 +254,9 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
   } else if (s.N != s.B) {
     return KDA_ERR_INVALID_ARGUMENT;
   }
-  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
+  if (flags & ~7u) return KDA_ERR_INVALID_ARGUMENT;
+  const bool gate_here = !(flags & KDA_GATE_PREACTIVATED);
+  if (gate_here && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
   const int64_t rows = s.B * s.T;
   // q, k, g, v are read by TMA (16-byte aligned base); beta and out are accessed
@@ -253,7 +268,7 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
       if (p == nullptr || !aligned16(p)) return KDA_ERR_INVALID_ARGUMENT;
     if (beta == nullptr || out == nullptr || !aligned(beta, 2) || !aligned(out, 2)) return KDA_ERR_INVALID_ARGUMENT;
   }
-  if (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned(dt_bias, 4))
+  if (gate_here && (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned(dt_bias, 4)))
     return KDA_ERR_INVALID_ARGUMENT;
   // states: README "accept None (stateless), bf16, or fp32 ... When both are provided, their dtypes must match"
   auto dtype_ok = [](kda_state_dtype d) { return d == KDA_STATE_BF16 || d == KDA_STATE_FP32; };
@@ -322,6 +337,7 @@ kda_status kda_fwd(const kda_shape* shape, const void* q, const void* k, const v
   cp.final_dtype = (int)final_dtype;
   cp.scale = scale;
   cp.lower_bound = lower_bound;
+  cp.flags = (int)flags;
 
   if (L.cap_phase1 > 0) {
     cp.items = sp.phase1;

@@ -159,7 +159,8 @@ __device__ __forceinline__ void pair_bar(int pair) { named_bar(1 + pair, 64); }
 __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, PairScratch& sc, int pair, int w, int nv,
                                                     const float nr, const float lbl2,
                                                     const float* __restrict__ dtb, float beta_a, float beta_b,
-                                                    int lane, bool v_used) {
+                                                    int lane, bool v_used, int flags) {
+  const bool gate_pre = flags & kGatePreactivated;
   const int gid = lane >> 2, tig = lane & 3;
   const int ra = 2 * gid, rb = 2 * gid + 1;
   const bool va = ra < nv, vb = rb < nv;
@@ -209,8 +210,9 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
     const float2 a = *reinterpret_cast<const float2*>(&sc.normx[0][ra + hr][0]);
     const float2 b = *reinterpret_cast<const float2*>(&sc.normx[1][ra + hr][0]);
     const bool valid = hr == 0 ? va : vb;
-    rq[hr] = valid ? rsqrt_approx(a.x + b.x + 1e-6f) : 0.f;
-    rk[hr] = valid ? rsqrt_approx(a.y + b.y + 1e-6f) : 0.f;
+    const bool norm = !(flags & kNoQkL2Norm);
+    rq[hr] = valid ? (norm ? rsqrt_approx(a.x + b.x + 1e-6f) : 1.f) : 0.f;
+    rk[hr] = valid ? (norm ? rsqrt_approx(a.y + b.y + 1e-6f) : 1.f) : 0.f;
   }
 
   float ck0[4] = {0, 0, 0, 0}, ck1[4] = {0, 0, 0, 0}, cq0[4] = {0, 0, 0, 0}, cq1[4] = {0, 0, 0, 0};
@@ -219,8 +221,8 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
     const int p = 2 * w + pp;
     const int j16 = 4 * (p & 1) + tig;
     const int ch0 = 32 * p + 8 * tig;
-    float nrdb[8];
-    {
+    float nrdb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (!gate_pre) {
       const float4 d0 = *reinterpret_cast<const float4*>(dtb + ch0);
       const float4 d1 = *reinterpret_cast<const float4*>(dtb + ch0 + 4);
       nrdb[0] = nr * d0.x; nrdb[1] = nr * d0.y; nrdb[2] = nr * d0.z; nrdb[3] = nr * d0.w;
@@ -250,14 +252,24 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
         q[hr][2 * u + 1] = bf16hi_to_f32(aq[u]);
         k[hr][2 * u] = bf16lo_to_f32(ak[u]);
         k[hr][2 * u + 1] = bf16hi_to_f32(ak[u]);
-        // gate: base-2 log-decay lb * log2(e) * sigmoid(exp(A_log) (g + dt_bias)); 0 past the end
-        float x0, x1;
-        ffma2(x0, x1, nr, nr, bf16lo_to_f32(ag[u]), bf16hi_to_f32(ag[u]), nrdb[2 * u], nrdb[2 * u + 1]);
-        float t0 = ex2_approx(x0), t1 = ex2_approx(x1);
-        fadd2(t0, t1, 1.f, 1.f);
-        float r0 = rcp_approx(t0), r1 = rcp_approx(t1);
-        const float lv = valid ? lbl2 : 0.f;
-        fmul2(r0, r1, lv, lv);
+        // gate: base-2 log-decay lb * log2(e) * sigmoid(exp(A_log) (g + dt_bias)), or
+        // log2(e) g for a gate activated by the caller; 0 past the end
+        float r0, r1;
+        if (gate_pre) {
+          r0 = bf16lo_to_f32(ag[u]);
+          r1 = bf16hi_to_f32(ag[u]);
+          const float lv = valid ? kLog2e : 0.f;
+          fmul2(r0, r1, lv, lv);
+        } else {
+          float x0, x1;
+          ffma2(x0, x1, nr, nr, bf16lo_to_f32(ag[u]), bf16hi_to_f32(ag[u]), nrdb[2 * u], nrdb[2 * u + 1]);
+          float t0 = ex2_approx(x0), t1 = ex2_approx(x1);
+          fadd2(t0, t1, 1.f, 1.f);
+          r0 = rcp_approx(t0);
+          r1 = rcp_approx(t1);
+          const float lv = valid ? lbl2 : 0.f;
+          fmul2(r0, r1, lv, lv);
+        }
         G[hr][2 * u] = (partial && !valid) ? 0.f : r0;
         G[hr][2 * u + 1] = (partial && !valid) ? 0.f : r1;
       }
@@ -353,8 +365,9 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
   }
   pair_bar(pair);
   // beta of the lane's tokens
-  const float sa = va ? rcp_approx(1.f + ex2_approx(-beta_a * kLog2e)) : 0.f;
-  const float sb = vb ? rcp_approx(1.f + ex2_approx(-beta_b * kLog2e)) : 0.f;
+  const bool beta_pre = flags & kBetaPreactivated;
+  const float sa = va ? (beta_pre ? beta_a : rcp_approx(1.f + ex2_approx(-beta_a * kLog2e))) : 0.f;
+  const float sb = vb ? (beta_pre ? beta_b : rcp_approx(1.f + ex2_approx(-beta_b * kLog2e))) : 0.f;
   if (w == 0) {
     // full Gk = own partial + warp 1's; store column m of -Akk contiguous: AT[m][i] = -beta_i Gk[i][m]
     const float4 xa = *reinterpret_cast<const float4*>(&sc.GkX[ra][4 * tig]);
@@ -519,8 +532,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       PairScratch& sc = S.ps[pair];
       const int h = it.head;
       const int H = p.H;
-      const float nr = -expf(p.A_log[h]) * kLog2e;
-      const float* dtb = p.dt_bias + (size_t)h * kDimK;
+      const bool gate_pre = p.flags & kGatePreactivated;   // then A_log and dt_bias may be null
+      const float nr = gate_pre ? 0.f : -expf(p.A_log[h]) * kLog2e;
+      const float* dtb = gate_pre ? nullptr : p.dt_bias + (size_t)h * kDimK;
       const float lbl2 = p.lower_bound * kLog2e;
       const int gid = lane >> 2;
       auto load_beta = [&](int c, float& b0, float& b1) {
@@ -543,7 +557,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         if (lane == 0) sc.okf[iter & 1][w] = okw ? 1 : 0;
         pair_bar(pair);
         if (!(sc.okf[iter & 1][0] && sc.okf[iter & 1][1])) break;
-        prologue_pair_chunk(S.st[s], S.sm[s], sc, pair, w, nv, nr, lbl2, dtb, cb0, cb1, lane, it.mode != kModeTransition);
+        prologue_pair_chunk(S.st[s], S.sm[s], sc, pair, w, nv, nr, lbl2, dtb, cb0, cb1, lane, it.mode != kModeTransition,
+                            p.flags);
         if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
     } else {

@@ -5,8 +5,8 @@
 // S^T (row v holds S[:, v] over the 128 key channels k), the step is the KDA
 // recurrence itself (FlashKDA README "Kernel API" parameter table for the
 // inputs, gate and layout):
-//   ghat  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h, :]))
-//   beta  = sigmoid(beta logit);   qh, kh = x / sqrt(|x|^2 + 1e-6)
+//   ghat  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h, :]))   (or g_t given)
+//   beta  = sigmoid(beta logit) (or given);  qh, kh = x / sqrt(|x|^2 + 1e-6) (or as given)
 //   row v of S^T:  s <- s * exp(ghat);  s <- s + beta (v_v - s . kh) kh
 //   o_v   = scale * s . qh        (from the updated row)
 // Rows are independent, so the work is bandwidth-bound: one CTA per (n, h),
@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
       st[r] = make_float4(bf(w.x & 0xffffu), bf(w.x >> 16), bf(w.y & 0xffffu), bf(w.y >> 16));
     }
   }
-  const float rate = expf(p.A_log[h]);
+  const bool gate_pre = p.flags & kGatePreactivated;    // then A_log and dt_bias may be null
+  const float rate = gate_pre ? 0.f : expf(p.A_log[h]);
 
 #pragma unroll 1
   for (int t = 0; t < p.T; ++t) {
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
     float kk = 0.f, qq = 0.f;
     if (tid < 128) {
       const float gt = bf(p.g[tok * 128 + tid]);
-      const float ghat = p.lower_bound * sigmoidf(rate * (gt + p.dt_bias[(size_t)h * 128 + tid]));
+      const float ghat = gate_pre ? gt : p.lower_bound * sigmoidf(rate * (gt + p.dt_bias[(size_t)h * 128 + tid]));
       s_alpha[tid] = expf(ghat);
       kk = bf(p.k[tok * 128 + tid]);
       qq = bf(p.q[tok * 128 + tid]);
@@ -84,13 +85,14 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
         s_norm[1][warp] = sq;
       }
     }
-    if (tid == 0) s_beta = sigmoidf(bf(p.beta[tok]));
+    if (tid == 0) s_beta = (p.flags & kBetaPreactivated) ? bf(p.beta[tok]) : sigmoidf(bf(p.beta[tok]));
     __syncthreads();
     if (tid < 128) {
       const float nk = s_norm[0][0] + s_norm[0][1] + s_norm[0][2] + s_norm[0][3];
       const float nq = s_norm[1][0] + s_norm[1][1] + s_norm[1][2] + s_norm[1][3];
-      s_kh[tid] = kk / sqrtf(nk + 1e-6f);
-      s_qh[tid] = qq / sqrtf(nq + 1e-6f);
+      const bool norm = !(p.flags & kNoQkL2Norm);
+      s_kh[tid] = norm ? kk / sqrtf(nk + 1e-6f) : kk;
+      s_qh[tid] = norm ? qq / sqrtf(nq + 1e-6f) : qq;
     }
     __syncthreads();
     // ---- the rows: decay, delta update, output from the updated row

@@ -65,6 +65,7 @@ struct ChainParams {
   int final_dtype;
   float scale;
   float lower_bound;
+  int flags;                           // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm
 };
 
 struct ComposeParams {
@@ -88,6 +89,11 @@ struct ScheduleParams {
   long long cap_phase1, cap_forward, cap_compose, cap_slots;
 };
 
+// Steps the caller already did (include/kda.h KDA_GATE_PREACTIVATED, ...).
+constexpr int kGatePreactivated = 1;
+constexpr int kBetaPreactivated = 2;
+constexpr int kNoQkL2Norm = 4;
+
 struct DecodeParams {
   const uint16_t *q, *k, *v, *g, *beta;  // bf16 [B, T, H, 128] (beta [B, T, H], logits)
   uint16_t* out;                          // bf16 [B, T, H, 128]
@@ -95,6 +101,7 @@ struct DecodeParams {
   const float* dt_bias;                   // [H, 128]
   void* state;                            // [B, H, 128 (v), 128 (k)], read and written in place
   int state_dtype;                        // 1 bf16, 2 fp32
+  int flags;                              // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm
   int B, T, H;
   float scale, lower_bound;
 };

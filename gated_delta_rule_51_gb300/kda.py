@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPOR
                 6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_BAD_SEQLENS"}
 EXPORTED_SYMBOLS = ("kda_status_string", "kda_workspace_size", "kda_fwd", "kda_check_device_error",
                     "kda_set_profile_events", "kda_last_launch_count", "kda_fwd_static_workspace",
-                    "kda_decode")
+                    "kda_decode", "kda_fwd_ex")
+KDA_GATE_PREACTIVATED, KDA_BETA_PREACTIVATED, KDA_NO_QK_L2NORM = 1, 2, 4
 
 
 class kda_shape(ctypes.Structure):
@@ -70,7 +71,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_last_launch_count.argtypes = []
         lib.kda_last_launch_count.restype = ctypes.c_int
         lib.kda_decode.argtypes = [ctypes.POINTER(kda_shape), p, p, p, p, p, ctypes.c_float, p, p, p,
-                                   ctypes.c_float, p, ctypes.c_int, p]
+                                   ctypes.c_float, p, ctypes.c_int, ctypes.c_uint, p]
+        lib.kda_fwd_ex.argtypes = [ctypes.POINTER(kda_shape), p, p, p, p, p, ctypes.c_float, p, p, p,
+                                   ctypes.c_float, p, ctypes.c_int, p, ctypes.c_int, p, ctypes.c_uint, p,
+                                   ctypes.c_size_t, p]
+        lib.kda_fwd_ex.restype = ctypes.c_int
         lib.kda_decode.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -126,14 +131,25 @@ def _check(t: torch.Tensor, name: str, dtype: torch.dtype, shape: Tuple[int, ...
         raise ValueError(f"{name} must be contiguous")
 
 
+def _flags(use_gate_in_kernel: bool, use_beta_sigmoid_in_kernel: bool, use_qk_l2norm_in_kernel: bool) -> int:
+    return ((0 if use_gate_in_kernel else KDA_GATE_PREACTIVATED)
+            | (0 if use_beta_sigmoid_in_kernel else KDA_BETA_PREACTIVATED)
+            | (0 if use_qk_l2norm_in_kernel else KDA_NO_QK_L2NORM))
+
+
 def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
         final_state=None, cu_seqlens=None, workspace: Optional[torch.Tensor] = None,
-        stream: Optional[torch.cuda.Stream] = None):
+        stream: Optional[torch.cuda.Stream] = None, use_gate_in_kernel: bool = True,
+        use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True):
     """KDA forward on the GPU; writes ``out`` (and ``final_state``) and returns them.
 
     q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,128] bf16; beta: [B,T,H] bf16 logits;
     A_log: [H] fp32; dt_bias: [H,128] fp32; states: [N,H,128,128] bf16/fp32 or None;
     cu_seqlens: int64 [N+1] on the device (then B must be 1).
+    The use_* switches (default on, FlashKDA's behaviour) say which steps run in
+    the kernel; off means the caller did them: g is then the natural-log decay in
+    [-5, 0] (A_log and dt_bias may be None), beta is beta itself, q and k are used
+    without L2 norms.
     """
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
@@ -148,7 +164,10 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
                              ("out", out, torch.bfloat16, (B, T, H, V)),
                              ("beta", beta, torch.bfloat16, (B, T, H)),
                              ("A_log", A_log, torch.float32, (H,)), ("dt_bias", dt_bias, torch.float32, (H, K))):
+        if t is None and not use_gate_in_kernel and name in ("A_log", "dt_bias"):
+            continue
         _check(t, name, dt, shp, dev)
+    flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel)
     for name, t in (("initial_state", initial_state), ("final_state", final_state)):
         if t is not None:
             _check(t, name, t.dtype, (N, H, V, K), dev)
@@ -162,19 +181,20 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
         workspace = _workspace(dev, s.cuda_stream, need)
     elif workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace needs {need} bytes")
-    st = lib.kda_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                     ctypes.c_float(scale), _ptr(out), _ptr(A_log), _ptr(dt_bias),
-                     ctypes.c_float(lower_bound), _ptr(initial_state), _state_code(initial_state),
-                     _ptr(final_state), _state_code(final_state), _ptr(cu_seqlens), _ptr(workspace),
-                     ctypes.c_size_t(workspace.numel() * workspace.element_size()),
-                     ctypes.c_void_p(s.cuda_stream))
+    st = lib.kda_fwd_ex(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                        ctypes.c_float(scale), _ptr(out), _ptr(A_log), _ptr(dt_bias),
+                        ctypes.c_float(lower_bound), _ptr(initial_state), _state_code(initial_state),
+                        _ptr(final_state), _state_code(final_state), _ptr(cu_seqlens), ctypes.c_uint(flags),
+                        _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                        ctypes.c_void_p(s.cuda_stream))
     if st != KDA_OK:
         raise KDAError(st, "kda_fwd")
     return out, final_state
 
 
 def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
-           stream: Optional[torch.cuda.Stream] = None):
+           stream: Optional[torch.cuda.Stream] = None, use_gate_in_kernel: bool = True,
+           use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True):
     """Recurrent KDA step(s) for decoding; updates ``state`` in place, writes ``out``.
 
     q, k, g, v, out: [B,T,H,128] bf16 (T new tokens per sequence, usually 1);
@@ -192,14 +212,17 @@ def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
                              ("out", out, torch.bfloat16, (B, T, H, K)),
                              ("beta", beta, torch.bfloat16, (B, T, H)),
                              ("A_log", A_log, torch.float32, (H,)), ("dt_bias", dt_bias, torch.float32, (H, K))):
+        if t is None and not use_gate_in_kernel and name in ("A_log", "dt_bias"):
+            continue
         _check(t, name, dt, shp, dev)
     _check(state, "state", state.dtype, (B, H, K, K), dev)
+    flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel)
     lib = load_library()
     shape = make_shape(B, T, H, B, K, K)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     st = lib.kda_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                         ctypes.c_float(scale), _ptr(out), _ptr(A_log), _ptr(dt_bias), ctypes.c_float(lower_bound),
-                        _ptr(state), _state_code(state), ctypes.c_void_p(s.cuda_stream))
+                        _ptr(state), _state_code(state), ctypes.c_uint(flags), ctypes.c_void_p(s.cuda_stream))
     if st != KDA_OK:
         raise KDAError(st, "kda_decode")
     return out, state

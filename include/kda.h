@@ -62,6 +62,27 @@ typedef enum {
 typedef enum { KDA_STATE_NONE = 0, KDA_STATE_BF16 = 1, KDA_STATE_FP32 = 2 } kda_state_dtype;
 
 /*
+ * Steps the caller has already done, as flags (0 = FlashKDA's fixed behaviour:
+ * the gate, the beta sigmoid and the q/k L2 norms are all computed in the
+ * kernel).  They mirror the reference call's use_gate_in_kernel,
+ * use_beta_sigmoid_in_kernel and use_qk_l2norm_in_kernel switches, set here
+ * when the switch is off:
+ *   KDA_GATE_PREACTIVATED : g holds the natural-log decay ghat itself; A_log,
+ *                           dt_bias and lower_bound are not read (A_log and
+ *                           dt_bias may be NULL).  For kda_fwd_ex every value
+ *                           must lie in [-5, 0], the range the in-kernel gate
+ *                           guarantees (the 16-token chunked form relies on
+ *                           it); kda_decode takes any value <= 0.
+ *   KDA_BETA_PREACTIVATED : beta holds beta itself, not its logit.
+ *   KDA_NO_QK_L2NORM      : q and k are used as given.
+ */
+typedef enum {
+    KDA_GATE_PREACTIVATED = 1,
+    KDA_BETA_PREACTIVATED = 2,
+    KDA_NO_QK_L2NORM = 4
+} kda_flags;
+
+/*
  * Problem shape (README parameter table):
  *   q, k, g : [B, T, H, K] bf16      v, out : [B, T, H, V] bf16
  *   beta    : [B, T, H]    bf16 (logits)
@@ -115,6 +136,17 @@ KDA_API kda_status kda_fwd(const kda_shape *shape, const void *q, const void *k,
                    kda_state_dtype init_dtype, void *final_state, kda_state_dtype final_dtype,
                    const int64_t *cu_seqlens, void *workspace, size_t workspace_bytes,
                    kda_stream_t stream);
+
+/*
+ * kda_fwd with `flags` (kda_flags, or-ed): steps the caller has already done.
+ * kda_fwd(...) is kda_fwd_ex(..., 0, ...).
+ */
+KDA_API kda_status kda_fwd_ex(const kda_shape *shape, const void *q, const void *k, const void *v,
+                              const void *g, const void *beta, float scale, void *out, const float *A_log,
+                              const float *dt_bias, float lower_bound, const void *initial_state,
+                              kda_state_dtype init_dtype, void *final_state, kda_state_dtype final_dtype,
+                              const int64_t *cu_seqlens, unsigned flags, void *workspace,
+                              size_t workspace_bytes, kda_stream_t stream);
 
 /*
  * Synchronises `stream`, reads the error word that the last kda_fwd on this
@@ -180,6 +212,7 @@ KDA_API kda_status kda_fwd_static_workspace(const kda_shape *shape, const void *
  *   q, k, v, g, beta : bf16 [B, T, H, 128] (beta [B, T, H], logits), 2-byte aligned.
  *   out              : bf16 [B, T, H, V], written for every token, 2-byte aligned.
  *   A_log, dt_bias, lower_bound, scale : as for kda_fwd.
+ *   flags            : kda_flags, as for kda_fwd_ex.
  *   state            : [B, H, V, K] of state_dtype (bf16 or fp32), 16-byte aligned;
  *                      read as the state before the first token and overwritten with
  *                      the state after the last (a bf16 state is rounded once, at the
@@ -189,7 +222,7 @@ KDA_API kda_status kda_fwd_static_workspace(const kda_shape *shape, const void *
 KDA_API kda_status kda_decode(const kda_shape *shape, const void *q, const void *k, const void *v,
                               const void *g, const void *beta, float scale, void *out, const float *A_log,
                               const float *dt_bias, float lower_bound, void *state,
-                              kda_state_dtype state_dtype, kda_stream_t stream);
+                              kda_state_dtype state_dtype, unsigned flags, kda_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -99,11 +99,11 @@ def test_python_binding_requires_cuda_tensors():
                 torch.zeros(1), torch.zeros(1, 128), -1.0)
 
 
-def _decode_call(shape, q=FAKE, out=FAKE, A_log=FAKE, state=FAKE, dtype=2, lb=-1.0):
+def _decode_call(shape, q=FAKE, out=FAKE, A_log=FAKE, state=FAKE, dtype=2, lb=-1.0, flags=0):
     lib = kda.load_library()
     p = lambda a: ctypes.c_void_p(a) if a else None
     return lib.kda_decode(ctypes.byref(shape), p(q), p(FAKE), p(FAKE), p(FAKE), p(FAKE), ctypes.c_float(0.1),
-                          p(out), p(A_log), p(FAKE), ctypes.c_float(lb), p(state), dtype, None)
+                          p(out), p(A_log), p(FAKE), ctypes.c_float(lb), p(state), dtype, ctypes.c_uint(flags), None)
 
 
 @pytest.mark.parametrize("case,expected", [
@@ -116,6 +116,7 @@ def _decode_call(shape, q=FAKE, out=FAKE, A_log=FAKE, state=FAKE, dtype=2, lb=-1
     (dict(shape=kda.make_shape(4, 1, 2, 4), q=0), 1),
     (dict(shape=kda.make_shape(4, 1, 2, 4), out=FAKE + 1), 1),       # 2-byte aligned tokens
     (dict(shape=kda.make_shape(4, 1, 2, 4), A_log=FAKE + 2), 1),
+    (dict(shape=kda.make_shape(4, 1, 2, 4), flags=8), 1),            # unknown flag
 ])
 def test_decode_host_side_argument_errors(case, expected):
     shape = case.pop("shape")
@@ -124,3 +125,21 @@ def test_decode_host_side_argument_errors(case, expected):
 
 def test_decode_valid_arguments_reach_the_device_query():
     assert _decode_call(kda.make_shape(4, 1, 2, 4), q=FAKE + 2, out=FAKE + 6) in (4, 5)
+    # a gate activated by the caller needs neither A_log nor dt_bias, nor a lower bound in range
+    assert _decode_call(kda.make_shape(4, 1, 2, 4), A_log=0, lb=7.0, flags=1) in (4, 5)
+
+
+def _fwd_ex_call(flags, A_log=FAKE, lb=-1.0):
+    lib = kda.load_library()
+    p = lambda a: ctypes.c_void_p(a) if a else None
+    shape = kda.make_shape(1, 64, 1, 1)
+    return lib.kda_fwd_ex(ctypes.byref(shape), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), ctypes.c_float(0.1),
+                          p(FAKE), p(A_log), p(A_log), ctypes.c_float(lb), None, 0, None, 0, None,
+                          ctypes.c_uint(flags), p(FAKE), ctypes.c_size_t(1 << 30), None)
+
+
+def test_fwd_ex_flags_on_the_host():
+    assert _fwd_ex_call(8) == 1                       # unknown flag
+    assert _fwd_ex_call(0, A_log=0) == 1              # the in-kernel gate needs its parameters
+    assert _fwd_ex_call(1, A_log=0, lb=9.0) in (4, 5)  # a pre-activated gate does not
+    assert _fwd_ex_call(6) in (4, 5)
