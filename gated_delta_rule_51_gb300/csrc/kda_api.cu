@@ -95,11 +95,22 @@ Layout make_layout(const kda_shape& s, int sms) {
 
 kda_status check_shape(const kda_shape* s) {
   if (s == nullptr) return KDA_ERR_INVALID_ARGUMENT;
-  if (s->K != 128 || s->V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (s->K != 128 || (s->V != 128 && s->V != 256)) return KDA_ERR_UNSUPPORTED_SHAPE;
   if (s->B < 0 || s->T < 0 || s->H <= 0 || s->N < 0) return KDA_ERR_INVALID_ARGUMENT;
   if (s->B > 0 && s->T > (int64_t)0x7fffffff / std::max<int64_t>(s->B, 1)) return KDA_ERR_INVALID_ARGUMENT;
-  if (s->H > 65535 || s->N > (int64_t)0x7fffffff / s->H) return KDA_ERR_INVALID_ARGUMENT;
+  const int64_t Hv = s->H * (s->V / 128);
+  if (Hv > 65535 || s->N > (int64_t)0x7fffffff / Hv) return KDA_ERR_INVALID_ARGUMENT;
   return KDA_OK;
+}
+
+// The value columns of a state are independent, so V = 256 runs as two chains of
+// 128 state rows per head: the work lists, segment slots and split policy see
+// H x V/128 "heads" of width 128.
+kda_shape chain_shape(const kda_shape& s) {
+  kda_shape c = s;
+  c.H = s.H * (s.V / 128);
+  c.V = 128;
+  return c;
 }
 
 cudaEvent_t g_profile_events[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -139,14 +150,16 @@ bool encode_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H) 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The same tensor seen as 4-D {64, H, rows, 2}: the two 64-channel halves of a row
+// The same tensor seen as 4-D {64, H, rows, width / 64}: the 64-channel pieces of a row
 // become the outermost dimension, so box {64, 1, 16, 2} lands in shared memory as
-// [half][16 rows][64 channels] -- two consecutive swizzled tiles -- in one copy.
-bool encode_halves_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H) {
+// [piece][16 rows][64 channels] -- two consecutive swizzled tiles -- in one copy.
+// `width` is the row length in elements (128, or V for v): its 64-channel pieces are
+// the outermost dimension, and a box takes two consecutive pieces.
+bool encode_halves_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int64_t width = 128) {
   auto enc = get_encode();
   if (!enc) return false;
-  cuuint64_t dims[4] = {64, (cuuint64_t)H, (cuuint64_t)std::max<int64_t>(rows, 1), 2};
-  cuuint64_t strides[3] = {256, (cuuint64_t)(H * 256), 128};
+  cuuint64_t dims[4] = {64, (cuuint64_t)H, (cuuint64_t)std::max<int64_t>(rows, 1), (cuuint64_t)(width / 64)};
+  cuuint64_t strides[3] = {(cuuint64_t)(width * 2), (cuuint64_t)(H * width * 2), 128};
   cuuint32_t box[4] = {64, 1, 16, 2};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
@@ -162,7 +175,7 @@ const char* kda_status_string(kda_status s) {
   switch (s) {
     case KDA_OK: return "ok";
     case KDA_ERR_INVALID_ARGUMENT: return "invalid argument";
-    case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K and V must be 128)";
+    case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K must be 128, V 128 or 256)";
     case KDA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case KDA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3, sm_103a)";
     case KDA_ERR_CUDA: return "CUDA error";
@@ -178,7 +191,7 @@ kda_status kda_workspace_size(const kda_shape* shape, size_t* bytes) {
   if (st != KDA_OK) return st;
   DeviceInfo d;
   if (device_info(&d) != KDA_OK) d.sms = 152;   // sizing only; kda_fwd checks the device
-  *bytes = make_layout(*shape, d.sms).total;
+  *bytes = make_layout(chain_shape(*shape), d.sms).total;
   return KDA_OK;
 }
 
@@ -190,7 +203,7 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
   if (st != KDA_OK) return st;
   const kda_shape s = *shape;
   if (s.N != s.B) return KDA_ERR_INVALID_ARGUMENT;
-  if ((long long)s.B * s.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
+  if ((long long)s.B * s.H * (s.V / 128) > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
   if (flags & ~7u) return KDA_ERR_INVALID_ARGUMENT;
   const bool gate_here = !(flags & KDA_GATE_PREACTIVATED);
   if (gate_here && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
@@ -222,6 +235,7 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
   dp.B = (int)s.B;
   dp.T = (int)s.T;
   dp.H = (int)s.H;
+  dp.vsplit = (int)(s.V / 128);
   dp.scale = scale;
   dp.lower_bound = lower_bound;
   dp.flags = (int)flags;
@@ -278,14 +292,15 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   if (final_state == nullptr && final_dtype != KDA_STATE_NONE) return KDA_ERR_INVALID_ARGUMENT;
   if (initial_state != nullptr && final_state != nullptr) {
     if (init_dtype != final_dtype) return KDA_ERR_INVALID_ARGUMENT;
-    const size_t bytes = (size_t)s.N * s.H * 128 * 128 * (init_dtype == KDA_STATE_FP32 ? 4 : 2);
+    const size_t bytes = (size_t)s.N * s.H * s.V * 128 * (init_dtype == KDA_STATE_FP32 ? 4 : 2);
     const uintptr_t a = reinterpret_cast<uintptr_t>(initial_state), b = reinterpret_cast<uintptr_t>(final_state);
     if (a != b && a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARGUMENT;   // partial overlap
   }
   DeviceInfo d;
   if (device_info(&d) != KDA_OK) return KDA_ERR_CUDA;
   if (d.major != 10 || d.minor != 3) return KDA_ERR_UNSUPPORTED_DEVICE;
-  const Layout L = make_layout(s, d.sms);
+  const kda_shape sc = chain_shape(s);
+  const Layout L = make_layout(sc, d.sms);
   if (workspace == nullptr || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return KDA_ERR_WORKSPACE_TOO_SMALL;
   if (s.N == 0) return KDA_OK;
@@ -297,7 +312,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   sp.cu_seqlens = cu_seqlens;
   sp.B = s.B;
   sp.T = s.T;
-  sp.H = s.H;
+  sp.H = sc.H;
   sp.N = s.N;
   sp.seg_tokens = (int)L.seg_tokens;
   sp.seg_forced = forced_seg_tokens() != 0;
@@ -321,7 +336,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   std::memset(&cp, 0, sizeof(cp));
   if (rows > 0) {
     if (!encode_tile_map(&cp.tm_q, q, rows, s.H) || !encode_halves_map(&cp.tm_k, k, rows, s.H) ||
-        !encode_halves_map(&cp.tm_g, g, rows, s.H) || !encode_halves_map(&cp.tm_v, v, rows, s.H))
+        !encode_halves_map(&cp.tm_g, g, rows, s.H) || !encode_halves_map(&cp.tm_v, v, rows, s.H, s.V))
       return KDA_ERR_CUDA;
   }
   cp.beta = static_cast<const uint16_t*>(beta);
@@ -333,6 +348,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   cp.ws_states = reinterpret_cast<float*>(ws + L.off_slots);
   cp.err = &hdr->err;
   cp.H = (int)s.H;
+  cp.vsplit = (int)(s.V / 128);
   cp.init_dtype = (int)init_dtype;
   cp.final_dtype = (int)final_dtype;
   cp.scale = scale;

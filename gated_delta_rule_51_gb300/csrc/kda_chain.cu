@@ -482,6 +482,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   const WorkItem it = p.items[blockIdx.x];
   if (it.len < 0) return;   // placeholder entry of a work list
   const int nchunks = (it.len + kChunk - 1) / kChunk;
+  // work items count heads x value blocks: V = 128 * vsplit columns are independent
+  // chains of 128 state rows each, sharing the head's q, k, g and beta
+  const int head = it.head / p.vsplit, vblk = it.head - head * p.vsplit;
+  const size_t vstride = (size_t)p.vsplit * kDimV;   // V
 
   extern __shared__ uint8_t smem_dyn[];
   SmemLayout& S = *reinterpret_cast<SmemLayout*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
@@ -530,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       const int pw = warp - kWarpProlog0;
       const int pair = pw >> 1, w = pw & 1;      // pair 0: even chunks, pair 1: odd chunks
       PairScratch& sc = S.ps[pair];
-      const int h = it.head;
+      const int h = head;
       const int H = p.H;
       const bool gate_pre = p.flags & kGatePreactivated;   // then A_log and dt_bias may be null
       const float nr = gate_pre ? 0.f : -expf(p.A_log[h]) * kLog2e;
@@ -574,8 +578,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       const uint32_t tS = tmem + kColState + loff;
       const uint32_t tSb = tmem + kColSbf + loff;
       const uint32_t tD1 = tmem + kColD1 + loff;
-      const int h = it.head;
-      const size_t srow = ((size_t)it.seq * p.H + h) * kDimV + vrow;   // user state row (n, h, v)
+      const int h = head;
+      const size_t srow = ((size_t)it.seq * p.H + h) * vstride + (size_t)kDimV * vblk + vrow;   // state row (n, h, v)
       const bool with_u = it.mode != kModeTransition;
       const bool with_o = it.mode == kModeForward;
       // instruction and shared-memory descriptors (stage s adds s * sizeof(Stage))
@@ -640,11 +644,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         Stage& st = S.st[s];
         mbar_arrive_expect_tx(&bar_full[s], load_v ? 16384u : 12288u);
         // q: one 64-channel half into each S-side operand tile; k, g, v: both halves at once
-        tma_load_3d(st.X[0] + 2048, &p.tm_q, &bar_full[s], 0, it.head, row);
-        tma_load_3d(st.X[1] + 2048, &p.tm_q, &bar_full[s], 64, it.head, row);
-        tma_load_4d(st.K, &p.tm_k, &bar_full[s], 0, it.head, row, 0);
-        tma_load_4d(st.G, &p.tm_g, &bar_full[s], 0, it.head, row, 0);
-        if (load_v) tma_load_4d(st.V, &p.tm_v, &bar_full[s], 0, it.head, row, 0);
+        tma_load_3d(st.X[0] + 2048, &p.tm_q, &bar_full[s], 0, head, row);
+        tma_load_3d(st.X[1] + 2048, &p.tm_q, &bar_full[s], 64, head, row);
+        tma_load_4d(st.K, &p.tm_k, &bar_full[s], 0, head, row, 0);
+        tma_load_4d(st.G, &p.tm_g, &bar_full[s], 0, head, row, 0);
+        if (load_v) tma_load_4d(st.V, &p.tm_v, &bar_full[s], 0, head, row, 2 * vblk);
         ++tma_issued;
       };
       if (tma_thread) {
@@ -836,8 +840,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
             *reinterpret_cast<uint16_t*>(&S.ostage[i][2 * vrow]) =
                 __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * __uint_as_float(r[i])));
           __syncwarp();
-          const size_t row_elems = (size_t)p.H * kDimV;
-          uint16_t* obase = p.out + ((size_t)(it.row0 + c * kChunk) * p.H + h) * kDimV;
+          const size_t row_elems = (size_t)p.H * vstride;
+          uint16_t* obase = p.out + ((size_t)(it.row0 + c * kChunk) * p.H + h) * vstride + (size_t)kDimV * vblk;
           if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0) {
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
@@ -867,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
     // zero-length run: the final state equals the initial state
     const int q4 = warp & 3;
     const int vrow = q4 * 32 + lane;
-    const size_t srow = ((size_t)it.seq * p.H + it.head) * kDimV + vrow;
+    const size_t srow = ((size_t)it.seq * p.H + head) * vstride + (size_t)kDimV * vblk + vrow;
     for (int t = 0; t < 128; ++t) {
       float x = 0.f;
       if (it.in_slot == kInIdentity) x = (t == vrow) ? 1.f : 0.f;

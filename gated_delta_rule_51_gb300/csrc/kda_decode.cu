@@ -43,7 +43,10 @@ __device__ __forceinline__ void warp_sum16(float (&x)[kRowsPerWarp]) {
 __device__ __forceinline__ float sigmoidf(float x) { return 1.f / (1.f + expf(-x)); }
 
 __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeParams p) {
-  const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
+  // one CTA per (sequence, head, 128-row value block); V = 128 * vsplit
+  const int vblk = blockIdx.x % p.vsplit;
+  const int n = (blockIdx.x / p.vsplit) / p.H, h = (blockIdx.x / p.vsplit) % p.H;
+  const size_t V = (size_t)p.vsplit * 128;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ __align__(16) float s_alpha[128], s_kh[128], s_qh[128], s_v[128];
   __shared__ float s_norm[2][4];
@@ -51,13 +54,14 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
 
   // ---- the state rows of this warp, four key channels per lane
   const size_t head = (size_t)n * p.H + h;
+  const size_t srow0 = head * V + (size_t)128 * vblk;   // first state row of this CTA
   float4 st[kRowsPerWarp];
   if (p.state_dtype == 2) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.state) + head * 16384);
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.state) + srow0 * 128);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) st[r] = src[(kRowsPerWarp * warp + r) * 32 + lane];
   } else {
-    const uint2* src = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.state) + head * 16384);
+    const uint2* src = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.state) + srow0 * 128);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
       const uint2 w = src[(kRowsPerWarp * warp + r) * 32 + lane];
@@ -78,7 +82,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
       s_alpha[tid] = expf(ghat);
       kk = bf(p.k[tok * 128 + tid]);
       qq = bf(p.q[tok * 128 + tid]);
-      s_v[tid] = bf(p.v[tok * 128 + tid]);
+      s_v[tid] = bf(p.v[tok * V + 128 * vblk + tid]);
       const float sk = warp_sum(kk * kk), sq = warp_sum(qq * qq);
       if (lane == 0) {
         s_norm[0][warp] = sk;
@@ -119,18 +123,19 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
       float o = d[0];
 #pragma unroll
       for (int r = 1; r < kRowsPerWarp; ++r) o = lane == r ? d[r] : o;
-      p.out[tok * 128 + kRowsPerWarp * warp + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * o));
+      p.out[tok * V + 128 * vblk + kRowsPerWarp * warp + lane] =
+          __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * o));
     }
     __syncthreads();   // the per-channel vectors are rewritten by the next token
   }
 
   // ---- write the rows back
   if (p.state_dtype == 2) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.state) + head * 16384);
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.state) + srow0 * 128);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) dst[(kRowsPerWarp * warp + r) * 32 + lane] = st[r];
   } else {
-    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.state) + head * 16384);
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.state) + srow0 * 128);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r)
       dst[(kRowsPerWarp * warp + r) * 32 + lane] = make_uint2(pack_bf16x2(st[r].x, st[r].y), pack_bf16x2(st[r].z, st[r].w));
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
-  const long long grid = (long long)p.B * p.H;
+  const long long grid = (long long)p.B * p.H * p.vsplit;
   if (grid <= 0 || p.T <= 0) return cudaSuccess;
   kda_decode_kernel<<<(unsigned)grid, kDecThreads, 0, s>>>(p);
   return cudaGetLastError();

@@ -49,7 +49,7 @@ struct ComposeItem {
 
 struct ChainParams {
   CUtensorMap tm_q;                  // 3-D map over [B*T, H, 128] bf16, box {64, 1, 16}
-  CUtensorMap tm_k, tm_g, tm_v;      // 4-D maps {64, H, B*T, 2 halves}, box {64, 1, 16, 2}
+  CUtensorMap tm_k, tm_g, tm_v;      // 4-D maps {64, H, B*T, 2 halves (v: 2 V/128)}, box {64, 1, 16, 2}
   const uint16_t* beta;                // [B*T, H] bf16 logits
   const float* A_log;                  // [H]
   const float* dt_bias;                // [H, 128]
@@ -66,6 +66,7 @@ struct ChainParams {
   float scale;
   float lower_bound;
   int flags;                           // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm
+  int vsplit;                          // V / 128: work-item heads are (head, 128-column value block)
 };
 
 struct ComposeParams {
@@ -101,6 +102,7 @@ struct DecodeParams {
   const float* dt_bias;                   // [H, 128]
   void* state;                            // [B, H, 128 (v), 128 (k)], read and written in place
   int state_dtype;                        // 1 bf16, 2 fp32
+  int vsplit;                             // V / 128
   int flags;                              // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm
   int B, T, H;
   float scale, lower_bound;

@@ -197,9 +197,10 @@ def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
            use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True):
     """Recurrent KDA step(s) for decoding; updates ``state`` in place, writes ``out``.
 
-    q, k, g, v, out: [B,T,H,128] bf16 (T new tokens per sequence, usually 1);
-    beta: [B,T,H] bf16 logits; A_log: [H] fp32; dt_bias: [H,128] fp32;
-    state: [B,H,128,128] bf16 or fp32, read before the first token and overwritten.
+    q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,V] bf16 with V = 128 or 256 (T new
+    tokens per sequence, usually 1); beta: [B,T,H] bf16 logits; A_log: [H] fp32;
+    dt_bias: [H,128] fp32; state: [B,H,V,128] bf16 or fp32, read before the first
+    token and overwritten.
     """
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
@@ -207,18 +208,19 @@ def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("kda.decode runs on CUDA tensors only")
+    V = v.shape[-1]
     for name, t, dt, shp in (("q", q, torch.bfloat16, (B, T, H, K)), ("k", k, torch.bfloat16, (B, T, H, K)),
-                             ("g", g, torch.bfloat16, (B, T, H, K)), ("v", v, torch.bfloat16, (B, T, H, K)),
-                             ("out", out, torch.bfloat16, (B, T, H, K)),
+                             ("g", g, torch.bfloat16, (B, T, H, K)), ("v", v, torch.bfloat16, (B, T, H, V)),
+                             ("out", out, torch.bfloat16, (B, T, H, V)),
                              ("beta", beta, torch.bfloat16, (B, T, H)),
                              ("A_log", A_log, torch.float32, (H,)), ("dt_bias", dt_bias, torch.float32, (H, K))):
         if t is None and not use_gate_in_kernel and name in ("A_log", "dt_bias"):
             continue
         _check(t, name, dt, shp, dev)
-    _check(state, "state", state.dtype, (B, H, K, K), dev)
+    _check(state, "state", state.dtype, (B, H, V, K), dev)
     flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel)
     lib = load_library()
-    shape = make_shape(B, T, H, B, K, K)
+    shape = make_shape(B, T, H, B, K, V)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     st = lib.kda_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                         ctypes.c_float(scale), _ptr(out), _ptr(A_log), _ptr(dt_bias), ctypes.c_float(lower_bound),

@@ -63,7 +63,7 @@ def _call(shape, q=FAKE, beta=FAKE, out=FAKE, A_log=FAKE, dt_bias=FAKE, lb=-1.0,
 
 @pytest.mark.parametrize("case,expected", [
     (dict(shape=kda.make_shape(1, 64, 1, 1, K=64)), 2),
-    (dict(shape=kda.make_shape(1, 64, 1, 1, V=256)), 2),
+    (dict(shape=kda.make_shape(1, 64, 1, 1, V=384)), 2),
     (dict(shape=kda.make_shape(2, 64, 1, 2), cu=FAKE), 1),          # cu_seqlens needs B = 1
     (dict(shape=kda.make_shape(2, 64, 1, 3)), 1),                   # N must equal B
     (dict(shape=kda.make_shape(1, 64, 1, 1), lb=0.5), 1),           # lower_bound in [-5, 0]
@@ -143,3 +143,10 @@ def test_fwd_ex_flags_on_the_host():
     assert _fwd_ex_call(0, A_log=0) == 1              # the in-kernel gate needs its parameters
     assert _fwd_ex_call(1, A_log=0, lb=9.0) in (4, 5)  # a pre-activated gate does not
     assert _fwd_ex_call(6) in (4, 5)
+
+
+def test_v256_passes_the_shape_checks():
+    # V = 256 is accepted (two 128-row chains per head); without a GPU the call stops at the device query
+    assert _call(kda.make_shape(1, 64, 1, 1, V=256)) in (4, 5)
+    assert _decode_call(kda.make_shape(4, 1, 2, 4, V=256)) in (4, 5)
+    assert kda.workspace_size(kda.make_shape(1, 64, 2, 1, V=256)) >= kda.workspace_size(kda.make_shape(1, 64, 2, 1))
