@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -25,13 +26,29 @@ struct DeviceInfo {
   int major = 0, minor = 0;
 };
 
+// Attributes of the current device, queried once per device and cached (every call
+// needs them; the queries cost more than the rest of the host-side work).
 kda_status device_info(DeviceInfo* out) {
+  constexpr int kMaxDevices = 64;
+  static DeviceInfo cache[kMaxDevices];
+  static std::atomic<bool> have[kMaxDevices];
+  static std::mutex fill;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  const bool cacheable = dev >= 0 && dev < kMaxDevices;
+  if (cacheable && have[dev].load(std::memory_order_acquire)) {
+    *out = cache[dev];
+    return KDA_OK;
+  }
   DeviceInfo d;
   if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KDA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return KDA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return KDA_ERR_CUDA;
+  if (cacheable) {
+    std::lock_guard<std::mutex> lock(fill);
+    cache[dev] = d;
+    have[dev].store(true, std::memory_order_release);
+  }
   *out = d;
   return KDA_OK;
 }
@@ -117,8 +134,11 @@ cudaEvent_t g_profile_events[4] = {nullptr, nullptr, nullptr, nullptr};
 bool g_profile = false;
 thread_local int t_last_launches = 0;
 
+// External records, so that a call captured into a CUDA graph records the events each
+// time the graph runs (outside a capture the flag changes nothing).
 void mark(int i, cudaStream_t s) {
-  if (g_profile && g_profile_events[i] != nullptr) cudaEventRecord(g_profile_events[i], s);
+  if (g_profile && g_profile_events[i] != nullptr)
+    cudaEventRecordWithFlags(g_profile_events[i], s, cudaEventRecordExternal);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -32,6 +32,8 @@
 // Precision: the S-side GEMM runs on bf16 copies of S^T, W and qh*2^G; the
 // rank-16 state update, U and Aqk*Vn use a split-bf16 (hi + lo) scheme, and
 // the Grams use tf32, which keeps the fp32 state within ~1e-6 of exact.
+#include <atomic>
+
 #include "kda_device.cuh"
 #include "kda_internal.h"
 
@@ -896,8 +898,17 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
 
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
   const size_t smem = chain_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(kda_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the shared-memory opt-in is a per-device setting: made once per device
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> opted_in[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kda_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
+  }
   if (grid <= 0) return cudaSuccess;
   kda_chain_kernel<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();
