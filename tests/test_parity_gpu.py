@@ -197,3 +197,31 @@ def test_long_workload_sampled():
     ref_out, ref_fin = run_oracle(x, out_rows=rows)
     check_out(out, ref_out, rows=rows, label=w.name)
     check_state(fin, ref_fin, label=w.name)
+
+
+def test_forward_captured_in_a_cuda_graph_replays_identically():
+    # kda_fwd allocates nothing and never waits on the host, so a call can be captured
+    # once and replayed; each replay gives the direct call's result bit for bit
+    from gated_delta_rule_51_gb300 import kda
+
+    x = random_case(1, 700, 3, seed=951, lens=[300, 17, 383])
+    out_ref, fin_ref = run_gpu(x)
+    ws = torch.empty(kda.workspace_size(kda.make_shape(1, 700, 3, 3)), dtype=torch.uint8, device="cuda")
+    out = torch.full_like(out_ref, float("nan"))
+    fin = torch.full_like(fin_ref, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], out, x["A_log"], x["dt_bias"],
+                    x["lower_bound"], initial_state=x["initial_state"], final_state=fin,
+                    cu_seqlens=x["cu_seqlens"], workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        fin.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, out_ref)
+        assert torch.equal(fin, fin_ref)
