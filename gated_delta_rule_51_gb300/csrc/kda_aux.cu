@@ -28,6 +28,7 @@ namespace kda {
 // The first-phase list has one entry per slot (entry i writes slot i); the
 // entries of the unused transitions P_0 are no-ops (len = -1).
 constexpr int kSchedThreads = 1024;
+static_assert(kSchedThreads == 32 * 32, "block_scan scans one total per warp in one warp");
 
 __device__ __forceinline__ WorkItem make_item(long long row0, long long len, long long h, int mode, long long n,
                                               long long in_slot, long long out_slot, long long aux_slot) {
@@ -43,19 +44,29 @@ __device__ __forceinline__ WorkItem make_item(long long row0, long long len, lon
   return w;
 }
 
-// inclusive scan of one value per thread across the block
+// inclusive scan of one value per thread across the block: shuffles within each
+// warp, then the 32 warp totals scanned by warp 0 (two block barriers in all)
 __device__ long long block_scan(long long x, long long* buf) {
-  const int tid = threadIdx.x;
-  buf[tid] = x;
-  __syncthreads();
-  for (int off = 1; off < kSchedThreads; off <<= 1) {
-    const long long a = tid >= off ? buf[tid - off] : 0;
-    __syncthreads();
-    buf[tid] += a;
-    __syncthreads();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
   }
-  const long long r = buf[tid];
+  if (lane == 31) buf[warp] = x;
   __syncthreads();
+  if (warp == 0) {
+    long long t = buf[lane];   // kSchedThreads / 32 == 32 warp totals
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += y;
+    }
+    buf[lane] = t;
+  }
+  __syncthreads();
+  const long long r = x + (warp > 0 ? buf[warp - 1] : 0);
+  __syncthreads();   // buf is reused by the next scan
   return r;
 }
 
