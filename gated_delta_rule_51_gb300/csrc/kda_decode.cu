@@ -42,19 +42,21 @@ __device__ __forceinline__ void warp_sum16(float (&x)[kRowsPerWarp]) {
 
 __device__ __forceinline__ float sigmoidf(float x) { return 1.f / (1.f + expf(-x)); }
 
+template <int kVsplit, int kFlags>
 __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeParams p) {
-  // one CTA per (sequence, head, 128-row value block); V = 128 * vsplit
-  const int vblk = blockIdx.x % p.vsplit;
-  const int n = (blockIdx.x / p.vsplit) / p.H, h = (blockIdx.x / p.vsplit) % p.H;
-  const size_t V = (size_t)p.vsplit * 128;
+  // one CTA per (sequence, head, 128-row value block); V = 128 * kVsplit.  The CTA's
+  // 128 state rows are block blockIdx.x of the [B * H * V / 128, 128, 128] state.
+  const int vblk = kVsplit == 1 ? 0 : (int)(blockIdx.x % kVsplit);
+  const int nh = kVsplit == 1 ? (int)blockIdx.x : (int)(blockIdx.x / kVsplit);
+  const int n = nh / p.H, h = nh - n * p.H;
+  constexpr int V = kVsplit * 128;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ __align__(16) float s_alpha[128], s_kh[128], s_qh[128], s_v[128];
   __shared__ float s_norm[2][4];
   __shared__ float s_beta;
 
   // ---- the state rows of this warp, four key channels per lane
-  const size_t head = (size_t)n * p.H + h;
-  const size_t srow0 = head * V + (size_t)128 * vblk;   // first state row of this CTA
+  const size_t srow0 = (size_t)blockIdx.x * 128;   // first state row of this CTA
   float4 st[kRowsPerWarp];
   if (p.state_dtype == 2) {
     const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.state) + srow0 * 128);
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
       st[r] = make_float4(bf(w.x & 0xffffu), bf(w.x >> 16), bf(w.y & 0xffffu), bf(w.y >> 16));
     }
   }
-  const bool gate_pre = p.flags & kGatePreactivated;    // then A_log and dt_bias may be null
+  constexpr bool gate_pre = kFlags & kGatePreactivated;    // then A_log and dt_bias may be null
   const float rate = gate_pre ? 0.f : expf(p.A_log[h]);
 
 #pragma unroll 1
@@ -89,12 +91,12 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
         s_norm[1][warp] = sq;
       }
     }
-    if (tid == 0) s_beta = (p.flags & kBetaPreactivated) ? bf(p.beta[tok]) : sigmoidf(bf(p.beta[tok]));
+    if (tid == 0) s_beta = (kFlags & kBetaPreactivated) ? bf(p.beta[tok]) : sigmoidf(bf(p.beta[tok]));
     __syncthreads();
     if (tid < 128) {
       const float nk = s_norm[0][0] + s_norm[0][1] + s_norm[0][2] + s_norm[0][3];
       const float nq = s_norm[1][0] + s_norm[1][1] + s_norm[1][2] + s_norm[1][3];
-      const bool norm = !(p.flags & kNoQkL2Norm);
+      constexpr bool norm = !(kFlags & kNoQkL2Norm);
       s_kh[tid] = norm ? kk / sqrtf(nk + 1e-6f) : kk;
       s_qh[tid] = norm ? qq / sqrtf(nq + 1e-6f) : qq;
     }
@@ -147,7 +149,15 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
   const long long grid = (long long)p.B * p.H * p.vsplit;
   if (grid <= 0 || p.T <= 0) return cudaSuccess;
-  kda_decode_kernel<<<(unsigned)grid, kDecThreads, 0, s>>>(p);
+  // the value split and the flags are template parameters: the common case (V = 128,
+  // every step in the kernel) carries no per-thread tests of either
+  using Kernel = void (*)(DecodeParams);
+  static constexpr Kernel kernels[2][8] = {
+      {kda_decode_kernel<1, 0>, kda_decode_kernel<1, 1>, kda_decode_kernel<1, 2>, kda_decode_kernel<1, 3>,
+       kda_decode_kernel<1, 4>, kda_decode_kernel<1, 5>, kda_decode_kernel<1, 6>, kda_decode_kernel<1, 7>},
+      {kda_decode_kernel<2, 0>, kda_decode_kernel<2, 1>, kda_decode_kernel<2, 2>, kda_decode_kernel<2, 3>,
+       kda_decode_kernel<2, 4>, kda_decode_kernel<2, 5>, kda_decode_kernel<2, 6>, kda_decode_kernel<2, 7>}};
+  kernels[p.vsplit == 2 ? 1 : 0][p.flags & 7]<<<(unsigned)grid, kDecThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
