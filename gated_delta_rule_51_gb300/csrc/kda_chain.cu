@@ -158,11 +158,12 @@ __device__ __forceinline__ void pair_bar(int pair) { named_bar(1 + pair, 64); }
 // 2 gid / 2 gid + 1 play the fragment rows gid / gid + 8, and the channel pair
 // (8 tig + 2 s, + 1) the k positions (tig, tig + 4) of k-step s; the partial
 // Grams of the two warps are summed through shared memory.
+template <int kFlags>
 __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, PairScratch& sc, int pair, int w, int nv,
                                                     const float nr, const float lbl2,
                                                     const float* __restrict__ dtb, float beta_a, float beta_b,
-                                                    int lane, bool v_used, int flags) {
-  const bool gate_pre = flags & kGatePreactivated;
+                                                    int lane, bool v_used) {
+  constexpr bool gate_pre = kFlags & kGatePreactivated;
   const int gid = lane >> 2, tig = lane & 3;
   const int ra = 2 * gid, rb = 2 * gid + 1;
   const bool va = ra < nv, vb = rb < nv;
@@ -212,7 +213,7 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
     const float2 a = *reinterpret_cast<const float2*>(&sc.normx[0][ra + hr][0]);
     const float2 b = *reinterpret_cast<const float2*>(&sc.normx[1][ra + hr][0]);
     const bool valid = hr == 0 ? va : vb;
-    const bool norm = !(flags & kNoQkL2Norm);
+    constexpr bool norm = !(kFlags & kNoQkL2Norm);
     rq[hr] = valid ? (norm ? rsqrt_approx(a.x + b.x + 1e-6f) : 1.f) : 0.f;
     rk[hr] = valid ? (norm ? rsqrt_approx(a.y + b.y + 1e-6f) : 1.f) : 0.f;
   }
@@ -367,7 +368,7 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
   }
   pair_bar(pair);
   // beta of the lane's tokens
-  const bool beta_pre = flags & kBetaPreactivated;
+  constexpr bool beta_pre = kFlags & kBetaPreactivated;
   const float sa = va ? (beta_pre ? beta_a : rcp_approx(1.f + ex2_approx(-beta_a * kLog2e))) : 0.f;
   const float sb = vb ? (beta_pre ? beta_b : rcp_approx(1.f + ex2_approx(-beta_b * kLog2e))) : 0.f;
   if (w == 0) {
@@ -479,6 +480,9 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
   __syncwarp();
 }
 
+// kFlags (steps the caller already did) is a template parameter: the prologue's inner
+// loops then carry no per-element tests of it
+template <int kFlags>
 __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_constant__ ChainParams p) {
   if ((int)blockIdx.x >= *p.item_count) return;
   const WorkItem it = p.items[blockIdx.x];
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       PairScratch& sc = S.ps[pair];
       const int h = head;
       const int H = p.H;
-      const bool gate_pre = p.flags & kGatePreactivated;   // then A_log and dt_bias may be null
+      constexpr bool gate_pre = kFlags & kGatePreactivated;   // then A_log and dt_bias may be null
       const float nr = gate_pre ? 0.f : -expf(p.A_log[h]) * kLog2e;
       const float* dtb = gate_pre ? nullptr : p.dt_bias + (size_t)h * kDimK;
       const float lbl2 = p.lower_bound * kLog2e;
@@ -563,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         if (lane == 0) sc.okf[iter & 1][w] = okw ? 1 : 0;
         pair_bar(pair);
         if (!(sc.okf[iter & 1][0] && sc.okf[iter & 1][1])) break;
-        prologue_pair_chunk(S.st[s], S.sm[s], sc, pair, w, nv, nr, lbl2, dtb, cb0, cb1, lane, it.mode != kModeTransition,
-                            p.flags);
+        prologue_pair_chunk<kFlags>(S.st[s], S.sm[s], sc, pair, w, nv, nr, lbl2, dtb, cb0, cb1, lane,
+                                    it.mode != kModeTransition);
         if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
     } else {
@@ -897,6 +901,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
 }
 
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
+  using Kernel = void (*)(ChainParams);
+  static constexpr Kernel kernels[8] = {kda_chain_kernel<0>, kda_chain_kernel<1>, kda_chain_kernel<2>,
+                                        kda_chain_kernel<3>, kda_chain_kernel<4>, kda_chain_kernel<5>,
+                                        kda_chain_kernel<6>, kda_chain_kernel<7>};
   const size_t smem = chain_smem_bytes();
   // the shared-memory opt-in is a per-device setting: made once per device
   constexpr int kMaxDevices = 64;
@@ -905,12 +913,14 @@ cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(kda_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    for (Kernel k : kernels) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
   if (grid <= 0) return cudaSuccess;
-  kda_chain_kernel<<<grid, kThreads, smem, s>>>(p);
+  kernels[p.flags & 7]<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
