@@ -481,7 +481,7 @@ def run_decode(args, w):
     hbm_gbs, _, peak_kind = load_peaks()
     achieved = nbytes / (ms / 1000.0) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                "traffic": None, "kernel": "kda_decode_kernel",
+                "traffic": measured_traffic(w.name), "kernel": "kda_decode_kernel",
                 "peak_source": "measured, MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": nbytes}
