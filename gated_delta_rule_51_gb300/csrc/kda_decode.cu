@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
       s_alpha[tid] = expf(ghat);
       kk = bf(p.k[tok * 128 + tid]);
       qq = bf(p.q[tok * 128 + tid]);
+      s_kh[tid] = kk;
+      s_qh[tid] = qq;
       s_v[tid] = bf(p.v[tok * V + 128 * vblk + tid]);
       const float sk = warp_sum(kk * kk), sq = warp_sum(qq * qq);
       if (lane == 0) {
@@ -93,18 +95,17 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
     }
     if (tid == 0) s_beta = (kFlags & kBetaPreactivated) ? bf(p.beta[tok]) : sigmoidf(bf(p.beta[tok]));
     __syncthreads();
-    if (tid < 128) {
-      const float nk = s_norm[0][0] + s_norm[0][1] + s_norm[0][2] + s_norm[0][3];
-      const float nq = s_norm[1][0] + s_norm[1][1] + s_norm[1][2] + s_norm[1][3];
-      constexpr bool norm = !(kFlags & kNoQkL2Norm);
-      s_kh[tid] = norm ? kk / sqrtf(nk + 1e-6f) : kk;
-      s_qh[tid] = norm ? qq / sqrtf(nq + 1e-6f) : qq;
-    }
-    __syncthreads();
-    // ---- the rows: decay, delta update, output from the updated row
+    // ---- the rows: decay, delta update, output from the updated row (each lane
+    //      normalises its own four channels of k and q)
     const float4 al = reinterpret_cast<const float4*>(s_alpha)[lane];
-    const float4 kh = reinterpret_cast<const float4*>(s_kh)[lane];
-    const float4 qh = reinterpret_cast<const float4*>(s_qh)[lane];
+    float4 kh = reinterpret_cast<const float4*>(s_kh)[lane];
+    float4 qh = reinterpret_cast<const float4*>(s_qh)[lane];
+    if (!(kFlags & kNoQkL2Norm)) {
+      const float rk = 1.f / sqrtf(s_norm[0][0] + s_norm[0][1] + s_norm[0][2] + s_norm[0][3] + 1e-6f);
+      const float rq = 1.f / sqrtf(s_norm[1][0] + s_norm[1][1] + s_norm[1][2] + s_norm[1][3] + 1e-6f);
+      kh.x *= rk; kh.y *= rk; kh.z *= rk; kh.w *= rk;
+      qh.x *= rq; qh.y *= rq; qh.z *= rq; qh.w *= rq;
+    }
     const float beta = s_beta;
     float d[kRowsPerWarp];
 #pragma unroll
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
       p.out[tok * V + 128 * vblk + kRowsPerWarp * warp + lane] =
           __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * o));
     }
-    __syncthreads();   // the per-channel vectors are rewritten by the next token
+    if (t + 1 < p.T) __syncthreads();   // the per-channel vectors are rewritten by the next token
   }
 
   // ---- write the rows back
