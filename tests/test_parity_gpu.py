@@ -225,3 +225,19 @@ def test_forward_captured_in_a_cuda_graph_replays_identically():
         torch.cuda.synchronize()
         assert torch.equal(out, out_ref)
         assert torch.equal(fin, fin_ref)
+
+
+@pytest.mark.parametrize("total,H", [(262144, 32), (262144, 64)])
+def test_sweep_workloads_largest_cells_sampled(total, H):
+    """The largest sweep cells (16.8M token-heads at H = 64): every final state in full,
+    outputs on sampled rows (the first and last rows of every sequence and random ones)."""
+    w = I.sweep_workload(total, H)
+    x = I.make_inputs(w, device="cuda")
+    out, fin = run_gpu(x)
+    cu = x["cu_seqlens"].cpu().numpy()
+    rng = np.random.default_rng(total + H)
+    rows = np.unique(np.concatenate([cu[:-1], np.maximum(cu[1:] - 1, 0), rng.integers(0, total, 2048)]))
+    rows = rows[rows < total]
+    ref_out, ref_fin = run_oracle(x, out_rows=rows)
+    check_out(out, ref_out, rows=rows, label=w.name)
+    check_state(fin, ref_fin, label=w.name)
