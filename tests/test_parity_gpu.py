@@ -241,3 +241,23 @@ def test_sweep_workloads_largest_cells_sampled(total, H):
     ref_out, ref_fin = run_oracle(x, out_rows=rows)
     check_out(out, ref_out, rows=rows, label=w.name)
     check_state(fin, ref_fin, label=w.name)
+
+
+@pytest.mark.parametrize("lb,T,state_bound", [(-0.1, 2000, 1e-3), (0.0, 2000, 2.5e-3)])
+def test_weak_and_no_decay_long_runs(lb, T, state_bound):
+    """Near lower_bound = 0 nothing fades from the state, so the rounding of its bf16 copy (the
+    A operand of the S-side GEMM, relative error 2^-9 each chunk) builds up instead of
+    decaying away: the fp32 final state's rel-Fro error plateaus near 1.9e-3 at lower_bound = 0
+    (3e-4 at -0.1, 3e-5 to 6e-5 at the workloads' -1, -2 and -5). Outputs stay within their
+    bounds throughout. The 1e-3 state bound is asserted where it holds and the plateau is
+    pinned at lower_bound = 0."""
+    x = random_case(1, T, 4, seed=77, lb=lb)
+    ref_out, ref_fin = run_oracle(x)
+    out, fin = run_gpu(x)
+    check_out(out, ref_out, label=f"lb={lb} T={T}")
+    g = fin.double().cpu().numpy()
+    from tests.gpu_helpers import _report, rel_fro
+
+    rf = rel_fro(g, ref_fin)
+    _report(f"lb={lb} T={T}", "state_rel_fro_float32", rf)
+    assert rf <= state_bound, f"state rel-Fro {rf:.3e} > {state_bound}"
