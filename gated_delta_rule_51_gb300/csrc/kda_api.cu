@@ -81,8 +81,8 @@ int64_t choose_seg_tokens(const kda_shape& s, int sms) {
 
 struct Layout {
   int64_t seg_tokens = 0;
-  int64_t cap_forward = 0, cap_phase1 = 0, cap_compose = 0, cap_slots = 0;
-  size_t off_hdr = 0, off_forward = 0, off_phase1 = 0, off_compose = 0, off_slots = 0, total = 0;
+  int64_t cap_forward = 0, cap_phase1 = 0, cap_compose = 0, cap_slots = 0, cap_ranks = 0;
+  size_t off_hdr = 0, off_forward = 0, off_phase1 = 0, off_compose = 0, off_slots = 0, off_ranks = 0, total = 0;
 };
 
 Layout make_layout(const kda_shape& s, int sms) {
@@ -91,6 +91,7 @@ Layout make_layout(const kda_shape& s, int sms) {
   L.seg_tokens = choose_seg_tokens(s, sms);
   const int64_t splits = rows / L.seg_tokens;   // bound on sum over sequences of (nseg - 1)
   L.cap_forward = s.H * (splits + s.N);
+  L.cap_ranks = splits + s.N;
   const int64_t qcap = s.H * splits;
   L.cap_slots = 2 * qcap;
   L.cap_phase1 = 2 * qcap;
@@ -104,6 +105,8 @@ Layout make_layout(const kda_shape& s, int sms) {
   off = align_up(off + (size_t)L.cap_phase1 * sizeof(WorkItem));
   L.off_compose = off;
   off = align_up(off + (size_t)L.cap_compose * sizeof(ComposeItem));
+  L.off_ranks = off;
+  off = align_up(off + (size_t)L.cap_ranks * sizeof(int));
   L.off_slots = off;
   off = align_up(off + (size_t)L.cap_slots * kSlotBytes);
   L.total = off;
@@ -347,6 +350,8 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   sp.cap_forward = L.cap_forward;
   sp.cap_compose = L.cap_compose;
   sp.cap_slots = L.cap_slots;
+  sp.seg_rank = reinterpret_cast<int*>(ws + L.off_ranks);
+  sp.cap_ranks = L.cap_ranks;
   int launches = 0;
   if (launch_schedule(sp, stream) != cudaSuccess) return KDA_ERR_CUDA;
   ++launches;

@@ -70,7 +70,19 @@ __device__ long long block_scan(long long x, long long* buf) {
   return r;
 }
 
+// Forward runs are listed longest first, so that the first wave puts the longest runs one to
+// an SM and the short ones fill the second CTA slots and finish early: the long chains then
+// run alone for most of their length.  Runs are ranked by a length bucket, four buckets per
+// octave of chunk count (ties in arbitrary order; every run computes the same either way).
+constexpr int kLenBuckets = 4 * 32;
+__device__ __forceinline__ int len_bucket(long long chunks) {
+  if (chunks < 4) return (int)(chunks < 0 ? 0 : chunks);
+  const int msb = 63 - __clzll(chunks);
+  return 4 * msb + (int)((chunks >> (msb - 2)) & 3);
+}
+
 __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const ScheduleParams p) {
+  __shared__ unsigned int s_hist[kLenBuckets];
   __shared__ long long s_buf[kSchedThreads];
   __shared__ long long s_tot[3];   // segments, q slots, compose chains (running totals)
   __shared__ int s_start[kSchedThreads], s_len[kSchedThreads], s_nseg[kSchedThreads], s_incl[kSchedThreads];
@@ -87,6 +99,7 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
     s_max_chunks = 0;
     s_sum_chunks = 0;
   }
+  for (int i = tid; i < kLenBuckets; i += kSchedThreads) s_hist[i] = 0;
   __syncthreads();
   // Split long sequences only when one of them would outlast the rest of the
   // work by a wide margin: a split run costs a second pass over its tokens
@@ -122,6 +135,14 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
   const long long L = s_L;
   long long q_total = 0;
   for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1 && tid == 0) {   // bucket counts -> first rank of each bucket, longest first
+      unsigned int start = 0;
+      for (int bk = kLenBuckets - 1; bk >= 0; --bk) {
+        const unsigned int c = s_hist[bk];
+        s_hist[bk] = start;
+        start += c;
+      }
+    }
     if (tid == 0) s_tot[0] = s_tot[1] = s_tot[2] = 0;
     __syncthreads();
     for (long long base = 0; base < p.N; base += kSchedThreads) {
@@ -140,6 +161,16 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
           len = p.T;
         }
         nseg = len <= 0 ? 1 : (len + L - 1) / L;
+      }
+      // pass 0: histogram of the forward runs' lengths; pass 1: each run's rank
+      const long long seg0_scan = block_scan(nseg, s_buf) - nseg + s_tot[0];
+      if (n < p.N) {
+        for (long long sg = 0; sg < nseg; ++sg) {
+          const long long flen = len <= 0 ? 0 : (len - sg * L < L ? len - sg * L : L);
+          const int bk = len_bucket((flen + 15) / 16);
+          if (pass == 0) atomicAdd(&s_hist[bk], 1u);
+          else if (seg0_scan + sg < p.cap_ranks) p.seg_rank[seg0_scan + sg] = (int)atomicAdd(&s_hist[bk], 1u);
+        }
       }
       const long long nq = nseg >= 2 ? nseg - 1 : 0;
       const long long nc = nseg >= 3 ? 1 : 0;
@@ -176,7 +207,8 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
           const long long qb = s_q0[nl] * H + h * nq_;    // q slot of segment 0
           const long long pb = qb + q_total * H;          // p slot of segment 0
           const long long nn = base + nl;
-          const long long fi = (s_seg0[nl] + s) * H + h;
+          const long long sgi = s_seg0[nl] + s;
+          const long long fi = (sgi < p.cap_ranks ? (long long)p.seg_rank[sgi] : sgi) * H + h;
           const long long flen = ln <= 0 ? 0 : (ln - s * L < L ? ln - s * L : L);
           long long in_slot;
           if (s == 0) in_slot = (ns >= 2 && p.has_init) ? pb : in_user;

@@ -88,6 +88,8 @@ struct ScheduleParams {
   WorkItem* forward;
   ComposeItem* compose;
   long long cap_phase1, cap_forward, cap_compose, cap_slots;
+  int* seg_rank;              // scratch: position of each forward run's segment in the list
+  long long cap_ranks;
 };
 
 // Steps the caller already did (include/kda.h KDA_GATE_PREACTIVATED, ...).
