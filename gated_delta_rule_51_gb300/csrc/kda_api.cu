@@ -82,7 +82,8 @@ int64_t choose_seg_tokens(const kda_shape& s, int sms) {
 struct Layout {
   int64_t seg_tokens = 0;
   int64_t cap_forward = 0, cap_phase1 = 0, cap_compose = 0, cap_slots = 0, cap_ranks = 0;
-  size_t off_hdr = 0, off_forward = 0, off_phase1 = 0, off_compose = 0, off_slots = 0, off_ranks = 0, total = 0;
+  size_t off_hdr = 0, off_forward = 0, off_phase1 = 0, off_compose = 0, off_slots = 0, off_ranks = 0, off_sm = 0;
+  size_t total = 0;
 };
 
 Layout make_layout(const kda_shape& s, int sms) {
@@ -107,6 +108,8 @@ Layout make_layout(const kda_shape& s, int sms) {
   off = align_up(off + (size_t)L.cap_compose * sizeof(ComposeItem));
   L.off_ranks = off;
   off = align_up(off + (size_t)L.cap_ranks * sizeof(int));
+  L.off_sm = off;
+  off = align_up(off + (size_t)kMaxSmIds * sizeof(int));
   L.off_slots = off;
   off = align_up(off + (size_t)L.cap_slots * kSlotBytes);
   L.total = off;
@@ -352,6 +355,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   sp.cap_slots = L.cap_slots;
   sp.seg_rank = reinterpret_cast<int*>(ws + L.off_ranks);
   sp.cap_ranks = L.cap_ranks;
+  sp.sm_arrivals = reinterpret_cast<int*>(ws + L.off_sm);
   int launches = 0;
   if (launch_schedule(sp, stream) != cudaSuccess) return KDA_ERR_CUDA;
   ++launches;
@@ -379,6 +383,8 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   cp.scale = scale;
   cp.lower_bound = lower_bound;
   cp.flags = (int)flags;
+  cp.take = nullptr;
+  cp.sm_arrivals = nullptr;
 
   if (L.cap_phase1 > 0) {
     cp.items = sp.phase1;
@@ -399,6 +405,8 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   }
   cp.items = sp.forward;
   cp.item_count = &hdr->n_forward;
+  cp.take = hdr->take;
+  cp.sm_arrivals = sp.sm_arrivals;
   if (launch_chain(cp, (int)L.cap_forward, stream) != cudaSuccess) return KDA_ERR_CUDA;
   ++launches;
   mark(3, stream);

@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
     s_sum_chunks = 0;
   }
   for (int i = tid; i < kLenBuckets; i += kSchedThreads) s_hist[i] = 0;
+  for (int i = tid; i < kMaxSmIds; i += kSchedThreads) p.sm_arrivals[i] = 0;
+  if (tid < 3) p.hdr->take[tid] = 0;
   __syncthreads();
   // Split long sequences only when one of them would outlast the rest of the
   // work by a wide margin: a split run costs a second pass over its tokens

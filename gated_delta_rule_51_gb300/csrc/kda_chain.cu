@@ -484,8 +484,30 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
 // loops then carry no per-element tests of it
 template <int kFlags>
 __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_constant__ ChainParams p) {
-  if ((int)blockIdx.x >= *p.item_count) return;
-  const WorkItem it = p.items[blockIdx.x];
+  // Item of this CTA.  The forward launch pairs runs by SM: the list is longest first, the
+  // first CTA to start on an SM takes the longest run left and the second the shortest, so
+  // a long chain shares its SM with a short one and then runs alone.
+  int item = blockIdx.x;
+  if (p.take != nullptr) {
+    __shared__ int s_item;
+    if (threadIdx.x == 0) {
+      const int n_items = *p.item_count;
+      int pick = -1;
+      if (atomicAdd(&p.take[0], 1) < n_items) {   // at most n_items picks: head and tail never meet
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        const int arrival = atomicAdd(&p.sm_arrivals[smid % kMaxSmIds], 1);
+        pick = (arrival & 1) == 0 ? atomicAdd(&p.take[1], 1) : n_items - 1 - atomicAdd(&p.take[2], 1);
+      }
+      s_item = pick;
+    }
+    __syncthreads();
+    item = s_item;
+    if (item < 0) return;
+  } else if (item >= *p.item_count) {
+    return;
+  }
+  const WorkItem it = p.items[item];
   if (it.len < 0) return;   // placeholder entry of a work list
   const int nchunks = (it.len + kChunk - 1) / kChunk;
   // work items count heads x value blocks: V = 128 * vsplit columns are independent

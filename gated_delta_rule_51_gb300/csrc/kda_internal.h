@@ -35,8 +35,10 @@ struct WorkHeader {
   int n_phase1;        // number of segment items of the first phase
   int n_forward;       // number of forward items
   int n_compose;       // number of (sequence, head) carry chains to compose
-  int pad[4];
+  int take[3];         // forward runs handed out: total, from the head, from the tail
+  int pad;
 };
+constexpr int kMaxSmIds = 256;   // per-SM arrival counters of the forward launch
 
 struct ComposeItem {
   int head;
@@ -59,6 +61,8 @@ struct ChainParams {
   float* ws_states;                    // workspace state slots, 128*128 fp32 each
   const WorkItem* items;
   const int* item_count;
+  int* take;                           // non-null: CTAs pick items by SM pairing (WorkHeader::take)
+  int* sm_arrivals;                    // [kMaxSmIds] CTAs that started on each SM
   int* err;
   int H;
   int init_dtype;                      // kda_state_dtype
@@ -90,6 +94,7 @@ struct ScheduleParams {
   long long cap_phase1, cap_forward, cap_compose, cap_slots;
   int* seg_rank;              // scratch: position of each forward run's segment in the list
   long long cap_ranks;
+  int* sm_arrivals;           // [kMaxSmIds], zeroed here for the forward launch
 };
 
 // Steps the caller already did (include/kda.h KDA_GATE_PREACTIVATED, ...).
