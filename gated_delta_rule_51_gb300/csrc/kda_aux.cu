@@ -271,50 +271,102 @@ cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s) {
 // S^T_{s+1} = S^T_s P^T_s + Q^T_s, all 128 x 128 fp32 in the [V, K] layout:
 // out[v][k] = sum_m in[v][m] * Pst[m][k] + Qst[v][k] where Pst is the stored
 // transition slot (row m = column m of P).  Rows of S^T are independent, so
-// each CTA owns 16 rows of one (sequence, head) chain and walks its segments.
+// each CTA owns 16 rows of one (sequence, head) chain and walks its segments:
+// S_{s+1} = S_s P_s + Q_s on its rows.  The chain is sequential, so each step's
+// operands (the 64 KiB transition P_s and the CTA's 8 KiB of Q_s) are brought into
+// shared memory by bulk copies one step ahead, while the current step computes.
 constexpr int kComposeRows = 16;
 constexpr int kComposeThreads = 256;
+constexpr uint32_t kPBytes = 128 * 128 * 4;
+constexpr uint32_t kQBytes = kComposeRows * 128 * 4;
+
+struct ComposeSmem {
+  float P[2][128][128];
+  float Q[2][kComposeRows][128];
+  float S[kComposeRows][128];
+};
+
+__device__ __forceinline__ void bulk_load_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 
 __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const ComposeParams p) {
   const int item = blockIdx.x / (128 / kComposeRows);
   const int part = blockIdx.x % (128 / kComposeRows);
   if (item >= *p.item_count) return;
   const ComposeItem ci = p.items[item];
-  __shared__ float s_in[kComposeRows][128];
+  extern __shared__ __align__(128) uint8_t csm[];
+  ComposeSmem& S = *reinterpret_cast<ComposeSmem*>(csm);
+  __shared__ __align__(8) uint64_t bar[2];
   const int tid = threadIdx.x;
   const int k = tid & 127;
   const int vh = tid >> 7;   // rows vh*8 .. vh*8+7 of this CTA's 16
   const int v0 = part * kComposeRows;
   float* slots = p.ws_states;
+  auto P_src = [&](int st) { return slots + (size_t)(ci.first_p_slot + st - 1) * 16384; };
+  auto Q_row0 = [&](int st) { return slots + (size_t)(ci.first_q_slot + st) * 16384 + (size_t)v0 * 128; };
+  auto fetch = [&](int st) {   // operands of step st into buffer st & 1 (thread 0)
+    uint64_t* b = &bar[st & 1];
+    mbar_arrive_expect_tx(b, kPBytes + kQBytes);
+    bulk_load_g2s(&S.P[st & 1][0][0], P_src(st), kPBytes, b);
+    bulk_load_g2s(&S.Q[st & 1][0][0], Q_row0(st), kQBytes, b);
+  };
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    mbar_fence_init();
+  }
   // S_1 = Q slot 0 (already the true state after segment 0)
   for (int i = tid; i < kComposeRows * 128; i += kComposeThreads)
-    s_in[i / 128][i % 128] = slots[(size_t)ci.first_q_slot * 16384 + (size_t)(v0 + i / 128) * 128 + i % 128];
+    S.S[i / 128][i % 128] = slots[(size_t)ci.first_q_slot * 16384 + (size_t)(v0 + i / 128) * 128 + i % 128];
   __syncthreads();
-  for (int s = 1; s <= ci.n_steps; ++s) {
-    const float* P = slots + (size_t)(ci.first_p_slot + s - 1) * 16384;
-    float* Q = slots + (size_t)(ci.first_q_slot + s) * 16384;
+  if (tid == 0) {
+    if (ci.n_steps >= 1) fetch(1);
+    if (ci.n_steps >= 2) fetch(2);
+  }
+  for (int st = 1; st <= ci.n_steps; ++st) {
+    const int b = st & 1;
+    {
+      const long long t0 = clock64();   // bounded: the copy always lands; the data is garbage otherwise
+      while (!mbar_try_wait(&bar[b], ((st - 1) >> 1) & 1))
+        if (clock64() - t0 > kWaitTimeoutCycles) break;
+    }
     float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = Q[(size_t)(v0 + vh * 8 + i) * 128 + k];
-#pragma unroll 4
+    for (int i = 0; i < 8; ++i) acc[i] = S.Q[b][vh * 8 + i][k];
+#pragma unroll 8
     for (int m = 0; m < 128; ++m) {
-      const float pm = P[(size_t)m * 128 + k];
+      const float pm = S.P[b][m][k];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(s_in[vh * 8 + i][m], pm, acc[i]);
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(S.S[vh * 8 + i][m], pm, acc[i]);
     }
-    __syncthreads();
+    __syncthreads();   // every thread is done with S and with buffer b
+    float* Q = Q_row0(st);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      s_in[vh * 8 + i][k] = acc[i];
-      Q[(size_t)(v0 + vh * 8 + i) * 128 + k] = acc[i];
+      S.S[vh * 8 + i][k] = acc[i];
+      Q[(size_t)(vh * 8 + i) * 128 + k] = acc[i];
+    }
+    if (tid == 0 && st + 2 <= ci.n_steps) {
+      fence_proxy_async_smem();   // the generic reads of buffer b are ordered before the refill
+      fetch(st + 2);
     }
     __syncthreads();
   }
 }
 
+size_t compose_smem_bytes() { return sizeof(ComposeSmem); }
+
 cudaError_t launch_compose(const ComposeParams& p, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
-  kda_compose_kernel<<<grid * (128 / kComposeRows), kComposeThreads, 0, s>>>(p);
+  const int smem = (int)compose_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(kda_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kda_compose_kernel<<<grid * (128 / kComposeRows), kComposeThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
