@@ -92,7 +92,8 @@ def _ptr(a: Optional[np.ndarray]):
 def kda_forward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None,
                 cu_seqlens=None, out_rows=None, want_out=True, want_final_state=True,
                 nthreads: Optional[int] = None, use_gate_in_kernel: bool = True,
-                use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True):
+                use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True,
+                safe_gate: bool = True):
     """Run the fp64 token recurrence.
 
     q, k, g: [B,T,H,K] bf16; v: [B,T,H,V] bf16; beta: [B,T,H] bf16 (torch
@@ -105,7 +106,12 @@ def kda_forward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_st
     The three use_* switches mirror the reference call's flags: when False, g
     already holds the natural-log decay (A_log, dt_bias and lower_bound are then
     unused), beta already holds beta, or q and k are used without L2 norms.
+    safe_gate=False selects the gate without a lower bound,
+    ghat = -exp(A_log) * softplus(g + dt_bias) (lower_bound unused); it needs
+    use_gate_in_kernel=True.
     """
+    if not safe_gate and not use_gate_in_kernel:
+        raise ValueError("safe_gate=False applies to the in-kernel gate only")
     qb, kb, vb, gb, bb = (_bits(x) for x in (q, k, v, g, beta))
     B, T, H, K = qb.shape
     V = vb.shape[-1]
@@ -133,7 +139,7 @@ def kda_forward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_st
     if nthreads is None:
         nthreads = os.cpu_count() or 1
     flags = ((0 if use_gate_in_kernel else 1) | (0 if use_beta_sigmoid_in_kernel else 2)
-             | (0 if use_qk_l2norm_in_kernel else 4))
+             | (0 if use_qk_l2norm_in_kernel else 4) | (0 if safe_gate else 8))
     rc = _load().kda_oracle_fwd(B, T, H, K, V, N, flags, _ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb),
                                 _ptr(bb), float(np.float32(scale)), _ptr(A), _ptr(D),
                                 float(np.float32(lower_bound)), _ptr(s0), _ptr(out),

@@ -23,7 +23,12 @@
  *   ORACLE_GATE_PREACTIVATED (1): g already holds ghat (natural-log decay), so
  *       alpha_t = exp(g_t); A_log, dt_bias and lower_bound are not used;
  *   ORACLE_BETA_PREACTIVATED (2): beta already holds beta_t (no sigmoid);
- *   ORACLE_NO_QK_L2NORM      (4): qh = q_t and kh = k_t as given.
+ *   ORACLE_NO_QK_L2NORM      (4): qh = q_t and kh = k_t as given;
+ * and one selects the other gate of the reference call (its safe_gate switch
+ * turned off):
+ *   ORACLE_GATE_SOFTPLUS     (8): ghat_t[c] = -exp(A_log[h]) * softplus(g_t[c] + dt_bias[h,c]),
+ *       softplus(x) = log(1 + exp(x)); lower_bound is not used.  It cannot be
+ *       combined with ORACLE_GATE_PREACTIVATED.
  *
  * Readings where the pages are silent: the gate is a sigmoid scaled by the
  * lower bound (README "safe_gate", "Gate lower bound (range from -5.0 to 0)");
@@ -52,7 +57,11 @@ static double bf16_to_double(uint16_t bits) {
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
-enum { ORACLE_GATE_PREACTIVATED = 1, ORACLE_BETA_PREACTIVATED = 2, ORACLE_NO_QK_L2NORM = 4 };
+enum { ORACLE_GATE_PREACTIVATED = 1, ORACLE_BETA_PREACTIVATED = 2, ORACLE_NO_QK_L2NORM = 4,
+       ORACLE_GATE_SOFTPLUS = 8 };
+
+/* log(1 + exp(x)) without overflow: x + log1p(exp(-x)) for x > 0 */
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
 
 typedef struct {
     int64_t B, T, H, K, V, N;
@@ -90,6 +99,7 @@ static void run_pair(oracle_job *J, int64_t n, int64_t h, double *S, double *qh,
         memset(S, 0, sizeof(double) * (size_t)(K * V));
     }
     const int gate_pre = J->flags & ORACLE_GATE_PREACTIVATED;
+    const int gate_softplus = J->flags & ORACLE_GATE_SOFTPLUS;
     const double rate = gate_pre ? 0.0 : exp((double)J->A_log[h]);
     for (int64_t t = t0; t < t1; ++t) {
         const uint16_t *qt = J->q + (t * H + h) * K;
@@ -110,6 +120,8 @@ static void run_pair(oracle_job *J, int64_t n, int64_t h, double *S, double *qh,
             kh[c] *= kinv;
             if (gate_pre) {
                 alpha[c] = exp(bf16_to_double(gt[c]));
+            } else if (gate_softplus) {
+                alpha[c] = exp(-rate * softplus(bf16_to_double(gt[c]) + (double)J->dt_bias[h * K + c]));
             } else {
                 double x = rate * (bf16_to_double(gt[c]) + (double)J->dt_bias[h * K + c]);
                 alpha[c] = exp(J->lower_bound * sigmoid(x));
@@ -183,6 +195,7 @@ int kda_oracle_fwd(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, int64_
     if (B < 0 || T < 0 || H <= 0 || K <= 0 || V <= 0 || N < 0) return -1;
     if (!cu_seqlens && N != B) return -1;
     if (cu_seqlens && B != 1) return -1;
+    if ((flags & ORACLE_GATE_PREACTIVATED) && (flags & ORACLE_GATE_SOFTPLUS)) return -1;
     if (nthreads < 1) nthreads = 1;
     oracle_job J;
     J.B = B; J.T = T; J.H = H; J.K = K; J.V = V; J.N = N; J.flags = flags;
