@@ -207,6 +207,7 @@ const char* kda_status_string(kda_status s) {
     case KDA_ERR_CUDA: return "CUDA error";
     case KDA_ERR_TIMEOUT: return "a device-side wait timed out";
     case KDA_ERR_BAD_SEQLENS: return "malformed cu_seqlens";
+    case KDA_ERR_GATE_RANGE: return "a 16-token chunk's decay left the range the chunked form factors exactly";
   }
   return "unknown status";
 }
@@ -221,6 +222,14 @@ kda_status kda_workspace_size(const kda_shape* shape, size_t* bytes) {
   return KDA_OK;
 }
 
+// kda_flags: known bits only, and the preactivated and softplus gates exclude each other
+static bool valid_flags(unsigned flags) {
+  if (flags & ~kda::kValidFlags) return false;
+  return !((flags & KDA_GATE_PREACTIVATED) && (flags & KDA_GATE_SOFTPLUS));
+}
+// only the in-kernel safe gate reads lower_bound
+static bool uses_lower_bound(unsigned flags) { return !(flags & (KDA_GATE_PREACTIVATED | KDA_GATE_SOFTPLUS)); }
+
 kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, const void* v, const void* g,
                       const void* beta, float scale, void* out, const float* A_log, const float* dt_bias,
                       float lower_bound, void* state, kda_state_dtype state_dtype, unsigned flags,
@@ -230,9 +239,9 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
   const kda_shape s = *shape;
   if (s.N != s.B) return KDA_ERR_INVALID_ARGUMENT;
   if ((long long)s.B * s.H * (s.V / 128) > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
-  if (flags & ~7u) return KDA_ERR_INVALID_ARGUMENT;
+  if (!valid_flags(flags)) return KDA_ERR_INVALID_ARGUMENT;
   const bool gate_here = !(flags & KDA_GATE_PREACTIVATED);
-  if (gate_here && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
+  if (uses_lower_bound(flags) && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
   auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
   if (s.B * s.T > 0) {
@@ -294,9 +303,9 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   } else if (s.N != s.B) {
     return KDA_ERR_INVALID_ARGUMENT;
   }
-  if (flags & ~7u) return KDA_ERR_INVALID_ARGUMENT;
+  if (!valid_flags(flags)) return KDA_ERR_INVALID_ARGUMENT;
   const bool gate_here = !(flags & KDA_GATE_PREACTIVATED);
-  if (gate_here && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
+  if (uses_lower_bound(flags) && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
   const int64_t rows = s.B * s.T;
   // q, k, g, v are read by TMA (16-byte aligned base); beta and out are accessed
@@ -438,6 +447,7 @@ kda_status kda_check_device_error(const void* workspace, kda_stream_t stream_, i
   *flags = err;
   if (err & kErrTimeout) return KDA_ERR_TIMEOUT;
   if (err & kErrBadSeqlens) return KDA_ERR_BAD_SEQLENS;
+  if (err & kErrGateRange) return KDA_ERR_GATE_RANGE;
   return KDA_OK;
 }
 

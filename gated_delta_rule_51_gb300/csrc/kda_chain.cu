@@ -7,6 +7,9 @@
 //
 //   G    = within-chunk inclusive cumsum of the base-2 log-decay (per channel)
 //   Akk  = tril(beta_i * (kh*2^G)(kh*2^-G)^T, -1)   Aqk = tril((qh*2^G)(kh*2^-G)^T, 0)
+//          (the Gram factors are taken about a = G_C / 2, 2^(G-a) and 2^(a-G), so that
+//          no factor leaves 2^+-125 while |G_C| <= 250; beyond that the chunk sets the
+//          gate-range error bit)
 //   Tm   = (I + Akk)^-1 Diag(beta)          (forward substitution, fp32)
 //   W    = Tm (kh*2^G),  U = Tm v,  Vn = U - W S
 //   O    = scale * ((qh*2^G) S + Aqk Vn)
@@ -160,10 +163,14 @@ __device__ __forceinline__ void pair_bar(int pair) { named_bar(1 + pair, 64); }
 // Grams of the two warps are summed through shared memory.
 template <int kFlags>
 __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, PairScratch& sc, int pair, int w, int nv,
-                                                    const float nr, const float lbl2,
+                                                    int* err, const float nr, const float lbl2,
                                                     const float* __restrict__ dtb, float beta_a, float beta_b,
                                                     int lane, bool v_used) {
   constexpr bool gate_pre = kFlags & kGatePreactivated;
+  constexpr bool gate_sp = kFlags & kGateSoftplus;   // then nr = log2(e), lbl2 = -exp(A_log)
+  // the safe gate keeps |G_C| <= 16 * 5 * log2(e) < 126, where the Gram factors 2^+-G are
+  // exact as they are; the other two gates factor about the anchor a = G_C / 2
+  constexpr bool anchored = gate_pre || gate_sp;
   const int gid = lane >> 2, tig = lane & 3;
   const int ra = 2 * gid, rb = 2 * gid + 1;
   const bool va = ra < nv, vb = rb < nv;
@@ -256,12 +263,24 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
         k[hr][2 * u] = bf16lo_to_f32(ak[u]);
         k[hr][2 * u + 1] = bf16hi_to_f32(ak[u]);
         // gate: base-2 log-decay lb * log2(e) * sigmoid(exp(A_log) (g + dt_bias)), or
-        // log2(e) g for a gate activated by the caller; 0 past the end
+        // -exp(A_log) log2(1 + 2^y) with y = log2(e) (g + dt_bias) (the gate without a
+        // lower bound: log2(e) softplus), or log2(e) g for a gate activated by the
+        // caller; 0 past the end
         float r0, r1;
         if (gate_pre) {
           r0 = bf16lo_to_f32(ag[u]);
           r1 = bf16hi_to_f32(ag[u]);
           const float lv = valid ? kLog2e : 0.f;
+          fmul2(r0, r1, lv, lv);
+        } else if (gate_sp) {
+          float y0, y1;
+          ffma2(y0, y1, nr, nr, bf16lo_to_f32(ag[u]), bf16hi_to_f32(ag[u]), nrdb[2 * u], nrdb[2 * u + 1]);
+          // log2(1 + 2^y) = max(y, 0) + log2(1 + 2^-|y|)
+          float t0 = ex2_approx(-fabsf(y0)), t1 = ex2_approx(-fabsf(y1));
+          fadd2(t0, t1, 1.f, 1.f);
+          r0 = fmaxf(y0, 0.f) + lg2_approx(t0);
+          r1 = fmaxf(y1, 0.f) + lg2_approx(t1);
+          const float lv = valid ? lbl2 : 0.f;
           fmul2(r0, r1, lv, lv);
         } else {
           float x0, x1;
@@ -293,17 +312,26 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
       G[1][j] = incl;
       gC[j] = __shfl_sync(0xffffffffu, incl, 28 + tig);
     }
-    float eC[8];
+    // the chunk's decay must stay within the anchored factors' range on every channel
+    if (anchored) {
+      bool bad = false;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) eC[j] = ex2_approx(gC[j]);
-    // ---- decay-scaled operands
+      for (int j = 0; j < 8; ++j) bad = bad || !(fabsf(gC[j]) <= 250.f);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrGateRange);
+    }
+    float eA[8];   // 2^a with the anchor a = G_C / 2 (anchored), else 2^G_C
+#pragma unroll
+    for (int j = 0; j < 8; ++j) eA[j] = ex2_approx(anchored ? 0.5f * gC[j] : gC[j]);
+    // ---- decay-scaled operands: the Gram factors about the anchor (2^(G-a), 2^(a-G))
     float kg[2][8], ki[2][8], qg[2][8];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
-        const float gam0 = ex2_approx(G[hr][j]), gam1 = ex2_approx(G[hr][j + 1]);
-        const float gin0 = ex2_approx(-G[hr][j]), gin1 = ex2_approx(-G[hr][j + 1]);
+        const float d0 = anchored ? fmaf(-0.5f, gC[j], G[hr][j]) : G[hr][j];
+        const float d1 = anchored ? fmaf(-0.5f, gC[j + 1], G[hr][j + 1]) : G[hr][j + 1];
+        const float gam0 = ex2_approx(d0), gam1 = ex2_approx(d1);
+        const float gin0 = ex2_approx(-d0), gin1 = ex2_approx(-d1);
         float kh0 = k[hr][j], kh1 = k[hr][j + 1];
         fmul2(kh0, kh1, rk[hr], rk[hr]);
         float qh0 = q[hr][j], qh1 = q[hr][j + 1];
@@ -331,29 +359,47 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
       mma_tf32_16x8x8(cq0, aq, b0);
       mma_tf32_16x8x8(cq1, aq, b1);
     }
-    // ---- operand tiles, written in place
+    // ---- operand tiles, written in place: qh*2^G and kh*2^G (anchored: the factor times 2^a),
+    //      kfac = kh*2^(G_C-G) (2^-G times 2^G_C; anchored: 2^(a-G) times 2^a)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const uint32_t o = sw_off(ra + hr, j16);
-      *reinterpret_cast<uint4*>(qb + o) =
-          make_uint4(pack_bf16x2(qg[hr][0], qg[hr][1]), pack_bf16x2(qg[hr][2], qg[hr][3]),
-                     pack_bf16x2(qg[hr][4], qg[hr][5]), pack_bf16x2(qg[hr][6], qg[hr][7]));
-      *reinterpret_cast<uint4*>(wb + o) =
-          make_uint4(pack_bf16x2(kg[hr][0], kg[hr][1]), pack_bf16x2(kg[hr][2], kg[hr][3]),
-                     pack_bf16x2(kg[hr][4], kg[hr][5]), pack_bf16x2(kg[hr][6], kg[hr][7]));
+      {
+        uint32_t qw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float a0 = qg[hr][2 * u], a1 = qg[hr][2 * u + 1];
+          if (anchored) fmul2(a0, a1, eA[2 * u], eA[2 * u + 1]);
+          qw[u] = pack_bf16x2(a0, a1);
+        }
+        *reinterpret_cast<uint4*>(qb + o) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+      }
+      {
+        uint32_t kw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float b0 = kg[hr][2 * u], b1 = kg[hr][2 * u + 1];
+          if (anchored) fmul2(b0, b1, eA[2 * u], eA[2 * u + 1]);
+          kw[u] = pack_bf16x2(b0, b1);
+        }
+        *reinterpret_cast<uint4*>(wb + o) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+      }
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         float f0 = ki[hr][2 * u], f1 = ki[hr][2 * u + 1];
-        fmul2(f0, f1, eC[2 * u], eC[2 * u + 1]);
+        fmul2(f0, f1, eA[2 * u], eA[2 * u + 1]);
         split_bf16x2(f0, f1, hw[u], lw[u]);
       }
       *reinterpret_cast<uint4*>(kb + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *reinterpret_cast<uint4*>(gb + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
-    if (gid == 0) {
-      *reinterpret_cast<float4*>(&sm.gamC[ch0]) = make_float4(eC[0], eC[1], eC[2], eC[3]);
-      *reinterpret_cast<float4*>(&sm.gamC[ch0 + 4]) = make_float4(eC[4], eC[5], eC[6], eC[7]);
+    if (gid == 0) {   // 2^G_C (anchored: (2^a)^2)
+      float e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) e[j] = anchored ? eA[j] * eA[j] : eA[j];
+      *reinterpret_cast<float4*>(&sm.gamC[ch0]) = make_float4(e[0], e[1], e[2], e[3]);
+      *reinterpret_cast<float4*>(&sm.gamC[ch0 + 4]) = make_float4(e[4], e[5], e[6], e[7]);
     }
   }
   // ---- Gram exchange: warp 1 hands its Gk partial to warp 0, warp 0 its Gq partial
@@ -565,9 +611,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       const int h = head;
       const int H = p.H;
       constexpr bool gate_pre = kFlags & kGatePreactivated;   // then A_log and dt_bias may be null
-      const float nr = gate_pre ? 0.f : -expf(p.A_log[h]) * kLog2e;
+      constexpr bool gate_sp = kFlags & kGateSoftplus;
+      const float rate = gate_pre ? 0.f : expf(p.A_log[h]);
+      // the gate's scale terms: the sigmoid gate takes -exp(A_log) log2(e) (g + dt_bias) and
+      // lower_bound log2(e); the softplus gate log2(e) (g + dt_bias) and -exp(A_log)
+      const float nr = gate_pre ? 0.f : (gate_sp ? kLog2e : -rate * kLog2e);
       const float* dtb = gate_pre ? nullptr : p.dt_bias + (size_t)h * kDimK;
-      const float lbl2 = p.lower_bound * kLog2e;
+      const float lbl2 = gate_sp ? -rate : p.lower_bound * kLog2e;
       const int gid = lane >> 2;
       auto load_beta = [&](int c, float& b0, float& b1) {
         const int base = it.row0 + c * kChunk;
@@ -589,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         if (lane == 0) sc.okf[iter & 1][w] = okw ? 1 : 0;
         pair_bar(pair);
         if (!(sc.okf[iter & 1][0] && sc.okf[iter & 1][1])) break;
-        prologue_pair_chunk<kFlags>(S.st[s], S.sm[s], sc, pair, w, nv, nr, lbl2, dtb, cb0, cb1, lane,
+        prologue_pair_chunk<kFlags>(S.st[s], S.sm[s], sc, pair, w, nv, p.err, nr, lbl2, dtb, cb0, cb1, lane,
                                     it.mode != kModeTransition);
         if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
@@ -924,9 +974,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
 
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
   using Kernel = void (*)(ChainParams);
-  static constexpr Kernel kernels[8] = {kda_chain_kernel<0>, kda_chain_kernel<1>, kda_chain_kernel<2>,
-                                        kda_chain_kernel<3>, kda_chain_kernel<4>, kda_chain_kernel<5>,
-                                        kda_chain_kernel<6>, kda_chain_kernel<7>};
+  // (the preactivated and softplus gates exclude each other: no kernel for both)
+  static constexpr Kernel kernels[16] = {
+      kda_chain_kernel<0>, kda_chain_kernel<1>, kda_chain_kernel<2>, kda_chain_kernel<3>,
+      kda_chain_kernel<4>, kda_chain_kernel<5>, kda_chain_kernel<6>, kda_chain_kernel<7>,
+      kda_chain_kernel<8>, nullptr, kda_chain_kernel<10>, nullptr,
+      kda_chain_kernel<12>, nullptr, kda_chain_kernel<14>, nullptr};
   const size_t smem = chain_smem_bytes();
   // the shared-memory opt-in is a per-device setting: made once per device
   constexpr int kMaxDevices = 64;
@@ -936,13 +989,16 @@ cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
     for (Kernel k : kernels) {
+      if (k == nullptr) continue;
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
     }
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
   if (grid <= 0) return cudaSuccess;
-  kernels[p.flags & 7]<<<grid, kThreads, smem, s>>>(p);
+  const Kernel k = kernels[p.flags & 15];
+  if (k == nullptr) return cudaErrorInvalidValue;
+  k<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -5,7 +5,8 @@
 // S^T (row v holds S[:, v] over the 128 key channels k), the step is the KDA
 // recurrence itself (FlashKDA README "Kernel API" parameter table for the
 // inputs, gate and layout):
-//   ghat  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h, :]))   (or g_t given)
+//   ghat  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h, :]))   (or g_t given, or
+//           -exp(A_log[h]) * softplus(g_t + dt_bias[h, :]) for the gate without a lower bound)
 //   beta  = sigmoid(beta logit) (or given);  qh, kh = x / sqrt(|x|^2 + 1e-6) (or as given)
 //   row v of S^T:  s <- s * exp(ghat);  s <- s + beta (v_v - s . kh) kh
 //   o_v   = scale * s . qh        (from the updated row)
@@ -41,6 +42,8 @@ __device__ __forceinline__ void warp_sum16(float (&x)[kRowsPerWarp]) {
 }
 
 __device__ __forceinline__ float sigmoidf(float x) { return 1.f / (1.f + expf(-x)); }
+// log(1 + exp(x)) without overflow
+__device__ __forceinline__ float softplusf(float x) { return x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x)); }
 
 template <int kVsplit, int kFlags>
 __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeParams p) {
@@ -80,7 +83,11 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
     float kk = 0.f, qq = 0.f;
     if (tid < 128) {
       const float gt = bf(p.g[tok * 128 + tid]);
-      const float ghat = gate_pre ? gt : p.lower_bound * sigmoidf(rate * (gt + p.dt_bias[(size_t)h * 128 + tid]));
+      float ghat = gt;
+      if (!gate_pre) {
+        const float pre = gt + p.dt_bias[(size_t)h * 128 + tid];
+        ghat = (kFlags & kGateSoftplus) ? -rate * softplusf(pre) : p.lower_bound * sigmoidf(rate * pre);
+      }
       s_alpha[tid] = expf(ghat);
       kk = bf(p.k[tok * 128 + tid]);
       qq = bf(p.q[tok * 128 + tid]);
@@ -153,12 +160,19 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
   // the value split and the flags are template parameters: the common case (V = 128,
   // every step in the kernel) carries no per-thread tests of either
   using Kernel = void (*)(DecodeParams);
-  static constexpr Kernel kernels[2][8] = {
+  // (the preactivated and softplus gates exclude each other: no kernel for both)
+  static constexpr Kernel kernels[2][16] = {
       {kda_decode_kernel<1, 0>, kda_decode_kernel<1, 1>, kda_decode_kernel<1, 2>, kda_decode_kernel<1, 3>,
-       kda_decode_kernel<1, 4>, kda_decode_kernel<1, 5>, kda_decode_kernel<1, 6>, kda_decode_kernel<1, 7>},
+       kda_decode_kernel<1, 4>, kda_decode_kernel<1, 5>, kda_decode_kernel<1, 6>, kda_decode_kernel<1, 7>,
+       kda_decode_kernel<1, 8>, nullptr, kda_decode_kernel<1, 10>, nullptr,
+       kda_decode_kernel<1, 12>, nullptr, kda_decode_kernel<1, 14>, nullptr},
       {kda_decode_kernel<2, 0>, kda_decode_kernel<2, 1>, kda_decode_kernel<2, 2>, kda_decode_kernel<2, 3>,
-       kda_decode_kernel<2, 4>, kda_decode_kernel<2, 5>, kda_decode_kernel<2, 6>, kda_decode_kernel<2, 7>}};
-  kernels[p.vsplit == 2 ? 1 : 0][p.flags & 7]<<<(unsigned)grid, kDecThreads, 0, s>>>(p);
+       kda_decode_kernel<2, 4>, kda_decode_kernel<2, 5>, kda_decode_kernel<2, 6>, kda_decode_kernel<2, 7>,
+       kda_decode_kernel<2, 8>, nullptr, kda_decode_kernel<2, 10>, nullptr,
+       kda_decode_kernel<2, 12>, nullptr, kda_decode_kernel<2, 14>, nullptr}};
+  const Kernel k = kernels[p.vsplit == 2 ? 1 : 0][p.flags & 15];
+  if (k == nullptr) return cudaErrorInvalidValue;
+  k<<<(unsigned)grid, kDecThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

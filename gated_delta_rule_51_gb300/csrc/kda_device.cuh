@@ -15,7 +15,7 @@ namespace kda {
 // unwind instead of hanging the GPU.
 constexpr long long kWaitTimeoutCycles = 2000000000LL;
 
-enum : int { kErrTimeout = 1, kErrBadSeqlens = 2 };
+enum : int { kErrTimeout = 1, kErrBadSeqlens = 2, kErrGateRange = 4 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -244,6 +244,11 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t sad
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 __device__ __forceinline__ float rcp_approx(float x) {

@@ -69,7 +69,7 @@ struct ChainParams {
   int final_dtype;
   float scale;
   float lower_bound;
-  int flags;                           // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm
+  int flags;                           // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm | kGateSoftplus
   int vsplit;                          // V / 128: work-item heads are (head, 128-column value block)
 };
 
@@ -101,6 +101,8 @@ struct ScheduleParams {
 constexpr int kGatePreactivated = 1;
 constexpr int kBetaPreactivated = 2;
 constexpr int kNoQkL2Norm = 4;
+constexpr int kGateSoftplus = 8;   // ghat = -exp(A_log) softplus(g + dt_bias), no lower bound
+constexpr unsigned kValidFlags = 15;
 
 struct DecodeParams {
   const uint16_t *q, *k, *v, *g, *beta;  // bf16 [B, T, H, 128] (beta [B, T, H], logits)
@@ -110,7 +112,7 @@ struct DecodeParams {
   void* state;                            // [B, H, 128 (v), 128 (k)], read and written in place
   int state_dtype;                        // 1 bf16, 2 fp32
   int vsplit;                             // V / 128
-  int flags;                              // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm
+  int flags;                              // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm | kGateSoftplus
   int B, T, H;
   float scale, lower_bound;
 };

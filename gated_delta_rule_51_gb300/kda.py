@@ -23,11 +23,11 @@ KDA_OK = 0
 KDA_STATE_NONE, KDA_STATE_BF16, KDA_STATE_FP32 = 0, 1, 2
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
                 3: "KDA_ERR_WORKSPACE_TOO_SMALL", 4: "KDA_ERR_UNSUPPORTED_DEVICE", 5: "KDA_ERR_CUDA",
-                6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_BAD_SEQLENS"}
+                6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_BAD_SEQLENS", 8: "KDA_ERR_GATE_RANGE"}
 EXPORTED_SYMBOLS = ("kda_status_string", "kda_workspace_size", "kda_fwd", "kda_check_device_error",
                     "kda_set_profile_events", "kda_last_launch_count", "kda_fwd_static_workspace",
                     "kda_decode", "kda_fwd_ex")
-KDA_GATE_PREACTIVATED, KDA_BETA_PREACTIVATED, KDA_NO_QK_L2NORM = 1, 2, 4
+KDA_GATE_PREACTIVATED, KDA_BETA_PREACTIVATED, KDA_NO_QK_L2NORM, KDA_GATE_SOFTPLUS = 1, 2, 4, 8
 
 
 class kda_shape(ctypes.Structure):
@@ -131,25 +131,35 @@ def _check(t: torch.Tensor, name: str, dtype: torch.dtype, shape: Tuple[int, ...
         raise ValueError(f"{name} must be contiguous")
 
 
-def _flags(use_gate_in_kernel: bool, use_beta_sigmoid_in_kernel: bool, use_qk_l2norm_in_kernel: bool) -> int:
+def _flags(use_gate_in_kernel: bool, use_beta_sigmoid_in_kernel: bool, use_qk_l2norm_in_kernel: bool,
+           safe_gate: bool = True) -> int:
+    if not safe_gate and not use_gate_in_kernel:
+        raise ValueError("safe_gate=False selects the in-kernel gate without a lower bound; "
+                         "it needs use_gate_in_kernel=True")
     return ((0 if use_gate_in_kernel else KDA_GATE_PREACTIVATED)
             | (0 if use_beta_sigmoid_in_kernel else KDA_BETA_PREACTIVATED)
-            | (0 if use_qk_l2norm_in_kernel else KDA_NO_QK_L2NORM))
+            | (0 if use_qk_l2norm_in_kernel else KDA_NO_QK_L2NORM)
+            | (0 if safe_gate else KDA_GATE_SOFTPLUS))
 
 
 def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
         final_state=None, cu_seqlens=None, workspace: Optional[torch.Tensor] = None,
         stream: Optional[torch.cuda.Stream] = None, use_gate_in_kernel: bool = True,
-        use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True):
+        use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True,
+        safe_gate: bool = True):
     """KDA forward on the GPU; writes ``out`` (and ``final_state``) and returns them.
 
     q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,128] bf16; beta: [B,T,H] bf16 logits;
     A_log: [H] fp32; dt_bias: [H,128] fp32; states: [N,H,128,128] bf16/fp32 or None;
     cu_seqlens: int64 [N+1] on the device (then B must be 1).
     The use_* switches (default on, FlashKDA's behaviour) say which steps run in
-    the kernel; off means the caller did them: g is then the natural-log decay in
-    [-5, 0] (A_log and dt_bias may be None), beta is beta itself, q and k are used
-    without L2 norms.
+    the kernel; off means the caller did them: g is then the natural-log decay, at
+    most 0 (A_log and dt_bias may be None), beta is beta itself, q and k are used
+    without L2 norms.  safe_gate=False selects the gate without a lower bound,
+    ghat = -exp(A_log) softplus(g + dt_bias) (lower_bound is then not read).  With
+    either of those two gates, a 16-token chunk whose decay leaves the range the
+    chunked form factors exactly (a sum of ghat below -173 on some channel) sets
+    the gate-range bit of the workspace's error word (check_device_error).
     """
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
@@ -167,7 +177,7 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
         if t is None and not use_gate_in_kernel and name in ("A_log", "dt_bias"):
             continue
         _check(t, name, dt, shp, dev)
-    flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel)
+    flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate)
     for name, t in (("initial_state", initial_state), ("final_state", final_state)):
         if t is not None:
             _check(t, name, t.dtype, (N, H, V, K), dev)
@@ -194,13 +204,14 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
 
 def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
            stream: Optional[torch.cuda.Stream] = None, use_gate_in_kernel: bool = True,
-           use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True):
+           use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True,
+           safe_gate: bool = True):
     """Recurrent KDA step(s) for decoding; updates ``state`` in place, writes ``out``.
 
     q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,V] bf16 with V = 128 or 256 (T new
     tokens per sequence, usually 1); beta: [B,T,H] bf16 logits; A_log: [H] fp32;
     dt_bias: [H,128] fp32; state: [B,H,V,128] bf16 or fp32, read before the first
-    token and overwritten.
+    token and overwritten.  The switches are those of fwd.
     """
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
@@ -218,7 +229,7 @@ def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
             continue
         _check(t, name, dt, shp, dev)
     _check(state, "state", state.dtype, (B, H, V, K), dev)
-    flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel)
+    flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate)
     lib = load_library()
     shape = make_shape(B, T, H, B, K, V)
     s = stream if stream is not None else torch.cuda.current_stream(dev)

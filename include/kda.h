@@ -5,7 +5,8 @@
  * stated by the FlashKDA README ("Kernel API", flash_kda.fwd parameter table)
  * together with the KDA recurrence, per sequence n and head h, K = V = 128:
  *
- *   ghat_t  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h,:]))  (per channel)
+ *   ghat_t  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h,:]))  (per channel;
+ *             the reference call's safe gate, the default; see kda_flags for the others)
  *   S_t     = (I - beta_t k_t k_t^T) Diag(exp(ghat_t)) S_{t-1} + beta_t k_t v_t^T
  *   o_t     = scale * S_t^T q_t
  *
@@ -55,7 +56,8 @@ typedef enum {
     KDA_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
     KDA_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
     KDA_ERR_TIMEOUT = 6,            /* a device-side wait ran out of time (error word) */
-    KDA_ERR_BAD_SEQLENS = 7         /* cu_seqlens not monotone or not ending at T (error word) */
+    KDA_ERR_BAD_SEQLENS = 7,        /* cu_seqlens not monotone or not ending at T (error word) */
+    KDA_ERR_GATE_RANGE = 8          /* a 16-token chunk decayed past 2^-250 on some channel (error word) */
 } kda_status;
 
 /* State dtype for initial_state / final_state (README: "bf16/fp32/None"). */
@@ -69,17 +71,26 @@ typedef enum { KDA_STATE_NONE = 0, KDA_STATE_BF16 = 1, KDA_STATE_FP32 = 2 } kda_
  * when the switch is off:
  *   KDA_GATE_PREACTIVATED : g holds the natural-log decay ghat itself; A_log,
  *                           dt_bias and lower_bound are not read (A_log and
- *                           dt_bias may be NULL).  For kda_fwd_ex every value
- *                           must lie in [-5, 0], the range the in-kernel gate
- *                           guarantees (the 16-token chunked form relies on
- *                           it); kda_decode takes any value <= 0.
+ *                           dt_bias may be NULL).  Values must be <= 0.
  *   KDA_BETA_PREACTIVATED : beta holds beta itself, not its logit.
  *   KDA_NO_QK_L2NORM      : q and k are used as given.
+ * and one selects the reference call's other gate (its safe_gate switch off):
+ *   KDA_GATE_SOFTPLUS     : ghat = -exp(A_log[h]) * softplus(g + dt_bias[h,:]),
+ *                           with no lower bound; lower_bound is not read.  Not
+ *                           together with KDA_GATE_PREACTIVATED.
+ * The chunked form of kda_fwd_ex factors the decay inside each 16-token chunk
+ * about half the chunk's total, which is exact while that total stays within
+ * 2^-250 (a sum of ghat above -173 over the chunk's 16 tokens on every
+ * channel).  The in-kernel safe gate never leaves this range (16 x 5 < 173); a
+ * preactivated or softplus gate that does sets KDA_ERR_GATE_RANGE in the error
+ * word, and the outputs of that call are then unspecified.  kda_decode runs the
+ * token recurrence itself and takes any gate values.
  */
 typedef enum {
     KDA_GATE_PREACTIVATED = 1,
     KDA_BETA_PREACTIVATED = 2,
-    KDA_NO_QK_L2NORM = 4
+    KDA_NO_QK_L2NORM = 4,
+    KDA_GATE_SOFTPLUS = 8
 } kda_flags;
 
 /*
@@ -117,7 +128,8 @@ KDA_API kda_status kda_workspace_size(const kda_shape *shape, size_t *bytes);
  *   scale            : output scale (README "scaling factor").
  *   out              : bf16 [B, T, H, V], written for every token.
  *   A_log, dt_bias   : fp32 gate parameters.
- *   lower_bound      : gate lower bound, must lie in [-5, 0] (README range).
+ *   lower_bound      : gate lower bound, must lie in [-5, 0] (README range);
+ *                      not read with KDA_GATE_PREACTIVATED or KDA_GATE_SOFTPLUS.
  *   initial_state    : NULL (zeros) or [N, H, V, K] of init_dtype.
  *   final_state      : NULL (not written) or [N, H, V, K] of final_dtype;
  *                      when both states are given their dtypes must match
@@ -153,8 +165,9 @@ KDA_API kda_status kda_fwd_ex(const kda_shape *shape, const void *q, const void 
 /*
  * Synchronises `stream`, reads the error word that the last kda_fwd on this
  * workspace left behind, stores it in *flags (0 = none; bit 0 = a device wait
- * timed out; bit 1 = malformed cu_seqlens) and returns KDA_OK, KDA_ERR_TIMEOUT
- * or KDA_ERR_BAD_SEQLENS accordingly.
+ * timed out; bit 1 = malformed cu_seqlens; bit 2 = a chunk's decay out of the
+ * gate range above) and returns KDA_OK, KDA_ERR_TIMEOUT, KDA_ERR_BAD_SEQLENS or
+ * KDA_ERR_GATE_RANGE accordingly.
  */
 KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t stream, int *flags);
 

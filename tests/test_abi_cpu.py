@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings():
     lib = kda.load_library()
-    for code in range(8):
+    for code in range(9):
         s = lib.kda_status_string(code)
         assert s and isinstance(s, bytes)
     assert lib.kda_status_string(0) == b"ok"
@@ -90,6 +90,12 @@ def test_element_aligned_beta_and_out_pass_the_argument_checks():
     assert _call(kda.make_shape(1, 64, 1, 1), beta=FAKE + 2, out=FAKE + 6) in (4, 5)
 
 
+def test_python_binding_rejects_softplus_with_a_preactivated_gate():
+    with pytest.raises(ValueError):
+        kda._flags(False, True, True, safe_gate=False)
+    assert kda._flags(True, True, True, safe_gate=False) == kda.KDA_GATE_SOFTPLUS
+
+
 def test_python_binding_requires_cuda_tensors():
     import torch
 
@@ -116,7 +122,8 @@ def _decode_call(shape, q=FAKE, out=FAKE, A_log=FAKE, state=FAKE, dtype=2, lb=-1
     (dict(shape=kda.make_shape(4, 1, 2, 4), q=0), 1),
     (dict(shape=kda.make_shape(4, 1, 2, 4), out=FAKE + 1), 1),       # 2-byte aligned tokens
     (dict(shape=kda.make_shape(4, 1, 2, 4), A_log=FAKE + 2), 1),
-    (dict(shape=kda.make_shape(4, 1, 2, 4), flags=8), 1),            # unknown flag
+    (dict(shape=kda.make_shape(4, 1, 2, 4), flags=16), 1),           # unknown flag
+    (dict(shape=kda.make_shape(4, 1, 2, 4), flags=9), 1),            # preactivated and softplus gates
 ])
 def test_decode_host_side_argument_errors(case, expected):
     shape = case.pop("shape")
@@ -127,6 +134,9 @@ def test_decode_valid_arguments_reach_the_device_query():
     assert _decode_call(kda.make_shape(4, 1, 2, 4), q=FAKE + 2, out=FAKE + 6) in (4, 5)
     # a gate activated by the caller needs neither A_log nor dt_bias, nor a lower bound in range
     assert _decode_call(kda.make_shape(4, 1, 2, 4), A_log=0, lb=7.0, flags=1) in (4, 5)
+    # the softplus gate reads A_log and dt_bias but no lower bound
+    assert _decode_call(kda.make_shape(4, 1, 2, 4), lb=7.0, flags=8) in (4, 5)
+    assert _decode_call(kda.make_shape(4, 1, 2, 4), A_log=0, flags=8) == 1
 
 
 def _fwd_ex_call(flags, A_log=FAKE, lb=-1.0):
@@ -139,7 +149,11 @@ def _fwd_ex_call(flags, A_log=FAKE, lb=-1.0):
 
 
 def test_fwd_ex_flags_on_the_host():
-    assert _fwd_ex_call(8) == 1                       # unknown flag
+    assert _fwd_ex_call(16) == 1                      # unknown flag
+    assert _fwd_ex_call(9) == 1                       # preactivated and softplus gates exclude each other
+    assert _fwd_ex_call(8, lb=9.0) in (4, 5)          # the softplus gate reads no lower bound
+    assert _fwd_ex_call(8, A_log=0) == 1              # but needs A_log and dt_bias
+    assert _fwd_ex_call(8 | 2 | 4) in (4, 5)
     assert _fwd_ex_call(0, A_log=0) == 1              # the in-kernel gate needs its parameters
     assert _fwd_ex_call(1, A_log=0, lb=9.0) in (4, 5)  # a pre-activated gate does not
     assert _fwd_ex_call(6) in (4, 5)

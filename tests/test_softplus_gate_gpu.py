@@ -1,0 +1,149 @@
+"""Parity of the GPU path with the oracle for the reference call's gate without a lower
+bound (safe_gate off): ghat = -exp(A_log) softplus(g + dt_bias).
+
+Inputs follow the workloads' recipe (g ~ N(0, 1), A_log ~ U(-1, 1), dt_bias ~ 0.1 N(0, 1));
+one case shifts g so that a 16-token chunk decays by 2^-130 .. 2^-250 per channel, past the
+range an unanchored factorisation of the decay holds (2^+-126) and inside the anchored one;
+one shifts it further, past 2^-250, where the chunked form must raise the gate-range bit of
+the error word instead of answering silently.  Same bounds as the other parity tests.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_helpers import check_out, check_state, random_case, to_cpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_51_gb300 import kda
+
+    kda.load_library()
+
+
+def _oracle(x, **kw):
+    import oracle
+
+    xc = to_cpu(x)
+    return oracle.kda_forward(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["scale"], xc["A_log"],
+                              xc["dt_bias"], xc["lower_bound"], xc.get("initial_state"), xc.get("cu_seqlens"),
+                              safe_gate=False, **kw)
+
+
+def _gpu(x, workspace=None, **kw):
+    from gated_delta_rule_51_gb300 import kda
+
+    out = torch.full_like(x["v"], float("nan"))
+    fin = None
+    if x.get("initial_state") is not None:
+        fin = torch.full_like(x["initial_state"], float("nan"))
+    kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], out, x["A_log"], x["dt_bias"],
+            float("nan"), initial_state=x.get("initial_state"), final_state=fin, cu_seqlens=x.get("cu_seqlens"),
+            workspace=workspace, safe_gate=False, **kw)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def _shift_g(x, shift, a_log=None):
+    x["g"] = (x["g"].float() + shift).to(torch.bfloat16)
+    if a_log is not None:
+        x["A_log"] = torch.full_like(x["A_log"], a_log)
+    return x
+
+
+@pytest.mark.parametrize("init_dtype", [torch.float32, torch.bfloat16])
+def test_varlen_with_partial_chunks(init_dtype):
+    lens = [300, 17, 1000, 64, 129, 5]
+    x = random_case(1, sum(lens), 3, seed=1201, lens=lens, init_dtype=init_dtype)
+    ref_out, ref_fin = _oracle(x)
+    out, fin = _gpu(x)
+    check_out(out, ref_out.reshape(out.shape[1], 3, 128), label=f"softplus {init_dtype}")
+    check_state(fin, ref_fin, label=f"softplus {init_dtype}")
+
+
+def test_through_the_segment_scan(monkeypatch):
+    # 64-token segments: local, transition and carried runs all use the same gate
+    monkeypatch.setenv("KDA_SEG_TOKENS", "64")
+    x = random_case(2, 700, 2, seed=1202)
+    ref_out, ref_fin = _oracle(x)
+    out, fin = _gpu(x)
+    check_out(out, ref_out.reshape(2 * 700, 2, 128), label="softplus seg 64")
+    check_state(fin, ref_fin, label="softplus seg 64")
+
+
+def test_strong_decay_inside_the_anchored_range():
+    # A_log = 0 and g + dt_bias near 8: ghat near -8 a token, so a chunk decays by about
+    # 2^-185 per channel (and the state is nearly forgotten each chunk)
+    from gated_delta_rule_51_gb300 import kda
+
+    x = _shift_g(random_case(1, 500, 2, seed=1203), 8.0, a_log=0.0)
+    gsum = torch.nn.functional.softplus(x["g"].float() + x["dt_bias"].view(1, 1, 2, 128)).cpu().numpy()
+    chunk = gsum[0, :496].reshape(31, 16, 2, 128).sum(axis=1) / np.log(2.0)
+    assert chunk.max() > 130 and chunk.max() < 245
+    ws = torch.empty(kda.workspace_size(kda.make_shape(1, 500, 2, 1)), dtype=torch.uint8, device="cuda")
+    ref_out, ref_fin = _oracle(x)
+    out, fin = _gpu(x, workspace=ws)
+    assert kda.check_device_error(ws) == 0
+    check_out(out, ref_out.reshape(500, 2, 128), label="softplus strong decay")
+    check_state(fin, ref_fin, label="softplus strong decay")
+
+
+def test_out_of_range_decay_is_flagged_not_trapped():
+    from gated_delta_rule_51_gb300 import kda
+
+    x = _shift_g(random_case(1, 64, 1, seed=1204), 20.0, a_log=0.0)     # about 2^-460 a chunk
+    ws = torch.empty(kda.workspace_size(kda.make_shape(1, 64, 1, 1)), dtype=torch.uint8, device="cuda")
+    _gpu(x, workspace=ws)
+    assert kda.check_device_error(ws) & 4
+    # a call within range on the same workspace clears the word
+    _gpu(random_case(1, 64, 1, seed=1205), workspace=ws)
+    assert kda.check_device_error(ws) == 0
+
+
+def test_preactivated_gate_beyond_the_safe_range():
+    # g given in [-9, 0] (past the safe gate's -5): chunks decay by up to 2^-207, inside the
+    # anchored range; the chunked form stays exact
+    from gated_delta_rule_51_gb300 import kda
+    import oracle
+
+    x = random_case(1, 400, 2, seed=1206)
+    gen = torch.Generator(device="cuda").manual_seed(1207)
+    x["g"] = (-9.0 * torch.rand(x["g"].shape, generator=gen, device="cuda")).to(torch.bfloat16)
+    xc = to_cpu(x)
+    ref_out, ref_fin = oracle.kda_forward(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["scale"], xc["A_log"],
+                                          xc["dt_bias"], xc["lower_bound"], xc["initial_state"],
+                                          use_gate_in_kernel=False)
+    out = torch.full_like(x["v"], float("nan"))
+    fin = torch.full_like(x["initial_state"], float("nan"))
+    ws = torch.empty(kda.workspace_size(kda.make_shape(1, 400, 2, 1)), dtype=torch.uint8, device="cuda")
+    kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], out, None, None, 0.0,
+            initial_state=x["initial_state"], final_state=fin, workspace=ws, use_gate_in_kernel=False)
+    torch.cuda.synchronize()
+    assert kda.check_device_error(ws) == 0
+    check_out(out, ref_out.reshape(400, 2, 128), label="preactivated [-9, 0]")
+    check_state(fin, ref_fin, label="preactivated [-9, 0]")
+
+
+@pytest.mark.parametrize("shift", [0.0, 20.0])
+def test_decode_step(shift):
+    # the decode kernel runs the token recurrence itself: any decay is fine
+    from gated_delta_rule_51_gb300 import kda
+    import oracle
+
+    x = _shift_g(random_case(8, 3, 4, seed=1208 + int(shift)), shift)
+    xc = to_cpu(x)
+    ref_out, ref_fin = oracle.kda_forward(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["scale"], xc["A_log"],
+                                          xc["dt_bias"], xc["lower_bound"], xc["initial_state"], safe_gate=False)
+    state = x["initial_state"].clone()
+    out = torch.full_like(x["v"], float("nan"))
+    kda.decode(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], out, x["A_log"], x["dt_bias"], float("nan"),
+               state, safe_gate=False)
+    torch.cuda.synchronize()
+    check_out(out, ref_out.reshape(8 * 3, 4, 128), label=f"decode softplus {shift}")
+    check_state(state, ref_fin, label=f"decode softplus {shift}")
