@@ -147,3 +147,46 @@ def test_decode_step(shift):
     torch.cuda.synchronize()
     check_out(out, ref_out.reshape(8 * 3, 4, 128), label=f"decode softplus {shift}")
     check_state(state, ref_fin, label=f"decode softplus {shift}")
+
+
+@pytest.mark.parametrize("beta_pre,no_norm", [(True, False), (False, True), (True, True)])
+def test_with_the_other_switches(beta_pre, no_norm):
+    import math
+
+    x = random_case(1, 500, 2, seed=1210 + 2 * beta_pre + no_norm, lens=[200, 300])
+    gen = torch.Generator(device="cuda").manual_seed(1215)
+    if beta_pre:
+        x["beta"] = torch.rand(x["beta"].shape, generator=gen, device="cuda").to(torch.bfloat16)
+    if no_norm:
+        x["q"] = (x["q"].float() / math.sqrt(128)).to(torch.bfloat16)
+        x["k"] = (x["k"].float() / math.sqrt(128)).to(torch.bfloat16)
+    kw = dict(use_beta_sigmoid_in_kernel=not beta_pre, use_qk_l2norm_in_kernel=not no_norm)
+    ref_out, ref_fin = _oracle(x, **kw)
+    out, fin = _gpu(x, **kw)
+    label = f"softplus b{int(beta_pre)} n{int(no_norm)}"
+    check_out(out, ref_out.reshape(500, 2, 128), label=label)
+    check_state(fin, ref_fin, label=label)
+
+
+def test_v256_heads():
+    from gated_delta_rule_51_gb300 import kda
+
+    x = random_case(1, 300, 2, seed=1220, lens=[120, 180], V=256)
+    ref_out, ref_fin = _oracle(x)
+    out, fin = _gpu(x)
+    check_out(out, ref_out.reshape(300, 2, 256), label="softplus V=256")
+    check_state(fin, ref_fin, label="softplus V=256")
+    # and the decode step on the same heads
+    import oracle
+
+    y = random_case(4, 2, 2, seed=1221, V=256)
+    yc = to_cpu(y)
+    d_out, d_fin = oracle.kda_forward(yc["q"], yc["k"], yc["v"], yc["g"], yc["beta"], yc["scale"], yc["A_log"],
+                                      yc["dt_bias"], yc["lower_bound"], yc["initial_state"], safe_gate=False)
+    state = y["initial_state"].clone()
+    o = torch.full_like(y["v"], float("nan"))
+    kda.decode(y["q"], y["k"], y["v"], y["g"], y["beta"], y["scale"], o, y["A_log"], y["dt_bias"], float("nan"),
+               state, safe_gate=False)
+    torch.cuda.synchronize()
+    check_out(o, d_out.reshape(8, 2, 256), label="decode softplus V=256")
+    check_state(state, d_fin, label="decode softplus V=256")
