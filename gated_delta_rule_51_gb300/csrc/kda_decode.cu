@@ -10,10 +10,11 @@
 //   beta  = sigmoid(beta logit) (or given);  qh, kh = x / sqrt(|x|^2 + 1e-6) (or as given)
 //   row v of S^T:  s <- s * exp(ghat);  s <- s + beta (v_v - s . kh) kh
 //   o_v   = scale * s . qh        (from the updated row)
-// Rows are independent, so the work is bandwidth-bound: one CTA per (n, h),
-// eight warps with sixteen rows each, every lane holding four key channels of
-// each of its rows in registers for all the call's tokens.  The state is read
-// once (64 KiB fp32 or 32 KiB bf16) and written once.
+// Rows are independent, so the work is bandwidth-bound: kSub CTAs per (n, h,
+// 128-row value block), each of kDecRows rows in warps of sixteen, every lane
+// holding four key channels of each of its rows in registers for all the call's
+// tokens.  The state is read once (64 KiB fp32 or 32 KiB bf16 per head) and
+// written once.
 #include <cuda_bf16.h>
 
 #include "kda_device.cuh"
@@ -22,8 +23,11 @@
 namespace kda {
 namespace {
 
-constexpr int kDecThreads = 256;
 constexpr int kRowsPerWarp = 16;
+constexpr int kDecRows = 64;                        // state rows per CTA (four CTAs per SM)
+constexpr int kDecThreads = 2 * kDecRows;           // 16 rows a warp; at least 128 threads
+constexpr int kSub = 128 / kDecRows;                // CTAs per 128-row value block
+static_assert(kDecThreads >= 128, "the per-channel vectors take 128 threads");
 
 __device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
@@ -46,11 +50,15 @@ __device__ __forceinline__ float sigmoidf(float x) { return 1.f / (1.f + expf(-x
 __device__ __forceinline__ float softplusf(float x) { return x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x)); }
 
 template <int kVsplit, int kFlags>
-__global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeParams p) {
-  // one CTA per (sequence, head, 128-row value block); V = 128 * kVsplit.  The CTA's
-  // 128 state rows are block blockIdx.x of the [B * H * V / 128, 128, 128] state.
-  const int vblk = kVsplit == 1 ? 0 : (int)(blockIdx.x % kVsplit);
-  const int nh = kVsplit == 1 ? (int)blockIdx.x : (int)(blockIdx.x / kVsplit);
+__global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decode_kernel(const DecodeParams p) {
+  // kSub CTAs per (sequence, head, 128-row value block); V = 128 * kVsplit.  The CTA's
+  // kDecRows state rows are block blockIdx.x of the [B * H * V / kDecRows, kDecRows, 128]
+  // state.
+  const int sub = (int)(blockIdx.x % kSub);
+  const int blk = (int)(blockIdx.x / kSub);
+  const int vblk = kVsplit == 1 ? 0 : blk % kVsplit;
+  const int nh = kVsplit == 1 ? blk : blk / kVsplit;
+  const int rowbase = sub * kDecRows;   // first row of this CTA within its value block
   const int n = nh / p.H, h = nh - n * p.H;
   constexpr int V = kVsplit * 128;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -59,7 +67,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
   __shared__ float s_beta;
 
   // ---- the state rows of this warp, four key channels per lane
-  const size_t srow0 = (size_t)blockIdx.x * 128;   // first state row of this CTA
+  const size_t srow0 = (size_t)blockIdx.x * kDecRows;   // first state row of this CTA
   float4 st[kRowsPerWarp];
   if (p.state_dtype == 2) {
     const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.state) + srow0 * 128);
@@ -123,7 +131,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
     warp_sum16(d);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-      const float c = beta * (s_v[kRowsPerWarp * warp + r] - d[r]);
+      const float c = beta * (s_v[rowbase + kRowsPerWarp * warp + r] - d[r]);
       st[r].x = fmaf(c, kh.x, st[r].x); st[r].y = fmaf(c, kh.y, st[r].y);
       st[r].z = fmaf(c, kh.z, st[r].z); st[r].w = fmaf(c, kh.w, st[r].w);
       d[r] = st[r].x * qh.x + st[r].y * qh.y + st[r].z * qh.z + st[r].w * qh.w;
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
       float o = d[0];
 #pragma unroll
       for (int r = 1; r < kRowsPerWarp; ++r) o = lane == r ? d[r] : o;
-      p.out[tok * V + 128 * vblk + kRowsPerWarp * warp + lane] =
+      p.out[tok * V + 128 * vblk + rowbase + kRowsPerWarp * warp + lane] =
           __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * o));
     }
     if (t + 1 < p.T) __syncthreads();   // the per-channel vectors are rewritten by the next token
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodePar
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
-  const long long grid = (long long)p.B * p.H * p.vsplit;
+  const long long grid = (long long)p.B * p.H * p.vsplit * kSub;
   if (grid <= 0 || p.T <= 0) return cudaSuccess;
   // the value split and the flags are template parameters: the common case (V = 128,
   // every step in the kernel) carries no per-thread tests of either
