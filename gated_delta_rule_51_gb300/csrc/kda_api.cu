@@ -405,7 +405,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
     cmp.items = sp.compose;
     cmp.item_count = &hdr->n_compose;
     mark(1, stream);
-    if (launch_compose(cmp, (int)L.cap_compose, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_compose(cmp, (int)L.cap_compose, d.sms, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (L.cap_compose > 0) ++launches;
     mark(2, stream);
   } else {

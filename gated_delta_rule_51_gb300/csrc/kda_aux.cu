@@ -271,19 +271,23 @@ cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s) {
 // S^T_{s+1} = S^T_s P^T_s + Q^T_s, all 128 x 128 fp32 in the [V, K] layout:
 // out[v][k] = sum_m in[v][m] * Pst[m][k] + Qst[v][k] where Pst is the stored
 // transition slot (row m = column m of P).  Rows of S^T are independent, so
-// each CTA owns 16 rows of one (sequence, head) chain and walks its segments:
+// each CTA owns kRows (16 or 32) rows of one (sequence, head) chain and walks its segments:
 // S_{s+1} = S_s P_s + Q_s on its rows.  The chain is sequential, so each step's
 // operands (the 64 KiB transition P_s and the CTA's 8 KiB of Q_s) are brought into
 // shared memory by bulk copies one step ahead, while the current step computes.
-constexpr int kComposeRows = 16;
+// Each thread computes kRows / 4 rows x 2 columns: per m, float4s of S (kept
+// transposed, St[m][v]) and one float2 of P feed the FMAs.  32-row CTAs are used when
+// 16-row ones would not all fit on the GPU at once (one CTA per SM: the double-buffered
+// transition takes 128 KiB).
 constexpr int kComposeThreads = 256;
 constexpr uint32_t kPBytes = 128 * 128 * 4;
-constexpr uint32_t kQBytes = kComposeRows * 128 * 4;
 
+template <int kRows>
 struct ComposeSmem {
+  static constexpr int kPitch = kRows + 4;   // floats per St row (16-byte aligned, spreads banks)
   float P[2][128][128];
-  float Q[2][kComposeRows][128];
-  float S[kComposeRows][128];
+  float Q[2][kRows][128];
+  float St[128][kPitch];   // this CTA's rows of S^T, transposed: St[m][v]
 };
 
 __device__ __forceinline__ void bulk_load_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
@@ -294,18 +298,21 @@ __device__ __forceinline__ void bulk_load_g2s(void* smem_dst, const void* gmem_s
       : "memory");
 }
 
+template <int kRows>
 __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const ComposeParams p) {
-  const int item = blockIdx.x / (128 / kComposeRows);
-  const int part = blockIdx.x % (128 / kComposeRows);
+  constexpr int kRowsPerThread = kRows / 4;
+  constexpr uint32_t kQBytes = kRows * 128 * 4;
+  const int item = blockIdx.x / (128 / kRows);
+  const int part = blockIdx.x % (128 / kRows);
   if (item >= *p.item_count) return;
   const ComposeItem ci = p.items[item];
   extern __shared__ __align__(128) uint8_t csm[];
-  ComposeSmem& S = *reinterpret_cast<ComposeSmem*>(csm);
+  ComposeSmem<kRows>& S = *reinterpret_cast<ComposeSmem<kRows>*>(csm);
   __shared__ __align__(8) uint64_t bar[2];
   const int tid = threadIdx.x;
-  const int k = tid & 127;
-  const int vh = tid >> 7;   // rows vh*8 .. vh*8+7 of this CTA's 16
-  const int v0 = part * kComposeRows;
+  const int k2 = 2 * (tid & 63);                // columns k2, k2 + 1
+  const int r4 = kRowsPerThread * (tid >> 6);   // rows r4 .. r4 + kRowsPerThread - 1 of this CTA's
+  const int v0 = part * kRows;
   float* slots = p.ws_states;
   auto P_src = [&](int st) { return slots + (size_t)(ci.first_p_slot + st - 1) * 16384; };
   auto Q_row0 = [&](int st) { return slots + (size_t)(ci.first_q_slot + st) * 16384 + (size_t)v0 * 128; };
@@ -321,8 +328,8 @@ __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const Comp
     mbar_fence_init();
   }
   // S_1 = Q slot 0 (already the true state after segment 0)
-  for (int i = tid; i < kComposeRows * 128; i += kComposeThreads)
-    S.S[i / 128][i % 128] = slots[(size_t)ci.first_q_slot * 16384 + (size_t)(v0 + i / 128) * 128 + i % 128];
+  for (int i = tid; i < kRows * 128; i += kComposeThreads)
+    S.St[i % 128][i / 128] = slots[(size_t)ci.first_q_slot * 16384 + (size_t)(v0 + i / 128) * 128 + i % 128];
   __syncthreads();
   if (tid == 0) {
     if (ci.n_steps >= 1) fetch(1);
@@ -335,22 +342,34 @@ __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const Comp
       while (!mbar_try_wait(&bar[b], ((st - 1) >> 1) & 1))
         if (clock64() - t0 > kWaitTimeoutCycles) break;
     }
-    float acc[8];
+    float2 acc[kRowsPerThread];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = S.Q[b][vh * 8 + i][k];
+    for (int i = 0; i < kRowsPerThread; ++i) acc[i] = *reinterpret_cast<const float2*>(&S.Q[b][r4 + i][k2]);
 #pragma unroll 8
     for (int m = 0; m < 128; ++m) {
-      const float pm = S.P[b][m][k];
+      const float2 pm = *reinterpret_cast<const float2*>(&S.P[b][m][k2]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(S.S[vh * 8 + i][m], pm, acc[i]);
+      for (int i4 = 0; i4 < kRowsPerThread; i4 += 4) {
+        const float4 sv = *reinterpret_cast<const float4*>(&S.St[m][r4 + i4]);
+        const float s4[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[i4 + i].x = fmaf(s4[i], pm.x, acc[i4 + i].x);
+          acc[i4 + i].y = fmaf(s4[i], pm.y, acc[i4 + i].y);
+        }
+      }
     }
-    __syncthreads();   // every thread is done with S and with buffer b
+    __syncthreads();   // every thread is done with St and with buffer b
     float* Q = Q_row0(st);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      S.S[vh * 8 + i][k] = acc[i];
-      Q[(size_t)(vh * 8 + i) * 128 + k] = acc[i];
+    for (int i4 = 0; i4 < kRowsPerThread; i4 += 4) {
+      *reinterpret_cast<float4*>(&S.St[k2][r4 + i4]) =
+          make_float4(acc[i4].x, acc[i4 + 1].x, acc[i4 + 2].x, acc[i4 + 3].x);
+      *reinterpret_cast<float4*>(&S.St[k2 + 1][r4 + i4]) =
+          make_float4(acc[i4].y, acc[i4 + 1].y, acc[i4 + 2].y, acc[i4 + 3].y);
     }
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) *reinterpret_cast<float2*>(&Q[(size_t)(r4 + i) * 128 + k2]) = acc[i];
     if (tid == 0 && st + 2 <= ci.n_steps) {
       fence_proxy_async_smem();   // the generic reads of buffer b are ordered before the refill
       fetch(st + 2);
@@ -359,14 +378,18 @@ __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const Comp
   }
 }
 
-size_t compose_smem_bytes() { return sizeof(ComposeSmem); }
+size_t compose_smem_bytes() { return sizeof(ComposeSmem<32>); }
 
-cudaError_t launch_compose(const ComposeParams& p, int grid, cudaStream_t s) {
+// grid: compose items (chains); sms: SMs of the device
+cudaError_t launch_compose(const ComposeParams& p, int grid, int sms, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
-  const int smem = (int)compose_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(kda_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // 16-row CTAs while they fit on the GPU at once, else 32-row ones (half the CTAs)
+  const bool wide = (long long)grid * (128 / 16) > (long long)sms;
+  const int smem = wide ? (int)sizeof(ComposeSmem<32>) : (int)sizeof(ComposeSmem<16>);
+  const auto kernel = wide ? kda_compose_kernel<32> : kda_compose_kernel<16>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kda_compose_kernel<<<grid * (128 / kComposeRows), kComposeThreads, smem, s>>>(p);
+  kernel<<<grid * (128 / (wide ? 32 : 16)), kComposeThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 

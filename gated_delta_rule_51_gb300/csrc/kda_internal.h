@@ -120,7 +120,7 @@ struct DecodeParams {
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s);
-cudaError_t launch_compose(const ComposeParams& p, int grid, cudaStream_t s);
+cudaError_t launch_compose(const ComposeParams& p, int grid, int sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 size_t chain_smem_bytes();
 
