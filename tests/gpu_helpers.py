@@ -62,12 +62,13 @@ def run_oracle(x: dict, out_rows=None, want_out=True):
 
 
 def _report(label: str, what: str, value: float) -> None:
-    """With KDA_TEST_REPORT set, append the measured error to gpurun_out/parity_report.txt."""
-    if not os.environ.get("KDA_TEST_REPORT"):
+    """With KDA_TEST_REPORT naming a file, append the measured error to it (tab-separated)."""
+    path = os.environ.get("KDA_TEST_REPORT")
+    if not path:
         return
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    os.makedirs(os.path.join(root, "gpurun_out"), exist_ok=True)
-    with open(os.path.join(root, "gpurun_out", "parity_report.txt"), "a") as f:
+    d = os.path.dirname(os.path.abspath(path))
+    os.makedirs(d, exist_ok=True)
+    with open(path, "a") as f:
         f.write(f"{label}\t{what}\t{value:.3e}\n")
 
 

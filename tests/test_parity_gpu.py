@@ -261,3 +261,13 @@ def test_weak_and_no_decay_long_runs(lb, T, state_bound):
     rf = rel_fro(g, ref_fin)
     _report(f"lb={lb} T={T}", "state_rel_fro_float32", rf)
     assert rf <= state_bound, f"state rel-Fro {rf:.3e} > {state_bound}"
+
+
+def test_thousands_of_short_sequences():
+    """3000 sequences of 0-40 tokens (several of the schedule kernel's 1024-sequence tiles),
+    with empty ones and lengths on both sides of the 16-token chunk."""
+    rng = np.random.default_rng(3000)
+    lens = [int(x) for x in rng.integers(0, 41, 3000)]
+    lens[0], lens[1], lens[-1] = 0, 16, 1
+    x = random_case(1, sum(lens), 2, seed=3001, lens=lens)
+    _compare(x, torch.float32, "3000 short sequences")
