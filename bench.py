@@ -352,44 +352,97 @@ def run_ours(args, w):
     value = whole_job_rate(tokens, world, args.steps, total_ms)
     ms_per_step = total_ms / args.steps
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API with pinned host buffers.  Every step copies its
+    # inputs host -> device and reads its outputs back; the steps are pipelined the way a
+    # serving loop would run them: two sets of device buffers, the next step's inputs
+    # copied on four copy streams while this step computes, its outputs copied back on a
+    # fifth stream while the next step computes.
     e2e = None
     if not args.no_e2e:
         names = [n for n in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens") if x[n] is not None]
         host = {n: x[n].cpu().pin_memory() for n in names}
-        dev_in = {n: torch.empty_like(x[n]) for n in names}
+        host["A_log"], host["dt_bias"] = x["A_log"].cpu().pin_memory(), x["dt_bias"].cpu().pin_memory()
+        names_all = names + ["A_log", "dt_bias"]
+        nbuf = 2
+        dev_in = [{n: torch.empty_like(x[n]) for n in names_all} for _ in range(nbuf)]
+        outs = [torch.empty_like(out) for _ in range(nbuf)]
+        fins = [torch.empty_like(fin) if fin is not None else None for _ in range(nbuf)]
         h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h_fin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True) if fin is not None else None
-        h_A, h_dt = x["A_log"].cpu().pin_memory(), x["dt_bias"].cpu().pin_memory()
-        d_A, d_dt = torch.empty_like(x["A_log"]), torch.empty_like(x["dt_bias"])
-        h2d = sum(host[n].numel() * host[n].element_size() for n in names) + h_A.numel() * 4 + h_dt.numel() * 4
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names_all)
         d2h = h_out.numel() * 2 + (h_fin.numel() * h_fin.element_size() if h_fin is not None else 0)
+        copy_streams = [torch.cuda.Stream(dev) for _ in range(4)]
+        d2h_stream = torch.cuda.Stream(dev)
+        lane_of = {n: i % len(copy_streams) for i, n in enumerate(names_all)}
+        in_free = [None] * nbuf     # events: the kernel that read buffer b is done
+        out_free = [None] * nbuf    # events: the copy-back of output buffer b is done
+        in_ready = [None] * nbuf
 
-        def e2e_step():
-            for n in names:
-                dev_in[n].copy_(host[n], non_blocking=True)
-            d_A.copy_(h_A, non_blocking=True)
-            d_dt.copy_(h_dt, non_blocking=True)
-            kda.fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], x["scale"], out,
-                    d_A, d_dt, x["lower_bound"], initial_state=dev_in.get("initial_state"),
-                    final_state=fin, cu_seqlens=dev_in.get("cu_seqlens"), workspace=ws)
-            h_out.copy_(out, non_blocking=True)
-            if h_fin is not None:
-                h_fin.copy_(fin, non_blocking=True)
+        def issue_h2d(i):
+            b = i % nbuf
+            evs = []
+            for li, cs in enumerate(copy_streams):
+                if in_free[b] is not None:
+                    cs.wait_event(in_free[b])
+                with torch.cuda.stream(cs):
+                    for n in names_all:
+                        if lane_of[n] == li:
+                            dev_in[b][n].copy_(host[n], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                evs.append(ev)
+            in_ready[b] = evs
 
-        e2e_step()
+        def issue_compute(i):
+            b = i % nbuf
+            for ev in in_ready[b]:
+                stream.wait_event(ev)
+            if out_free[b] is not None:
+                stream.wait_event(out_free[b])
+            d = dev_in[b]
+            kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"], outs[b], d["A_log"], d["dt_bias"],
+                    x["lower_bound"], initial_state=d.get("initial_state"), final_state=fins[b],
+                    cu_seqlens=d.get("cu_seqlens"), workspace=ws, stream=stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            in_free[b] = ev
+            d2h_stream.wait_event(ev)
+            with torch.cuda.stream(d2h_stream):
+                h_out.copy_(outs[b], non_blocking=True)
+                if h_fin is not None:
+                    h_fin.copy_(fins[b], non_blocking=True)
+            ev2 = torch.cuda.Event()
+            ev2.record(d2h_stream)
+            out_free[b] = ev2
+
+        def run_pipeline(k_steps, e_start=None):
+            if e_start is not None:
+                for cs in copy_streams:
+                    cs.wait_event(e_start)
+            issue_h2d(0)
+            for i in range(k_steps):
+                if i + 1 < k_steps:
+                    issue_h2d(i + 1)
+                issue_compute(i)
+            stream.wait_stream(d2h_stream)
+
+        run_pipeline(2)   # warm-up: first use of the streams and buffers
         torch.cuda.synchronize(dev)
+        in_free = [None] * nbuf
+        out_free = [None] * nbuf
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        run_pipeline(args.steps, e0)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        if not (torch.equal(h_out, out.cpu()) and (h_fin is None or torch.equal(h_fin, fin.cpu()))):
+            raise SystemExit("end-to-end outputs differ from the device-timed ones")
         e2e = {"value": whole_job_rate(tokens, world, args.steps, e2e_ms), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
-        del host, dev_in
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "pipeline": "double-buffered: step i+1's inputs copied while step i computes"}
+        del host, dev_in, outs, fins
     if kda.check_device_error(ws, dev):
         raise SystemExit("device error flags set during the timed steps")
 
