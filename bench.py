@@ -13,7 +13,7 @@ compulsory HBM bytes (1282 B per token-head plus states and gate parameters)
 over its CUDA-event duration against the measured copy bandwidth.
 
 `--impl reference` times the fp64 CPU oracle on the host cores instead, on a
-bounded sample of the same workload (the pages ship no code to run).
+bounded sample of the same workload (no runnable FlashKDA code is available).
 Under torchrun every rank runs its own replica of the workload (weak scaling,
 no data-path collective); rank 0 prints the line.
 """

@@ -9,7 +9,7 @@
 // gives S_1 directly), the carries are then composed in order,
 // S_{s+1} = P_s S_s + Q_s, and finally every segment runs its forward pass
 // from its true initial state.  All of this is derived from the recurrence;
-// the pages describe state carry across calls but not a segment scan.
+// FlashKDA's README carries the state across calls, with no segment scan.
 #include "kda_device.cuh"
 #include "kda_internal.h"
 

@@ -16,19 +16,20 @@
 //   S'   = Diag(2^G_C) S + (kh*2^(G_C-G))^T Vn
 //
 // Warp roles (256 threads, two CTAs per SM):
-//   warp 0      TMA producer: the q, k, g and v tiles of a chunk into one stage
-//               of a four-stage ring.
-//   warp 1      tcgen05 issuer (one thread).  State GEMMs in the M = V = 128
-//               orientation:  D1 = V^T Tm^T + S^T [-W^T | (qh 2^G)^T]   (N = 32)
-//                             D2 += Vn^T kfac ;  D1[:,16:] += Vn^T Aqk^T
-//   warps 2-3   prologue: each warp prepares whole chunks on its own (even /
-//               odd chunks): gate, cumsum, L2 norms, Gram matrices (tf32 warp
-//               MMA), inverse, W (bf16 warp MMA).  The tcgen05 operands are
-//               written in place over the tiles they are made from: q -> qh*2^G,
-//               k -> kfac (hi), g -> kfac (lo), and a bf16 copy of kh*2^G next
-//               to q, which the W product then overwrites with -W.
-//   warps 4-7   epilogue: Vn read-out (split into bf16 hi + lo), outputs,
-//               state decay + bf16 copy of S^T for the next chunk's A operand.
+//   warps 0-3   prologue, two pairs (even / odd chunks); a pair splits the 128
+//               channels: gate, cumsum, L2 norms, Gram matrices (tf32 warp MMA),
+//               inverse, W (bf16 warp MMA).  The tcgen05 operands are written in
+//               place over the tiles they are made from: q -> qh*2^G, k -> kfac
+//               (hi), g -> kfac (lo), and a bf16 copy of kh*2^G next to q, which
+//               the W product then overwrites with -W.
+//   warps 4-7   epilogue, one TMEM lane quarter each: Vn read-out (split into
+//               bf16 hi + lo), outputs, state decay + bf16 copy of S^T for the
+//               next chunk's A operand.  Lane 0 of warp 4 issues every tcgen05
+//               MMA; lane 0 of warp 5 issues the TMA loads of each stage of a
+//               four-stage ring.
+// State GEMMs in the M = V = 128 orientation:
+//               D1 = V^T Tm^T + S^T [-W^T | (qh 2^G)^T]   (N = 32)
+//               D2 += Vn^T kfac ;  D1[:,16:] += Vn^T Aqk^T
 // TMEM (256 columns): [0,128) S^T fp32 accumulator, [128,192) S^T as packed
 // bf16 (A operand read straight from TMEM), [192,256) two 32-column D1 tiles.
 //

@@ -15,7 +15,7 @@
  * S (K x V) stored transposed as [.., V, K] (FLA transpose_state_layout=True).
  * The device computes it in 16-token chunks ("processes 16-token chunks"); the
  * chunk's unit lower-triangular system is inverted in fp32 by forward
- * substitution (the pages use a Neumann-series product; both give the exact
+ * substitution (FlashKDA's articles use a Neumann-series product; both give the exact
  * inverse of a 16 x 16 unit lower-triangular matrix).
  *
  * Conventions for every entry point:
@@ -172,7 +172,7 @@ KDA_API kda_status kda_fwd_ex(const kda_shape *shape, const void *q, const void 
 KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t stream, int *flags);
 
 /*
- * Measurement aid (no counterpart on the pages): while `events` is non-NULL,
+ * Measurement aid (no counterpart in flash_kda): while `events` is non-NULL,
  * every kda_fwd records events[i] (cudaEvent_t handles owned by the caller) on
  * its stream right after its i-th launch -- 0: work-list scheduling, 1: the
  * segment carry/transition runs, 2: carry composition, 3: the forward runs --
@@ -182,15 +182,15 @@ KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t st
 KDA_API kda_status kda_set_profile_events(void *const *events, int n_events);
 
 /*
- * Measurement aid (no counterpart on the pages): the number of kernels the
+ * Measurement aid (no counterpart in flash_kda): the number of kernels the
  * calling thread's most recent successful kda_fwd enqueued (2 to 4: work-list
  * scheduling, segment runs, carry composition, forward runs).
  */
 KDA_API int kda_last_launch_count(void);
 
 /*
- * kda_fwd for callers that cannot allocate device memory (no counterpart on
- * the pages).  Some callers have no way to hand over scratch memory: code that
+ * kda_fwd for callers that cannot allocate device memory (no counterpart in
+ * flash_kda).  Some callers have no way to hand over scratch memory: code that
  * runs where cudaMalloc is not allowed (a framework that owns every device
  * allocation through its own pool, a runtime that must not grow its footprint
  * after start-up, a plugin without access to the application's allocator).

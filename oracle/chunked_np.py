@@ -4,7 +4,7 @@ FlashKDA processes a sequence in 16-token chunks ("Delta Attention Algorithm
 ... processes 16-token chunks") and inverts the chunk's unit lower-triangular
 system with a Neumann-series product ("Neumann-series expansion ... matrix
 inversion").  This module writes that chunked form out plainly, one chunk at
-a time, with the chunk length C as a parameter (C = 16 is the pages'; any C
+a time, with the chunk length C as a parameter (C = 16 is FlashKDA's; any C
 reaches the same result as the token recurrence up to rounding).
 
 Per chunk, with S0 the state (K x V) on entry, rows i, j < n_valid:

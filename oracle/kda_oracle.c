@@ -17,7 +17,7 @@
  *   and the final S is written transposed, final[n,h,v,c] = S[c][v]
  *   (README: state shape [B,H,V,K] / [N,H,V,K], FLA transpose_state_layout).
  *
- * Three switches follow the flags of the pages' reference call (chunk_kda's
+ * Three switches follow the flags of the chunk_kda call in FlashKDA's README (chunk_kda's
  * use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel), each
  * set in `flags` when the step is NOT done here:
  *   ORACLE_GATE_PREACTIVATED (1): g already holds ghat (natural-log decay), so
@@ -30,7 +30,7 @@
  *       softplus(x) = log(1 + exp(x)); lower_bound is not used.  It cannot be
  *       combined with ORACLE_GATE_PREACTIVATED.
  *
- * Readings where the pages are silent: the gate is a sigmoid scaled by the
+ * Readings where FlashKDA's README and articles are silent: the gate is a sigmoid scaled by the
  * lower bound (README "safe_gate", "Gate lower bound (range from -5.0 to 0)");
  * the L2-norm epsilon is 1e-6 inside the square root; scale is applied after
  * normalisation.  Parity of these readings against the original library is

@@ -1,5 +1,5 @@
-"""Pins for the oracle's three switches, named after the flags of the pages' reference
-call (chunk_kda: use_gate_in_kernel, use_beta_sigmoid_in_kernel,
+"""Pins for the oracle's three switches, named after the flags of the chunk_kda
+call in FlashKDA's README (chunk_kda: use_gate_in_kernel, use_beta_sigmoid_in_kernel,
 use_qk_l2norm_in_kernel).  When a flag is off, that step was done by the caller:
 g holds the natural-log decay itself, beta holds beta itself, q and k are used as
 given.  Each pin recomputes the T = 1 step (or a decay-only run) in numpy from

@@ -1,6 +1,6 @@
-"""Pins for the CPU oracle: checks against what the pages and the mathematics fix.
+"""Pins for the CPU oracle: checks against what FlashKDA's README and the mathematics fix.
 
-No worked numbers are printed on the pages, so every pin is a closed form, an
+FlashKDA's README and articles print no worked numbers, so every pin is a closed form, an
 invariant, a special case with an exactly known answer, or an independent
 derivation (the 16-token chunked form) that must agree with the token
 recurrence.  Each pin is chosen so that a plausible slip in the oracle -- a
