@@ -118,20 +118,20 @@ Layout make_layout(const kda_shape& s, int sms) {
 
 kda_status check_shape(const kda_shape* s) {
   if (s == nullptr) return KDA_ERR_INVALID_ARGUMENT;
-  if (s->K != 128 || (s->V != 128 && s->V != 256)) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (s->K != 128 || (s->V != 64 && s->V != 128 && s->V != 256)) return KDA_ERR_UNSUPPORTED_SHAPE;
   if (s->B < 0 || s->T < 0 || s->H <= 0 || s->N < 0) return KDA_ERR_INVALID_ARGUMENT;
   if (s->B > 0 && s->T > (int64_t)0x7fffffff / std::max<int64_t>(s->B, 1)) return KDA_ERR_INVALID_ARGUMENT;
-  const int64_t Hv = s->H * (s->V / 128);
+  const int64_t Hv = s->H * std::max<int64_t>(s->V / 128, 1);
   if (Hv > 65535 || s->N > (int64_t)0x7fffffff / Hv) return KDA_ERR_INVALID_ARGUMENT;
   return KDA_OK;
 }
 
 // The value columns of a state are independent, so V = 256 runs as two chains of
 // 128 state rows per head: the work lists, segment slots and split policy see
-// H x V/128 "heads" of width 128.
+// H x V/128 "heads" of width 128.  V = 64 runs as one chain whose rows 64-127 stay zero.
 kda_shape chain_shape(const kda_shape& s) {
   kda_shape c = s;
-  c.H = s.H * (s.V / 128);
+  c.H = s.H * std::max<int64_t>(s.V / 128, 1);
   c.V = 128;
   return c;
 }
@@ -163,12 +163,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// [rows, H, 128] bf16 viewed as a 3-D tensor {128, H, rows}; box {64, 1, 16}, 128-byte swizzle.
-bool encode_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H) {
+// [rows, H, width] bf16 viewed as a 3-D tensor {width, H, rows}; box {64, 1, 16}, 128-byte
+// swizzle (width 128 for q and k, 64 for a V = 64 v).
+bool encode_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int64_t width = 128) {
   auto enc = get_encode();
   if (!enc) return false;
-  cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)std::max<int64_t>(rows, 1)};
-  cuuint64_t strides[2] = {256, (cuuint64_t)(H * 256)};
+  cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)H, (cuuint64_t)std::max<int64_t>(rows, 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)(width * 2), (cuuint64_t)(H * width * 2)};
   cuuint32_t box[3] = {64, 1, 16};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -238,7 +239,7 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
   if (st != KDA_OK) return st;
   const kda_shape s = *shape;
   if (s.N != s.B) return KDA_ERR_INVALID_ARGUMENT;
-  if ((long long)s.B * s.H * (s.V / 128) > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
+  if ((long long)s.B * s.H * (s.V / 64) > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
   if (!valid_flags(flags)) return KDA_ERR_INVALID_ARGUMENT;
   const bool gate_here = !(flags & KDA_GATE_PREACTIVATED);
   if (uses_lower_bound(flags) && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
@@ -270,7 +271,7 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
   dp.B = (int)s.B;
   dp.T = (int)s.T;
   dp.H = (int)s.H;
-  dp.vsplit = (int)(s.V / 128);
+  dp.vsplit = (int)(s.V / 64);   // 64-row CTAs per head
   dp.scale = scale;
   dp.lower_bound = lower_bound;
   dp.flags = (int)flags;
@@ -373,8 +374,10 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   ChainParams cp;
   std::memset(&cp, 0, sizeof(cp));
   if (rows > 0) {
+    const bool v_ok = s.V == 64 ? encode_tile_map(&cp.tm_v, v, rows, s.H, 64)
+                                : encode_halves_map(&cp.tm_v, v, rows, s.H, s.V);
     if (!encode_tile_map(&cp.tm_q, q, rows, s.H) || !encode_halves_map(&cp.tm_k, k, rows, s.H) ||
-        !encode_halves_map(&cp.tm_g, g, rows, s.H) || !encode_halves_map(&cp.tm_v, v, rows, s.H, s.V))
+        !encode_halves_map(&cp.tm_g, g, rows, s.H) || !v_ok)
       return KDA_ERR_CUDA;
   }
   cp.beta = static_cast<const uint16_t*>(beta);
@@ -386,7 +389,8 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   cp.ws_states = reinterpret_cast<float*>(ws + L.off_slots);
   cp.err = &hdr->err;
   cp.H = (int)s.H;
-  cp.vsplit = (int)(s.V / 128);
+  cp.vsplit = (int)std::max<int64_t>(s.V / 128, 1);
+  cp.vrows = s.V == 64 ? 64 : 128;
   cp.init_dtype = (int)init_dtype;
   cp.final_dtype = (int)final_dtype;
   cp.scale = scale;

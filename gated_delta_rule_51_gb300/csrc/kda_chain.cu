@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   // work items count heads x value blocks: V = 128 * vsplit columns are independent
   // chains of 128 state rows each, sharing the head's q, k, g and beta
   const int head = it.head / p.vsplit, vblk = it.head - head * p.vsplit;
-  const size_t vstride = (size_t)p.vsplit * kDimV;   // V
+  const size_t vstride = p.vrows == 64 ? 64 : (size_t)p.vsplit * kDimV;   // V
 
   extern __shared__ uint8_t smem_dyn[];
   SmemLayout& S = *reinterpret_cast<SmemLayout*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
@@ -587,8 +587,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
     mbar_fence_init();
   }
   if (warp >= kWarpProlog0 && warp < kWarpEpi0) {
-    // rows 16..31 of the [Tm ; 0] operands stay zero for the whole run
     const int t = threadIdx.x - kWarpProlog0 * 32;   // 0..127
+    // with V = 64 the v tile's second 64 columns are never loaded: zero for the whole run
+    // (128 threads x 16 bytes = the 2 KiB half-tile of each stage)
+    if (p.vrows == 64)
+      for (int s = 0; s < kStages; ++s)
+        reinterpret_cast<uint4*>(S.st[s].V + 2048)[t] = make_uint4(0u, 0u, 0u, 0u);
+    // rows 16..31 of the [Tm ; 0] operands stay zero for the whole run
     if (t < 64) {
       for (int s = 0; s < kStages; ++s) {
         reinterpret_cast<uint64_t*>(S.sm[s].TPhi + 512)[t] = 0ull;
@@ -721,13 +726,16 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         const int s = c % kStages;
         const int row = it.row0 + c * kChunk;
         Stage& st = S.st[s];
-        mbar_arrive_expect_tx(&bar_full[s], load_v ? 16384u : 12288u);
+        mbar_arrive_expect_tx(&bar_full[s], load_v ? (p.vrows == 64 ? 14336u : 16384u) : 12288u);
         // q: one 64-channel half into each S-side operand tile; k, g, v: both halves at once
         tma_load_3d(st.X[0] + 2048, &p.tm_q, &bar_full[s], 0, head, row);
         tma_load_3d(st.X[1] + 2048, &p.tm_q, &bar_full[s], 64, head, row);
         tma_load_4d(st.K, &p.tm_k, &bar_full[s], 0, head, row, 0);
         tma_load_4d(st.G, &p.tm_g, &bar_full[s], 0, head, row, 0);
-        if (load_v) tma_load_4d(st.V, &p.tm_v, &bar_full[s], 0, head, row, 2 * vblk);
+        if (load_v) {
+          if (p.vrows == 64) tma_load_3d(st.V, &p.tm_v, &bar_full[s], 0, head, row);   // V = 64: one tile
+          else tma_load_4d(st.V, &p.tm_v, &bar_full[s], 0, head, row, 2 * vblk);
+        }
         ++tma_issued;
       };
       if (tma_thread) {
@@ -759,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
               const float4 x = src[t];
               s[4 * t] = x.x; s[4 * t + 1] = x.y; s[4 * t + 2] = x.z; s[4 * t + 3] = x.w;
             }
-          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 2) {
+          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 2 && vrow < p.vrows) {
             const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) +
                                                                 srow * 128 + 32 * j);
 #pragma unroll
@@ -767,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
               const float4 x = src[t];
               s[4 * t] = x.x; s[4 * t + 1] = x.y; s[4 * t + 2] = x.z; s[4 * t + 3] = x.w;
             }
-          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 1) {
+          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 1 && vrow < p.vrows) {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.init_state) +
                                                               srow * 128 + 32 * j);
 #pragma unroll
@@ -879,13 +887,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
               for (int t = 0; t < 8; ++t)
                 dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
                                      __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2) {
+            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2 && vrow < p.vrows) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * 128 + 32 * j);
 #pragma unroll
               for (int t = 0; t < 8; ++t)
                 dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
                                      __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1) {
+            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1 && vrow < p.vrows) {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * 128 + 32 * j);
 #pragma unroll
               for (int t = 0; t < 4; ++t)
@@ -925,12 +933,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
               const int q = lane + 32 * rr, i = q >> 2, seg = q & 3;
-              if (i < nv)
+              if (i < nv && 32 * q4 < p.vrows)
                 *reinterpret_cast<uint4*>(obase + (size_t)i * row_elems + 32 * q4 + 8 * seg) =
                     *reinterpret_cast<const uint4*>(&S.ostage[i][64 * q4 + 16 * seg]);
             }
           } else {
-            for (int i = 0; i < nv; ++i)
+            for (int i = 0; i < nv && vrow < p.vrows; ++i)
               obase[(size_t)i * row_elems + vrow] = *reinterpret_cast<const uint16_t*>(&S.ostage[i][2 * vrow]);
           }
           __syncwarp();   // the staging rows are rewritten by the next chunk
@@ -955,14 +963,14 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       float x = 0.f;
       if (it.in_slot == kInIdentity) x = (t == vrow) ? 1.f : 0.f;
       else if (it.in_slot >= 0) x = p.ws_states[(size_t)it.in_slot * 16384 + (size_t)vrow * 128 + t];
-      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 2)
+      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 2 && vrow < p.vrows)
         x = static_cast<const float*>(p.init_state)[srow * 128 + t];
-      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1)
+      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1 && vrow < p.vrows)
         x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.init_state)[srow * 128 + t]);
       if (it.out_slot >= 0) p.ws_states[(size_t)it.out_slot * 16384 + (size_t)vrow * 128 + t] = x;
-      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2)
+      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2 && vrow < p.vrows)
         static_cast<float*>(p.final_state)[srow * 128 + t] = x;
-      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 1)
+      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 1 && vrow < p.vrows)
         static_cast<uint16_t*>(p.final_state)[srow * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
     }
   }

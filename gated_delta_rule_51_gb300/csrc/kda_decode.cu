@@ -10,11 +10,10 @@
 //   beta  = sigmoid(beta logit) (or given);  qh, kh = x / sqrt(|x|^2 + 1e-6) (or as given)
 //   row v of S^T:  s <- s * exp(ghat);  s <- s + beta (v_v - s . kh) kh
 //   o_v   = scale * s . qh        (from the updated row)
-// Rows are independent, so the work is bandwidth-bound: kSub CTAs per (n, h,
-// 128-row value block), each of kDecRows rows in warps of sixteen, every lane
-// holding four key channels of each of its rows in registers for all the call's
-// tokens.  The state is read once (64 KiB fp32 or 32 KiB bf16 per head) and
-// written once.
+// Rows are independent, so the work is bandwidth-bound: V / kDecRows CTAs per
+// (n, h), each of kDecRows rows in warps of sixteen, every lane holding four key
+// channels of each of its rows in registers for all the call's tokens.  The state
+// is read once (V x 128 fp32 or bf16 per head) and written once.
 #include <cuda_bf16.h>
 
 #include "kda_device.cuh"
@@ -26,7 +25,6 @@ namespace {
 constexpr int kRowsPerWarp = 16;
 constexpr int kDecRows = 64;                        // state rows per CTA (four CTAs per SM)
 constexpr int kDecThreads = 2 * kDecRows;           // 16 rows a warp; at least 128 threads
-constexpr int kSub = 128 / kDecRows;                // CTAs per 128-row value block
 static_assert(kDecThreads >= 128, "the per-channel vectors take 128 threads");
 
 __device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
@@ -49,20 +47,17 @@ __device__ __forceinline__ float sigmoidf(float x) { return 1.f / (1.f + expf(-x
 // log(1 + exp(x)) without overflow
 __device__ __forceinline__ float softplusf(float x) { return x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x)); }
 
-template <int kVsplit, int kFlags>
+template <int V, int kFlags>
 __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decode_kernel(const DecodeParams p) {
-  // kSub CTAs per (sequence, head, 128-row value block); V = 128 * kVsplit.  The CTA's
-  // kDecRows state rows are block blockIdx.x of the [B * H * V / kDecRows, kDecRows, 128]
-  // state.
-  const int sub = (int)(blockIdx.x % kSub);
-  const int blk = (int)(blockIdx.x / kSub);
-  const int vblk = kVsplit == 1 ? 0 : blk % kVsplit;
-  const int nh = kVsplit == 1 ? blk : blk / kVsplit;
-  const int rowbase = sub * kDecRows;   // first row of this CTA within its value block
+  // V / kDecRows CTAs per (sequence, head), V = 64, 128 or 256.  The CTA's kDecRows state
+  // rows are block blockIdx.x of the [B * H * V / kDecRows, kDecRows, 128] state.
+  constexpr int kSubs = V / kDecRows;
+  const int sub = kSubs == 1 ? 0 : (int)(blockIdx.x % kSubs);
+  const int nh = kSubs == 1 ? (int)blockIdx.x : (int)(blockIdx.x / kSubs);
+  const int vbase = sub * kDecRows;   // value index of this CTA's first row
   const int n = nh / p.H, h = nh - n * p.H;
-  constexpr int V = kVsplit * 128;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  __shared__ __align__(16) float s_alpha[128], s_kh[128], s_qh[128], s_v[128];
+  __shared__ __align__(16) float s_alpha[128], s_kh[128], s_qh[128], s_v[kDecRows];
   __shared__ float s_norm[2][4];
   __shared__ float s_beta;
 
@@ -101,7 +96,7 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
       qq = bf(p.q[tok * 128 + tid]);
       s_kh[tid] = kk;
       s_qh[tid] = qq;
-      s_v[tid] = bf(p.v[tok * V + 128 * vblk + tid]);
+      if (tid < kDecRows) s_v[tid] = bf(p.v[tok * V + vbase + tid]);   // this CTA's rows' values
       const float sk = warp_sum(kk * kk), sq = warp_sum(qq * qq);
       if (lane == 0) {
         s_norm[0][warp] = sk;
@@ -131,7 +126,7 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
     warp_sum16(d);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-      const float c = beta * (s_v[rowbase + kRowsPerWarp * warp + r] - d[r]);
+      const float c = beta * (s_v[kRowsPerWarp * warp + r] - d[r]);
       st[r].x = fmaf(c, kh.x, st[r].x); st[r].y = fmaf(c, kh.y, st[r].y);
       st[r].z = fmaf(c, kh.z, st[r].z); st[r].w = fmaf(c, kh.w, st[r].w);
       d[r] = st[r].x * qh.x + st[r].y * qh.y + st[r].z * qh.z + st[r].w * qh.w;
@@ -141,7 +136,7 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
       float o = d[0];
 #pragma unroll
       for (int r = 1; r < kRowsPerWarp; ++r) o = lane == r ? d[r] : o;
-      p.out[tok * V + 128 * vblk + rowbase + kRowsPerWarp * warp + lane] =
+      p.out[tok * V + vbase + kRowsPerWarp * warp + lane] =
           __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * o));
     }
     if (t + 1 < p.T) __syncthreads();   // the per-channel vectors are rewritten by the next token
@@ -163,22 +158,28 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
-  const long long grid = (long long)p.B * p.H * p.vsplit * kSub;
+  // p.vsplit carries V / 64 (1, 2 or 4): one 64-row CTA per 64 value rows
+  const long long grid = (long long)p.B * p.H * p.vsplit;
   if (grid <= 0 || p.T <= 0) return cudaSuccess;
-  // the value split and the flags are template parameters: the common case (V = 128,
-  // every step in the kernel) carries no per-thread tests of either
+  // V and the flags are template parameters: the common case (V = 128, every step in the
+  // kernel) carries no per-thread tests of either (the preactivated and softplus gates
+  // exclude each other: no kernel for both)
   using Kernel = void (*)(DecodeParams);
-  // (the preactivated and softplus gates exclude each other: no kernel for both)
-  static constexpr Kernel kernels[2][16] = {
-      {kda_decode_kernel<1, 0>, kda_decode_kernel<1, 1>, kda_decode_kernel<1, 2>, kda_decode_kernel<1, 3>,
-       kda_decode_kernel<1, 4>, kda_decode_kernel<1, 5>, kda_decode_kernel<1, 6>, kda_decode_kernel<1, 7>,
-       kda_decode_kernel<1, 8>, nullptr, kda_decode_kernel<1, 10>, nullptr,
-       kda_decode_kernel<1, 12>, nullptr, kda_decode_kernel<1, 14>, nullptr},
-      {kda_decode_kernel<2, 0>, kda_decode_kernel<2, 1>, kda_decode_kernel<2, 2>, kda_decode_kernel<2, 3>,
-       kda_decode_kernel<2, 4>, kda_decode_kernel<2, 5>, kda_decode_kernel<2, 6>, kda_decode_kernel<2, 7>,
-       kda_decode_kernel<2, 8>, nullptr, kda_decode_kernel<2, 10>, nullptr,
-       kda_decode_kernel<2, 12>, nullptr, kda_decode_kernel<2, 14>, nullptr}};
-  const Kernel k = kernels[p.vsplit == 2 ? 1 : 0][p.flags & 15];
+  static constexpr Kernel kernels[3][16] = {
+      {kda_decode_kernel<64, 0>, kda_decode_kernel<64, 1>, kda_decode_kernel<64, 2>, kda_decode_kernel<64, 3>,
+       kda_decode_kernel<64, 4>, kda_decode_kernel<64, 5>, kda_decode_kernel<64, 6>, kda_decode_kernel<64, 7>,
+       kda_decode_kernel<64, 8>, nullptr, kda_decode_kernel<64, 10>, nullptr,
+       kda_decode_kernel<64, 12>, nullptr, kda_decode_kernel<64, 14>, nullptr},
+      {kda_decode_kernel<128, 0>, kda_decode_kernel<128, 1>, kda_decode_kernel<128, 2>, kda_decode_kernel<128, 3>,
+       kda_decode_kernel<128, 4>, kda_decode_kernel<128, 5>, kda_decode_kernel<128, 6>, kda_decode_kernel<128, 7>,
+       kda_decode_kernel<128, 8>, nullptr, kda_decode_kernel<128, 10>, nullptr,
+       kda_decode_kernel<128, 12>, nullptr, kda_decode_kernel<128, 14>, nullptr},
+      {kda_decode_kernel<256, 0>, kda_decode_kernel<256, 1>, kda_decode_kernel<256, 2>, kda_decode_kernel<256, 3>,
+       kda_decode_kernel<256, 4>, kda_decode_kernel<256, 5>, kda_decode_kernel<256, 6>, kda_decode_kernel<256, 7>,
+       kda_decode_kernel<256, 8>, nullptr, kda_decode_kernel<256, 10>, nullptr,
+       kda_decode_kernel<256, 12>, nullptr, kda_decode_kernel<256, 14>, nullptr}};
+  const int vi = p.vsplit == 1 ? 0 : (p.vsplit == 2 ? 1 : 2);
+  const Kernel k = kernels[vi][p.flags & 15];
   if (k == nullptr) return cudaErrorInvalidValue;
   k<<<(unsigned)grid, kDecThreads, 0, s>>>(p);
   return cudaGetLastError();

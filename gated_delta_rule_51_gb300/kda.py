@@ -208,7 +208,7 @@ def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
            safe_gate: bool = True):
     """Recurrent KDA step(s) for decoding; updates ``state`` in place, writes ``out``.
 
-    q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,V] bf16 with V = 128 or 256 (T new
+    q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,V] bf16 with V = 64, 128 or 256 (T new
     tokens per sequence, usually 1); beta: [B,T,H] bf16 logits; A_log: [H] fp32;
     dt_bias: [H,128] fp32; state: [B,H,V,128] bf16 or fp32, read before the first
     token and overwritten.  The switches are those of fwd.

@@ -51,7 +51,7 @@ typedef struct CUstream_st *kda_stream_t; /* a cudaStream_t */
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, bad size, lower_bound out of range */
-    KDA_ERR_UNSUPPORTED_SHAPE = 2,  /* K other than 128, or V other than 128 and 256 */
+    KDA_ERR_UNSUPPORTED_SHAPE = 2,  /* K other than 128, or V other than 64, 128 and 256 */
     KDA_ERR_WORKSPACE_TOO_SMALL = 3,
     KDA_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
     KDA_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
@@ -96,7 +96,7 @@ typedef enum {
 /*
  * Problem shape (README parameter table; the README requires K = V = 128, this
  * library also takes V = 256, run as two independent 128-row halves of each
- * state):
+ * state, and V = 64, run as one 128-row chain whose last 64 rows stay zero):
  *   q, k, g : [B, T, H, K] bf16      v, out : [B, T, H, V] bf16
  *   beta    : [B, T, H]    bf16 (logits)
  *   A_log   : [H] fp32               dt_bias : [H, K] fp32

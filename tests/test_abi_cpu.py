@@ -159,6 +159,14 @@ def test_fwd_ex_flags_on_the_host():
     assert _fwd_ex_call(6) in (4, 5)
 
 
+def test_v64_passes_the_shape_checks():
+    # V = 64 is accepted (one chain whose last 64 state rows stay zero); V = 32 is not
+    assert _call(kda.make_shape(1, 64, 1, 1, V=64)) in (4, 5)
+    assert _decode_call(kda.make_shape(4, 1, 2, 4, V=64)) in (4, 5)
+    assert _call(kda.make_shape(1, 64, 1, 1, V=32)) == 2
+    assert kda.workspace_size(kda.make_shape(1, 64, 2, 1, V=64)) == kda.workspace_size(kda.make_shape(1, 64, 2, 1))
+
+
 def test_v256_passes_the_shape_checks():
     # V = 256 is accepted (two 128-row chains per head); without a GPU the call stops at the device query
     assert _call(kda.make_shape(1, 64, 1, 1, V=256)) in (4, 5)
