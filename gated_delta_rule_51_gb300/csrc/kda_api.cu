@@ -118,7 +118,7 @@ Layout make_layout(const kda_shape& s, int sms) {
 
 kda_status check_shape(const kda_shape* s) {
   if (s == nullptr) return KDA_ERR_INVALID_ARGUMENT;
-  if (s->K != 128 || (s->V != 64 && s->V != 128 && s->V != 256)) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if ((s->K != 64 && s->K != 128) || (s->V != 64 && s->V != 128 && s->V != 256)) return KDA_ERR_UNSUPPORTED_SHAPE;
   if (s->B < 0 || s->T < 0 || s->H <= 0 || s->N < 0) return KDA_ERR_INVALID_ARGUMENT;
   if (s->B > 0 && s->T > (int64_t)0x7fffffff / std::max<int64_t>(s->B, 1)) return KDA_ERR_INVALID_ARGUMENT;
   const int64_t Hv = s->H * std::max<int64_t>(s->V / 128, 1);
@@ -128,10 +128,12 @@ kda_status check_shape(const kda_shape* s) {
 
 // The value columns of a state are independent, so V = 256 runs as two chains of
 // 128 state rows per head: the work lists, segment slots and split policy see
-// H x V/128 "heads" of width 128.  V = 64 runs as one chain whose rows 64-127 stay zero.
+// H x V/128 "heads" of width 128.  V = 64 runs as one chain whose rows 64-127 stay zero,
+// and K = 64 as a chain whose channels 64-127 are zero.
 kda_shape chain_shape(const kda_shape& s) {
   kda_shape c = s;
   c.H = s.H * std::max<int64_t>(s.V / 128, 1);
+  c.K = 128;
   c.V = 128;
   return c;
 }
@@ -202,7 +204,7 @@ const char* kda_status_string(kda_status s) {
   switch (s) {
     case KDA_OK: return "ok";
     case KDA_ERR_INVALID_ARGUMENT: return "invalid argument";
-    case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K must be 128, V 128 or 256)";
+    case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K must be 64 or 128, V 64, 128 or 256)";
     case KDA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case KDA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3, sm_103a)";
     case KDA_ERR_CUDA: return "CUDA error";
@@ -272,6 +274,7 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
   dp.T = (int)s.T;
   dp.H = (int)s.H;
   dp.vsplit = (int)(s.V / 64);   // 64-row CTAs per head
+  dp.kdim = (int)s.K;
   dp.scale = scale;
   dp.lower_bound = lower_bound;
   dp.flags = (int)flags;
@@ -318,7 +321,8 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
       if (p == nullptr || !aligned16(p)) return KDA_ERR_INVALID_ARGUMENT;
     if (beta == nullptr || out == nullptr || !aligned(beta, 2) || !aligned(out, 2)) return KDA_ERR_INVALID_ARGUMENT;
   }
-  if (gate_here && (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned(dt_bias, 4)))
+  // the chain kernel reads dt_bias four values at a time
+  if (gate_here && (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned16(dt_bias)))
     return KDA_ERR_INVALID_ARGUMENT;
   // states: README "accept None (stateless), bf16, or fp32 ... When both are provided, their dtypes must match"
   auto dtype_ok = [](kda_state_dtype d) { return d == KDA_STATE_BF16 || d == KDA_STATE_FP32; };
@@ -328,7 +332,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   if (final_state == nullptr && final_dtype != KDA_STATE_NONE) return KDA_ERR_INVALID_ARGUMENT;
   if (initial_state != nullptr && final_state != nullptr) {
     if (init_dtype != final_dtype) return KDA_ERR_INVALID_ARGUMENT;
-    const size_t bytes = (size_t)s.N * s.H * s.V * 128 * (init_dtype == KDA_STATE_FP32 ? 4 : 2);
+    const size_t bytes = (size_t)s.N * s.H * s.V * s.K * (init_dtype == KDA_STATE_FP32 ? 4 : 2);
     const uintptr_t a = reinterpret_cast<uintptr_t>(initial_state), b = reinterpret_cast<uintptr_t>(final_state);
     if (a != b && a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARGUMENT;   // partial overlap
   }
@@ -376,8 +380,12 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   if (rows > 0) {
     const bool v_ok = s.V == 64 ? encode_tile_map(&cp.tm_v, v, rows, s.H, 64)
                                 : encode_halves_map(&cp.tm_v, v, rows, s.H, s.V);
-    if (!encode_tile_map(&cp.tm_q, q, rows, s.H) || !encode_halves_map(&cp.tm_k, k, rows, s.H) ||
-        !encode_halves_map(&cp.tm_g, g, rows, s.H) || !v_ok)
+    // K = 64: one 64-channel tile each of q, k and g
+    const bool kg_ok = s.K == 64 ? encode_tile_map(&cp.tm_k, k, rows, s.H, 64) &&
+                                       encode_tile_map(&cp.tm_g, g, rows, s.H, 64)
+                                 : encode_halves_map(&cp.tm_k, k, rows, s.H) &&
+                                       encode_halves_map(&cp.tm_g, g, rows, s.H);
+    if (!encode_tile_map(&cp.tm_q, q, rows, s.H, s.K) || !kg_ok || !v_ok)
       return KDA_ERR_CUDA;
   }
   cp.beta = static_cast<const uint16_t*>(beta);
@@ -391,6 +399,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   cp.H = (int)s.H;
   cp.vsplit = (int)std::max<int64_t>(s.V / 128, 1);
   cp.vrows = s.V == 64 ? 64 : 128;
+  cp.kdim = (int)s.K;
   cp.init_dtype = (int)init_dtype;
   cp.final_dtype = (int)final_dtype;
   cp.scale = scale;

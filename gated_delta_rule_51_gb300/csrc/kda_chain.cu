@@ -593,6 +593,15 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
     if (p.vrows == 64)
       for (int s = 0; s < kStages; ++s)
         reinterpret_cast<uint4*>(S.st[s].V + 2048)[t] = make_uint4(0u, 0u, 0u, 0u);
+    // with K = 64 the q, k and g tiles' channels 64-127 are never loaded: zero (the prologue
+    // then writes zeros there as the gated operands of those channels)
+    if (p.kdim == 64)
+      for (int s = 0; s < kStages; ++s) {
+        reinterpret_cast<uint4*>(S.st[s].X[1])[t] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(S.st[s].X[1] + 2048)[t] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(S.st[s].K + 2048)[t] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(S.st[s].G + 2048)[t] = make_uint4(0u, 0u, 0u, 0u);
+      }
     // rows 16..31 of the [Tm ; 0] operands stay zero for the whole run
     if (t < 64) {
       for (int s = 0; s < kStages; ++s) {
@@ -622,8 +631,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       // the gate's scale terms: the sigmoid gate takes -exp(A_log) log2(e) (g + dt_bias) and
       // lower_bound log2(e); the softplus gate log2(e) (g + dt_bias) and -exp(A_log)
       const float nr = gate_pre ? 0.f : (gate_sp ? kLog2e : -rate * kLog2e);
-      const float* dtb = gate_pre ? nullptr : p.dt_bias + (size_t)h * kDimK;
-      const float lbl2 = gate_sp ? -rate : p.lower_bound * kLog2e;
+      // the head's dt_bias (K values).  With K = 64, warp 1 of a pair holds channels 64-127
+      // (zero q, k and g): it reads the head's own 64 values again, and a zero output scale
+      // gives those channels the decay 1 whatever they are
+      const bool kpad = p.kdim == 64 && w == 1;
+      const float* dtb = gate_pre ? nullptr : p.dt_bias + (kpad ? h * 64 - 64 : h * p.kdim);
+      const float lbl2 = kpad ? 0.f : (gate_sp ? -rate : p.lower_bound * kLog2e);
       const int gid = lane >> 2;
       auto load_beta = [&](int c, float& b0, float& b1) {
         const int base = it.row0 + c * kChunk;
@@ -726,12 +739,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         const int s = c % kStages;
         const int row = it.row0 + c * kChunk;
         Stage& st = S.st[s];
-        mbar_arrive_expect_tx(&bar_full[s], load_v ? (p.vrows == 64 ? 14336u : 16384u) : 12288u);
+        const uint32_t qkg_bytes = p.kdim == 64 ? 6144u : 12288u;
+        mbar_arrive_expect_tx(&bar_full[s], qkg_bytes + (load_v ? (p.vrows == 64 ? 2048u : 4096u) : 0u));
         // q: one 64-channel half into each S-side operand tile; k, g, v: both halves at once
+        // (K = 64: one 64-channel tile of each)
         tma_load_3d(st.X[0] + 2048, &p.tm_q, &bar_full[s], 0, head, row);
-        tma_load_3d(st.X[1] + 2048, &p.tm_q, &bar_full[s], 64, head, row);
-        tma_load_4d(st.K, &p.tm_k, &bar_full[s], 0, head, row, 0);
-        tma_load_4d(st.G, &p.tm_g, &bar_full[s], 0, head, row, 0);
+        if (p.kdim == 64) {
+          tma_load_3d(st.K, &p.tm_k, &bar_full[s], 0, head, row);
+          tma_load_3d(st.G, &p.tm_g, &bar_full[s], 0, head, row);
+        } else {
+          tma_load_3d(st.X[1] + 2048, &p.tm_q, &bar_full[s], 64, head, row);
+          tma_load_4d(st.K, &p.tm_k, &bar_full[s], 0, head, row, 0);
+          tma_load_4d(st.G, &p.tm_g, &bar_full[s], 0, head, row, 0);
+        }
         if (load_v) {
           if (p.vrows == 64) tma_load_3d(st.V, &p.tm_v, &bar_full[s], 0, head, row);   // V = 64: one tile
           else tma_load_4d(st.V, &p.tm_v, &bar_full[s], 0, head, row, 2 * vblk);
@@ -767,17 +787,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
               const float4 x = src[t];
               s[4 * t] = x.x; s[4 * t + 1] = x.y; s[4 * t + 2] = x.z; s[4 * t + 3] = x.w;
             }
-          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 2 && vrow < p.vrows) {
+          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 2 && vrow < p.vrows &&
+                     32 * j < p.kdim) {
             const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) +
-                                                                srow * 128 + 32 * j);
+                                                                srow * p.kdim + 32 * j);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const float4 x = src[t];
               s[4 * t] = x.x; s[4 * t + 1] = x.y; s[4 * t + 2] = x.z; s[4 * t + 3] = x.w;
             }
-          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 1 && vrow < p.vrows) {
+          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 1 && vrow < p.vrows &&
+                     32 * j < p.kdim) {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.init_state) +
-                                                              srow * 128 + 32 * j);
+                                                              srow * p.kdim + 32 * j);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               const uint4 x = src[t];
@@ -887,14 +909,16 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
               for (int t = 0; t < 8; ++t)
                 dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
                                      __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2 && vrow < p.vrows) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * 128 + 32 * j);
+            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2 && vrow < p.vrows &&
+                       32 * j < p.kdim) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * p.kdim + 32 * j);
 #pragma unroll
               for (int t = 0; t < 8; ++t)
                 dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
                                      __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1 && vrow < p.vrows) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * 128 + 32 * j);
+            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1 && vrow < p.vrows &&
+                       32 * j < p.kdim) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * p.kdim + 32 * j);
 #pragma unroll
               for (int t = 0; t < 4; ++t)
                 dst[t] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * t]), __uint_as_float(r[8 * t + 1])),
@@ -963,15 +987,15 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       float x = 0.f;
       if (it.in_slot == kInIdentity) x = (t == vrow) ? 1.f : 0.f;
       else if (it.in_slot >= 0) x = p.ws_states[(size_t)it.in_slot * 16384 + (size_t)vrow * 128 + t];
-      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 2 && vrow < p.vrows)
-        x = static_cast<const float*>(p.init_state)[srow * 128 + t];
-      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1 && vrow < p.vrows)
-        x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.init_state)[srow * 128 + t]);
+      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 2 && vrow < p.vrows && t < p.kdim)
+        x = static_cast<const float*>(p.init_state)[srow * p.kdim + t];
+      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1 && vrow < p.vrows && t < p.kdim)
+        x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.init_state)[srow * p.kdim + t]);
       if (it.out_slot >= 0) p.ws_states[(size_t)it.out_slot * 16384 + (size_t)vrow * 128 + t] = x;
-      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2 && vrow < p.vrows)
-        static_cast<float*>(p.final_state)[srow * 128 + t] = x;
-      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 1 && vrow < p.vrows)
-        static_cast<uint16_t*>(p.final_state)[srow * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2 && vrow < p.vrows && t < p.kdim)
+        static_cast<float*>(p.final_state)[srow * p.kdim + t] = x;
+      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 1 && vrow < p.vrows && t < p.kdim)
+        static_cast<uint16_t*>(p.final_state)[srow * p.kdim + t] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
     }
   }
 

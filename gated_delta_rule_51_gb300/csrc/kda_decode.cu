@@ -61,18 +61,23 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
   __shared__ float s_norm[2][4];
   __shared__ float s_beta;
 
-  // ---- the state rows of this warp, four key channels per lane
+  // ---- the state rows of this warp, four key channels per lane (K = 64: lanes 16-31 hold
+  //      the channels 64-127, which stay zero)
+  const int K = p.kdim;
+  const int kq = K / 4;                                   // four-channel groups a state row holds
+  const bool kl = lane < kq;                              // this lane's channels exist
   const size_t srow0 = (size_t)blockIdx.x * kDecRows;   // first state row of this CTA
   float4 st[kRowsPerWarp];
   if (p.state_dtype == 2) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.state) + srow0 * 128);
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.state) + srow0 * K);
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) st[r] = src[(kRowsPerWarp * warp + r) * 32 + lane];
+    for (int r = 0; r < kRowsPerWarp; ++r)
+      st[r] = kl ? src[(kRowsPerWarp * warp + r) * kq + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
   } else {
-    const uint2* src = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.state) + srow0 * 128);
+    const uint2* src = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.state) + srow0 * K);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-      const uint2 w = src[(kRowsPerWarp * warp + r) * 32 + lane];
+      const uint2 w = kl ? src[(kRowsPerWarp * warp + r) * kq + lane] : make_uint2(0u, 0u);
       st[r] = make_float4(bf(w.x & 0xffffu), bf(w.x >> 16), bf(w.y & 0xffffu), bf(w.y >> 16));
     }
   }
@@ -85,15 +90,16 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
     // ---- per-channel vectors of this token (threads 0-127, channel = tid)
     float kk = 0.f, qq = 0.f;
     if (tid < 128) {
-      const float gt = bf(p.g[tok * 128 + tid]);
+      const bool ch = tid < K;   // channel tid exists (K = 64: channels 64-127 are zero)
+      const float gt = ch ? bf(p.g[tok * K + tid]) : 0.f;
       float ghat = gt;
-      if (!gate_pre) {
-        const float pre = gt + p.dt_bias[(size_t)h * 128 + tid];
+      if (!gate_pre && ch) {
+        const float pre = gt + p.dt_bias[(size_t)h * K + tid];
         ghat = (kFlags & kGateSoftplus) ? -rate * softplusf(pre) : p.lower_bound * sigmoidf(rate * pre);
       }
       s_alpha[tid] = expf(ghat);
-      kk = bf(p.k[tok * 128 + tid]);
-      qq = bf(p.q[tok * 128 + tid]);
+      kk = ch ? bf(p.k[tok * K + tid]) : 0.f;
+      qq = ch ? bf(p.q[tok * K + tid]) : 0.f;
       s_kh[tid] = kk;
       s_qh[tid] = qq;
       if (tid < kDecRows) s_v[tid] = bf(p.v[tok * V + vbase + tid]);   // this CTA's rows' values
@@ -144,14 +150,19 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
 
   // ---- write the rows back
   if (p.state_dtype == 2) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.state) + srow0 * 128);
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.state) + srow0 * K);
+    if (kl) {
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) dst[(kRowsPerWarp * warp + r) * 32 + lane] = st[r];
+      for (int r = 0; r < kRowsPerWarp; ++r) dst[(kRowsPerWarp * warp + r) * kq + lane] = st[r];
+    }
   } else {
-    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.state) + srow0 * 128);
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.state) + srow0 * K);
+    if (kl) {
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r)
-      dst[(kRowsPerWarp * warp + r) * 32 + lane] = make_uint2(pack_bf16x2(st[r].x, st[r].y), pack_bf16x2(st[r].z, st[r].w));
+      for (int r = 0; r < kRowsPerWarp; ++r)
+        dst[(kRowsPerWarp * warp + r) * kq + lane] =
+            make_uint2(pack_bf16x2(st[r].x, st[r].y), pack_bf16x2(st[r].z, st[r].w));
+    }
   }
 }
 

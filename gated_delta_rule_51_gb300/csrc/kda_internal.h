@@ -71,6 +71,7 @@ struct ChainParams {
   float lower_bound;
   int flags;                           // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm | kGateSoftplus
   int vsplit;                          // V / 128: work-item heads are (head, 128-column value block)
+  int kdim;                            // K: 128, or 64 (channels 64-127 then run as zeros)
   int vrows;                           // value rows a chain carries to the caller: 128, or 64 for V = 64
                                        // (rows 64-127 then stay zero: v's second 64 columns read as 0)
 };
@@ -114,6 +115,7 @@ struct DecodeParams {
   void* state;                            // [B, H, 128 (v), 128 (k)], read and written in place
   int state_dtype;                        // 1 bf16, 2 fp32
   int vsplit;                             // V / 64: 64-row CTAs per (sequence, head)
+  int kdim;                               // K: 128, or 64 (channels 64-127 then run as zeros)
   int flags;                              // kGatePreactivated | kBetaPreactivated | kNoQkL2Norm | kGateSoftplus
   int B, T, H;
   float scale, lower_bound;

@@ -118,9 +118,10 @@ def sweep_workload(total: int, H: int) -> Workload:
 
 def custom_workload(name: str, B: int, T: int, H: int, seq_lens=None, state_dtype=torch.float32,
                     has_initial_state=True, has_final_state=True, lower_bound=-5.0,
-                    seed=1234, V: int = V_DIM) -> Workload:
+                    seed=1234, V: int = V_DIM, K: int = K_DIM) -> Workload:
     return Workload(name, B, T, H, list(seq_lens) if seq_lens is not None else None,
-                    state_dtype, has_initial_state, has_final_state, lower_bound, seed, V=V)
+                    state_dtype, has_initial_state, has_final_state, lower_bound, seed, K=K, V=V,
+                    scale=1.0 / math.sqrt(K))
 
 
 def named_workloads() -> Dict[str, Workload]:

@@ -149,8 +149,9 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
         safe_gate: bool = True):
     """KDA forward on the GPU; writes ``out`` (and ``final_state``) and returns them.
 
-    q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,128] bf16; beta: [B,T,H] bf16 logits;
-    A_log: [H] fp32; dt_bias: [H,128] fp32; states: [N,H,128,128] bf16/fp32 or None;
+    q, k, g: [B,T,H,K] bf16 with K = 64 or 128; v, out: [B,T,H,V] bf16 with V = 64, 128
+    or 256; beta: [B,T,H] bf16 logits; A_log: [H] fp32; dt_bias: [H,K] fp32 (16-byte
+    aligned); states: [N,H,V,K] bf16/fp32 or None;
     cu_seqlens: int64 [N+1] on the device (then B must be 1).
     The use_* switches (default on, FlashKDA's behaviour) say which steps run in
     the kernel; off means the caller did them: g is then the natural-log decay, at
@@ -208,9 +209,9 @@ def decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state,
            safe_gate: bool = True):
     """Recurrent KDA step(s) for decoding; updates ``state`` in place, writes ``out``.
 
-    q, k, g: [B,T,H,128] bf16; v, out: [B,T,H,V] bf16 with V = 64, 128 or 256 (T new
-    tokens per sequence, usually 1); beta: [B,T,H] bf16 logits; A_log: [H] fp32;
-    dt_bias: [H,128] fp32; state: [B,H,V,128] bf16 or fp32, read before the first
+    q, k, g: [B,T,H,K] bf16 with K = 64 or 128; v, out: [B,T,H,V] bf16 with V = 64, 128
+    or 256 (T new tokens per sequence, usually 1); beta: [B,T,H] bf16 logits; A_log: [H]
+    fp32; dt_bias: [H,K] fp32; state: [B,H,V,K] bf16 or fp32, read before the first
     token and overwritten.  The switches are those of fwd.
     """
     if q.dim() != 4:

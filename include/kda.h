@@ -21,7 +21,7 @@
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers to contiguous row-major tensors.
  *    q, k, v, g and the states must be 16-byte aligned, beta and out 2-byte,
- *    A_log and dt_bias 4-byte.  The caller owns all memory; the library allocates none
+ *    A_log 4-byte, and dt_bias 16-byte for kda_fwd (4-byte for kda_decode).  The caller owns all memory; the library allocates none
  *    and never synchronises the host (except kda_check_device_error).
  *  - Work is stream-ordered on `stream` (0 = legacy default stream).
  *  - Inputs are never modified; `out` and `final_state` are fully overwritten.
@@ -51,7 +51,7 @@ typedef struct CUstream_st *kda_stream_t; /* a cudaStream_t */
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, bad size, lower_bound out of range */
-    KDA_ERR_UNSUPPORTED_SHAPE = 2,  /* K other than 128, or V other than 64, 128 and 256 */
+    KDA_ERR_UNSUPPORTED_SHAPE = 2,  /* K other than 64 and 128, or V other than 64, 128 and 256 */
     KDA_ERR_WORKSPACE_TOO_SMALL = 3,
     KDA_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
     KDA_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
@@ -96,7 +96,9 @@ typedef enum {
 /*
  * Problem shape (README parameter table; the README requires K = V = 128, this
  * library also takes V = 256, run as two independent 128-row halves of each
- * state, and V = 64, run as one 128-row chain whose last 64 rows stay zero):
+ * state, V = 64, run as one 128-row chain whose last 64 rows stay zero, and
+ * K = 64, run with key channels 64-127 held at zero: q = k = 0 and decay 1
+ * there, so those state columns stay zero and add nothing to the outputs):
  *   q, k, g : [B, T, H, K] bf16      v, out : [B, T, H, V] bf16
  *   beta    : [B, T, H]    bf16 (logits)
  *   A_log   : [H] fp32               dt_bias : [H, K] fp32
@@ -223,8 +225,10 @@ KDA_API kda_status kda_fwd_static_workspace(const kda_shape *shape, const void *
  * (T = 1 for one decoding step), with the state updated IN PLACE.  Every
  * (sequence, head) state is read from HBM once and written back once per call,
  * whatever T is; no workspace is needed.
- *   shape            : B sequences, T >= 0 tokens each, H heads, K = V = 128, N = B.
- *   q, k, v, g, beta : bf16 [B, T, H, 128] (beta [B, T, H], logits), 2-byte aligned.
+ *   shape            : B sequences, T >= 0 tokens each, H heads, K = 64 or 128,
+ *                      V = 64, 128 or 256, N = B.
+ *   q, k, g          : bf16 [B, T, H, K]; v : bf16 [B, T, H, V]; beta : bf16 [B, T, H]
+ *                      (logits); all 2-byte aligned.
  *   out              : bf16 [B, T, H, V], written for every token, 2-byte aligned.
  *   A_log, dt_bias, lower_bound, scale : as for kda_fwd.
  *   flags            : kda_flags, as for kda_fwd_ex.

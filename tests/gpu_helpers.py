@@ -43,7 +43,7 @@ def run_gpu(x: dict, final_dtype: Optional[torch.dtype] = torch.float32, out=Non
     init = x.get("initial_state")
     if final_state is None and final_dtype is not None:
         fd = init.dtype if init is not None else final_dtype
-        final_state = torch.full((N, H, V, 128), float("nan"), dtype=fd, device=q.device)
+        final_state = torch.full((N, H, V, K), float("nan"), dtype=fd, device=q.device)
     kda.fwd(q, x["k"], x["v"], x["g"], x["beta"], x["scale"], out, x["A_log"], x["dt_bias"],
             x["lower_bound"], initial_state=init, final_state=final_state, cu_seqlens=cu,
             workspace=workspace)
@@ -102,9 +102,9 @@ def check_state(gpu_state: torch.Tensor, ref: np.ndarray, label=""):
     return rf
 
 
-def random_case(B, T, H, seed, lens=None, lb=-5.0, init_dtype=torch.float32, device="cuda", V=128):
+def random_case(B, T, H, seed, lens=None, lb=-5.0, init_dtype=torch.float32, device="cuda", V=128, K=128):
     """Inputs in the workloads' distributions (N(0,1) bf16, gate params as the recipes)."""
     from gated_delta_rule_51_gb300 import inputs as I
 
-    w = I.custom_workload("case", B, T, H, lens, init_dtype, init_dtype is not None, True, lb, seed, V=V)
+    w = I.custom_workload("case", B, T, H, lens, init_dtype, init_dtype is not None, True, lb, seed, V=V, K=K)
     return I.make_inputs(w, device=device)

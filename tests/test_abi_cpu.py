@@ -46,7 +46,7 @@ def test_workspace_size_linear_in_heads_and_tiles():
     assert n8 > 0
     lib = kda.load_library()
     n = ctypes.c_size_t(0)
-    bad = kda.make_shape(1, 64, 1, 1, K=64)
+    bad = kda.make_shape(1, 64, 1, 1, K=32)
     assert lib.kda_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
     assert lib.kda_workspace_size(None, ctypes.byref(n)) == 1
 
@@ -62,7 +62,7 @@ def _call(shape, q=FAKE, beta=FAKE, out=FAKE, A_log=FAKE, dt_bias=FAKE, lb=-1.0,
 
 
 @pytest.mark.parametrize("case,expected", [
-    (dict(shape=kda.make_shape(1, 64, 1, 1, K=64)), 2),
+    (dict(shape=kda.make_shape(1, 64, 1, 1, K=32)), 2),
     (dict(shape=kda.make_shape(1, 64, 1, 1, V=384)), 2),
     (dict(shape=kda.make_shape(2, 64, 1, 2), cu=FAKE), 1),          # cu_seqlens needs B = 1
     (dict(shape=kda.make_shape(2, 64, 1, 3)), 1),                   # N must equal B
@@ -73,6 +73,7 @@ def _call(shape, q=FAKE, beta=FAKE, out=FAKE, A_log=FAKE, dt_bias=FAKE, lb=-1.0,
     (dict(shape=kda.make_shape(1, 64, 1, 1), q=FAKE + 2), 1),       # misaligned input
     (dict(shape=kda.make_shape(1, 64, 1, 1), out=0), 1),
     (dict(shape=kda.make_shape(1, 64, 1, 1), A_log=0), 1),
+    (dict(shape=kda.make_shape(1, 64, 1, 1), dt_bias=FAKE + 4), 1),  # dt_bias is read as float4
     (dict(shape=kda.make_shape(1, 64, 1, 1), init=FAKE, init_dt=1, fin=FAKE + (1 << 24), fin_dt=2), 1),
     (dict(shape=kda.make_shape(1, 64, 1, 1), init=FAKE, init_dt=0), 1),   # dtype missing
     (dict(shape=kda.make_shape(1, 64, 2, 1), init=FAKE, init_dt=2, fin=FAKE + 4096, fin_dt=2), 1),  # overlap
@@ -113,7 +114,7 @@ def _decode_call(shape, q=FAKE, out=FAKE, A_log=FAKE, state=FAKE, dtype=2, lb=-1
 
 
 @pytest.mark.parametrize("case,expected", [
-    (dict(shape=kda.make_shape(4, 1, 2, 4, K=64)), 2),
+    (dict(shape=kda.make_shape(4, 1, 2, 4, K=96)), 2),
     (dict(shape=kda.make_shape(4, 1, 2, 3)), 1),                     # N must equal B
     (dict(shape=kda.make_shape(4, 1, 2, 4), lb=0.25), 1),            # lower_bound in [-5, 0]
     (dict(shape=kda.make_shape(4, 1, 2, 4), state=0), 1),            # the state is required
@@ -172,3 +173,14 @@ def test_v256_passes_the_shape_checks():
     assert _call(kda.make_shape(1, 64, 1, 1, V=256)) in (4, 5)
     assert _decode_call(kda.make_shape(4, 1, 2, 4, V=256)) in (4, 5)
     assert kda.workspace_size(kda.make_shape(1, 64, 2, 1, V=256)) >= kda.workspace_size(kda.make_shape(1, 64, 2, 1))
+
+
+def test_k64_passes_the_shape_checks():
+    # K = 64 is accepted (key channels 64-127 held at zero), alone and with V = 64 or 256;
+    # the workspace does not depend on K
+    for V in (64, 128, 256):
+        assert _call(kda.make_shape(1, 64, 1, 1, K=64, V=V)) in (4, 5)
+        assert _decode_call(kda.make_shape(4, 1, 2, 4, K=64, V=V)) in (4, 5)
+        assert kda.workspace_size(kda.make_shape(1, 64, 2, 1, K=64, V=V)) == \
+            kda.workspace_size(kda.make_shape(1, 64, 2, 1, V=V))
+    assert _call(kda.make_shape(1, 64, 1, 1, K=256)) == 2
