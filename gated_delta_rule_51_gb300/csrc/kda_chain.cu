@@ -531,6 +531,10 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, StageSmall& sm, P
 // loops then carry no per-element tests of it
 template <int kFlags>
 __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_constant__ ChainParams p) {
+  // K = V = 128 is a compile-time shape; the kChainPadded variant reads K = 64 or V = 64 from p
+  constexpr bool kPadded = kFlags & kChainPadded;
+  const int kdim = kPadded ? p.kdim : 128;    // key channels the caller's tensors hold
+  const int vrows = kPadded ? p.vrows : 128;  // state rows of a chain the caller's tensors hold
   // Item of this CTA.  The forward launch pairs runs by SM: the list is longest first, the
   // first CTA to start on an SM takes the longest run left and the second the shortest, so
   // a long chain shares its SM with a short one and then runs alone.
@@ -560,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
   // work items count heads x value blocks: V = 128 * vsplit columns are independent
   // chains of 128 state rows each, sharing the head's q, k, g and beta
   const int head = it.head / p.vsplit, vblk = it.head - head * p.vsplit;
-  const size_t vstride = p.vrows == 64 ? 64 : (size_t)p.vsplit * kDimV;   // V
+  const size_t vstride = vrows == 64 ? 64 : (size_t)p.vsplit * kDimV;   // V
 
   extern __shared__ uint8_t smem_dyn[];
   SmemLayout& S = *reinterpret_cast<SmemLayout*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
@@ -590,12 +594,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
     const int t = threadIdx.x - kWarpProlog0 * 32;   // 0..127
     // with V = 64 the v tile's second 64 columns are never loaded: zero for the whole run
     // (128 threads x 16 bytes = the 2 KiB half-tile of each stage)
-    if (p.vrows == 64)
+    if (vrows == 64)
       for (int s = 0; s < kStages; ++s)
         reinterpret_cast<uint4*>(S.st[s].V + 2048)[t] = make_uint4(0u, 0u, 0u, 0u);
     // with K = 64 the q, k and g tiles' channels 64-127 are never loaded: zero (the prologue
     // then writes zeros there as the gated operands of those channels)
-    if (p.kdim == 64)
+    if (kdim == 64)
       for (int s = 0; s < kStages; ++s) {
         reinterpret_cast<uint4*>(S.st[s].X[1])[t] = make_uint4(0u, 0u, 0u, 0u);
         reinterpret_cast<uint4*>(S.st[s].X[1] + 2048)[t] = make_uint4(0u, 0u, 0u, 0u);
@@ -634,8 +638,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       // the head's dt_bias (K values).  With K = 64, warp 1 of a pair holds channels 64-127
       // (zero q, k and g): it reads the head's own 64 values again, and a zero output scale
       // gives those channels the decay 1 whatever they are
-      const bool kpad = p.kdim == 64 && w == 1;
-      const float* dtb = gate_pre ? nullptr : p.dt_bias + (kpad ? h * 64 - 64 : h * p.kdim);
+      const bool kpad = kdim == 64 && w == 1;
+      const float* dtb = gate_pre ? nullptr : p.dt_bias + (kpad ? h * 64 - 64 : h * kdim);
       const float lbl2 = kpad ? 0.f : (gate_sp ? -rate : p.lower_bound * kLog2e);
       const int gid = lane >> 2;
       auto load_beta = [&](int c, float& b0, float& b1) {
@@ -658,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         if (lane == 0) sc.okf[iter & 1][w] = okw ? 1 : 0;
         pair_bar(pair);
         if (!(sc.okf[iter & 1][0] && sc.okf[iter & 1][1])) break;
-        prologue_pair_chunk<kFlags>(S.st[s], S.sm[s], sc, pair, w, nv, p.err, nr, lbl2, dtb, cb0, cb1, lane,
+        prologue_pair_chunk<kFlags & kValidFlags>(S.st[s], S.sm[s], sc, pair, w, nv, p.err, nr, lbl2, dtb, cb0, cb1, lane,
                                     it.mode != kModeTransition);
         if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
@@ -739,12 +743,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         const int s = c % kStages;
         const int row = it.row0 + c * kChunk;
         Stage& st = S.st[s];
-        const uint32_t qkg_bytes = p.kdim == 64 ? 6144u : 12288u;
-        mbar_arrive_expect_tx(&bar_full[s], qkg_bytes + (load_v ? (p.vrows == 64 ? 2048u : 4096u) : 0u));
+        const uint32_t qkg_bytes = kdim == 64 ? 6144u : 12288u;
+        mbar_arrive_expect_tx(&bar_full[s], qkg_bytes + (load_v ? (vrows == 64 ? 2048u : 4096u) : 0u));
         // q: one 64-channel half into each S-side operand tile; k, g, v: both halves at once
         // (K = 64: one 64-channel tile of each)
         tma_load_3d(st.X[0] + 2048, &p.tm_q, &bar_full[s], 0, head, row);
-        if (p.kdim == 64) {
+        if (kdim == 64) {
           tma_load_3d(st.K, &p.tm_k, &bar_full[s], 0, head, row);
           tma_load_3d(st.G, &p.tm_g, &bar_full[s], 0, head, row);
         } else {
@@ -753,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
           tma_load_4d(st.G, &p.tm_g, &bar_full[s], 0, head, row, 0);
         }
         if (load_v) {
-          if (p.vrows == 64) tma_load_3d(st.V, &p.tm_v, &bar_full[s], 0, head, row);   // V = 64: one tile
+          if (vrows == 64) tma_load_3d(st.V, &p.tm_v, &bar_full[s], 0, head, row);   // V = 64: one tile
           else tma_load_4d(st.V, &p.tm_v, &bar_full[s], 0, head, row, 2 * vblk);
         }
         ++tma_issued;
@@ -787,19 +791,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
               const float4 x = src[t];
               s[4 * t] = x.x; s[4 * t + 1] = x.y; s[4 * t + 2] = x.z; s[4 * t + 3] = x.w;
             }
-          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 2 && vrow < p.vrows &&
-                     32 * j < p.kdim) {
+          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 2 && vrow < vrows &&
+                     32 * j < kdim) {
             const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) +
-                                                                srow * p.kdim + 32 * j);
+                                                                srow * kdim + 32 * j);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const float4 x = src[t];
               s[4 * t] = x.x; s[4 * t + 1] = x.y; s[4 * t + 2] = x.z; s[4 * t + 3] = x.w;
             }
-          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 1 && vrow < p.vrows &&
-                     32 * j < p.kdim) {
+          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 1 && vrow < vrows &&
+                     32 * j < kdim) {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.init_state) +
-                                                              srow * p.kdim + 32 * j);
+                                                              srow * kdim + 32 * j);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               const uint4 x = src[t];
@@ -909,16 +913,16 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
               for (int t = 0; t < 8; ++t)
                 dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
                                      __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2 && vrow < p.vrows &&
-                       32 * j < p.kdim) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * p.kdim + 32 * j);
+            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2 && vrow < vrows &&
+                       32 * j < kdim) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * kdim + 32 * j);
 #pragma unroll
               for (int t = 0; t < 8; ++t)
                 dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
                                      __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1 && vrow < p.vrows &&
-                       32 * j < p.kdim) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * p.kdim + 32 * j);
+            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1 && vrow < vrows &&
+                       32 * j < kdim) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * kdim + 32 * j);
 #pragma unroll
               for (int t = 0; t < 4; ++t)
                 dst[t] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * t]), __uint_as_float(r[8 * t + 1])),
@@ -957,12 +961,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
               const int q = lane + 32 * rr, i = q >> 2, seg = q & 3;
-              if (i < nv && 32 * q4 < p.vrows)
+              if (i < nv && 32 * q4 < vrows)
                 *reinterpret_cast<uint4*>(obase + (size_t)i * row_elems + 32 * q4 + 8 * seg) =
                     *reinterpret_cast<const uint4*>(&S.ostage[i][64 * q4 + 16 * seg]);
             }
           } else {
-            for (int i = 0; i < nv && vrow < p.vrows; ++i)
+            for (int i = 0; i < nv && vrow < vrows; ++i)
               obase[(size_t)i * row_elems + vrow] = *reinterpret_cast<const uint16_t*>(&S.ostage[i][2 * vrow]);
           }
           __syncwarp();   // the staging rows are rewritten by the next chunk
@@ -987,15 +991,15 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       float x = 0.f;
       if (it.in_slot == kInIdentity) x = (t == vrow) ? 1.f : 0.f;
       else if (it.in_slot >= 0) x = p.ws_states[(size_t)it.in_slot * 16384 + (size_t)vrow * 128 + t];
-      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 2 && vrow < p.vrows && t < p.kdim)
-        x = static_cast<const float*>(p.init_state)[srow * p.kdim + t];
-      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1 && vrow < p.vrows && t < p.kdim)
-        x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.init_state)[srow * p.kdim + t]);
+      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 2 && vrow < vrows && t < kdim)
+        x = static_cast<const float*>(p.init_state)[srow * kdim + t];
+      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1 && vrow < vrows && t < kdim)
+        x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.init_state)[srow * kdim + t]);
       if (it.out_slot >= 0) p.ws_states[(size_t)it.out_slot * 16384 + (size_t)vrow * 128 + t] = x;
-      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2 && vrow < p.vrows && t < p.kdim)
-        static_cast<float*>(p.final_state)[srow * p.kdim + t] = x;
-      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 1 && vrow < p.vrows && t < p.kdim)
-        static_cast<uint16_t*>(p.final_state)[srow * p.kdim + t] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2 && vrow < vrows && t < kdim)
+        static_cast<float*>(p.final_state)[srow * kdim + t] = x;
+      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 1 && vrow < vrows && t < kdim)
+        static_cast<uint16_t*>(p.final_state)[srow * kdim + t] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
     }
   }
 
@@ -1008,11 +1012,16 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
   using Kernel = void (*)(ChainParams);
   // (the preactivated and softplus gates exclude each other: no kernel for both)
-  static constexpr Kernel kernels[16] = {
+  // (entries 16-31: the same for K = 64 or V = 64)
+  static constexpr Kernel kernels[32] = {
       kda_chain_kernel<0>, kda_chain_kernel<1>, kda_chain_kernel<2>, kda_chain_kernel<3>,
       kda_chain_kernel<4>, kda_chain_kernel<5>, kda_chain_kernel<6>, kda_chain_kernel<7>,
       kda_chain_kernel<8>, nullptr, kda_chain_kernel<10>, nullptr,
-      kda_chain_kernel<12>, nullptr, kda_chain_kernel<14>, nullptr};
+      kda_chain_kernel<12>, nullptr, kda_chain_kernel<14>, nullptr,
+      kda_chain_kernel<16>, kda_chain_kernel<17>, kda_chain_kernel<18>, kda_chain_kernel<19>,
+      kda_chain_kernel<20>, kda_chain_kernel<21>, kda_chain_kernel<22>, kda_chain_kernel<23>,
+      kda_chain_kernel<24>, nullptr, kda_chain_kernel<26>, nullptr,
+      kda_chain_kernel<28>, nullptr, kda_chain_kernel<30>, nullptr};
   const size_t smem = chain_smem_bytes();
   // the shared-memory opt-in is a per-device setting: made once per device
   constexpr int kMaxDevices = 64;
@@ -1029,7 +1038,8 @@ cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
   if (grid <= 0) return cudaSuccess;
-  const Kernel k = kernels[p.flags & 15];
+  const bool padded = p.kdim != 128 || p.vrows != 128;
+  const Kernel k = kernels[(p.flags & kValidFlags) | (padded ? kChainPadded : 0)];
   if (k == nullptr) return cudaErrorInvalidValue;
   k<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();

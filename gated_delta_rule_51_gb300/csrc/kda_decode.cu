@@ -13,8 +13,11 @@
 // Rows are independent, so the work is bandwidth-bound: V / kDecRows CTAs per
 // (n, h), each of kDecRows rows in warps of sixteen, every lane holding four key
 // channels of each of its rows in registers for all the call's tokens.  The state
-// is read once (V x 128 fp32 or bf16 per head) and written once.
+// is read once (V x K fp32 or bf16 per head) and written once.
 #include <cuda_bf16.h>
+
+#include <array>
+#include <utility>
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -25,6 +28,7 @@ namespace {
 constexpr int kRowsPerWarp = 16;
 constexpr int kDecRows = 64;                        // state rows per CTA (four CTAs per SM)
 constexpr int kDecThreads = 2 * kDecRows;           // 16 rows a warp; at least 128 threads
+constexpr int kDecK64 = 16;                          // kernel variant bit: K = 64
 static_assert(kDecThreads >= 128, "the per-channel vectors take 128 threads");
 
 __device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
@@ -63,8 +67,8 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
 
   // ---- the state rows of this warp, four key channels per lane (K = 64: lanes 16-31 hold
   //      the channels 64-127, which stay zero)
-  const int K = p.kdim;
-  const int kq = K / 4;                                   // four-channel groups a state row holds
+  constexpr int K = (kFlags & kDecK64) ? 64 : 128;       // key channels of the caller's tensors
+  constexpr int kq = K / 4;                               // four-channel groups a state row holds
   const bool kl = lane < kq;                              // this lane's channels exist
   const size_t srow0 = (size_t)blockIdx.x * kDecRows;   // first state row of this CTA
   float4 st[kRowsPerWarp];
@@ -168,29 +172,32 @@ __global__ void __launch_bounds__(kDecThreads, 2048 / kDecThreads / 4) kda_decod
 
 }  // namespace
 
+using DecodeKernel = void (*)(DecodeParams);
+
+// One kernel per V and flag set, K = 64 as a flag bit (the preactivated and softplus gates
+// exclude each other: no kernel for both)
+template <int V, int F>
+constexpr DecodeKernel decode_entry() {
+  if constexpr ((F & kGatePreactivated) && (F & kGateSoftplus)) return nullptr;
+  else return kda_decode_kernel<V, F>;
+}
+template <int V, int... F>
+constexpr std::array<DecodeKernel, sizeof...(F)> decode_row(std::integer_sequence<int, F...>) {
+  return {decode_entry<V, F>()...};
+}
+constexpr auto kDecodeV64 = decode_row<64>(std::make_integer_sequence<int, 2 * kDecK64>{});
+constexpr auto kDecodeV128 = decode_row<128>(std::make_integer_sequence<int, 2 * kDecK64>{});
+constexpr auto kDecodeV256 = decode_row<256>(std::make_integer_sequence<int, 2 * kDecK64>{});
+
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
   // p.vsplit carries V / 64 (1, 2 or 4): one 64-row CTA per 64 value rows
   const long long grid = (long long)p.B * p.H * p.vsplit;
   if (grid <= 0 || p.T <= 0) return cudaSuccess;
-  // V and the flags are template parameters: the common case (V = 128, every step in the
-  // kernel) carries no per-thread tests of either (the preactivated and softplus gates
-  // exclude each other: no kernel for both)
-  using Kernel = void (*)(DecodeParams);
-  static constexpr Kernel kernels[3][16] = {
-      {kda_decode_kernel<64, 0>, kda_decode_kernel<64, 1>, kda_decode_kernel<64, 2>, kda_decode_kernel<64, 3>,
-       kda_decode_kernel<64, 4>, kda_decode_kernel<64, 5>, kda_decode_kernel<64, 6>, kda_decode_kernel<64, 7>,
-       kda_decode_kernel<64, 8>, nullptr, kda_decode_kernel<64, 10>, nullptr,
-       kda_decode_kernel<64, 12>, nullptr, kda_decode_kernel<64, 14>, nullptr},
-      {kda_decode_kernel<128, 0>, kda_decode_kernel<128, 1>, kda_decode_kernel<128, 2>, kda_decode_kernel<128, 3>,
-       kda_decode_kernel<128, 4>, kda_decode_kernel<128, 5>, kda_decode_kernel<128, 6>, kda_decode_kernel<128, 7>,
-       kda_decode_kernel<128, 8>, nullptr, kda_decode_kernel<128, 10>, nullptr,
-       kda_decode_kernel<128, 12>, nullptr, kda_decode_kernel<128, 14>, nullptr},
-      {kda_decode_kernel<256, 0>, kda_decode_kernel<256, 1>, kda_decode_kernel<256, 2>, kda_decode_kernel<256, 3>,
-       kda_decode_kernel<256, 4>, kda_decode_kernel<256, 5>, kda_decode_kernel<256, 6>, kda_decode_kernel<256, 7>,
-       kda_decode_kernel<256, 8>, nullptr, kda_decode_kernel<256, 10>, nullptr,
-       kda_decode_kernel<256, 12>, nullptr, kda_decode_kernel<256, 14>, nullptr}};
+  // V, K and the flags are template parameters: the common case (K = V = 128, every step in
+  // the kernel) carries no per-thread tests of any of them
   const int vi = p.vsplit == 1 ? 0 : (p.vsplit == 2 ? 1 : 2);
-  const Kernel k = kernels[vi][p.flags & 15];
+  const int f = (int)(p.flags & kValidFlags) | (p.kdim == 64 ? kDecK64 : 0);
+  const DecodeKernel k = vi == 0 ? kDecodeV64[f] : (vi == 1 ? kDecodeV128[f] : kDecodeV256[f]);
   if (k == nullptr) return cudaErrorInvalidValue;
   k<<<(unsigned)grid, kDecThreads, 0, s>>>(p);
   return cudaGetLastError();

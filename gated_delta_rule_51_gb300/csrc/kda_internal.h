@@ -106,6 +106,8 @@ constexpr int kBetaPreactivated = 2;
 constexpr int kNoQkL2Norm = 4;
 constexpr int kGateSoftplus = 8;   // ghat = -exp(A_log) softplus(g + dt_bias), no lower bound
 constexpr unsigned kValidFlags = 15;
+// chain-kernel variant bit (not a caller flag): K = 64 or V = 64, the padded shapes
+constexpr int kChainPadded = 16;
 
 struct DecodeParams {
   const uint16_t *q, *k, *v, *g, *beta;  // bf16 [B, T, H, 128] (beta [B, T, H], logits)
