@@ -39,6 +39,10 @@ L2_BYTES = 126 * 1024 * 1024
 ALIASES = {"tiny": "tiny_B1_T64_H1", "fixed": "fixed_B2_T4096_H16",
            "varlen": "varlen_T32768_N8_H32", "long": "long_T1048576_H8", "decode": "decode_B256_T1_H32"}
 DECODE_METRIC = "KDA decode tokens/s and % of HBM roofline on 1xGB300"
+BWD_METRIC = "KDA bwd tokens/s and % of HBM roofline on 1xGB300"
+# the backward's compulsory traffic per token-head: q, k, v, g, dout (bf16) and beta read;
+# dq, dk, dv, dg (fp32) and dbeta written
+BWD_BYTES_PER_TOKEN_HEAD = 5 * 128 * 2 + 2 + 4 * 128 * 4 + 4
 
 
 def workload(name):
@@ -625,6 +629,115 @@ def run_decode(args, w):
         dist.destroy_process_group()
 
 
+def run_bwd(args, w):
+    """The backward pass (kda_bwd) on workload w, with random bf16 dout and fp32 dfinal:
+    every step reads the forward's inputs and writes every gradient; CUDA events around
+    each phase (prep, stored-state forward, reverse, chain rule)."""
+    import torch
+
+    from gated_delta_rule_51_gb300 import inputs as I
+    from gated_delta_rule_51_gb300 import kda
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    kda.load_library()
+    x = I.make_inputs(w, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 100)
+    dout = torch.randn(x["v"].shape, generator=gen, device=dev).to(torch.bfloat16)
+    dfinal = 0.1 * torch.randn((w.N, w.H, 128, 128), generator=gen, device=dev)
+    shape = kda.make_shape(w.B, w.T, w.H, w.N)
+    ws = torch.empty(kda.bwd_workspace_size(shape), dtype=torch.uint8, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    B, T, H = w.B, w.T, w.H
+    outs = dict(dq=torch.empty((B, T, H, 128), **f32), dk=torch.empty((B, T, H, 128), **f32),
+                dv=torch.empty((B, T, H, 128), **f32), dg=torch.empty((B, T, H, 128), **f32),
+                dbeta=torch.empty((B, T, H), **f32), dh0=torch.empty((w.N, H, 128, 128), **f32),
+                dA_log=torch.empty((H,), **f32), ddt_bias=torch.empty((H, 128), **f32))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["A_log"], x["dt_bias"],
+                x["lower_bound"], dout, initial_state=x["initial_state"], dfinal=dfinal,
+                cu_seqlens=x["cu_seqlens"], workspace=ws, out=outs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if kda.check_device_error(ws, dev):
+        raise SystemExit("device error flags set during warm-up")
+    launches = kda.last_launch_count()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e in ev:
+        for t in e:
+            t.record(stream)        # creates the events before their handles are handed out
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            kda.set_profile_events(ev[i][1:])
+            step()
+        kda.set_profile_events(None)
+        torch.cuda.synchronize(dev)
+    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    ph = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+          for j, name in enumerate(("prep", "stored_state_forward", "reverse", "chain_rule"))}
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    ms = total_ms / args.steps
+    tokens = w.B * w.T
+    value = whole_job_rate(tokens, world, args.steps, total_ms)
+    state_bytes = w.N * w.H * 128 * 128 * 4 * (int(w.has_initial_state) + 2)   # h0 and dfinal in, dh0 out
+    nbytes = w.token_heads * BWD_BYTES_PER_TOKEN_HEAD + state_bytes + 2 * w.H * (4 + 128 * 4)
+    hbm_gbs, _, peak_kind = load_peaks()
+    achieved = nbytes / (ph["reverse"] / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+                "traffic": None, "kernel": "kda_bwd_reverse_kernel",
+                "peak_source": "measured, MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": nbytes,
+                "step_frac": (nbytes / (ms / 1000.0) / 1e9) / hbm_gbs, "phase_ms": ph}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        # bounded sample: the first 512 tokens of every sequence, two heads
+        tt, hs = min(512, w.T), [0, 1]
+        c = lambda t: t[:, :tt][:, :, hs].cpu().double().numpy()
+        t0 = time.perf_counter()
+        oracle.kda_backward(c(x["q"]), c(x["k"]), c(x["v"]), c(x["g"]), c(x["beta"]), float(x["scale"]),
+                            x["A_log"][hs].cpu().double().numpy(), x["dt_bias"][hs].cpu().double().numpy(),
+                            float(x["lower_bound"]), c(dout), x["initial_state"][:, hs].cpu().double().numpy(),
+                            dfinal[:, hs].cpu().double().numpy(), None, nthreads=os.cpu_count())
+        dt = time.perf_counter() - t0
+        th = w.B * tt * len(hs)
+        cpu = {"value": th / dt / w.H, "unit": "tokens/s", "cores": min(os.cpu_count() or 1, w.B * len(hs)),
+               "kind": "oracle",
+               "sample": f"{th} token-heads ({w.B}x{tt} tokens x {len(hs)} of {w.H} heads); "
+                         "tokens/s scaled by covered token-heads / H"}
+    if rank == 0:
+        line = {"metric": BWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": config_dict(w, {"pass": "backward", "dout": "bf16 N(0,1)", "dfinal": "fp32 0.1 N(0,1)",
+                                          "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                          "l2": "flushed between timed steps (252 MB write)",
+                                          "launch": "direct calls"}),
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks.summary(), "e2e": None,
+                "gpu_launches": launches * args.steps}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -635,6 +748,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.config.startswith("bwd"):
+        # the backward pass on a forward workload: "bwd" is the fixed batch, "bwd_<name>" any other
+        name = args.config[4:] if args.config.startswith("bwd_") else "fixed"
+        if args.impl == "reference":
+            raise SystemExit("the reference arm times the forward")
+        run_bwd(args, workload(name))
+        return
     w = workload(args.config)
     if args.impl == "reference":
         run_reference(args, w)

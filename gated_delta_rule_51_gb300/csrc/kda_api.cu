@@ -116,6 +116,36 @@ Layout make_layout(const kda_shape& s, int sms) {
   return L;
 }
 
+// The backward pass's workspace: header (error word), per token-head prepared vectors,
+// the stored states, the row-slice partials, the per-token dA_log terms and the
+// parameter-reduction blocks.
+struct BwdLayout {
+  size_t off_hdr = 0, off_prep = 0, off_ckpt = 0, off_part = 0, off_dA = 0, off_ppart = 0, total = 0;
+  int nblk = 0;
+};
+
+BwdLayout make_bwd_layout(const kda_shape& s) {
+  BwdLayout L;
+  const size_t BT = (size_t)(s.B * s.T), TH = BT * (size_t)s.H;
+  const size_t nslot = BT / kBwdChunk + (size_t)s.N + 1;
+  L.nblk = (int)((BT + kBwdParamTokens - 1) / kBwdParamTokens);
+  size_t off = 0;
+  L.off_hdr = off;
+  off = align_up(off + sizeof(WorkHeader));
+  L.off_prep = off;
+  off = align_up(off + TH * kBwdRowStride * sizeof(float));
+  L.off_ckpt = off;
+  off = align_up(off + nslot * (size_t)s.H * kSlotBytes);
+  L.off_part = off;
+  off = align_up(off + (size_t)kBwdSlices * TH * kBwdRowStride * sizeof(float));
+  L.off_dA = off;
+  off = align_up(off + TH * sizeof(float));
+  L.off_ppart = off;
+  off = align_up(off + (size_t)L.nblk * (size_t)s.H * kBwdParamStride * sizeof(float));
+  L.total = off;
+  return L;
+}
+
 kda_status check_shape(const kda_shape* s) {
   if (s == nullptr) return KDA_ERR_INVALID_ARGUMENT;
   if ((s->K != 64 && s->K != 128) || (s->V != 64 && s->V != 128 && s->V != 256)) return KDA_ERR_UNSUPPORTED_SHAPE;
@@ -461,6 +491,105 @@ kda_status kda_check_device_error(const void* workspace, kda_stream_t stream_, i
   if (err & kErrTimeout) return KDA_ERR_TIMEOUT;
   if (err & kErrBadSeqlens) return KDA_ERR_BAD_SEQLENS;
   if (err & kErrGateRange) return KDA_ERR_GATE_RANGE;
+  return KDA_OK;
+}
+
+kda_status kda_bwd_workspace_size(const kda_shape* shape, size_t* bytes) {
+  if (bytes == nullptr) return KDA_ERR_INVALID_ARGUMENT;
+  kda_status st = check_shape(shape);
+  if (st != KDA_OK) return st;
+  if (shape->K != 128 || shape->V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  *bytes = make_bwd_layout(*shape).total;
+  return KDA_OK;
+}
+
+kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const void* v, const void* g,
+                   const void* beta, float scale, const float* A_log, const float* dt_bias, float lower_bound,
+                   const void* initial_state, kda_state_dtype init_dtype, const int64_t* cu_seqlens,
+                   const void* dout, const float* dfinal, float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                   float* dh0, float* dA_log, float* ddt_bias, unsigned flags, void* workspace,
+                   size_t workspace_bytes, kda_stream_t stream_) {
+  kda_status st = check_shape(shape);
+  if (st != KDA_OK) return st;
+  const kda_shape s = *shape;
+  if (s.K != 128 || s.V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (cu_seqlens != nullptr && s.B != 1) return KDA_ERR_INVALID_ARGUMENT;
+  if (cu_seqlens == nullptr && s.N != s.B) return KDA_ERR_INVALID_ARGUMENT;
+  if ((long long)s.N * s.H * kBwdSlices > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
+  if (!valid_flags(flags)) return KDA_ERR_INVALID_ARGUMENT;
+  const bool gate_here = !(flags & KDA_GATE_PREACTIVATED);
+  if (uses_lower_bound(flags) && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
+  auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  // token tensors are read and written four channels at a time
+  if (s.B * s.T > 0) {
+    const void* tok16[] = {q, k, v, g, dout, dq, dk, dv, dg};
+    for (const void* p : tok16)
+      if (p == nullptr || !aligned16(p)) return KDA_ERR_INVALID_ARGUMENT;
+    if (beta == nullptr || dbeta == nullptr || !aligned(beta, 2) || !aligned(dbeta, 4))
+      return KDA_ERR_INVALID_ARGUMENT;
+  }
+  if (gate_here && (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned16(dt_bias)))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (initial_state != nullptr &&
+      ((init_dtype != KDA_STATE_BF16 && init_dtype != KDA_STATE_FP32) || !aligned16(initial_state)))
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (initial_state == nullptr && init_dtype != KDA_STATE_NONE) return KDA_ERR_INVALID_ARGUMENT;
+  if ((dfinal != nullptr && !aligned16(dfinal)) || (dh0 != nullptr && !aligned16(dh0)) ||
+      (dA_log != nullptr && !aligned(dA_log, 4)) || (ddt_bias != nullptr && !aligned(ddt_bias, 4)))
+    return KDA_ERR_INVALID_ARGUMENT;
+  const BwdLayout L = make_bwd_layout(s);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+    return KDA_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo d;
+  if (device_info(&d) != KDA_OK) return KDA_ERR_CUDA;
+  if (d.major != 10 || d.minor != 3) return KDA_ERR_UNSUPPORTED_DEVICE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.g = static_cast<const uint16_t*>(g);
+  p.beta = static_cast<const uint16_t*>(beta);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.dfinal = dfinal;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.init_state = initial_state;
+  p.init_dtype = initial_state == nullptr ? 0 : (init_dtype == KDA_STATE_FP32 ? 2 : 1);
+  p.cu = cu_seqlens;
+  p.dq = dq;
+  p.dk = dk;
+  p.dg = dg;
+  p.dv = dv;
+  p.dbeta = dbeta;
+  p.dh0 = dh0;
+  p.dA_log = dA_log;
+  p.ddt_bias = ddt_bias;
+  p.prep = reinterpret_cast<float*>(ws + L.off_prep);
+  p.ckpt = reinterpret_cast<float*>(ws + L.off_ckpt);
+  p.part = reinterpret_cast<float*>(ws + L.off_part);
+  p.dA_tok = reinterpret_cast<float*>(ws + L.off_dA);
+  p.ppart = reinterpret_cast<float*>(ws + L.off_ppart);
+  p.err = &reinterpret_cast<WorkHeader*>(ws + L.off_hdr)->err;
+  p.T = s.T;
+  p.BT = s.B * s.T;
+  p.N = (int)s.N;
+  p.H = (int)s.H;
+  p.flags = (int)flags;
+  p.nblk = L.nblk;
+  p.scale = scale;
+  p.lower_bound = lower_bound;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // profile marks after each phase: prep, stored-state forward, reverse, chain rule
+  for (int phase = 0; phase < 4; ++phase) {
+    if (launch_bwd(p, phase, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    mark(phase, stream);
+  }
+  t_last_launches = (p.BT * p.H > 0 ? 2 : 0) + (p.N > 0 ? 2 : 0) +
+                    ((flags & KDA_GATE_PREACTIVATED) || (dA_log == nullptr && ddt_bias == nullptr)
+                         ? 0 : (L.nblk > 0 ? 2 : 1));
   return KDA_OK;
 }
 

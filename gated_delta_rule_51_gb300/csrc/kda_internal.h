@@ -123,11 +123,45 @@ struct DecodeParams {
   float scale, lower_bound;
 };
 
+// The backward pass (kda_bwd.cu): K = V = 128.
+struct BwdParams {
+  const uint16_t *q, *k, *v, *g, *beta;   // bf16 inputs of the forward ([B, T, H, 128]; beta [B, T, H])
+  const uint16_t* dout;                   // bf16 [B, T, H, 128]: dL/d out
+  const float* dfinal;                    // fp32 [N, H, 128, 128]: dL/d final_state, or null
+  const float* A_log;                     // [H]
+  const float* dt_bias;                   // [H, 128]
+  const void* init_state;                 // [N, H, 128, 128] of init_dtype, or null
+  int init_dtype;                         // 0 none, 1 bf16, 2 fp32
+  const int64_t* cu;                      // [N + 1] or null
+  float *dq, *dk, *dg, *dv, *dbeta;       // fp32 gradients ([B, T, H, 128]; dbeta [B, T, H])
+  float* dh0;                             // fp32 [N, H, 128, 128] or null
+  float *dA_log, *ddt_bias;               // fp32 [H], [H, 128] or null
+  float* prep;                            // workspace: per token-head alpha, kh, qh, beta, rq, rk
+  float* ckpt;                            // workspace: the state every kBwdChunk tokens
+  float* part;                            // workspace: per row-slice partial dqh, dkh, dalpha, dbeta
+  float* dA_tok;                          // workspace: per token-head dA_log terms
+  float* ppart;                           // workspace: per token-block parameter sums
+  int* err;                               // error word (kErrBadSeqlens)
+  int64_t T;                              // tokens per sequence (cu == null) or the total
+  int64_t BT;                             // B * T
+  int N, H, flags, nblk;
+  float scale, lower_bound;
+};
+
+// Backward workspace regions, in floats per unit.
+constexpr int kBwdChunk = 8;              // tokens between two stored states
+constexpr int kBwdRowStride = 388;        // floats per token-head in prep and part (128 x 3 + 4)
+constexpr int kBwdSlices = 4;             // row slices (CTAs) per head in the recurrences
+constexpr int kBwdParamTokens = 256;      // tokens per block of the parameter reduction
+constexpr int kBwdParamStride = 132;      // floats per (block, head): 128 ddt_bias + dA_log + pad
+
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_compose(const ComposeParams& p, int grid, int sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+// phases 0-3: prep, stored-state forward, reverse, chain rule and parameter sums
+cudaError_t launch_bwd(const BwdParams& p, int phase, cudaStream_t s);
 size_t chain_smem_bytes();
 
 }  // namespace kda

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPOR
                 6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_BAD_SEQLENS", 8: "KDA_ERR_GATE_RANGE"}
 EXPORTED_SYMBOLS = ("kda_status_string", "kda_workspace_size", "kda_fwd", "kda_check_device_error",
                     "kda_set_profile_events", "kda_last_launch_count", "kda_fwd_static_workspace",
-                    "kda_decode", "kda_fwd_ex")
+                    "kda_decode", "kda_fwd_ex", "kda_bwd_workspace_size", "kda_bwd")
 KDA_GATE_PREACTIVATED, KDA_BETA_PREACTIVATED, KDA_NO_QK_L2NORM, KDA_GATE_SOFTPLUS = 1, 2, 4, 8
 
 
@@ -77,6 +77,12 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
                                    ctypes.c_size_t, p]
         lib.kda_fwd_ex.restype = ctypes.c_int
         lib.kda_decode.restype = ctypes.c_int
+        lib.kda_bwd_workspace_size.argtypes = [ctypes.POINTER(kda_shape), ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_bwd_workspace_size.restype = ctypes.c_int
+        lib.kda_bwd.argtypes = [ctypes.POINTER(kda_shape), p, p, p, p, p, ctypes.c_float, p, p, ctypes.c_float,
+                                p, ctypes.c_int, p, p, p, p, p, p, p, p, p, p, p, ctypes.c_uint, p,
+                                ctypes.c_size_t, p]
+        lib.kda_bwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -271,3 +277,69 @@ def set_profile_events(events) -> None:
 def last_launch_count() -> int:
     """Kernels enqueued by this thread's most recent fwd call."""
     return int(load_library().kda_last_launch_count())
+
+
+def bwd_workspace_size(shape: kda_shape) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    st = lib.kda_bwd_workspace_size(ctypes.byref(shape), ctypes.byref(n))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_bwd_workspace_size")
+    return int(n.value)
+
+
+def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None, dfinal=None,
+        cu_seqlens=None, workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+        use_gate_in_kernel: bool = True, use_beta_sigmoid_in_kernel: bool = True,
+        use_qk_l2norm_in_kernel: bool = True, safe_gate: bool = True, out: Optional[dict] = None) -> dict:
+    """Gradients of sum(dout * out) + sum(dfinal * final_state) for the forward fwd() computes
+    with the same arguments (K = V = 128).  dout: bf16 [B,T,H,128]; dfinal: fp32 [N,H,128,128]
+    or None.  Returns fp32 tensors dq, dk, dg [B,T,H,128], dv [B,T,H,128], dbeta [B,T,H],
+    dh0 [N,H,128,128], dA_log [H] and ddt_bias [H,128] (allocated here unless ``out`` holds
+    them).  dg is the gradient for the raw g passed in; dbeta for the beta logits."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda.bwd needs CUDA tensors")
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    V = v.shape[-1]
+    flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate)
+    for name, t, dt, shp in (("q", q, torch.bfloat16, (B, T, H, K)), ("k", k, torch.bfloat16, (B, T, H, K)),
+                             ("g", g, torch.bfloat16, (B, T, H, K)), ("v", v, torch.bfloat16, (B, T, H, V)),
+                             ("beta", beta, torch.bfloat16, (B, T, H)), ("dout", dout, torch.bfloat16, (B, T, H, V))):
+        _check(t, name, dt, shp, dev)
+    if use_gate_in_kernel:
+        _check(A_log, "A_log", torch.float32, (H,), dev)
+        _check(dt_bias, "dt_bias", torch.float32, (H, K), dev)
+    if initial_state is not None:
+        _check(initial_state, "initial_state", initial_state.dtype, (N, H, V, K), dev)
+    if dfinal is not None:
+        _check(dfinal, "dfinal", torch.float32, (N, H, V, K), dev)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int64, (N + 1,), dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    r = out if out is not None else dict(
+        dq=torch.empty((B, T, H, K), **f32), dk=torch.empty((B, T, H, K), **f32),
+        dv=torch.empty((B, T, H, V), **f32), dg=torch.empty((B, T, H, K), **f32),
+        dbeta=torch.empty((B, T, H), **f32), dh0=torch.empty((N, H, V, K), **f32),
+        dA_log=torch.empty((H,), **f32), ddt_bias=torch.empty((H, K), **f32))
+    shape = make_shape(B, T, H, N, K, V)
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    st = lib.kda_bwd_workspace_size(ctypes.byref(shape), ctypes.byref(n))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_bwd_workspace_size")
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = torch.empty(max(int(n.value), 256), dtype=torch.uint8, device=dev)
+    st = lib.kda_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
+                     _ptr(A_log), _ptr(dt_bias), ctypes.c_float(lower_bound), _ptr(initial_state),
+                     _state_code(initial_state), _ptr(cu_seqlens), _ptr(dout), _ptr(dfinal), _ptr(r["dq"]),
+                     _ptr(r["dk"]), _ptr(r["dv"]), _ptr(r["dg"]), _ptr(r["dbeta"]), _ptr(r.get("dh0")),
+                     _ptr(r.get("dA_log")), _ptr(r.get("ddt_bias")), ctypes.c_uint(flags), _ptr(workspace),
+                     ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(s.cuda_stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_bwd")
+    return r

@@ -21,8 +21,9 @@
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers to contiguous row-major tensors.
  *    q, k, v, g and the states must be 16-byte aligned, beta and out 2-byte,
- *    A_log 4-byte, and dt_bias 16-byte for kda_fwd (4-byte for kda_decode).  The caller owns all memory; the library allocates none
- *    and never synchronises the host (except kda_check_device_error).
+ *    A_log 4-byte, and dt_bias 16-byte for kda_fwd and kda_bwd (4-byte for
+ *    kda_decode).  The caller owns all memory; the library allocates none and
+ *    never synchronises the host (except kda_check_device_error).
  *  - Work is stream-ordered on `stream` (0 = legacy default stream).
  *  - Inputs are never modified; `out` and `final_state` are fully overwritten.
  *  - Errors in the arguments are reported by the return code before anything
@@ -242,6 +243,42 @@ KDA_API kda_status kda_decode(const kda_shape *shape, const void *q, const void 
                               const void *g, const void *beta, float scale, void *out, const float *A_log,
                               const float *dt_bias, float lower_bound, void *state,
                               kda_state_dtype state_dtype, unsigned flags, kda_stream_t stream);
+
+/*
+ * The backward pass: gradients of L = sum(dout * out) + sum(dfinal * final_state) for the
+ * forward kda_fwd_ex computes with the same arguments.  FlashKDA's README defines the forward
+ * only ("Kernel API"); the gradient is that of its recurrence (above), taken through the
+ * gate, the beta sigmoid and the L2 norms the flags leave in the kernel.  K = V = 128.
+ *   q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state, init_dtype,
+ *   cu_seqlens, flags : the forward's inputs, as for kda_fwd_ex (q, k, v, g 16-byte aligned).
+ *   dout             : bf16 [B, T, H, V], dL/d out, 16-byte aligned.
+ *   dfinal           : NULL (the final state is not part of L) or fp32 [N, H, V, K],
+ *                      dL/d final_state, 16-byte aligned.
+ * Outputs, all fp32 and fully overwritten:
+ *   dq, dk, dg       : [B, T, H, K], 16-byte aligned.  dg is dL/dg for the raw g the
+ *                      caller passed (through the gate unless KDA_GATE_PREACTIVATED).
+ *   dv               : [B, T, H, V], 16-byte aligned.
+ *   dbeta            : [B, T, H], dL/d beta logits (dL/d beta with KDA_BETA_PREACTIVATED).
+ *   dh0              : NULL or [N, H, V, K], dL/d initial_state (defined with or without
+ *                      an initial state: the gradient at a zero state).
+ *   dA_log, ddt_bias : NULL or [H] and [H, K], summed over every token of every
+ *                      sequence; zero with KDA_GATE_PREACTIVATED.
+ *   workspace        : device scratch of at least kda_bwd_workspace_size bytes, 256-byte
+ *                      aligned; it begins with the error word kda_check_device_error reads
+ *                      (malformed cu_seqlens are clamped and flagged, as in kda_fwd).  It
+ *                      holds the state at every 8th token: (B T / 8 + N + 1) x H x 64 KiB.
+ * The result is deterministic (fixed-order sums, no atomics on values).  Returns KDA_OK
+ * once the kernels are enqueued; argument errors as for kda_fwd (K or V other than 128:
+ * KDA_ERR_UNSUPPORTED_SHAPE).
+ */
+KDA_API kda_status kda_bwd_workspace_size(const kda_shape *shape, size_t *bytes);
+KDA_API kda_status kda_bwd(const kda_shape *shape, const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, float scale, const float *A_log, const float *dt_bias,
+                           float lower_bound, const void *initial_state, kda_state_dtype init_dtype,
+                           const int64_t *cu_seqlens, const void *dout, const float *dfinal, float *dq,
+                           float *dk, float *dv, float *dg, float *dbeta, float *dh0, float *dA_log,
+                           float *ddt_bias, unsigned flags, void *workspace, size_t workspace_bytes,
+                           kda_stream_t stream);
 
 #ifdef __cplusplus
 }

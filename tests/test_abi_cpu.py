@@ -184,3 +184,47 @@ def test_k64_passes_the_shape_checks():
         assert kda.workspace_size(kda.make_shape(1, 64, 2, 1, K=64, V=V)) == \
             kda.workspace_size(kda.make_shape(1, 64, 2, 1, V=V))
     assert _call(kda.make_shape(1, 64, 1, 1, K=256)) == 2
+
+
+def _bwd_call(shape, q=FAKE, dout=FAKE, dq=FAKE, dt_bias=FAKE, lb=-1.0, ws=FAKE, ws_bytes=1 << 40, flags=0,
+              init=None, init_dt=0, dh0=FAKE):
+    lib = kda.load_library()
+    p = lambda a: ctypes.c_void_p(a) if a else None
+    return lib.kda_bwd(ctypes.byref(shape), p(q), p(FAKE), p(FAKE), p(FAKE), p(FAKE), ctypes.c_float(0.1),
+                       p(FAKE), p(dt_bias), ctypes.c_float(lb), p(init), init_dt, None, p(dout), None, p(dq),
+                       p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(dh0), p(FAKE), p(FAKE), ctypes.c_uint(flags),
+                       p(ws), ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("case,expected", [
+    (dict(shape=kda.make_shape(1, 64, 2, 1, K=64)), 2),             # the backward takes K = V = 128 only
+    (dict(shape=kda.make_shape(1, 64, 2, 1, V=256)), 2),
+    (dict(shape=kda.make_shape(1, 64, 2, 1), dout=FAKE + 8), 1),     # dout read four values at a time
+    (dict(shape=kda.make_shape(1, 64, 2, 1), dq=FAKE + 4), 1),       # gradients written as float4
+    (dict(shape=kda.make_shape(1, 64, 2, 1), dt_bias=FAKE + 4), 1),
+    (dict(shape=kda.make_shape(1, 64, 2, 1), dh0=FAKE + 8), 1),
+    (dict(shape=kda.make_shape(1, 64, 2, 1), lb=0.5), 1),
+    (dict(shape=kda.make_shape(1, 64, 2, 1), flags=9), 1),
+    (dict(shape=kda.make_shape(1, 64, 2, 1), init=FAKE, init_dt=0), 1),
+    (dict(shape=kda.make_shape(1, 64, 2, 1), ws=FAKE + 16), 1),      # 256-byte aligned workspace
+    (dict(shape=kda.make_shape(1, 64, 2, 1), ws_bytes=1024), 3),     # too small
+    (dict(shape=kda.make_shape(2, 64, 2, 3)), 1),                    # N must equal B
+])
+def test_bwd_host_side_argument_errors(case, expected):
+    shape = case.pop("shape")
+    assert _bwd_call(shape, **case) == expected
+
+
+def test_bwd_valid_arguments_reach_the_device_query():
+    assert _bwd_call(kda.make_shape(1, 64, 2, 1)) in (4, 5)
+    assert _bwd_call(kda.make_shape(1, 64, 2, 1), dh0=0, lb=9.0, flags=1, dt_bias=0) in (4, 5)
+
+
+def test_bwd_workspace_holds_a_state_every_eighth_token():
+    n1 = kda.bwd_workspace_size(kda.make_shape(1, 4096, 2, 1))
+    n2 = kda.bwd_workspace_size(kda.make_shape(1, 8192, 2, 1))
+    # per extra 4096 tokens and 2 heads: 512 stored states of 64 KiB per head, the per
+    # token-head vectors and four row-slice partials (1552 B x 5), the dA_log terms, and
+    # 16 more parameter blocks of 528 B per head (regions are 256-byte aligned)
+    expected = 4096 * 2 * (64 * 1024 // 8 + 1552 * 5 + 4) + 16 * 2 * 528
+    assert abs((n2 - n1) - expected) <= 6 * 256
