@@ -172,11 +172,18 @@ cudaEvent_t g_profile_events[4] = {nullptr, nullptr, nullptr, nullptr};
 bool g_profile = false;
 thread_local int t_last_launches = 0;
 
-// External records, so that a call captured into a CUDA graph records the events each
-// time the graph runs (outside a capture the flag changes nothing).
+// Inside a stream capture the record is external, so that a call captured into a CUDA
+// graph records the event each time the graph runs; outside it is a plain record.  A
+// profiling mark never fails the call: an error of its own is cleared at once.
 void mark(int i, cudaStream_t s) {
-  if (g_profile && g_profile_events[i] != nullptr)
-    cudaEventRecordWithFlags(g_profile_events[i], s, cudaEventRecordExternal);
+  if (!g_profile || g_profile_events[i] == nullptr) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e == cudaSuccess)
+    e = cs == cudaStreamCaptureStatusActive
+            ? cudaEventRecordWithFlags(g_profile_events[i], s, cudaEventRecordExternal)
+            : cudaEventRecord(g_profile_events[i], s);
+  if (e != cudaSuccess) (void)cudaGetLastError();
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

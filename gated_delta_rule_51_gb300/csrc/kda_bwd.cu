@@ -14,15 +14,18 @@
 //
 // Every value column j of S (a row of the [V, K] state layout) evolves independently given
 // the per-token vectors alpha, kh, qh, beta; only dqh, dkh, dalpha and dbeta sum over
-// columns.  So the recurrences split the 128 state rows of a head over four CTAs of four
-// warps, eight rows a warp, each lane holding four key channels of each of its rows in
+// columns.  So the recurrences split the 128 state rows of a head over four CTAs of eight
+// warps, four rows a warp, each lane holding four key channels of each of its rows in
 // registers (the decode step's layout), and sum the column partials in a fixed order.
+// Each chunk's per-token vectors, v and dout are staged in shared memory once, so the
+// per-token steps read no global memory.
 //
 // Kernels, in launch order:
 //   prep     per token-head: alpha = exp(ghat), beta, qh, kh and the norms' scales;
 //   ckpt     the forward recurrence, storing the state at every kBwdChunk-th token;
 //   reverse  per chunk, last first: for each token (last first) the state before it is
-//            recomputed from the chunk's stored state, then the reverse step runs; the
+//            recomputed from the chunk's stored state (or from the state before the
+//            chunk's middle token, kept once per chunk), then the reverse step runs; the
 //            per-token column partials of dqh, dkh, dalpha, dbeta go to the workspace;
 //   finish   per token-head: the partials summed, then the norms, the sigmoid and the gate;
 //   param    dA_log and dt_bias summed over tokens in blocks, then over blocks.
@@ -39,12 +42,21 @@
 namespace kda {
 namespace {
 
-constexpr int kRowsPerWarp = 8;
-constexpr int kWarps = 4;
+constexpr int kRowsPerWarp = 4;
+constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kRows = kRowsPerWarp * kWarps;   // state rows per CTA
 static_assert(kRows * kBwdSlices == 128, "four CTAs cover the 128 state rows of a head");
-static_assert(kThreads == 128, "one thread per key channel in the column sums");
+static_assert(kThreads >= 128, "one thread per key channel in the column sums");
+static_assert(kBwdRowStride % 4 == 0, "prep rows are copied as float4");
+
+// A chunk's per-token vectors (alpha, kh, qh, beta, rq, rk) and the CTA's rows of v and
+// scale * dout, staged in shared memory once per chunk by the whole CTA.
+struct ChunkStage {
+  float prep[kBwdChunk][kBwdRowStride];
+  float v[kBwdChunk][kRows];
+  float dout[kBwdChunk][kRows];
+};
 
 __device__ __forceinline__ float bfv(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
@@ -116,20 +128,59 @@ __global__ void __launch_bounds__(128) kda_bwd_prep_kernel(const BwdParams p) {
   }
 }
 
-// One forward step of a warp's eight rows for token-head th: P = alpha S; u = v - P^T kh;
-// S = P + beta kh u.
-__device__ __forceinline__ void fwd_step(float4 (&S)[kRowsPerWarp], const BwdParams& p, int64_t th, int row0,
-                                         int lane) {
-  const float* pr = p.prep + th * kBwdRowStride;
+// One forward step of a warp's rows for a staged token: P = alpha S; u = v - P^T kh;
+// S = P + beta kh u.  pr: the token's prep row; vr: its v values of this warp's rows.
+__device__ __forceinline__ void fwd_step(float4 (&S)[kRowsPerWarp], const float* pr, const float* vr, int lane) {
   const float4 al = ld4(pr + 4 * lane), kh = ld4(pr + 128 + 4 * lane);
   const float b = pr[384];
-  const float vv = lane < kRowsPerWarp ? bfv(p.v[th * 128 + row0 + lane]) : 0.f;
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
     const float4 sp = make_float4(al.x * S[i].x, al.y * S[i].y, al.z * S[i].z, al.w * S[i].w);
-    const float u = __shfl_sync(0xffffffffu, vv, i) - warp_sum(dot4(sp, kh));
+    const float u = vr[i] - warp_sum(dot4(sp, kh));
     const float bu = b * u;
     S[i] = make_float4(sp.x + bu * kh.x, sp.y + bu * kh.y, sp.z + bu * kh.z, sp.w + bu * kh.w);
+  }
+}
+
+// Staging of tokens tc .. tc + nv - 1 of head h (rows r0 .. r0 + kRows - 1 of v and dout)
+// in two halves: stage_load reads a chunk into registers (issued a chunk ahead, so the
+// loads are in flight while the current chunk computes), stage_store writes them to
+// shared memory between two barriers.
+constexpr int kPrepF4 = kBwdRowStride / 4;                                  // float4 per prep row
+constexpr int kStagePasses = (kBwdChunk * kPrepF4 + kThreads - 1) / kThreads;
+static_assert(kBwdChunk * kRows <= kThreads, "one v (and dout) value per thread");
+struct StageRegs {
+  float4 pr[kStagePasses];
+  float v, d;
+};
+
+__device__ __forceinline__ void stage_load(StageRegs& R, const BwdParams& p, int64_t tc, int nv, int h, int r0,
+                                           bool with_dout) {
+#pragma unroll
+  for (int k = 0; k < kStagePasses; ++k) {
+    const int idx = threadIdx.x + k * kThreads;
+    if (idx < nv * kPrepF4) {
+      const int i = idx / kPrepF4, f = idx % kPrepF4;
+      R.pr[k] = ld4(p.prep + ((tc + i) * p.H + h) * kBwdRowStride + 4 * f);
+    }
+  }
+  if ((int)threadIdx.x < nv * kRows) {
+    const int i = threadIdx.x / kRows, r = threadIdx.x % kRows;
+    const size_t e = ((size_t)(tc + i) * p.H + h) * 128 + r0 + r;
+    R.v = bfv(p.v[e]);
+    R.d = with_dout ? bfv(p.dout[e]) * p.scale : 0.f;
+  }
+}
+
+__device__ __forceinline__ void stage_store(ChunkStage& cs, const StageRegs& R, int nv) {
+#pragma unroll
+  for (int k = 0; k < kStagePasses; ++k) {
+    const int idx = threadIdx.x + k * kThreads;
+    if (idx < nv * kPrepF4) st4(&cs.prep[idx / kPrepF4][4 * (idx % kPrepF4)], R.pr[k]);
+  }
+  if ((int)threadIdx.x < nv * kRows) {
+    cs.v[threadIdx.x / kRows][threadIdx.x % kRows] = R.v;
+    cs.dout[threadIdx.x / kRows][threadIdx.x % kRows] = R.d;
   }
 }
 
@@ -139,12 +190,13 @@ __device__ __forceinline__ void load_rows(float4 (&S)[kRowsPerWarp], const float
 }
 
 // ---------------------------------------------------------------------------- ckpt
-// Grid: N x H x kBwdSlices CTAs; warp w of slice s owns state rows 32 s + 8 w .. + 7.
+// Grid: N x H x kBwdSlices CTAs; warp w of slice s owns state rows 32 s + 4 w .. + 3.
 __global__ void __launch_bounds__(kThreads) kda_bwd_ckpt_kernel(const BwdParams p) {
+  __shared__ __align__(16) ChunkStage cs;
   const int slice = blockIdx.x % kBwdSlices, nh = blockIdx.x / kBwdSlices;
   const int n = nh / p.H, h = nh % p.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = slice * kRows + warp * kRowsPerWarp;
+  const int r0 = slice * kRows, row0 = r0 + warp * kRowsPerWarp;
   const SeqRange r = seq_range(p, n, slice == 0 && threadIdx.x == 0);
   float4 S[kRowsPerWarp];
   const size_t srow = ((size_t)nh * 128 + row0) * 128;   // element offset of this warp's first row
@@ -158,23 +210,31 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_ckpt_kernel(const BwdParams 
     for (int i = 0; i < kRowsPerWarp; ++i) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const int64_t base = r.t0 / kBwdChunk + n;   // this sequence's first stored-state slot
-  for (int64_t i = 0; i < r.len; ++i) {
-    if (i % kBwdChunk == 0) {
-      float* dst = p.ckpt + (((size_t)(base + i / kBwdChunk) * p.H + h) * 128 + row0) * 128;
+  const int64_t nch = (r.len + kBwdChunk - 1) / kBwdChunk;
+  auto chunk_len = [&](int64_t j) { return (int)min((int64_t)kBwdChunk, r.len - j * kBwdChunk); };
+  StageRegs R;
+  if (nch > 0) stage_load(R, p, r.t0, chunk_len(0), h, r0, false);
+  for (int64_t j = 0; j < nch; ++j) {
+    const int nv = chunk_len(j);
+    float* dst = p.ckpt + (((size_t)(base + j) * p.H + h) * 128 + row0) * 128;
 #pragma unroll
-      for (int j = 0; j < kRowsPerWarp; ++j) st4(dst + j * 128 + 4 * lane, S[j]);
-    }
-    fwd_step(S, p, (r.t0 + i) * p.H + h, row0, lane);
+    for (int i = 0; i < kRowsPerWarp; ++i) st4(dst + i * 128 + 4 * lane, S[i]);
+    __syncthreads();   // the previous chunk's staged values are read
+    stage_store(cs, R, nv);
+    __syncthreads();
+    if (j + 1 < nch) stage_load(R, p, r.t0 + (j + 1) * kBwdChunk, chunk_len(j + 1), h, r0, false);
+    for (int i = 0; i < nv; ++i) fwd_step(S, cs.prep[i], &cs.v[i][warp * kRowsPerWarp], lane);
   }
 }
 
 // ---------------------------------------------------------------------------- reverse
 __global__ void __launch_bounds__(kThreads) kda_bwd_reverse_kernel(const BwdParams p) {
   __shared__ __align__(16) float red[2][kWarps][kBwdRowStride];
+  __shared__ __align__(16) ChunkStage cs;
   const int slice = blockIdx.x % kBwdSlices, nh = blockIdx.x / kBwdSlices;
   const int n = nh / p.H, h = nh % p.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = slice * kRows + warp * kRowsPerWarp;
+  const int r0 = slice * kRows, row0 = r0 + warp * kRowsPerWarp;
   const SeqRange r = seq_range(p, n, false);
   const int64_t TH = p.BT * p.H;
   const size_t srow = ((size_t)nh * 128 + row0) * 128;
@@ -188,31 +248,51 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_reverse_kernel(const BwdPara
   const int64_t base = r.t0 / kBwdChunk + n;
   const int64_t nch = (r.len + kBwdChunk - 1) / kBwdChunk;
   int par = 0;
+  auto chunk_len = [&](int64_t j) { return (int)min((int64_t)kBwdChunk, r.len - j * kBwdChunk); };
+  constexpr int kMid = kBwdChunk / 2;
+  StageRegs R;
+  if (nch > 0) stage_load(R, p, r.t0 + (nch - 1) * kBwdChunk, chunk_len(nch - 1), h, r0, true);
   for (int64_t j = nch - 1; j >= 0; --j) {
     const float* ck = p.ckpt + (((size_t)(base + j) * p.H + h) * 128 + row0) * 128;
     const int64_t tc = r.t0 + j * kBwdChunk;
-    const int nv = (int)min((int64_t)kBwdChunk, r.len - j * kBwdChunk);
+    const int nv = chunk_len(j);
+    __syncthreads();   // the previous chunk's staged values are read
+    stage_store(cs, R, nv);
+    __syncthreads();
+    if (j > 0) stage_load(R, p, tc - kBwdChunk, chunk_len(j - 1), h, r0, true);
+    const int wr = warp * kRowsPerWarp;   // this warp's rows within the staged ones
+    // the state before the chunk's middle token, for the second half's recomputations
+    float4 Sm[kRowsPerWarp];
+    if (nv > kMid) {
+      load_rows(Sm, ck, lane);
+      for (int jj = 0; jj < kMid; ++jj) fwd_step(Sm, cs.prep[jj], &cs.v[jj][wr], lane);
+    }
     for (int i = nv - 1; i >= 0; --i) {
-      // the state before token tc + i, recomputed from the chunk's stored state
+      // the state before token tc + i, recomputed from the chunk's stored state or its middle
       float4 S[kRowsPerWarp];
-      load_rows(S, ck, lane);
-      for (int jj = 0; jj < i; ++jj) fwd_step(S, p, (tc + jj) * p.H + h, row0, lane);
+      int from = 0;
+      if (i >= kMid) {
+#pragma unroll
+        for (int ii = 0; ii < kRowsPerWarp; ++ii) S[ii] = Sm[ii];
+        from = kMid;
+      } else {
+        load_rows(S, ck, lane);
+      }
+      for (int jj = from; jj < i; ++jj) fwd_step(S, cs.prep[jj], &cs.v[jj][wr], lane);
       const int64_t th = (tc + i) * p.H + h;
-      const float* pr = p.prep + th * kBwdRowStride;
+      const float* pr = cs.prep[i];
       const float4 al = ld4(pr + 4 * lane), kh = ld4(pr + 128 + 4 * lane), qh = ld4(pr + 256 + 4 * lane);
       const float b = pr[384];
-      const float vv = lane < kRowsPerWarp ? bfv(p.v[th * 128 + row0 + lane]) : 0.f;
-      const float dd = lane < kRowsPerWarp ? bfv(p.dout[th * 128 + row0 + lane]) * p.scale : 0.f;
       float4 aq = make_float4(0.f, 0.f, 0.f, 0.f), ak = aq, aa = aq;
       float dbeta = 0.f, dv_mine = 0.f;
 #pragma unroll
       for (int ii = 0; ii < kRowsPerWarp; ++ii) {
         const float4 s0 = S[ii];
         const float4 sp = make_float4(al.x * s0.x, al.y * s0.y, al.z * s0.z, al.w * s0.w);
-        const float u = __shfl_sync(0xffffffffu, vv, ii) - warp_sum(dot4(sp, kh));
+        const float u = cs.v[i][wr + ii] - warp_sum(dot4(sp, kh));
         const float bu = b * u;
         const float4 st = make_float4(sp.x + bu * kh.x, sp.y + bu * kh.y, sp.z + bu * kh.z, sp.w + bu * kh.w);
-        const float d = __shfl_sync(0xffffffffu, dd, ii);   // scale * dO for this row
+        const float d = cs.dout[i][wr + ii];   // scale * dO for this row
         aq.x += d * st.x; aq.y += d * st.y; aq.z += d * st.z; aq.w += d * st.w;
         float4 ds = dS[ii];
         ds.x += d * qh.x; ds.y += d * qh.y; ds.z += d * qh.z; ds.w += d * qh.w;
@@ -233,8 +313,8 @@ __global__ void __launch_bounds__(kThreads) kda_bwd_reverse_kernel(const BwdPara
       st4(rw + 256 + 4 * lane, aa);
       if (lane == 0) rw[384] = dbeta;
       __syncthreads();
-      {
-        // column sums over the CTA's four warps, in a fixed order; one thread per channel
+      if (threadIdx.x < 128) {
+        // column sums over the CTA's warps, in a fixed order; one thread per channel
         const int c = threadIdx.x;
         float sq = 0.f, sk = 0.f, sa = 0.f;
 #pragma unroll
