@@ -89,25 +89,35 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# the source files each measured kernel is built from (its own file, the device helpers and
+# the parameter structs): a committed DRAM count stands while none of them has changed
+KERNEL_FILES = {"chain": ("kda_chain.cu", "kda_device.cuh", "kda_internal.h"),
+                "decode": ("kda_decode.cu", "kda_device.cuh", "kda_internal.h"),
+                "bwd": ("kda_bwd.cu", "kda_device.cuh", "kda_internal.h")}
+
+
+def kernel_source_hash(files=None) -> str:
+    """sha256 (first 16 hex digits) over the given csrc files in order, default all of them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_51_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in (files if files is not None else sorted(os.listdir(csrc))):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(workload_name: str):
-    """DRAM bytes per forward-kernel launch from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
+    """DRAM bytes per launch of the workload's dominant kernel from the committed ncu
+    summary, if it was taken on that kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload_name)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    if not e or e.get("kernel_files") not in KERNEL_FILES:
+        return None
+    if e.get("kernel_source_hash") != kernel_source_hash(KERNEL_FILES[e["kernel_files"]]):
         return None
     return e.get("traffic_bytes_per_launch")
 
@@ -698,7 +708,7 @@ def run_bwd(args, w):
     hbm_gbs, _, peak_kind = load_peaks()
     achieved = nbytes / (ph["reverse"] / 1000.0) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                "traffic": None, "kernel": "kda_bwd_reverse_kernel",
+                "traffic": measured_traffic("bwd_" + w.name), "kernel": "kda_bwd_reverse_kernel",
                 "peak_source": "measured, MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": nbytes,
