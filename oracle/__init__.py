@@ -12,6 +12,8 @@ Contents:
   * ``token_np.py``   -- a NumPy twin of the same definition for tiny inputs.
   * ``chunked_np.py`` -- the 16-token chunked (WY/UT) form of the method in
     NumPy fp64, used to pin the token form and to study rounding.
+  * ``chunked_bwd_np.py`` -- the gradient through that chunked form (dense per-chunk
+    products, the shape a tensor-core backward takes), pinned to the token gradient.
 """
 from __future__ import annotations
 
