@@ -224,6 +224,80 @@ def cpu_oracle_sample(w, x_cpu, budget_s: float = 15.0):
     return tokens_per_s, threads, desc, dt
 
 
+def bwd_oracle_sample(w, x_cpu, dout, dfinal, tokens: int = 512, heads: int = 8):
+    """Time the fp64 gradient oracle, as it stands, on the first `tokens` tokens of every
+    sequence (each batch row) and the first `heads` heads (one thread per (sequence, head)
+    pair); tokens/s is scaled by the fraction of the workload's token-heads covered."""
+    import oracle
+
+    tt, hs = min(tokens, w.T), list(range(min(heads, w.H)))
+    cut = lambda t: t[:, :tt][:, :, hs].double().numpy()
+    cu = None
+    if x_cpu["cu_seqlens"] is not None:
+        # the first sequences that fit in tt tokens
+        import numpy as np
+
+        c = x_cpu["cu_seqlens"].numpy()
+        keep = [0] + [int(e) for e in c[1:] if e <= tt]
+        cu = np.array(keep if keep[-1] == tt else keep + [tt], dtype=np.int64)
+    nseq = (len(cu) - 1) if cu is not None else w.B
+    init = x_cpu["initial_state"]
+    init = init[:nseq][:, hs].double().numpy() if init is not None else None
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.kda_backward(cut(x_cpu["q"]), cut(x_cpu["k"]), cut(x_cpu["v"]), cut(x_cpu["g"]), cut(x_cpu["beta"]),
+                        float(x_cpu["scale"]), x_cpu["A_log"][hs].double().numpy(),
+                        x_cpu["dt_bias"][hs].double().numpy(), float(x_cpu["lower_bound"]), cut(dout), init,
+                        dfinal[:nseq][:, hs].double().numpy(), cu, nthreads=threads)
+    dt = time.perf_counter() - t0
+    th = w.B * tt * len(hs)
+    desc = (f"{th} token-heads ({w.B}x{tt} tokens x {len(hs)} of {w.H} heads); tokens/s scaled by "
+            "covered token-heads / H")
+    return th / dt / w.H, min(threads, nseq * len(hs)), desc, dt
+
+
+def bwd_upstream_grads(w, device, generator):
+    """dout (bf16 N(0, 1), the shape of out) and dfinal (fp32 0.1 N(0, 1)) for the backward."""
+    import torch
+
+    dout = torch.randn((w.B, w.T, w.H, 128), generator=generator, device=device).to(torch.bfloat16)
+    dfinal = 0.1 * torch.randn((w.N, w.H, 128, 128), generator=generator, device=device)
+    return dout, dfinal
+
+
+def run_bwd_reference(args, w):
+    """--impl reference for the backward: the fp64 gradient oracle on the host cores, timed
+    per step on a bounded sample of the workload (rank 0 only)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import torch
+
+    from gated_delta_rule_51_gb300 import inputs as I
+    import oracle
+
+    oracle.build()
+    x = I.make_inputs(w, device="cpu")
+    dout, dfinal = bwd_upstream_grads(w, "cpu", torch.Generator().manual_seed(w.seed + 100))
+    for _ in range(args.warmup):
+        bwd_oracle_sample(w, x, dout, dfinal)
+    vals, times = [], []
+    desc, threads = "", 1
+    for _ in range(args.steps):
+        v, threads, desc, dt = bwd_oracle_sample(w, x, dout, dfinal)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * statistics.mean(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, {"pass": "backward", "parallelism": "cpu threads"}),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest of every rank's value (timings: the job ends with its slowest rank)."""
     if world <= 1:
@@ -658,9 +732,7 @@ def run_bwd(args, w):
         dist.init_process_group("nccl", device_id=dev)
     kda.load_library()
     x = I.make_inputs(w, device=dev)
-    gen = torch.Generator(device=dev).manual_seed(w.seed + 100)
-    dout = torch.randn(x["v"].shape, generator=gen, device=dev).to(torch.bfloat16)
-    dfinal = 0.1 * torch.randn((w.N, w.H, 128, 128), generator=gen, device=dev)
+    dout, dfinal = bwd_upstream_grads(w, dev, torch.Generator(device=dev).manual_seed(w.seed + 100))
     shape = kda.make_shape(w.B, w.T, w.H, w.N)
     ws = torch.empty(kda.bwd_workspace_size(shape), dtype=torch.uint8, device=dev)
     f32 = dict(dtype=torch.float32, device=dev)
@@ -715,22 +787,9 @@ def run_bwd(args, w):
                 "step_frac": (nbytes / (ms / 1000.0) / 1e9) / hbm_gbs, "phase_ms": ph}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
-
-        # bounded sample: the first 512 tokens of every sequence, two heads
-        tt, hs = min(512, w.T), [0, 1]
-        c = lambda t: t[:, :tt][:, :, hs].cpu().double().numpy()
-        t0 = time.perf_counter()
-        oracle.kda_backward(c(x["q"]), c(x["k"]), c(x["v"]), c(x["g"]), c(x["beta"]), float(x["scale"]),
-                            x["A_log"][hs].cpu().double().numpy(), x["dt_bias"][hs].cpu().double().numpy(),
-                            float(x["lower_bound"]), c(dout), x["initial_state"][:, hs].cpu().double().numpy(),
-                            dfinal[:, hs].cpu().double().numpy(), None, nthreads=os.cpu_count())
-        dt = time.perf_counter() - t0
-        th = w.B * tt * len(hs)
-        cpu = {"value": th / dt / w.H, "unit": "tokens/s", "cores": min(os.cpu_count() or 1, w.B * len(hs)),
-               "kind": "oracle",
-               "sample": f"{th} token-heads ({w.B}x{tt} tokens x {len(hs)} of {w.H} heads); "
-                         "tokens/s scaled by covered token-heads / H"}
+        x_cpu = {n: (t.cpu() if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+        v, threads, desc, _ = bwd_oracle_sample(w, x_cpu, dout.cpu(), dfinal.cpu())
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
     if rank == 0:
         line = {"metric": BWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -761,9 +820,7 @@ def main():
     if args.config.startswith("bwd"):
         # the backward pass on a forward workload: "bwd" is the fixed batch, "bwd_<name>" any other
         name = args.config[4:] if args.config.startswith("bwd_") else "fixed"
-        if args.impl == "reference":
-            raise SystemExit("the reference arm times the forward")
-        run_bwd(args, workload(name))
+        (run_bwd_reference if args.impl == "reference" else run_bwd)(args, workload(name))
         return
     w = workload(args.config)
     if args.impl == "reference":

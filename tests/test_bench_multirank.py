@@ -59,3 +59,20 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     assert bench.run_reference(None, bench.workload("tiny")) is None
     assert capsys.readouterr().out == ""
+
+
+def test_backward_reference_arm_prints_one_oracle_line(monkeypatch, capsys):
+    import json
+    import types
+
+    monkeypatch.delenv("RANK", raising=False)
+    args = types.SimpleNamespace(steps=1, warmup=0, gpus=1)
+    bench.run_bwd_reference(args, bench.workload("tiny"))
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["impl"] == "reference" and line["metric"] == bench.BWD_METRIC
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] == line["cpu_baseline"]["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"]["pass"] == "backward"
+    monkeypatch.setenv("RANK", "1")
+    assert bench.run_bwd_reference(args, bench.workload("tiny")) is None
+    assert capsys.readouterr().out == ""
