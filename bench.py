@@ -96,13 +96,38 @@ KERNEL_FILES = {"chain": ("kda_chain.cu", "kda_device.cuh", "kda_internal.h"),
                 "bwd": ("kda_bwd.cu", "kda_device.cuh", "kda_internal.h")}
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines, each line's trailing spaces
+    dropped: the code a compiler sees, so that editing a comment leaves it unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":                                    # string or character literal
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash(files=None) -> str:
-    """sha256 (first 16 hex digits) over the given csrc files in order, default all of them."""
+    """sha256 (first 16 hex digits) over the given csrc files in order (default all of
+    them), comments and blank lines removed."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_51_gb300", "csrc")
     for f in (files if files is not None else sorted(os.listdir(csrc))):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,8 +1,8 @@
 // kda_decode.cu -- the recurrent step of KDA for decoding: a few tokens per
 // sequence, the state read from and written back to HBM once per call.
 //
-// Per (sequence n, head h) and token t, with K = V = 128 and the state kept as
-// S^T (row v holds S[:, v] over the 128 key channels k), the step is the KDA
+// Per (sequence n, head h) and token t, with K = 128 (or 64) and V = 64, 128 or 256, the
+// state kept as S^T (row v holds S[:, v] over the key channels k), the step is the KDA
 // recurrence itself (FlashKDA README "Kernel API" parameter table for the
 // inputs, gate and layout):
 //   ghat  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h, :]))   (or g_t given, or

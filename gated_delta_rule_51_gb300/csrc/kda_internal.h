@@ -110,11 +110,11 @@ constexpr unsigned kValidFlags = 15;
 constexpr int kChainPadded = 16;
 
 struct DecodeParams {
-  const uint16_t *q, *k, *v, *g, *beta;  // bf16 [B, T, H, 128] (beta [B, T, H], logits)
-  uint16_t* out;                          // bf16 [B, T, H, 128]
+  const uint16_t *q, *k, *v, *g, *beta;  // bf16 [B, T, H, K] (v [B, T, H, V]; beta [B, T, H], logits)
+  uint16_t* out;                          // bf16 [B, T, H, V]
   const float* A_log;                     // [H]
-  const float* dt_bias;                   // [H, 128]
-  void* state;                            // [B, H, 128 (v), 128 (k)], read and written in place
+  const float* dt_bias;                   // [H, K]
+  void* state;                            // [B, H, V, K], read and written in place
   int state_dtype;                        // 1 bf16, 2 fp32
   int vsplit;                             // V / 64: 64-row CTAs per (sequence, head)
   int kdim;                               // K: 128, or 64 (channels 64-127 then run as zeros)

@@ -1,9 +1,11 @@
 /*
- * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library.
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library: the chunked
+ * forward, the decode step and the backward pass.
  *
  * The operation is the chunked forward pass of Kimi Delta Attention (KDA), as
  * stated by the FlashKDA README ("Kernel API", flash_kda.fwd parameter table)
- * together with the KDA recurrence, per sequence n and head h, K = V = 128:
+ * together with the KDA recurrence, per sequence n and head h (K = V = 128 in the
+ * README; the shapes this library also takes are listed with kda_shape):
  *
  *   ghat_t  = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h,:]))  (per channel;
  *             the reference call's safe gate, the default; see kda_flags for the others)

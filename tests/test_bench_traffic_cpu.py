@@ -36,3 +36,12 @@ def test_a_count_is_reported_only_for_unchanged_kernel_sources(tmp_path, monkeyp
     assert bench.measured_traffic("stale") is None
     assert bench.measured_traffic("unnamed") is None
     assert bench.measured_traffic("missing") is None
+
+
+def test_the_source_hash_ignores_comments_but_not_code():
+    a = 'int f() { return 1; }  // one\n/* block\n */\nconst char* s = "x//y";\n'
+    b = '// header\nint f() { return 1; }\n\nconst char* s = "x//y";   /* trailing */\n'
+    c = 'int f() { return 2; }\nconst char* s = "x//y";\n'
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert bench.strip_comments(a) != bench.strip_comments(c)
+    assert '"x//y"' in bench.strip_comments(a)
