@@ -1,11 +1,12 @@
-"""The oracle at K = 64 or V = 64 against itself at K = V = 128 on zero-padded inputs.
+"""The oracle at K = 64, V = 64 and V = 256 against itself at K = V = 128.
 
 The GPU tests compare the K = 64 and V = 64 paths with the oracle at those sizes; this pins
 that the oracle's own K = 64 / V = 64 results are the K = V = 128 recurrence with the
 extra key channels (q = k = g = dt_bias = 0, initial state 0 there) or value columns
 (v = 0, initial state 0 there) padded in: the padded state columns stay zero and add
 nothing, so the results agree to fp64 rounding.  The forward oracle (bf16 inputs) and the
-gradient oracle (fp64 inputs) are both checked.
+gradient oracle (fp64 inputs) are both checked.  V = 256 is two independent V = 128
+problems that share q, k, g and beta (the value columns of the state never mix).
 """
 from __future__ import annotations
 
@@ -71,3 +72,16 @@ def test_gradient_oracle_at_small_head_dims_equals_the_padded_full_size(K, V):
                   ("dv", (..., slice(0, V))), ("dbeta", (...,)), ("dh0", (..., slice(0, V), slice(0, K))),
                   ("dA_log", (...,)), ("ddt_bias", (..., slice(0, K)))):
         np.testing.assert_allclose(r1[n], r2[n][sl], rtol=0, atol=tol(r1[n]), err_msg=n)
+
+
+def test_forward_oracle_at_v256_equals_two_independent_v128_halves():
+    """Value columns evolve independently: V = 256 is two V = 128 problems sharing q, k, g, beta."""
+    x = _inputs(31, 128, 256, [12, 29])
+    scale = 128 ** -0.5
+    o, f = oracle.kda_forward(x["q"], x["k"], x["v"], x["g"], x["beta"], scale, x["A_log"], x["dt_bias"], -2.0,
+                              x["s0"], x["cu"])
+    for half in (slice(0, 128), slice(128, 256)):
+        oh, fh = oracle.kda_forward(x["q"], x["k"], x["v"][..., half].contiguous(), x["g"], x["beta"], scale,
+                                    x["A_log"], x["dt_bias"], -2.0, x["s0"][:, :, half].contiguous(), x["cu"])
+        np.testing.assert_allclose(o[..., half], oh, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(f[:, :, half], fh, rtol=0, atol=1e-13)
