@@ -343,3 +343,58 @@ def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_stat
     if st != KDA_OK:
         raise KDAError(st, "kda_bwd")
     return r
+
+
+class KDAFunction(torch.autograd.Function):
+    """KDA as an autograd operation: forward through kda_fwd_ex, backward through kda_bwd
+    (K = V = 128 for gradients).  Inputs: q, k, v, g, beta (bf16), A_log, dt_bias (fp32),
+    initial_state (bf16/fp32 or None), cu_seqlens (int64 or None), then the scalars and
+    switches.  Outputs: out (bf16) and final_state (the initial state's dtype, fp32 when
+    there is none).  Gradients come back in each input's dtype."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, scale, lower_bound,
+                use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate):
+        B, T, H, K = q.shape
+        N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+        V = v.shape[-1]
+        out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=q.device)
+        fdt = initial_state.dtype if initial_state is not None else torch.float32
+        final_state = torch.empty((N, H, V, K), dtype=fdt, device=q.device)
+        sw = dict(use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+                  use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel, safe_gate=safe_gate)
+        fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=initial_state,
+            final_state=final_state, cu_seqlens=cu_seqlens, **sw)
+        ctx.save_for_backward(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens)
+        ctx.set_materialize_grads(False)   # an unused output's gradient arrives as None
+        ctx.scalars = (scale, lower_bound)
+        ctx.switches = sw
+        return out, final_state
+
+    @staticmethod
+    def backward(ctx, dout, dfinal):
+        q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens = ctx.saved_tensors
+        scale, lower_bound = ctx.scalars
+        if dout is None:
+            dout = torch.zeros(v.shape, dtype=torch.bfloat16, device=q.device)
+        r = bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout.to(torch.bfloat16).contiguous(),
+                initial_state=initial_state,
+                dfinal=None if dfinal is None else dfinal.to(torch.float32).contiguous(),
+                cu_seqlens=cu_seqlens, **ctx.switches)
+        gate = ctx.switches["use_gate_in_kernel"]
+
+        def cast(t, like):
+            return None if like is None else t.to(like.dtype)
+
+        return (cast(r["dq"], q), cast(r["dk"], k), cast(r["dv"], v), cast(r["dg"], g), cast(r["dbeta"], beta),
+                cast(r["dA_log"], A_log) if gate else None, cast(r["ddt_bias"], dt_bias) if gate else None,
+                cast(r["dh0"], initial_state), None, None, None, None, None, None, None)
+
+
+def kda_attention(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None, cu_seqlens=None,
+                  use_gate_in_kernel: bool = True, use_beta_sigmoid_in_kernel: bool = True,
+                  use_qk_l2norm_in_kernel: bool = True, safe_gate: bool = True):
+    """The forward with autograd: returns (out, final_state); gradients flow to q, k, v, g,
+    beta, A_log, dt_bias and initial_state through the CUDA backward."""
+    return KDAFunction.apply(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, scale, lower_bound,
+                             use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate)

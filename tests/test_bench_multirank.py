@@ -39,7 +39,7 @@ def _rank_main(rank: int, world: int, port: int, times, out):
 def test_two_ranks_take_the_slowest_time_and_count_every_rank():
     world, port = 2, _free_port()
     times = [12.5, 20.0]          # ms for 4 steps on each rank
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank_main, args=(world, port, times, out), nprocs=world, join=True)
         res = dict(out)

@@ -170,3 +170,32 @@ def test_backward_malformed_cu_seqlens_is_flagged():
     x["cu_seqlens"] = torch.tensor([0, 32, 64], dtype=torch.int64, device="cuda")
     _gpu(x, dout, dfinal, workspace=ws)
     assert kda.check_device_error(ws) == 0
+
+
+def test_autograd_function_matches_the_oracle_gradient():
+    """kda.kda_attention: the forward and backward kernels behind torch autograd.  Gradients
+    come back in the inputs' dtypes: the bf16 ones carry their own rounding (about 1.1e-3
+    relative Frobenius), so they get the 5e-3 bound of bf16 results; the fp32 ones (A_log,
+    dt_bias, the initial state) keep the 1e-5 bound."""
+    from gated_delta_rule_51_gb300 import kda
+
+    x = random_case(1, 200, 2, seed=975, lens=[80, 120])
+    leaves = {n: x[n].detach().clone().requires_grad_(True)
+              for n in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state")}
+    out, fin = kda.kda_attention(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"], x["scale"],
+                                 leaves["A_log"], leaves["dt_bias"], x["lower_bound"],
+                                 initial_state=leaves["initial_state"], cu_seqlens=x["cu_seqlens"])
+    gen = torch.Generator().manual_seed(976)
+    wo = torch.randn(out.shape, generator=gen).to(torch.bfloat16).cuda()
+    wf = (0.1 * torch.randn(fin.shape, generator=gen)).cuda()
+    ((out.float() * wo.float()).sum() + (fin * wf).sum()).backward()
+    torch.cuda.synchronize()
+    ref = _oracle(x, wo, wf)
+    for n, gname, bound in (("q", "dq", 5e-3), ("k", "dk", 5e-3), ("v", "dv", 5e-3), ("g", "dg", 5e-3),
+                            ("beta", "dbeta", 5e-3), ("A_log", "dA_log", BOUND), ("dt_bias", "ddt_bias", BOUND),
+                            ("initial_state", "dh0", BOUND)):
+        gr = leaves[n].grad
+        assert gr is not None and gr.dtype == x[n].dtype, n
+        e = rel_fro(gr.detach().cpu().double().numpy(), ref[gname])
+        _report("bwd autograd", f"{gname}_rel_fro", e)
+        assert e <= bound, f"{n}: rel-Fro {e:.3e} > {bound}"
