@@ -174,9 +174,10 @@ def test_backward_malformed_cu_seqlens_is_flagged():
 
 def test_autograd_function_matches_the_oracle_gradient():
     """kda.kda_attention: the forward and backward kernels behind torch autograd.  Gradients
-    come back in the inputs' dtypes: the bf16 ones carry their own rounding (about 1.1e-3
-    relative Frobenius), so they get the 5e-3 bound of bf16 results; the fp32 ones (A_log,
-    dt_bias, the initial state) keep the 1e-5 bound."""
+    come back in the inputs' dtypes: the bf16 ones carry their own rounding (relative error
+    at most 2^-8 = 3.9e-3 an element; 1.7e-3 to 2.6e-3 relative Frobenius measured on a
+    GB300), so they get the 5e-3 bound of bf16 results; the fp32 ones (A_log, dt_bias, the
+    initial state) keep the 1e-5 bound (measured 0.9e-7 to 3.2e-7)."""
     from gated_delta_rule_51_gb300 import kda
 
     x = random_case(1, 200, 2, seed=975, lens=[80, 120])
