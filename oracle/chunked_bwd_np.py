@@ -4,8 +4,9 @@ The gradient the token-level oracle (kda_oracle_bwd.c) computes, reached instead
 16-token chunked form of the forward (the form oracle/chunked_np.py writes out, FlashKDA's
 "Delta Attention Algorithm ... processes 16-token chunks"), differentiated chunk by chunk.
 Every step is a small dense product, the shape a tensor-core backward would take; this
-module states and checks that math before any kernel does.  Default switches only: the safe
-gate, the beta sigmoid and the L2 norms in the kernel.
+module states and checks that math before any kernel does.  The reference call's switches
+change only the per-token ends: the gate (safe sigmoid, softplus or pre-activated), the beta
+sigmoid and the L2 norms.
 
 Per chunk of m tokens with S0 (K x V) on entry, G the inclusive cumsum of ghat (natural log),
 Gam = exp(G), Gc = Gam[m-1]:
@@ -35,7 +36,8 @@ def _sigmoid(x):
 
 
 def backward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None, dfinal=None,
-             cu_seqlens=None, chunk=16):
+             cu_seqlens=None, chunk=16, use_gate_in_kernel=True, use_beta_sigmoid_in_kernel=True,
+             use_qk_l2norm_in_kernel=True, safe_gate=True):
     """fp64 arrays in the token oracle's conventions; returns the same dict of gradients."""
     B, T, H, K = q.shape
     V = v.shape[-1]
@@ -52,17 +54,27 @@ def backward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial
              dA_log=np.zeros(H), ddt_bias=np.zeros((H, K)))
     for n, (t0, t1) in enumerate(bounds):
         for h in range(H):
-            rate = np.exp(A_log[h])
+            rate = np.exp(A_log[h]) if use_gate_in_kernel else 0.0
 
             def prep(c0, c1):
                 qq, kk = qf[c0:c1, h], kf[c0:c1, h]
-                rq = 1.0 / np.sqrt(np.sum(qq * qq, axis=1) + 1e-6)
-                rk = 1.0 / np.sqrt(np.sum(kk * kk, axis=1) + 1e-6)
-                x = gf[c0:c1, h] + dt_bias[h][None, :]
-                s = _sigmoid(rate * x)
-                gh = lower_bound * s
-                return dict(qh=qq * rq[:, None], kh=kk * rk[:, None], rq=rq, rk=rk, x=x, s=s,
-                            b=_sigmoid(bf[c0:c1, h]), G=np.cumsum(gh, axis=0), V=vf[c0:c1, h])
+                ones = np.ones(c1 - c0)
+                rq = 1.0 / np.sqrt(np.sum(qq * qq, axis=1) + 1e-6) if use_qk_l2norm_in_kernel else ones
+                rk = 1.0 / np.sqrt(np.sum(kk * kk, axis=1) + 1e-6) if use_qk_l2norm_in_kernel else ones
+                if not use_gate_in_kernel:
+                    x = s = None
+                    gh = gf[c0:c1, h]
+                elif not safe_gate:
+                    x = gf[c0:c1, h] + dt_bias[h][None, :]
+                    s = _sigmoid(x)
+                    gh = -rate * np.where(x > 0, x + np.log1p(np.exp(-np.abs(x))), np.log1p(np.exp(np.minimum(x, 0))))
+                else:
+                    x = gf[c0:c1, h] + dt_bias[h][None, :]
+                    s = _sigmoid(rate * x)
+                    gh = lower_bound * s
+                b = bf[c0:c1, h] if not use_beta_sigmoid_in_kernel else _sigmoid(bf[c0:c1, h])
+                return dict(qh=qq * rq[:, None], kh=kk * rk[:, None], rq=rq, rk=rk, x=x, s=s, gh=gh,
+                            b=b, G=np.cumsum(gh, axis=0), V=vf[c0:c1, h])
 
             def chunk_terms(c, S0):
                 Gam = np.exp(c["G"])
@@ -121,15 +133,24 @@ def backward(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial
                 dgh = np.cumsum(dG[::-1], axis=0)[::-1]
                 # the norms, the beta sigmoid and the gate
                 qh, kh = c["qh"], c["kh"]
-                r["dq"][c0:c1, h] = c["rq"][:, None] * (dqh - qh * np.sum(qh * dqh, axis=1)[:, None])
-                r["dk"][c0:c1, h] = c["rk"][:, None] * (dkh - kh * np.sum(kh * dkh, axis=1)[:, None])
+                if use_qk_l2norm_in_kernel:
+                    dqh = c["rq"][:, None] * (dqh - qh * np.sum(qh * dqh, axis=1)[:, None])
+                    dkh = c["rk"][:, None] * (dkh - kh * np.sum(kh * dkh, axis=1)[:, None])
+                r["dq"][c0:c1, h] = dqh
+                r["dk"][c0:c1, h] = dkh
                 r["dv"][c0:c1, h] = dV
-                r["dbeta"][c0:c1, h] = dbeta * c["b"] * (1.0 - c["b"])
-                dz = dgh * lower_bound * c["s"] * (1.0 - c["s"])
-                dx = dz * rate
+                r["dbeta"][c0:c1, h] = dbeta * c["b"] * (1.0 - c["b"]) if use_beta_sigmoid_in_kernel else dbeta
+                if not use_gate_in_kernel:
+                    r["dg"][c0:c1, h] = dgh
+                    continue
+                if safe_gate:     # ghat = lb sigmoid(rate x): d/dx = rate lb s (1 - s), d/dA_log = x d/dx
+                    dx = dgh * lower_bound * c["s"] * (1.0 - c["s"]) * rate
+                    r["dA_log"][h] += np.sum(dx * c["x"])
+                else:             # ghat = -rate softplus(x): d/dx = -rate sigmoid(x), d/dA_log = ghat
+                    dx = dgh * (-rate) * c["s"]
+                    r["dA_log"][h] += np.sum(dgh * c["gh"])
                 r["dg"][c0:c1, h] = dx
                 r["ddt_bias"][h] += np.sum(dx, axis=0)
-                r["dA_log"][h] += np.sum(dx * c["x"])
             r["dh0"][n, h] = dS.T
     for key in ("dq", "dk", "dg"):
         r[key] = r[key].reshape(B, T, H, K)

@@ -252,17 +252,21 @@ def test_gradient_equals_autograd_of_a_torch_restatement(name):
         np.testing.assert_allclose(t[n].grad.numpy(), gr[gn], rtol=1e-10, atol=1e-12, err_msg=n)
 
 
-@pytest.mark.parametrize("chunk", [16, 5, 1])
-def test_chunked_form_gradient_equals_the_token_gradient(chunk):
+@pytest.mark.parametrize("chunk,name", [(16, "default"), (5, "default"), (1, "default"), (16, "softplus_gate"),
+                                        (7, "preactivated_gate"), (16, "softplus_beta_given_no_norm"),
+                                        (4, "beta_given"), (16, "no_l2norm")])
+def test_chunked_form_gradient_equals_the_token_gradient(chunk, name):
     """The chunked (WY/UT) gradient of oracle/chunked_bwd_np.py, a separate derivation through
-    dense per-chunk products, equals the token oracle's gradient to fp64 rounding."""
+    dense per-chunk products, equals the token oracle's gradient to fp64 rounding, for every
+    switch of the reference call."""
     from oracle import chunked_bwd_np
 
-    x, dout, dfinal = _case(91, T=45, H=2, K=6, V=4, lens=[17, 0, 3, 25])
-    ref = _grads(x, dout, dfinal, {})
+    kw = FLAG_SETS[name]
+    x, dout, dfinal = _case(91, T=45, H=2, K=6, V=4, lens=[17, 0, 3, 25], kw=kw)
+    ref = _grads(x, dout, dfinal, kw)
     got = chunked_bwd_np.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["A_log"],
                                   x["dt_bias"], x["lower_bound"], dout, x["initial_state"], dfinal,
-                                  x["cu_seqlens"], chunk=chunk)
+                                  x["cu_seqlens"], chunk=chunk, **kw)
     for n in GRAD_OF.values():
         np.testing.assert_allclose(got[n], ref[n], rtol=1e-9, atol=1e-11 * max(1.0, np.abs(ref[n]).max()),
                                    err_msg=n)
