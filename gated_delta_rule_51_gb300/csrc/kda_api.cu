@@ -337,7 +337,8 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   if (st != KDA_OK) return st;
   const kda_shape s = *shape;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  // README: "When cu_seqlens is provided, B must be 1"; otherwise N = B.
+  // FlashKDA README, "Kernel API": a varlen call (cu_seqlens given) takes a batch of one row;
+  // otherwise every one of the B rows is its own sequence (N = B).
   if (cu_seqlens != nullptr) {
     if (s.B != 1 || s.N < 0) return KDA_ERR_INVALID_ARGUMENT;
     if (s.N == 0 && s.T != 0) return KDA_ERR_INVALID_ARGUMENT;
@@ -361,7 +362,8 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   // the chain kernel reads dt_bias four values at a time
   if (gate_here && (A_log == nullptr || dt_bias == nullptr || !aligned(A_log, 4) || !aligned16(dt_bias)))
     return KDA_ERR_INVALID_ARGUMENT;
-  // states: README "accept None (stateless), bf16, or fp32 ... When both are provided, their dtypes must match"
+  // states (FlashKDA README, "Kernel API"): each may be absent, bf16 or fp32, and two given
+  // states share one dtype
   auto dtype_ok = [](kda_state_dtype d) { return d == KDA_STATE_BF16 || d == KDA_STATE_FP32; };
   if (initial_state != nullptr && (!dtype_ok(init_dtype) || !aligned16(initial_state))) return KDA_ERR_INVALID_ARGUMENT;
   if (final_state != nullptr && (!dtype_ok(final_dtype) || !aligned16(final_state))) return KDA_ERR_INVALID_ARGUMENT;

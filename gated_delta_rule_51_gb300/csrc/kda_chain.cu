@@ -2,8 +2,8 @@
 //
 // One CTA walks one run of 16-token chunks of one (sequence, head) -- a whole
 // sequence, or one segment of a long one -- and keeps the 128 x 128 fp32 state
-// on chip for the whole run (FlashKDA: "processes 16-token chunks", "FP32 FMA
-// instructions for state updates").  Per chunk, with S the state on entry:
+// on chip for the whole run (FlashKDA works in chunks of 16 tokens and updates the
+// state in fp32; instagit index, kernel articles).  Per chunk, with S the state on entry:
 //
 //   G    = within-chunk inclusive cumsum of the base-2 log-decay (per channel)
 //   Akk  = tril(beta_i * (kh*2^G)(kh*2^-G)^T, -1)   Aqk = tril((qh*2^G)(kh*2^-G)^T, 0)

@@ -262,6 +262,16 @@ def check_device_error(workspace: Optional[torch.Tensor] = None, device=None) ->
     return int(flags.value)
 
 
+def raise_on_device_error(flags: int, what: str) -> None:
+    """Raise KDAError for a nonzero device error word (the bits of kda_check_device_error)."""
+    if flags & 1:
+        raise KDAError(6, what)
+    if flags & 2:
+        raise KDAError(7, what)
+    if flags & 4:
+        raise KDAError(8, what)
+
+
 def set_profile_events(events) -> None:
     """Record the given 4 torch.cuda.Events after each launch phase of fwd (None to stop)."""
     lib = load_library()
@@ -354,10 +364,16 @@ class KDAFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, scale, lower_bound,
-                use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate):
+                use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate,
+                check_errors=False):
         B, T, H, K = q.shape
         N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
         V = v.shape[-1]
+        # the backward (kda_bwd) takes K = V = 128 only: refuse before the forward runs rather
+        # than fail inside loss.backward()
+        if any(ctx.needs_input_grad) and (K != 128 or V != 128):
+            raise ValueError(f"gradients need K = V = 128 (got K = {K}, V = {V}); run the forward "
+                             "without requires_grad for the other head dimensions")
         out = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=q.device)
         fdt = initial_state.dtype if initial_state is not None else torch.float32
         final_state = torch.empty((N, H, V, K), dtype=fdt, device=q.device)
@@ -365,10 +381,13 @@ class KDAFunction(torch.autograd.Function):
                   use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel, safe_gate=safe_gate)
         fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=initial_state,
             final_state=final_state, cu_seqlens=cu_seqlens, **sw)
+        if check_errors:
+            raise_on_device_error(check_device_error(device=q.device), "kda_fwd")
         ctx.save_for_backward(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens)
         ctx.set_materialize_grads(False)   # an unused output's gradient arrives as None
         ctx.scalars = (scale, lower_bound)
         ctx.switches = sw
+        ctx.check_errors = check_errors
         return out, final_state
 
     @staticmethod
@@ -377,10 +396,18 @@ class KDAFunction(torch.autograd.Function):
         scale, lower_bound = ctx.scalars
         if dout is None:
             dout = torch.zeros(v.shape, dtype=torch.bfloat16, device=q.device)
+        ws = None
+        if ctx.check_errors:   # a workspace of our own, so that its error word can be read afterwards
+            B, T, H, K = q.shape
+            N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+            ws = torch.empty(max(bwd_workspace_size(make_shape(B, T, H, N, K, v.shape[-1])), 256),
+                             dtype=torch.uint8, device=q.device)
         r = bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout.to(torch.bfloat16).contiguous(),
                 initial_state=initial_state,
                 dfinal=None if dfinal is None else dfinal.to(torch.float32).contiguous(),
-                cu_seqlens=cu_seqlens, **ctx.switches)
+                cu_seqlens=cu_seqlens, workspace=ws, **ctx.switches)
+        if ctx.check_errors:
+            raise_on_device_error(check_device_error(workspace=ws, device=q.device), "kda_bwd")
         gate = ctx.switches["use_gate_in_kernel"]
 
         def cast(t, like):
@@ -388,13 +415,21 @@ class KDAFunction(torch.autograd.Function):
 
         return (cast(r["dq"], q), cast(r["dk"], k), cast(r["dv"], v), cast(r["dg"], g), cast(r["dbeta"], beta),
                 cast(r["dA_log"], A_log) if gate else None, cast(r["ddt_bias"], dt_bias) if gate else None,
-                cast(r["dh0"], initial_state), None, None, None, None, None, None, None)
+                cast(r["dh0"], initial_state), None, None, None, None, None, None, None, None)
 
 
 def kda_attention(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None, cu_seqlens=None,
                   use_gate_in_kernel: bool = True, use_beta_sigmoid_in_kernel: bool = True,
-                  use_qk_l2norm_in_kernel: bool = True, safe_gate: bool = True):
+                  use_qk_l2norm_in_kernel: bool = True, safe_gate: bool = True, check_errors: bool = False):
     """The forward with autograd: returns (out, final_state); gradients flow to q, k, v, g,
-    beta, A_log, dt_bias and initial_state through the CUDA backward."""
+    beta, A_log, dt_bias and initial_state through the CUDA backward (K = V = 128; other
+    head dimensions are refused when an input requires grad).
+
+    The kernels report malformed cu_seqlens, a gate whose decay leaves the chunked form's
+    range and timed-out waits through an error word, not an exception.  With
+    check_errors=True the forward and the backward each synchronise and raise KDAError when
+    that word is set; otherwise the caller validates cu_seqlens (and, for the gates without a
+    lower bound, the decay range) itself."""
     return KDAFunction.apply(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, scale, lower_bound,
-                             use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate)
+                             use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate,
+                             check_errors)

@@ -12,10 +12,10 @@
  *   S_t     = (I - beta_t k_t k_t^T) Diag(exp(ghat_t)) S_{t-1} + beta_t k_t v_t^T
  *   o_t     = scale * S_t^T q_t
  *
- * with beta_t = sigmoid(beta logit) ("sigmoid applied internally"), q_t and
+ * with beta_t = sigmoid(beta logit) (applied in the kernel, per the README), q_t and
  * k_t L2-normalised per token and head (x / sqrt(|x|^2 + 1e-6)), and the state
  * S (K x V) stored transposed as [.., V, K] (FLA transpose_state_layout=True).
- * The device computes it in 16-token chunks ("processes 16-token chunks"); the
+ * The device computes it in 16-token chunks, as FlashKDA does (instagit index); the
  * chunk's unit lower-triangular system is inverted in fp32 by forward
  * substitution (FlashKDA's articles use a Neumann-series product; both give the exact
  * inverse of a 16 x 16 unit lower-triangular matrix).
@@ -63,7 +63,7 @@ typedef enum {
     KDA_ERR_GATE_RANGE = 8          /* a 16-token chunk decayed past 2^-250 on some channel (error word) */
 } kda_status;
 
-/* State dtype for initial_state / final_state (README: "bf16/fp32/None"). */
+/* State dtype for initial_state / final_state (README: absent, bf16 or fp32). */
 typedef enum { KDA_STATE_NONE = 0, KDA_STATE_BF16 = 1, KDA_STATE_FP32 = 2 } kda_state_dtype;
 
 /*
@@ -106,8 +106,8 @@ typedef enum {
  *   beta    : [B, T, H]    bf16 (logits)
  *   A_log   : [H] fp32               dt_bias : [H, K] fp32
  *   states  : [N, H, V, K]           cu_seqlens : int64 [N + 1]
- * N is the number of sequences: N = B without cu_seqlens ("each batch element
- * is treated as an independent sequence"); with cu_seqlens B must be 1 and T
+ * N is the number of sequences: N = B without cu_seqlens (the README treats every
+ * batch row as its own sequence); with cu_seqlens B must be 1 and T
  * is the total length across all sequences.
  */
 typedef struct {
@@ -119,8 +119,8 @@ KDA_API const char *kda_status_string(kda_status s);
 
 /*
  * Bytes of device workspace kda_fwd needs for this shape.  The size is linear
- * in the number of heads and of sequence tiles ("workspace size ... linear
- * scaling with attention heads and sequence tiles"): it holds the device-side
+ * in the number of heads and of sequence tiles (the instagit workspace-size article
+ * states the same growth): it holds the device-side
  * work list and, for sequences split into segments, one pair of 128 x 128
  * fp32 segment transition/carry matrices per (segment, head).
  * Returns KDA_ERR_INVALID_ARGUMENT / KDA_ERR_UNSUPPORTED_SHAPE for bad shapes.
@@ -130,7 +130,7 @@ KDA_API kda_status kda_workspace_size(const kda_shape *shape, size_t *bytes);
 /*
  * The forward pass (README flash_kda.fwd).
  *   q, k, v, g, beta : bf16 inputs as above.
- *   scale            : output scale (README "scaling factor").
+ *   scale            : output scale (the README's scale argument).
  *   out              : bf16 [B, T, H, V], written for every token.
  *   A_log, dt_bias   : fp32 gate parameters.
  *   lower_bound      : gate lower bound, must lie in [-5, 0] (README range);

@@ -1,8 +1,8 @@
 """Chunked (WY/UT) form of the KDA gradient in NumPy fp64 -- TEST INFRASTRUCTURE ONLY.
 
 The gradient the token-level oracle (kda_oracle_bwd.c) computes, reached instead through the
-16-token chunked form of the forward (the form oracle/chunked_np.py writes out, FlashKDA's
-"Delta Attention Algorithm ... processes 16-token chunks"), differentiated chunk by chunk.
+16-token chunked form of the forward (the form oracle/chunked_np.py writes out; FlashKDA works
+in chunks of 16 tokens, instagit index, delta-attention article), differentiated chunk by chunk.
 Every step is a small dense product, the shape a tensor-core backward would take; this
 module states and checks that math before any kernel does.  The reference call's switches
 change only the per-token ends: the gate (safe sigmoid, softplus or pre-activated), the beta

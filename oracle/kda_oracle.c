@@ -9,7 +9,7 @@
  *   initial state S (K x V; zeros when no initial state is given):
  *     ghat_t[c] = lower_bound * sigmoid(exp(A_log[h]) * (g_t[c] + dt_bias[h,c]))
  *     alpha_t   = exp(ghat_t)                       (per channel c < K)
- *     beta_t    = sigmoid(beta_logit_t)            ("sigmoid applied internally")
+ *     beta_t    = sigmoid(beta_logit_t)            (the README applies it in the kernel)
  *     qh = q_t / sqrt(|q_t|^2 + 1e-6),  kh = k_t / sqrt(|k_t|^2 + 1e-6)
  *     S   <- Diag(alpha_t) S                        (decay first)
  *     S   <- S + beta_t * kh (v_t - S^T kh)^T        (delta-rule update)
@@ -31,7 +31,7 @@
  *       combined with ORACLE_GATE_PREACTIVATED.
  *
  * Readings where FlashKDA's README and articles are silent: the gate is a sigmoid scaled by the
- * lower bound (README "safe_gate", "Gate lower bound (range from -5.0 to 0)");
+ * lower bound (README: the safe_gate switch, and a lower bound that lies in [-5, 0]);
  * the L2-norm epsilon is 1e-6 inside the square root; scale is applied after
  * normalisation.  Parity of these readings against the original library is
  * unpinned (no printed values exist); everything else is pinned by the tests.

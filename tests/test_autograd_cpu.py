@@ -25,8 +25,9 @@ CALLS = []
 
 
 def _fake_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None, dfinal=None,
-              cu_seqlens=None, **sw):
-    CALLS.append(dict(dout_dtype=dout.dtype, dfinal_dtype=None if dfinal is None else dfinal.dtype))
+              cu_seqlens=None, workspace=None, **sw):
+    CALLS.append(dict(dout_dtype=dout.dtype, dfinal_dtype=None if dfinal is None else dfinal.dtype,
+                      workspace=workspace is not None))
     d = lambda t: None if t is None else t.detach().double().numpy()
     r = oracle.kda_backward(d(q), d(k), d(v), d(g), d(beta), float(np.float32(scale)), d(A_log), d(dt_bias),
                             float(np.float32(lower_bound)), d(dout), d(initial_state), d(dfinal),
@@ -63,7 +64,7 @@ def test_gradients_reach_every_input_in_its_dtype(init_dtype, lens):
     wo = torch.randn(out.shape, generator=gen).to(torch.bfloat16)
     wf = torch.randn(fin.shape, generator=gen)
     ((out.float() * wo.float()).sum() + (fin.float() * wf).sum()).backward()
-    assert CALLS == [dict(dout_dtype=torch.bfloat16, dfinal_dtype=torch.float32)]
+    assert CALLS == [dict(dout_dtype=torch.bfloat16, dfinal_dtype=torch.float32, workspace=False)]
     ref = _fake_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], 0.088, x["A_log"], x["dt_bias"], -3.0, wo,
                     init, wf.to(fin.dtype).float(), cu)
     for n, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"), ("A_log", "dA_log"),
@@ -86,3 +87,57 @@ def test_a_preactivated_gate_gives_its_parameters_no_gradient():
     assert A.grad is None and D.grad is None
     assert g.grad is not None and g.grad.dtype == torch.bfloat16
     assert CALLS[0]["dfinal_dtype"] is None      # the final state was not used
+
+
+def _small(K=128, V=128, seed=5):
+    gen = torch.Generator().manual_seed(seed)
+    bf = lambda *s: torch.randn(*s, generator=gen).to(torch.bfloat16)
+    return dict(q=_leaf(bf(1, 6, 1, K)), k=_leaf(bf(1, 6, 1, K)), v=_leaf(bf(1, 6, 1, V)), g=_leaf(bf(1, 6, 1, K)),
+                beta=_leaf(bf(1, 6, 1)), A_log=_leaf(torch.zeros(1)), dt_bias=_leaf(torch.zeros(1, K)))
+
+
+@pytest.mark.parametrize("K,V", [(64, 128), (128, 256), (128, 64)])
+def test_other_head_dims_with_grad_are_refused_before_the_forward(monkeypatch, K, V):
+    ran = []
+    monkeypatch.setattr(kda, "fwd", lambda *a, **kw: ran.append(1))
+    x = _small(K, V)
+    with pytest.raises(ValueError, match="K = V = 128"):
+        kda.kda_attention(x["q"], x["k"], x["v"], x["g"], x["beta"], 0.1, x["A_log"], x["dt_bias"], -1.0)
+    assert ran == []
+    # without gradients the same shapes run
+    d = {n: t.detach() for n, t in x.items()}
+    monkeypatch.setattr(kda, "fwd", lambda *a, **kw: ran.append(1))
+    kda.kda_attention(d["q"], d["k"], d["v"], d["g"], d["beta"], 0.1, d["A_log"], d["dt_bias"], -1.0)
+    assert ran == [1]
+
+
+def test_check_errors_raises_on_the_device_error_word(monkeypatch):
+    seen = []
+
+    def fake_check(workspace=None, device=None):
+        seen.append(workspace is not None)
+        return 2   # malformed cu_seqlens
+
+    monkeypatch.setattr(kda, "check_device_error", fake_check)
+    x = _small()
+    with pytest.raises(kda.KDAError, match="BAD_SEQLENS"):
+        kda.kda_attention(x["q"], x["k"], x["v"], x["g"], x["beta"], 0.1, x["A_log"], x["dt_bias"], -1.0,
+                          check_errors=True)
+    assert seen == [False]   # the forward's own (cached) workspace
+    # unchecked calls never read the word
+    seen.clear()
+    out, fin = kda.kda_attention(x["q"], x["k"], x["v"], x["g"], x["beta"], 0.1, x["A_log"], x["dt_bias"], -1.0)
+    assert seen == []
+    # the backward reads the error word of a workspace it allocated itself
+    monkeypatch.setattr(kda, "check_device_error", lambda workspace=None, device=None: seen.append(workspace) or 0)
+    out, fin = kda.kda_attention(x["q"], x["k"], x["v"], x["g"], x["beta"], 0.1, x["A_log"], x["dt_bias"], -1.0,
+                                 check_errors=True)
+    out.float().sum().backward()
+    assert seen[0] is None and seen[1] is not None and CALLS[-1]["workspace"]
+
+
+def test_raise_on_device_error_maps_each_bit():
+    kda.raise_on_device_error(0, "x")
+    for bit, name in ((1, "TIMEOUT"), (2, "BAD_SEQLENS"), (4, "GATE_RANGE")):
+        with pytest.raises(kda.KDAError, match=name):
+            kda.raise_on_device_error(bit, "x")

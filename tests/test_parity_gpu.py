@@ -227,10 +227,11 @@ def test_forward_captured_in_a_cuda_graph_replays_identically():
         assert torch.equal(fin, fin_ref)
 
 
-@pytest.mark.parametrize("total,H", [(262144, 32), (262144, 64)])
-def test_sweep_workloads_largest_cells_sampled(total, H):
-    """The largest sweep cells (16.8M token-heads at H = 64): every final state in full,
-    outputs on sampled rows (the first and last rows of every sequence and random ones)."""
+@pytest.mark.parametrize("total,H", [(32768, 64), (131072, 32), (131072, 64), (262144, 32), (262144, 64)])
+def test_sweep_workloads_large_cells_sampled(total, H):
+    """The sweep cells past the three small ones (up to 16.8M token-heads at H = 64): every
+    final state in full, outputs on sampled rows (the first and last rows of every sequence
+    and random ones). With the small cells above, every cell of the sweep is compared."""
     w = I.sweep_workload(total, H)
     x = I.make_inputs(w, device="cuda")
     out, fin = run_gpu(x)

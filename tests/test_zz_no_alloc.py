@@ -98,3 +98,37 @@ def test_static_workspace_rejects_problems_beyond_its_size():
     st = fn(ctypes.byref(shape), p, p, p, p, p, ctypes.c_float(0.1), p, p, p, ctypes.c_float(-1.0), None, 0,
             None, 0, None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 3   # KDA_ERR_WORKSPACE_TOO_SMALL, nothing launched
+
+
+def test_static_workspace_at_its_size_limit():
+    """The largest problem of a family whose workspace still fits the built-in array runs and
+    matches kda_fwd; the next larger one is refused."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_51_gb300 import kda
+
+    fn = _declare(kda.load_library())
+    limit, H = 64 << 20, 8
+    ws = lambda n: kda.workspace_size(kda.make_shape(1, n, H, n))   # n one-token sequences
+    lo, hi = 1, 1
+    while ws(hi) <= limit:
+        lo, hi = hi, 2 * hi
+    while hi - lo > 1:   # ws(lo) <= limit < ws(hi)
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if ws(mid) <= limit else (lo, mid)
+    assert ws(lo) <= limit < ws(hi) and ws(lo) > limit // 2
+    # (no states: one per sequence would dwarf the rest of the problem)
+    x = random_case(1, lo, H, seed=503, lens=[1] * lo, init_dtype=None)
+    out_ref = torch.empty((1, lo, H, 128), dtype=torch.bfloat16, device="cuda")
+    kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], out_ref, x["A_log"], x["dt_bias"],
+            x["lower_bound"], cu_seqlens=x["cu_seqlens"])
+    out = torch.full_like(out_ref, float("nan"))
+    assert _no_alloc_call(fn, x, out, None) == kda.KDA_OK
+    torch.cuda.synchronize()
+    _compare(out.float(), out_ref.float(), OUT_REL_FRO, OUT_MAX_ABS)
+    # one size up: refused before anything runs, outputs untouched
+    y = random_case(1, hi, H, seed=504, lens=[1] * hi, init_dtype=None)
+    out2 = torch.full((1, hi, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert _no_alloc_call(fn, y, out2, None) == 3
+    torch.cuda.synchronize()
+    assert torch.isnan(out2.float()).all()
