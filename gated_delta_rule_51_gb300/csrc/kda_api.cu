@@ -81,8 +81,9 @@ int64_t choose_seg_tokens(const kda_shape& s, int sms) {
 
 struct Layout {
   int64_t seg_tokens = 0;
-  int64_t cap_forward = 0, cap_phase1 = 0, cap_compose = 0, cap_slots = 0, cap_ranks = 0;
-  size_t off_hdr = 0, off_forward = 0, off_phase1 = 0, off_compose = 0, off_slots = 0, off_ranks = 0, off_sm = 0;
+  int64_t cap_forward = 0, cap_correct = 0, cap_compose = 0, cap_slots = 0, cap_ranks = 0;
+  size_t off_hdr = 0, off_forward = 0, off_correct = 0, off_compose = 0, off_slots = 0, off_ranks = 0, off_sm = 0,
+         off_zero = 0;
   size_t total = 0;
 };
 
@@ -91,25 +92,27 @@ Layout make_layout(const kda_shape& s, int sms) {
   const int64_t rows = s.B * s.T;
   L.seg_tokens = choose_seg_tokens(s, sms);
   const int64_t splits = rows / L.seg_tokens;   // bound on sum over sequences of (nseg - 1)
-  L.cap_forward = s.H * (splits + s.N);
-  L.cap_ranks = splits + s.N;
-  const int64_t qcap = s.H * splits;
-  L.cap_slots = 2 * qcap;
-  L.cap_phase1 = 2 * qcap;
+  // runs of the first launch: nseg forward + (nseg - 2) transition runs per sequence
+  L.cap_ranks = s.N + 2 * splits;
+  L.cap_forward = s.H * L.cap_ranks;
+  L.cap_correct = s.H * splits;                 // nseg - 1 per sequence
+  L.cap_slots = 2 * s.H * splits;               // 2 (nseg - 1) per split sequence
   L.cap_compose = s.H * std::min<int64_t>(s.N, splits);
   size_t off = 0;
   L.off_hdr = off;
   off = align_up(off + sizeof(WorkHeader));
   L.off_forward = off;
   off = align_up(off + (size_t)L.cap_forward * sizeof(WorkItem));
-  L.off_phase1 = off;
-  off = align_up(off + (size_t)L.cap_phase1 * sizeof(WorkItem));
+  L.off_correct = off;
+  off = align_up(off + (size_t)L.cap_correct * sizeof(WorkItem));
   L.off_compose = off;
   off = align_up(off + (size_t)L.cap_compose * sizeof(ComposeItem));
   L.off_ranks = off;
   off = align_up(off + (size_t)L.cap_ranks * sizeof(int));
   L.off_sm = off;
   off = align_up(off + (size_t)kMaxSmIds * sizeof(int));
+  L.off_zero = off;
+  off = align_up(off + (size_t)L.cap_slots * sizeof(int));
   L.off_slots = off;
   off = align_up(off + (size_t)L.cap_slots * kSlotBytes);
   L.total = off;
@@ -399,10 +402,10 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   sp.has_init = initial_state != nullptr;
   sp.has_final = final_state != nullptr;
   sp.hdr = hdr;
-  sp.phase1 = reinterpret_cast<WorkItem*>(ws + L.off_phase1);
+  sp.correct = reinterpret_cast<WorkItem*>(ws + L.off_correct);
   sp.forward = reinterpret_cast<WorkItem*>(ws + L.off_forward);
   sp.compose = reinterpret_cast<ComposeItem*>(ws + L.off_compose);
-  sp.cap_phase1 = L.cap_phase1;
+  sp.cap_correct = L.cap_correct;
   sp.cap_forward = L.cap_forward;
   sp.cap_compose = L.cap_compose;
   sp.cap_slots = L.cap_slots;
@@ -434,6 +437,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   cp.init_state = initial_state;
   cp.final_state = final_state;
   cp.ws_states = reinterpret_cast<float*>(ws + L.off_slots);
+  cp.zero_flags = reinterpret_cast<int*>(ws + L.off_zero);
   cp.err = &hdr->err;
   cp.H = (int)s.H;
   cp.vsplit = (int)std::max<int64_t>(s.V / 128, 1);
@@ -447,29 +451,34 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   cp.take = nullptr;
   cp.sm_arrivals = nullptr;
 
-  if (L.cap_phase1 > 0) {
-    cp.items = sp.phase1;
-    cp.item_count = &hdr->n_phase1;
-    if (launch_chain(cp, (int)L.cap_phase1, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    ++launches;
-    ComposeParams cmp;
-    cmp.ws_states = cp.ws_states;
-    cmp.items = sp.compose;
-    cmp.item_count = &hdr->n_compose;
-    mark(1, stream);
-    if (launch_compose(cmp, (int)L.cap_compose, d.sms, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (L.cap_compose > 0) ++launches;
-    mark(2, stream);
-  } else {
-    mark(1, stream);
-    mark(2, stream);
-  }
+  // first launch: every segment's forward run (outputs, local carries) and the transition
+  // runs, longest first, two CTAs per SM paired long with short
   cp.items = sp.forward;
   cp.item_count = &hdr->n_forward;
   cp.take = hdr->take;
   cp.sm_arrivals = sp.sm_arrivals;
   if (launch_chain(cp, (int)L.cap_forward, stream) != cudaSuccess) return KDA_ERR_CUDA;
   ++launches;
+  mark(1, stream);
+  if (L.cap_correct > 0) {
+    ComposeParams cmp;
+    cmp.ws_states = cp.ws_states;
+    cmp.zero_flags = cp.zero_flags;
+    cmp.items = sp.compose;
+    cmp.item_count = &hdr->n_compose;
+    if (launch_compose(cmp, (int)L.cap_compose, d.sms, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (L.cap_compose > 0) ++launches;
+    mark(2, stream);
+    // last launch: the corrections of segments 1 .. n-1 from their true entering states
+    cp.items = sp.correct;
+    cp.item_count = &hdr->n_correct;
+    cp.take = nullptr;
+    cp.sm_arrivals = nullptr;
+    if (launch_chain(cp, (int)L.cap_correct, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    ++launches;
+  } else {
+    mark(2, stream);
+  }
   mark(3, stream);
   t_last_launches = launches;
   return KDA_OK;

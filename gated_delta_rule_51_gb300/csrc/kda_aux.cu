@@ -1,15 +1,19 @@
 // kda_aux.cu -- device-side work scheduling and the segment-carry composition.
 //
-// Long sequences are cut into segments of at most `seg_tokens` tokens so that
-// the sequential chunk recurrence of one (sequence, head) can run on several
-// SMs at once.  Because one chunk maps the state affinely, S_out = P S_in + Q,
-// a segment s >= 1 is first run twice from a known start -- once from the
-// identity with zero values (its transition P_s) and once from zero (its
-// local carry Q_s) -- segment 0 is run from the true initial state (which
-// gives S_1 directly), the carries are then composed in order,
-// S_{s+1} = P_s S_s + Q_s, and finally every segment runs its forward pass
-// from its true initial state.  All of this is derived from the recurrence;
-// FlashKDA's README carries the state across calls, with no segment scan.
+// Long sequences are cut into segments so that the sequential chunk recurrence of
+// one (sequence, head) can run on several SMs at once.  Because a segment maps the
+// state affinely, S_out = P S_in + Q, every segment first runs its forward pass from
+// a known start (segment 0 from the true initial state, the others from zero), which
+// writes its outputs and its local carry Q_s; segments 1 .. n-2 also run from the
+// identity with zero values, which gives their transitions P_s.  The carries are then
+// composed in order, S_{s+1} = P_s S_s + Q_s, and each segment s >= 1 finally runs a
+// correction: the recurrence with zero values started from S_s, whose outputs are
+// added to the ones already written (by linearity in (v, S_in) this is exactly the
+// forward from the true state).  Transition and correction runs stop as soon as the
+// state they carry is exactly zero in fp32 -- from then on it stays zero -- so for a
+// gate that forgets, a split costs little more than the forward pass itself.  All of
+// this is derived from the recurrence; FlashKDA's README carries the state across
+// calls, with no segment scan.
 #include "kda_device.cuh"
 #include "kda_internal.h"
 
@@ -19,14 +23,18 @@ namespace kda {
 // One CTA.  Reads cu_seqlens (or the fixed batch layout), validates it, and
 // writes the three work lists and their counts into the workspace.
 //
-// Slots (128 x 128 fp32 each) for a sequence with nseg >= 2 segments, head h:
-//   q slot (s) = qbase + h (nseg-1) + s,  s = 0 .. nseg-2   local carry Q_s
-//                (Q_0 is the true state after segment 0; the composition
-//                overwrites Q_s with the true state after segment s)
-//   p slot (s) = q slot (s) + q_total H                     transition P_s;
-//                p slot (0) keeps a copy of the initial state instead.
-// The first-phase list has one entry per slot (entry i writes slot i); the
-// entries of the unused transitions P_0 are no-ops (len = -1).
+// A sequence of len tokens is cut into nseg = ceil(len / L) segments of L tokens (the
+// last one shorter).  Per head, the lists get:
+//   first launch   F_s, s = 0 .. nseg-1: forward runs writing outputs; F_0 starts from
+//                  the caller's initial state, the others from zero.  F_s stores its final
+//                  state in slot Q_s (for s = nseg-1 only when there is a final state;
+//                  an unsplit sequence writes the caller's final state directly).
+//                  T_s, s = 1 .. nseg-2: transition runs into slot P_s (with a zero flag).
+//   compose        S_1 = Q_0; S_{s+1} = P_s S_s + Q_s into Q_s, s = 1 .. nseg-2.
+//   last launch    C_s, s = 1 .. nseg-1: correction runs from Q_{s-1} = S_s, adding to the
+//                  outputs of F_s; C_{nseg-1} writes the final state Q_{nseg-1} + D.
+// Slots of one (sequence, head), from base = slot0 H + h 2 (nseg-1):
+//   Q_s = base + s (s = 0 .. nseg-1),  P_s = base + nseg + s - 1 (s = 1 .. nseg-2).
 constexpr int kSchedThreads = 1024;
 static_assert(kSchedThreads == 32 * 32, "block_scan scans one total per warp in one warp");
 
@@ -70,10 +78,11 @@ __device__ long long block_scan(long long x, long long* buf) {
   return r;
 }
 
-// Forward runs are listed longest first, so that the first wave puts the longest runs one to
-// an SM and the short ones fill the second CTA slots and finish early: the long chains then
-// run alone for most of their length.  Runs are ranked by a length bucket, four buckets per
-// octave of chunk count (ties in arbitrary order; every run computes the same either way).
+// The first launch's runs are listed longest first, so that the first wave puts the longest
+// runs one to an SM and the short ones fill the second CTA slots and finish early: the long
+// chains then run alone for most of their length.  Runs are ranked by a length bucket, four
+// buckets per octave of chunk count (ties in arbitrary order; every run computes the same
+// either way).  Transition runs usually stop after a few chunks and are ranked shortest.
 constexpr int kLenBuckets = 4 * 32;
 __device__ __forceinline__ int len_bucket(long long chunks) {
   if (chunks < 4) return (int)(chunks < 0 ? 0 : chunks);
@@ -84,10 +93,10 @@ __device__ __forceinline__ int len_bucket(long long chunks) {
 __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const ScheduleParams p) {
   __shared__ unsigned int s_hist[kLenBuckets];
   __shared__ long long s_buf[kSchedThreads];
-  __shared__ long long s_tot[3];   // segments, q slots, compose chains (running totals)
+  __shared__ long long s_tot[4];   // runs, corrections, compose chains, slots (running totals)
   __shared__ int s_start[kSchedThreads], s_len[kSchedThreads], s_nseg[kSchedThreads], s_incl[kSchedThreads];
-  __shared__ long long s_seg0[kSchedThreads], s_q0[kSchedThreads];
-  __shared__ int s_c0[kSchedThreads];
+  __shared__ long long s_run0[kSchedThreads], s_corr0[kSchedThreads], s_slot0[kSchedThreads];
+  __shared__ int s_comp0[kSchedThreads];
   __shared__ int s_err;
   __shared__ unsigned long long s_max_chunks, s_sum_chunks;
   __shared__ long long s_L;
@@ -103,10 +112,10 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
   for (int i = tid; i < kMaxSmIds; i += kSchedThreads) p.sm_arrivals[i] = 0;
   if (tid < 3) p.hdr->take[tid] = 0;
   __syncthreads();
-  // Split long sequences only when one of them would outlast the rest of the
-  // work by a wide margin: a split run costs a second pass over its tokens
-  // (local state, transition), so with the longest sequence within 3x the mean
-  // load of a resident CTA the unsplit chains finish first.
+  // Split long sequences when the longest would outlast the mean load of a resident CTA by
+  // more than a quarter.  A split costs, per extra segment, a transition run and a correction
+  // run; both stop as soon as what they carry is exactly zero in fp32, which for a gate that
+  // forgets comes after a few chunks (a gate that keeps everything makes them full passes).
   if (!p.seg_forced && p.seg_tokens < total_rows) {
     unsigned long long mx = 0, sum = 0;
     for (long long n = tid; n < p.N; n += kSchedThreads) {
@@ -129,13 +138,12 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
     long long Lx = p.seg_tokens;
     if (!p.seg_forced && p.seg_tokens < total_rows) {
       const long long per_cta = ((long long)s_sum_chunks * H + p.resident - 1) / p.resident;
-      if ((long long)s_max_chunks <= 3 * per_cta) Lx = (total_rows + 15) / 16 * 16;   // no split
+      if (4 * (long long)s_max_chunks <= 5 * per_cta) Lx = (total_rows + 15) / 16 * 16;   // no split
     }
     s_L = Lx;
   }
   __syncthreads();
   const long long L = s_L;
-  long long q_total = 0;
   for (int pass = 0; pass < 2; ++pass) {
     if (pass == 1 && tid == 0) {   // bucket counts -> first rank of each bucket, longest first
       unsigned int start = 0;
@@ -145,7 +153,7 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
         start += c;
       }
     }
-    if (tid == 0) s_tot[0] = s_tot[1] = s_tot[2] = 0;
+    if (tid == 0) s_tot[0] = s_tot[1] = s_tot[2] = s_tot[3] = 0;
     __syncthreads();
     for (long long base = 0; base < p.N; base += kSchedThreads) {
       const long long n = base + tid;
@@ -164,99 +172,107 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
         }
         nseg = len <= 0 ? 1 : (len + L - 1) / L;
       }
-      // pass 0: histogram of the forward runs' lengths; pass 1: each run's rank
-      const long long seg0_scan = block_scan(nseg, s_buf) - nseg + s_tot[0];
+      const long long ntr = nseg >= 3 ? nseg - 2 : 0;
+      const long long nruns = nseg + ntr;
+      const long long ncorr = nseg >= 2 ? nseg - 1 : 0;
+      const long long ncomp = nseg >= 3 ? 1 : 0;
+      const long long nslot = nseg >= 2 ? 2 * (nseg - 1) : 0;
+      const long long incl = block_scan(nruns, s_buf);
+      const long long run0 = s_tot[0] + incl - nruns;
+      // pass 0: histogram of the runs' lengths; pass 1: each run's rank
       if (n < p.N) {
-        for (long long sg = 0; sg < nseg; ++sg) {
-          const long long flen = len <= 0 ? 0 : (len - sg * L < L ? len - sg * L : L);
-          const int bk = len_bucket((flen + 15) / 16);
+        for (long long r = 0; r < nruns; ++r) {
+          const long long flen = r < nseg ? (len <= 0 ? 0 : (len - r * L < L ? len - r * L : L)) : 0;
+          const int bk = r < nseg ? len_bucket((flen + 15) / 16) : 0;
           if (pass == 0) atomicAdd(&s_hist[bk], 1u);
-          else if (seg0_scan + sg < p.cap_ranks) p.seg_rank[seg0_scan + sg] = (int)atomicAdd(&s_hist[bk], 1u);
+          else if (run0 + r < p.cap_ranks) p.seg_rank[run0 + r] = (int)atomicAdd(&s_hist[bk], 1u);
         }
       }
-      const long long nq = nseg >= 2 ? nseg - 1 : 0;
-      const long long nc = nseg >= 3 ? 1 : 0;
-      const long long incl = block_scan(nseg, s_buf);
-      const long long seg0 = s_tot[0] + incl - nseg;
-      const long long q0 = s_tot[1] + block_scan(nq, s_buf) - nq;
-      const long long c0 = s_tot[2] + block_scan(nc, s_buf) - nc;
+      const long long corr0 = s_tot[1] + block_scan(ncorr, s_buf) - ncorr;
+      const long long comp0 = s_tot[2] + block_scan(ncomp, s_buf) - ncomp;
+      const long long slot0 = s_tot[3] + block_scan(nslot, s_buf) - nslot;
       const int count = (int)(p.N - base < kSchedThreads ? p.N - base : kSchedThreads);
       if (pass == 1) {
         s_start[tid] = (int)start;
         s_len[tid] = (int)len;
         s_nseg[tid] = (int)nseg;
         s_incl[tid] = (int)incl;
-        s_seg0[tid] = seg0;
-        s_q0[tid] = q0;
-        s_c0[tid] = (int)c0;
+        s_run0[tid] = run0;
+        s_corr0[tid] = corr0;
+        s_comp0[tid] = (int)comp0;
+        s_slot0[tid] = slot0;
         __syncthreads();
-        // every (head, segment) of this tile's sequences, spread over all threads
-        const long long tile_segs = s_incl[count - 1];
+        // every (head, run) of this tile's sequences, spread over all threads
+        const long long tile_runs = s_incl[count - 1];
         const long long in_user = p.has_init ? kInUser : kInZero;
-        for (long long idx = tid; idx < tile_segs * H; idx += kSchedThreads) {
-          const long long h = idx / tile_segs;
-          const int sl = (int)(idx - h * tile_segs);
-          int lo = 0, hi = count - 1;                 // first sequence with s_incl > sl
+        for (long long idx = tid; idx < tile_runs * H; idx += kSchedThreads) {
+          const long long h = idx / tile_runs;
+          const int rl = (int)(idx - h * tile_runs);
+          int lo = 0, hi = count - 1;                 // first sequence with s_incl > rl
           while (lo < hi) {
             const int mid = (lo + hi) >> 1;
-            if (s_incl[mid] > sl) hi = mid; else lo = mid + 1;
+            if (s_incl[mid] > rl) hi = mid; else lo = mid + 1;
           }
           const int nl = lo;
           const long long ns = s_nseg[nl];
-          const long long s = sl - (s_incl[nl] - ns);
+          const long long nr = ns + (ns >= 3 ? ns - 2 : 0);
+          const long long r = rl - (s_incl[nl] - nr);
           const long long st0 = s_start[nl], ln = s_len[nl];
-          const long long nq_ = ns >= 2 ? ns - 1 : 0;
-          const long long qb = s_q0[nl] * H + h * nq_;    // q slot of segment 0
-          const long long pb = qb + q_total * H;          // p slot of segment 0
           const long long nn = base + nl;
-          const long long sgi = s_seg0[nl] + s;
-          const long long fi = (sgi < p.cap_ranks ? (long long)p.seg_rank[sgi] : sgi) * H + h;
-          const long long flen = ln <= 0 ? 0 : (ln - s * L < L ? ln - s * L : L);
-          long long in_slot;
-          if (s == 0) in_slot = (ns >= 2 && p.has_init) ? pb : in_user;
-          else in_slot = qb + s - 1;
-          const long long out_slot = (s == ns - 1 && p.has_final) ? kOutUser : kOutNone;
-          if (fi < p.cap_forward)
-            p.forward[fi] = make_item(st0 + s * L, flen, h, kModeForward, nn, in_slot, out_slot, -1);
-          if (s <= ns - 2) {
-            const long long qs = qb + s, ps = pb + s;
-            if (ps < p.cap_phase1 && ps < p.cap_slots) {
-              p.phase1[qs] = make_item(st0 + s * L, L, h, kModeLocal, nn, s == 0 ? in_user : kInZero, qs,
-                                       (s == 0 && p.has_init) ? ps : -1);
-              p.phase1[ps] = s >= 1 ? make_item(st0 + s * L, L, h, kModeTransition, nn, kInIdentity, ps, -1)
-                                    : make_item(0, -1, h, kModeTransition, nn, kInZero, kOutNone, -1);
+          const long long gr = s_run0[nl] + r;
+          const long long fi = (gr < p.cap_ranks ? (long long)p.seg_rank[gr] : gr) * H + h;
+          const long long qb = s_slot0[nl] * H + h * 2 * (ns - 1);   // Q_0 (split sequences)
+          const bool slots_ok = ns < 2 || qb + 2 * (ns - 1) <= p.cap_slots;
+          if (r < ns) {
+            const long long s = r;
+            const long long flen = ln <= 0 ? 0 : (ln - s * L < L ? ln - s * L : L);
+            long long out_slot;
+            if (ns == 1) out_slot = p.has_final ? kOutUser : kOutNone;
+            else out_slot = (s <= ns - 2 || p.has_final) ? qb + s : kOutNone;
+            if (fi < p.cap_forward && slots_ok)
+              p.forward[fi] = make_item(st0 + s * L, flen, h, kModeForward, nn, s == 0 ? in_user : kInZero, out_slot,
+                                        -1);
+            if (s >= 1) {
+              const long long ci = (s_corr0[nl] + s - 1) * H + h;
+              const bool fin = s == ns - 1 && p.has_final;
+              if (ci < p.cap_correct && slots_ok)
+                p.correct[ci] = make_item(st0 + s * L, flen, h, kModeCorrect, nn, qb + s - 1,
+                                          fin ? kOutUser : kOutNone, fin ? qb + s : -1);
             }
-          }
-          if (s == 0 && ns >= 3) {
-            const long long ci = s_c0[nl] * H + h;
-            if (ci < p.cap_compose) {
-              ComposeItem it;
-              it.head = (int)h;
-              it.first_q_slot = (int)qb;
-              it.first_p_slot = (int)(pb + 1);
-              it.n_steps = (int)(ns - 2);
-              p.compose[ci] = it;
+            if (s == 0 && ns >= 3) {
+              const long long ci = (long long)s_comp0[nl] * H + h;
+              if (ci < p.cap_compose && slots_ok) {
+                ComposeItem it;
+                it.head = (int)h;
+                it.first_q_slot = (int)qb;
+                it.first_p_slot = (int)(qb + ns);
+                it.n_steps = (int)(ns - 2);
+                p.compose[ci] = it;
+              }
             }
+          } else {
+            const long long s = r - ns + 1;   // transition of segment s, 1 <= s <= ns - 2
+            if (fi < p.cap_forward && slots_ok)
+              p.forward[fi] = make_item(st0 + s * L, L, h, kModeTransition, nn, kInIdentity, qb + ns + s - 1, -1);
           }
         }
       }
       __syncthreads();
       if (tid == kSchedThreads - 1) {
-        s_tot[0] = seg0 + nseg;
-        s_tot[1] = q0 + nq;
-        s_tot[2] = c0 + nc;
+        s_tot[0] = run0 + nruns;
+        s_tot[1] = corr0 + ncorr;
+        s_tot[2] = comp0 + ncomp;
+        s_tot[3] = slot0 + nslot;
       }
       __syncthreads();
     }
-    q_total = s_tot[1];
-    __syncthreads();
   }
   if (tid == 0) {
     const long long nf = s_tot[0] * H;
-    const long long n1 = 2 * s_tot[1] * H;
+    const long long nc = s_tot[1] * H;
     const long long ncm = s_tot[2] * H;
     p.hdr->n_forward = (int)(nf < p.cap_forward ? nf : p.cap_forward);
-    p.hdr->n_phase1 = (int)(n1 < p.cap_phase1 ? n1 : p.cap_phase1);
+    p.hdr->n_correct = (int)(nc < p.cap_correct ? nc : p.cap_correct);
     p.hdr->n_compose = (int)(ncm < p.cap_compose ? ncm : p.cap_compose);
     p.hdr->err = s_err ? kErrBadSeqlens : 0;
   }
@@ -316,10 +332,13 @@ __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const Comp
   float* slots = p.ws_states;
   auto P_src = [&](int st) { return slots + (size_t)(ci.first_p_slot + st - 1) * 16384; };
   auto Q_row0 = [&](int st) { return slots + (size_t)(ci.first_q_slot + st) * 16384 + (size_t)v0 * 128; };
+  // a transition its run found exactly zero: S_{s+1} = Q_s, already in place
+  auto zero_p = [&](int st) { return p.zero_flags[ci.first_p_slot + st - 1] != 0; };
   auto fetch = [&](int st) {   // operands of step st into buffer st & 1 (thread 0)
     uint64_t* b = &bar[st & 1];
-    mbar_arrive_expect_tx(b, kPBytes + kQBytes);
-    bulk_load_g2s(&S.P[st & 1][0][0], P_src(st), kPBytes, b);
+    const bool z = zero_p(st);
+    mbar_arrive_expect_tx(b, (z ? 0u : kPBytes) + kQBytes);
+    if (!z) bulk_load_g2s(&S.P[st & 1][0][0], P_src(st), kPBytes, b);
     bulk_load_g2s(&S.Q[st & 1][0][0], Q_row0(st), kQBytes, b);
   };
   if (tid == 0) {
@@ -345,17 +364,20 @@ __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const Comp
     float2 acc[kRowsPerThread];
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) acc[i] = *reinterpret_cast<const float2*>(&S.Q[b][r4 + i][k2]);
+    const bool z = zero_p(st);
+    if (!z) {
 #pragma unroll 8
-    for (int m = 0; m < 128; ++m) {
-      const float2 pm = *reinterpret_cast<const float2*>(&S.P[b][m][k2]);
+      for (int m = 0; m < 128; ++m) {
+        const float2 pm = *reinterpret_cast<const float2*>(&S.P[b][m][k2]);
 #pragma unroll
-      for (int i4 = 0; i4 < kRowsPerThread; i4 += 4) {
-        const float4 sv = *reinterpret_cast<const float4*>(&S.St[m][r4 + i4]);
-        const float s4[4] = {sv.x, sv.y, sv.z, sv.w};
+        for (int i4 = 0; i4 < kRowsPerThread; i4 += 4) {
+          const float4 sv = *reinterpret_cast<const float4*>(&S.St[m][r4 + i4]);
+          const float s4[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[i4 + i].x = fmaf(s4[i], pm.x, acc[i4 + i].x);
-          acc[i4 + i].y = fmaf(s4[i], pm.y, acc[i4 + i].y);
+          for (int i = 0; i < 4; ++i) {
+            acc[i4 + i].x = fmaf(s4[i], pm.x, acc[i4 + i].x);
+            acc[i4 + i].y = fmaf(s4[i], pm.y, acc[i4 + i].y);
+          }
         }
       }
     }
@@ -368,8 +390,10 @@ __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const Comp
       *reinterpret_cast<float4*>(&S.St[k2 + 1][r4 + i4]) =
           make_float4(acc[i4].y, acc[i4 + 1].y, acc[i4 + 2].y, acc[i4 + 3].y);
     }
+    if (!z) {
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) *reinterpret_cast<float2*>(&Q[(size_t)(r4 + i) * 128 + k2]) = acc[i];
+      for (int i = 0; i < kRowsPerThread; ++i) *reinterpret_cast<float2*>(&Q[(size_t)(r4 + i) * 128 + k2]) = acc[i];
+    }
     if (tid == 0 && st + 2 <= ci.n_steps) {
       fence_proxy_async_smem();   // the generic reads of buffer b are ordered before the refill
       fetch(st + 2);

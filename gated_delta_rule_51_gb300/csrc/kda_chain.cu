@@ -573,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       bar_d1_full[2], bar_d2_full, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  __shared__ volatile int s_nz[2][4];   // per chunk parity: epilogue warp q4 saw a nonzero state
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -663,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         pair_bar(pair);
         if (!(sc.okf[iter & 1][0] && sc.okf[iter & 1][1])) break;
         prologue_pair_chunk<kFlags & kValidFlags>(S.st[s], S.sm[s], sc, pair, w, nv, p.err, nr, lbl2, dtb, cb0, cb1, lane,
-                                    it.mode != kModeTransition);
+                                    it.mode == kModeForward);
         if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
     } else {
@@ -681,8 +682,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       const uint32_t tD1 = tmem + kColD1 + loff;
       const int h = head;
       const size_t srow = ((size_t)it.seq * p.H + h) * vstride + (size_t)kDimV * vblk + vrow;   // state row (n, h, v)
-      const bool with_u = it.mode != kModeTransition;
-      const bool with_o = it.mode == kModeForward;
+      // the correction and transition runs take v as zero (no U); the transition writes no outputs
+      const bool with_u = it.mode == kModeForward;
+      const bool with_o = it.mode != kModeTransition;
+      const bool correct = it.mode == kModeCorrect;
+      // both v-free runs stop once their state is exactly zero (it then stays zero)
+      const bool track_zero = it.mode != kModeForward;
       // instruction and shared-memory descriptors (stage s adds s * sizeof(Stage))
       const uint32_t id_u = idesc_bf16_f32(128, 32, 1, 0);
       const uint32_t id_x = idesc_bf16_f32(128, 32, 0, 0);
@@ -737,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
       };
       // TMA loads of chunk c into stage c % kStages (lane 0 of warp kWarpTma only)
       const bool tma_thread = (warp == kWarpTma) && (lane == 0);
-      const bool load_v = it.mode != kModeTransition;
+      const bool load_v = with_u;
       int tma_issued = 0;
       auto issue_tma = [&](int c) {
         const int s = c % kStages;
@@ -818,12 +823,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
 #pragma unroll
             for (int t = 0; t < 32; ++t) s[t] = 0.f;
           }
-          if (it.aux_slot >= 0) {
-            float4* dst = reinterpret_cast<float4*>(p.ws_states + (size_t)it.aux_slot * 16384 +
-                                                    (size_t)vrow * 128 + 32 * j);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) dst[t] = make_float4(s[4 * t], s[4 * t + 1], s[4 * t + 2], s[4 * t + 3]);
-          }
           uint32_t pk[16];
 #pragma unroll
           for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(s[2 * t], s[2 * t + 1]);
@@ -845,6 +844,47 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         }
       }
       __syncwarp();
+      // Final state of the run's last chunk, column group j of row vrow: a workspace slot, or the
+      // caller's tensor in its dtype.  A correction run adds its local final state (aux slot).
+      auto write_final = [&](int j, uint32_t (&r)[32]) {
+        if (correct && it.aux_slot >= 0) {
+          const float4* a = reinterpret_cast<const float4*>(p.ws_states + (size_t)it.aux_slot * 16384 +
+                                                            (size_t)vrow * 128 + 32 * j);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const float4 x = a[t];
+            r[4 * t] = __float_as_uint(__uint_as_float(r[4 * t]) + x.x);
+            r[4 * t + 1] = __float_as_uint(__uint_as_float(r[4 * t + 1]) + x.y);
+            r[4 * t + 2] = __float_as_uint(__uint_as_float(r[4 * t + 2]) + x.z);
+            r[4 * t + 3] = __float_as_uint(__uint_as_float(r[4 * t + 3]) + x.w);
+          }
+        }
+        if (it.out_slot >= 0) {
+          float4* dst = reinterpret_cast<float4*>(p.ws_states + (size_t)it.out_slot * 16384 +
+                                                  (size_t)vrow * 128 + 32 * j);
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
+                                 __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
+        } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2 && vrow < vrows &&
+                   32 * j < kdim) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * kdim + 32 * j);
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
+                                 __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
+        } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1 && vrow < vrows &&
+                   32 * j < kdim) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * kdim + 32 * j);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            dst[t] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * t]), __uint_as_float(r[8 * t + 1])),
+                                pack_bf16x2(__uint_as_float(r[8 * t + 2]), __uint_as_float(r[8 * t + 3])),
+                                pack_bf16x2(__uint_as_float(r[8 * t + 4]), __uint_as_float(r[8 * t + 5])),
+                                pack_bf16x2(__uint_as_float(r[8 * t + 6]), __uint_as_float(r[8 * t + 7])));
+        }
+      };
+      bool stopped = false;   // a correction or transition run whose state became exactly zero
       for (int c = 0; c < nchunks; ++c) {
         const int b = c & 1;
         const int nv = min(kChunk, it.len - c * kChunk);
@@ -879,6 +919,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         if (!last)
           ok = ok && __all_sync(0xffffffffu,
                                 mbar_wait(&bar_op_full[(c + 1) % kStages], ((c + 1) / kStages) & 1, ab));
+        uint32_t nz = 0u;   // any nonzero bit of S' in this thread's row
         if (ok) {
           tc_fence_after();
           const StageSmall& stn = S.sm[(c + 1) % kStages];
@@ -888,6 +929,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
             tmem_ld32(tS + 32u * j, r);
             tmem_ld_wait();
             if (!last) {
+              if (track_zero) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) nz |= r[t] & 0x7fffffffu;
+              }
               uint32_t pk[16];
 #pragma unroll
               for (int t = 0; t < 16; ++t)
@@ -906,77 +951,93 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
                 r[4 * t + 3] = __float_as_uint(a3);
               }
               tmem_st32(tS + 32u * j, r);
-            } else if (it.out_slot >= 0) {
-              float4* dst = reinterpret_cast<float4*>(p.ws_states + (size_t)it.out_slot * 16384 +
-                                                      (size_t)vrow * 128 + 32 * j);
-#pragma unroll
-              for (int t = 0; t < 8; ++t)
-                dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
-                                     __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 2 && vrow < vrows &&
-                       32 * j < kdim) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.final_state) + srow * kdim + 32 * j);
-#pragma unroll
-              for (int t = 0; t < 8; ++t)
-                dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
-                                     __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
-            } else if (it.out_slot == kOutUser && p.final_state != nullptr && p.final_dtype == 1 && vrow < vrows &&
-                       32 * j < kdim) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.final_state) + srow * kdim + 32 * j);
-#pragma unroll
-              for (int t = 0; t < 4; ++t)
-                dst[t] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * t]), __uint_as_float(r[8 * t + 1])),
-                                    pack_bf16x2(__uint_as_float(r[8 * t + 2]), __uint_as_float(r[8 * t + 3])),
-                                    pack_bf16x2(__uint_as_float(r[8 * t + 4]), __uint_as_float(r[8 * t + 5])),
-                                    pack_bf16x2(__uint_as_float(r[8 * t + 6]), __uint_as_float(r[8 * t + 7])));
+            } else {
+              write_final(j, r);
             }
           }
           if (!last) tmem_st_wait();
         }
+        // Zero vote of the four epilogue warps.  Every warp writes its entry (a warp that has
+        // given up votes nonzero), so all four take the same decision after the barrier below.
+        if (track_zero && !last) {
+          const int any_nz = __any_sync(0xffffffffu, nz != 0u) ? 1 : 0;
+          if (lane == 0) s_nz[b][q4] = ok ? any_nz : 1;
+        }
         tc_fence_before();
         named_bar(kBarEpi, 128);
-        if (!last && leader && !s_abort) {
+        const bool stop_now =
+            track_zero && !last && (s_nz[b][0] | s_nz[b][1] | s_nz[b][2] | s_nz[b][3]) == 0;
+        if (stop_now && leader) s_abort = 1;   // no error: it tells the other roles to unwind
+        if (!last && !stop_now && leader && !s_abort) {
           tc_fence_after();
           const int c1 = c + 1;
           if (mbar_wait(&bar_full[c1 % kStages], (c1 / kStages) & 1, ab)) issue_gemm1(c1);
         }
         // stage c % kStages is free: this warp saw every MMA of chunk c complete (bar_d2_full)
-        if (tma_thread && ok && !s_abort && c + kStages < nchunks) issue_tma(c + kStages);
+        if (tma_thread && ok && !stop_now && !s_abort && c + kStages < nchunks) issue_tma(c + kStages);
         __syncwarp();
         // ---- outputs of this chunk (overlaps the next S-side GEMM): each warp stages its
         //      32 output columns of the 16 token rows in shared memory, then writes them as
-        //      16-byte pieces, four per row (64 contiguous bytes)
+        //      16-byte pieces, four per row (64 contiguous bytes).  A correction run adds its
+        //      term to the outputs its segment's forward run wrote.
         if (with_o && ok) {
           uint32_t r[16];
           tmem_ld16(tD1 + 32u * b + 16u, r);
           tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            *reinterpret_cast<uint16_t*>(&S.ostage[i][2 * vrow]) =
-                __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * __uint_as_float(r[i])));
-          __syncwarp();
           const size_t row_elems = (size_t)p.H * vstride;
           uint16_t* obase = p.out + ((size_t)(it.row0 + c * kChunk) * p.H + h) * vstride + (size_t)kDimV * vblk;
-          if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0) {
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-              const int q = lane + 32 * rr, i = q >> 2, seg = q & 3;
-              if (i < nv && 32 * q4 < vrows)
-                *reinterpret_cast<uint4*>(obase + (size_t)i * row_elems + 32 * q4 + 8 * seg) =
-                    *reinterpret_cast<const uint4*>(&S.ostage[i][64 * q4 + 16 * seg]);
-            }
+          if (correct) {
+            if (vrow < vrows)
+              for (int i = 0; i < nv; ++i) {
+                uint16_t* o = obase + (size_t)i * row_elems + vrow;
+                *o = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_f32(*o) + p.scale * __uint_as_float(r[i])));
+              }
           } else {
-            for (int i = 0; i < nv && vrow < vrows; ++i)
-              obase[(size_t)i * row_elems + vrow] = *reinterpret_cast<const uint16_t*>(&S.ostage[i][2 * vrow]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              *reinterpret_cast<uint16_t*>(&S.ostage[i][2 * vrow]) =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * __uint_as_float(r[i])));
+            __syncwarp();
+            if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0) {
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                const int q = lane + 32 * rr, i = q >> 2, seg = q & 3;
+                if (i < nv && 32 * q4 < vrows)
+                  *reinterpret_cast<uint4*>(obase + (size_t)i * row_elems + 32 * q4 + 8 * seg) =
+                      *reinterpret_cast<const uint4*>(&S.ostage[i][64 * q4 + 16 * seg]);
+              }
+            } else {
+              for (int i = 0; i < nv && vrow < vrows; ++i)
+                obase[(size_t)i * row_elems + vrow] = *reinterpret_cast<const uint16_t*>(&S.ostage[i][2 * vrow]);
+            }
+            __syncwarp();   // the staging rows are rewritten by the next chunk
           }
-          __syncwarp();   // the staging rows are rewritten by the next chunk
+        }
+        if (stop_now) {   // uniform across the four warps
+          stopped = true;
+          break;
         }
       }
-      if (leader && s_abort && issued_any) {  // wait for MMAs in flight before TMEM is released
+      // a correction run that stopped early ends with a zero difference: its final state is
+      // the local one from its aux slot
+      if (stopped && correct && it.out_slot != kOutNone) {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) r[t] = 0u;
+          write_final(j, r);
+        }
+      }
+      // a transition run records whether it ended exactly zero (then its slot is not written)
+      if (it.mode == kModeTransition && leader && it.out_slot >= 0)
+        p.zero_flags[it.out_slot] = stopped ? 1 : 0;
+      const bool unwind = s_abort || stopped;
+      if (leader && unwind && issued_any) {  // wait for MMAs in flight before TMEM is released
         tc_commit(&bar_drain);
         mbar_wait_drain(&bar_drain, 0);
       }
-      if (tma_thread && s_abort) {  // let loads in flight land before the CTA exits
+      if (tma_thread && unwind) {  // let loads in flight land before the CTA exits
         for (int c = (tma_issued > kStages ? tma_issued - kStages : 0); c < tma_issued; ++c)
           mbar_wait_drain(&bar_full[c % kStages], (c / kStages) & 1);
       }
@@ -984,6 +1045,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
     }
   } else if (warp >= kWarpEpi0) {
     // zero-length run: the final state equals the initial state
+    if (it.mode == kModeTransition && threadIdx.x == kWarpEpi0 * 32 && it.out_slot >= 0)
+      p.zero_flags[it.out_slot] = 0;   // the identity
     const int q4 = warp & 3;
     const int vrow = q4 * 32 + lane;
     const size_t srow = ((size_t)it.seq * p.H + head) * vstride + (size_t)kDimV * vblk + vrow;
@@ -995,6 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_chain_kernel(const __grid_con
         x = static_cast<const float*>(p.init_state)[srow * kdim + t];
       else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1 && vrow < vrows && t < kdim)
         x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.init_state)[srow * kdim + t]);
+      if (it.mode == kModeCorrect && it.aux_slot >= 0) x += p.ws_states[(size_t)it.aux_slot * 16384 + (size_t)vrow * 128 + t];
       if (it.out_slot >= 0) p.ws_states[(size_t)it.out_slot * 16384 + (size_t)vrow * 128 + t] = x;
       else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2 && vrow < vrows && t < kdim)
         static_cast<float*>(p.final_state)[srow * kdim + t] = x;

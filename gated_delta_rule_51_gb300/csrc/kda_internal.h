@@ -12,7 +12,14 @@ constexpr int kDimK = 128;
 constexpr int kDimV = 128;
 
 // One unit of sequential work: a run of chunks of one (sequence, head).
-enum : int { kModeForward = 0, kModeLocal = 1, kModeTransition = 2 };
+//   kModeForward     outputs written, state carried from in_slot to out_slot
+//   kModeCorrect     v taken as zero: propagates the difference D between a segment's true
+//                    entering state and the zero state its forward run started from; adds
+//                    scale * q^T D to the outputs that run wrote and stops once D is exactly
+//                    zero in fp32 (it then stays zero)
+//   kModeTransition  v taken as zero from the identity: the segment's transition matrix,
+//                    stopped (and flagged zero) once it is exactly zero in fp32
+enum : int { kModeForward = 0, kModeCorrect = 1, kModeTransition = 2 };
 // in_slot values below zero:
 enum : int { kInZero = -1, kInIdentity = -2, kInUser = -3 };
 // out_slot values below zero:
@@ -22,18 +29,19 @@ struct WorkItem {
   int row0;      // first token row in the flattened [B*T] token index
   int len;       // tokens in this run (may be 0)
   int head;
-  int mode;      // kModeForward / kModeLocal / kModeTransition
+  int mode;      // kModeForward / kModeCorrect / kModeTransition
   int seq;       // sequence index n (user state row)
   int in_slot;   // initial state source
   int out_slot;  // final state target
-  int aux_slot;  // >= 0: also store the (undecayed) initial state there
+  int aux_slot;  // kModeCorrect with a final state: the slot holding the segment's local final
+                 // state (from zero), which the run's own final difference is added to
 };
 
 // Device-side work list built by the scheduling kernel inside the workspace.
 struct WorkHeader {
   int err;             // error word (bit flags, see kda_device.cuh)
-  int n_phase1;        // number of segment items of the first phase
-  int n_forward;       // number of forward items
+  int n_correct;       // number of correction items (the last phase)
+  int n_forward;       // number of items of the first phase (forward and transition runs)
   int n_compose;       // number of (sequence, head) carry chains to compose
   int take[3];         // forward runs handed out: total, from the head, from the tail
   int pad;
@@ -46,7 +54,8 @@ struct ComposeItem {
   int first_p_slot;   // slot of the transition of segment 1 (P_1)
   int n_steps;        // number of compositions (segments 1 .. n_seg-2)
   // step s (1 <= s <= n_steps) uses P slot first_p_slot + (s-1) and Q slots
-  // first_q_slot + s - 1 (input) and first_q_slot + s (carry, overwritten)
+  // first_q_slot + s - 1 (input) and first_q_slot + s (carry, overwritten); a P slot
+  // flagged zero (ComposeParams::zero_flags) is neither read nor multiplied
 };
 
 struct ChainParams {
@@ -59,6 +68,7 @@ struct ChainParams {
   const void* init_state;              // [N, H, 128, 128] or null
   void* final_state;                   // [N, H, 128, 128] or null
   float* ws_states;                    // workspace state slots, 128*128 fp32 each
+  int* zero_flags;                     // per slot: 1 when a transition run found it exactly zero
   const WorkItem* items;
   const int* item_count;
   int* take;                           // non-null: CTAs pick items by SM pairing (WorkHeader::take)
@@ -78,6 +88,7 @@ struct ChainParams {
 
 struct ComposeParams {
   float* ws_states;
+  const int* zero_flags;
   const ComposeItem* items;
   const int* item_count;
 };
@@ -91,10 +102,10 @@ struct ScheduleParams {
   int has_init;
   int has_final;
   WorkHeader* hdr;
-  WorkItem* phase1;
+  WorkItem* correct;
   WorkItem* forward;
   ComposeItem* compose;
-  long long cap_phase1, cap_forward, cap_compose, cap_slots;
+  long long cap_correct, cap_forward, cap_compose, cap_slots;
   int* seg_rank;              // scratch: position of each forward run's segment in the list
   long long cap_ranks;
   int* sm_arrivals;           // [kMaxSmIds], zeroed here for the forward launch

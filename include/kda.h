@@ -180,8 +180,9 @@ KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t st
  * Measurement aid (no counterpart in flash_kda): while `events` is non-NULL,
  * every kda_fwd records events[i] (cudaEvent_t handles owned by the caller) on
  * its stream right after its i-th launch -- 0: work-list scheduling, 1: the
- * segment carry/transition runs, 2: carry composition, 3: the forward runs --
- * so each phase can be timed with cudaEventElapsedTime.  n_events must be 4.
+ * forward runs (with the segment transition runs), 2: carry composition, 3: the
+ * segment corrections -- so each phase can be timed with cudaEventElapsedTime
+ * (phases a call does not need are recorded empty).  n_events must be 4.
  * Pass NULL to stop.  The setting is process-wide and not thread-safe.
  */
 KDA_API kda_status kda_set_profile_events(void *const *events, int n_events);
@@ -189,7 +190,7 @@ KDA_API kda_status kda_set_profile_events(void *const *events, int n_events);
 /*
  * Measurement aid (no counterpart in flash_kda): the number of kernels the
  * calling thread's most recent successful kda_fwd enqueued (2 to 4: work-list
- * scheduling, segment runs, carry composition, forward runs).
+ * scheduling, forward runs, carry composition, segment corrections).
  */
 KDA_API int kda_last_launch_count(void);
 

@@ -96,6 +96,42 @@ def test_segment_scan_matches_oracle(seg_tokens, seg):
     _compare(x2, torch.bfloat16, f"seg={seg} bf16")
 
 
+@pytest.mark.parametrize("lb,seg,state_bound", [(-0.1, 48, 1e-3), (-0.1, 512, 1e-3), (0.0, 64, 2.5e-3)])
+def test_segment_scan_with_a_gate_that_keeps_its_state(seg_tokens, lb, seg, state_bound):
+    """A gate that barely decays (lower_bound near 0): within a segment the transition never
+    becomes zero in fp32, so the transition and correction runs go through every chunk and the
+    composition multiplies every transition.  At lower_bound = 0 the state bound is the
+    no-decay plateau of test_weak_and_no_decay_long_runs."""
+    seg_tokens(seg)
+    lens = [1500, 17, 700, 64]
+    x = random_case(1, sum(lens), 2, seed=21 + seg, lens=lens, lb=lb)
+    out, fin = run_gpu(x)
+    ref_out, ref_fin = run_oracle(x)
+    check_out(out, ref_out.reshape(sum(lens), 2, 128), label=f"keep lb={lb} seg={seg}")
+    from tests.gpu_helpers import _report, rel_fro
+
+    rf = rel_fro(fin.double().cpu().numpy(), ref_fin)
+    _report(f"keep lb={lb} seg={seg}", "state_rel_fro_float32", rf)
+    assert rf <= state_bound, f"state rel-Fro {rf:.3e} > {state_bound}"
+
+
+def test_segment_scan_heads_that_forget_and_heads_that_keep(seg_tokens):
+    """In one call: head 0 decays slowly (A_log 0, dt_bias -4.6: sigmoid(g - 4.6) is about
+    0.01, a decay near exp(-0.05) per token), so within a 64-token segment its transition never
+    reaches zero and its transition and correction runs go to the end; head 1 forgets within a
+    few chunks, so its runs stop early.  Both must match the oracle."""
+    seg_tokens(64)
+    lens = [900, 300, 33]
+    x = random_case(1, sum(lens), 2, seed=31, lens=lens, lb=-5.0)
+    x["A_log"][0] = 0.0
+    x["dt_bias"][0].fill_(-4.6)
+    _compare(x, torch.float32, "forget and keep")
+    x2 = random_case(1, sum(lens), 2, seed=32, lens=lens, lb=-5.0, init_dtype=None)
+    x2["A_log"][1] = 0.0
+    x2["dt_bias"][1].fill_(-4.6)
+    _compare(x2, torch.float32, "forget and keep, no initial state")
+
+
 def test_segment_scan_without_initial_state(seg_tokens):
     seg_tokens(32)
     x = random_case(2, 200, 2, seed=13, init_dtype=None)
