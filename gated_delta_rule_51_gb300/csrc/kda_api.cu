@@ -267,7 +267,7 @@ kda_status kda_workspace_size(const kda_shape* shape, size_t* bytes) {
 
 // kda_flags: known bits only, and the preactivated and softplus gates exclude each other
 static bool valid_flags(unsigned flags) {
-  if (flags & ~kda::kValidFlags) return false;
+  if (flags & ~(kda::kValidFlags | (unsigned)KDA_PRECISE_STATE)) return false;
   return !((flags & KDA_GATE_PREACTIVATED) && (flags & KDA_GATE_SOFTPLUS));
 }
 // only the in-kernel safe gate reads lower_bound
@@ -317,7 +317,7 @@ kda_status kda_decode(const kda_shape* shape, const void* q, const void* k, cons
   dp.kdim = (int)s.K;
   dp.scale = scale;
   dp.lower_bound = lower_bound;
-  dp.flags = (int)flags;
+  dp.flags = (int)(flags & kValidFlags);
   if (launch_decode(dp, reinterpret_cast<cudaStream_t>(stream_)) != cudaSuccess) return KDA_ERR_CUDA;
   return KDA_OK;
 }
@@ -447,7 +447,11 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   cp.final_dtype = (int)final_dtype;
   cp.scale = scale;
   cp.lower_bound = lower_bound;
-  cp.flags = (int)flags;
+  cp.flags = (int)(flags & kValidFlags);
+  // the state read as bf16 hi + lo where a gate may keep it (no decay fades the rounding
+  // of a single bf16 copy): asked for, the safe gate near lower_bound 0, or a gate whose
+  // decay the host cannot bound
+  cp.precise = ((flags & KDA_PRECISE_STATE) != 0 || !uses_lower_bound(flags) || lower_bound > -0.25f) ? 1 : 0;
   cp.take = nullptr;
   cp.sm_arrivals = nullptr;
 
@@ -595,7 +599,7 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
   p.BT = s.B * s.T;
   p.N = (int)s.N;
   p.H = (int)s.H;
-  p.flags = (int)flags;
+  p.flags = (int)(flags & kValidFlags);
   p.nblk = L.nblk;
   p.scale = scale;
   p.lower_bound = lower_bound;

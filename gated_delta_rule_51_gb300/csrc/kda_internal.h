@@ -84,6 +84,7 @@ struct ChainParams {
   int kdim;                            // K: 128, or 64 (channels 64-127 then run as zeros)
   int vrows;                           // value rows a chain carries to the caller: 128, or 64 for V = 64
                                        // (rows 64-127 then stay zero: v's second 64 columns read as 0)
+  int precise;                         // 1: the precise-state kernels (state, W read as bf16 hi + lo)
 };
 
 struct ComposeParams {
@@ -117,8 +118,10 @@ constexpr int kBetaPreactivated = 2;
 constexpr int kNoQkL2Norm = 4;
 constexpr int kGateSoftplus = 8;   // ghat = -exp(A_log) softplus(g + dt_bias), no lower bound
 constexpr unsigned kValidFlags = 15;
-// chain-kernel variant bit (not a caller flag): K = 64 or V = 64, the padded shapes
+// chain-kernel variant bits (not caller flags): K = 64 or V = 64, the padded shapes; and the
+// precise-state kernels (one CTA per SM)
 constexpr int kChainPadded = 16;
+constexpr int kChainPrecise = 32;
 
 struct DecodeParams {
   const uint16_t *q, *k, *v, *g, *beta;  // bf16 [B, T, H, K] (v [B, T, H, V]; beta [B, T, H], logits)
@@ -169,10 +172,10 @@ constexpr int kBwdParamStride = 132;      // floats per (block, head): 128 ddt_b
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s);
+cudaError_t launch_chain_precise(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_compose(const ComposeParams& p, int grid, int sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 // phases 0-3: prep, stored-state forward, reverse, chain rule and parameter sums
 cudaError_t launch_bwd(const BwdParams& p, int phase, cudaStream_t s);
-size_t chain_smem_bytes();
 
 }  // namespace kda

@@ -28,6 +28,7 @@ EXPORTED_SYMBOLS = ("kda_status_string", "kda_workspace_size", "kda_fwd", "kda_c
                     "kda_set_profile_events", "kda_last_launch_count", "kda_fwd_static_workspace",
                     "kda_decode", "kda_fwd_ex", "kda_bwd_workspace_size", "kda_bwd")
 KDA_GATE_PREACTIVATED, KDA_BETA_PREACTIVATED, KDA_NO_QK_L2NORM, KDA_GATE_SOFTPLUS = 1, 2, 4, 8
+KDA_PRECISE_STATE = 16
 
 
 class kda_shape(ctypes.Structure):
@@ -152,7 +153,7 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
         final_state=None, cu_seqlens=None, workspace: Optional[torch.Tensor] = None,
         stream: Optional[torch.cuda.Stream] = None, use_gate_in_kernel: bool = True,
         use_beta_sigmoid_in_kernel: bool = True, use_qk_l2norm_in_kernel: bool = True,
-        safe_gate: bool = True):
+        safe_gate: bool = True, precise_state: bool = False):
     """KDA forward on the GPU; writes ``out`` (and ``final_state``) and returns them.
 
     q, k, g: [B,T,H,K] bf16 with K = 64 or 128; v, out: [B,T,H,V] bf16 with V = 64, 128
@@ -167,6 +168,8 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
     either of those two gates, a 16-token chunk whose decay leaves the range the
     chunked form factors exactly (a sum of ghat below -173 on some channel) sets
     the gate-range bit of the workspace's error word (check_device_error).
+    precise_state=True reads the carried state as a bf16 pair (KDA_PRECISE_STATE); the
+    library already does so for lower_bound > -0.25 and for the two gates without a bound.
     """
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
@@ -185,6 +188,8 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
             continue
         _check(t, name, dt, shp, dev)
     flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate)
+    if precise_state:
+        flags |= KDA_PRECISE_STATE
     for name, t in (("initial_state", initial_state), ("final_state", final_state)):
         if t is not None:
             _check(t, name, t.dtype, (N, H, V, K), dev)

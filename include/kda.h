@@ -88,12 +88,25 @@ typedef enum { KDA_STATE_NONE = 0, KDA_STATE_BF16 = 1, KDA_STATE_FP32 = 2 } kda_
  * preactivated or softplus gate that does sets KDA_ERR_GATE_RANGE in the error
  * word, and the outputs of that call are then unspecified.  kda_decode runs the
  * token recurrence itself and takes any gate values.
+ *
+ * One more flag is not a step of the method but a precision request:
+ *   KDA_PRECISE_STATE     : the chunked form reads the carried state as a bf16 pair
+ *                           (hi + lo) instead of one bf16 copy, so the rounding of that
+ *                           copy (2^-9 relative, fed back every chunk) no longer builds
+ *                           up when the gate hardly decays.  Runs one CTA per SM
+ *                           (about half the throughput).  kda_fwd_ex turns it on by
+ *                           itself for the safe gate with lower_bound > -0.25 and for
+ *                           the preactivated and softplus gates, whose decay it cannot
+ *                           bound; with a decaying gate the single copy's error fades
+ *                           within a few chunks and the flag changes little.
+ *                           kda_decode and kda_bwd compute in fp32 and ignore it.
  */
 typedef enum {
     KDA_GATE_PREACTIVATED = 1,
     KDA_BETA_PREACTIVATED = 2,
     KDA_NO_QK_L2NORM = 4,
-    KDA_GATE_SOFTPLUS = 8
+    KDA_GATE_SOFTPLUS = 8,
+    KDA_PRECISE_STATE = 16
 } kda_flags;
 
 /*

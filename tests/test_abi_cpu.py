@@ -123,7 +123,7 @@ def _decode_call(shape, q=FAKE, out=FAKE, A_log=FAKE, state=FAKE, dtype=2, lb=-1
     (dict(shape=kda.make_shape(4, 1, 2, 4), q=0), 1),
     (dict(shape=kda.make_shape(4, 1, 2, 4), out=FAKE + 1), 1),       # 2-byte aligned tokens
     (dict(shape=kda.make_shape(4, 1, 2, 4), A_log=FAKE + 2), 1),
-    (dict(shape=kda.make_shape(4, 1, 2, 4), flags=16), 1),           # unknown flag
+    (dict(shape=kda.make_shape(4, 1, 2, 4), flags=32), 1),           # unknown flag
     (dict(shape=kda.make_shape(4, 1, 2, 4), flags=9), 1),            # preactivated and softplus gates
 ])
 def test_decode_host_side_argument_errors(case, expected):
@@ -150,7 +150,8 @@ def _fwd_ex_call(flags, A_log=FAKE, lb=-1.0):
 
 
 def test_fwd_ex_flags_on_the_host():
-    assert _fwd_ex_call(16) == 1                      # unknown flag
+    assert _fwd_ex_call(32) == 1                      # unknown flag
+    assert _fwd_ex_call(16) in (4, 5)                 # KDA_PRECISE_STATE passes the host checks
     assert _fwd_ex_call(9) == 1                       # preactivated and softplus gates exclude each other
     assert _fwd_ex_call(8, lb=9.0) in (4, 5)          # the softplus gate reads no lower bound
     assert _fwd_ex_call(8, A_log=0) == 1              # but needs A_log and dt_bias

@@ -190,3 +190,34 @@ def test_v256_heads():
     torch.cuda.synchronize()
     check_out(o, d_out.reshape(8, 2, 256), label="decode softplus V=256")
     check_state(state, d_fin, label="decode softplus V=256")
+
+
+@pytest.mark.parametrize("T", [2000, 8192])
+def test_weak_decay_keeps_the_state_bound(T):
+    """Gates that hardly decay: the softplus gate at A_log = -6 (a decay near exp(-0.0017) per
+    token) and a preactivated g in [-0.01, 0].  The state then keeps every chunk's rounding
+    unless it is read as a bf16 pair, which the library does for these gates; the fp32 final
+    state meets 1e-3."""
+    import oracle
+    from gated_delta_rule_51_gb300 import kda
+
+    x = _shift_g(random_case(1, T, 2, seed=1300 + T), 0.0, a_log=-6.0)
+    ref_out, ref_fin = _oracle(x)
+    out, fin = _gpu(x)
+    check_out(out, ref_out.reshape(T, 2, 128), label=f"softplus A_log -6 T={T}")
+    check_state(fin, ref_fin, label=f"softplus A_log -6 T={T}")
+
+    y = random_case(1, T, 2, seed=1310 + T)
+    gen = torch.Generator(device="cuda").manual_seed(1320 + T)
+    y["g"] = (-0.01 * torch.rand(y["g"].shape, generator=gen, device="cuda")).to(torch.bfloat16)
+    yc = to_cpu(y)
+    ref_out, ref_fin = oracle.kda_forward(yc["q"], yc["k"], yc["v"], yc["g"], yc["beta"], yc["scale"], yc["A_log"],
+                                          yc["dt_bias"], yc["lower_bound"], yc["initial_state"],
+                                          use_gate_in_kernel=False)
+    out = torch.full_like(y["v"], float("nan"))
+    fin = torch.full_like(y["initial_state"], float("nan"))
+    kda.fwd(y["q"], y["k"], y["v"], y["g"], y["beta"], y["scale"], out, None, None, 0.0,
+            initial_state=y["initial_state"], final_state=fin, use_gate_in_kernel=False)
+    torch.cuda.synchronize()
+    check_out(out, ref_out.reshape(T, 2, 128), label=f"preactivated [-0.01, 0] T={T}")
+    check_state(fin, ref_fin, label=f"preactivated [-0.01, 0] T={T}")
