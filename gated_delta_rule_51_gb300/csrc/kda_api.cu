@@ -250,7 +250,7 @@ const char* kda_status_string(kda_status s) {
     case KDA_ERR_CUDA: return "CUDA error";
     case KDA_ERR_TIMEOUT: return "a device-side wait timed out";
     case KDA_ERR_BAD_SEQLENS: return "malformed cu_seqlens";
-    case KDA_ERR_GATE_RANGE: return "a 16-token chunk's decay left the range the chunked form factors exactly";
+    case KDA_ERR_GATE_RANGE: return "a chunk's decay left the chunked form's range (reserved; no longer raised)";
   }
   return "unknown status";
 }

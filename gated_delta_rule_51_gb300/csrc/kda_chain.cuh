@@ -310,6 +310,12 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, uint8_t* wl, Stag
           const float lv = valid ? lbl2 : 0.f;
           fmul2(r0, r1, lv, lv);
         }
+        // (a token decaying by 2^-1000 or more wipes every factor that spans it to an fp32
+        // zero: clamping its log-decay there changes no result and keeps sums finite)
+        if (anchored) {
+          r0 = fmaxf(r0, -1000.f);
+          r1 = fmaxf(r1, -1000.f);
+        }
         G[hr][2 * u] = (partial && !valid) ? 0.f : r0;
         G[hr][2 * u + 1] = (partial && !valid) ? 0.f : r1;
       }
@@ -330,12 +336,106 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, uint8_t* wl, Stag
       G[1][j] = incl;
       gC[j] = __shfl_sync(0xffffffffu, incl, 28 + tig);
     }
-    // the chunk's decay must stay within the anchored factors' range on every channel
+    // The anchored factors stay finite while the chunk decays by at most 2^-250 on every
+    // channel.  Past that the precise-state kernels (the ones these gates run) take the
+    // direct route below; the others flag the chunk.
     if (anchored) {
       bool bad = false;
 #pragma unroll
       for (int j = 0; j < 8; ++j) bad = bad || !(fabsf(gC[j]) <= 250.f);
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrGateRange);
+      const bool out_of_range = __any_sync(0xffffffffu, bad);
+      if constexpr (!kPrecise) {
+        if (out_of_range && lane == 0) atomicOr(err, kErrGateRange);
+      } else if (out_of_range) {
+        // ---- direct route for this pass's 32 channels: every factor is a power of two of a
+        //      non-positive exponent (2^G, 2^(G_C - G), and 2^(G_i - G_j) per pair j <= i), so
+        //      nothing overflows and what underflows is below fp32's reach in the result too
+        float kh[2][8], qh[2][8];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            kh[hr][j] = k[hr][j] * rk[hr];
+            qh[hr][j] = q[hr][j] * rq[hr];
+          }
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const uint32_t o = sw_off(ra + hr, j16);
+          uint32_t qw[4], kw[4], kl[4], hw[4], lw[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j0 = 2 * u, j1 = 2 * u + 1;
+            const float e0 = ex2_approx(G[hr][j0]), e1 = ex2_approx(G[hr][j1]);
+            const float f0 = ex2_approx(gC[j0] - G[hr][j0]), f1 = ex2_approx(gC[j1] - G[hr][j1]);
+            qw[u] = pack_bf16x2(qh[hr][j0] * e0, qh[hr][j1] * e1);
+            split_bf16x2(kh[hr][j0] * e0, kh[hr][j1] * e1, kw[u], kl[u]);
+            split_bf16x2(kh[hr][j0] * f0, kh[hr][j1] * f1, hw[u], lw[u]);
+          }
+          *reinterpret_cast<uint4*>(qb + o) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+          *reinterpret_cast<uint4*>(wb + o) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+          *reinterpret_cast<uint4*>(wl + 2048 * (p >> 1) + o) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+          *reinterpret_cast<uint4*>(kb + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(gb + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        if (gid == 0) {
+          float e[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) e[j] = ex2_approx(gC[j]);
+          *reinterpret_cast<float4*>(&sm.gamC[ch0]) = make_float4(e[0], e[1], e[2], e[3]);
+          *reinterpret_cast<float4*>(&sm.gamC[ch0 + 4]) = make_float4(e[4], e[5], e[6], e[7]);
+        }
+        // Gram partials over the lane's 8 channels: token jt's values come from lane
+        // (gid = jt / 2, same tig), then the 4 lanes of a tig group are summed
+        float pk[2][16], pq[2][16];
+#pragma unroll
+        for (int jt = 0; jt < 16; ++jt) {
+          const int src = 4 * (jt >> 1) + tig;
+          float Gj[8], kj[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            Gj[c] = __shfl_sync(0xffffffffu, G[jt & 1][c], src);
+            kj[c] = __shfl_sync(0xffffffffu, kh[jt & 1][c], src);
+          }
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            float sk = 0.f, sq = 0.f;
+            if (jt <= ra + hr) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const float e = ex2_approx(G[hr][c] - Gj[c]) * kj[c];
+                sk = fmaf(kh[hr][c], e, sk);
+                sq = fmaf(qh[hr][c], e, sq);
+              }
+            }
+            pk[hr][jt] = sk;
+            pq[hr][jt] = sq;
+          }
+        }
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+          for (int jt = 0; jt < 16; ++jt)
+#pragma unroll
+            for (int m = 1; m <= 2; m <<= 1) {
+              pk[hr][jt] += __shfl_xor_sync(0xffffffffu, pk[hr][jt], m);
+              pq[hr][jt] += __shfl_xor_sync(0xffffffffu, pq[hr][jt], m);
+            }
+        // into the fragment accumulators: rows ra (c[0], c[1]) and rb (c[2], c[3]); token
+        // columns 4 tig, 4 tig + 2 in ck0 / cq0 and 4 tig + 1, 4 tig + 3 in ck1 / cq1
+#pragma unroll
+        for (int jt = 0; jt < 16; ++jt) {
+          if (jt == 4 * tig) {
+            ck0[0] += pk[0][jt]; ck0[2] += pk[1][jt]; cq0[0] += pq[0][jt]; cq0[2] += pq[1][jt];
+          } else if (jt == 4 * tig + 2) {
+            ck0[1] += pk[0][jt]; ck0[3] += pk[1][jt]; cq0[1] += pq[0][jt]; cq0[3] += pq[1][jt];
+          } else if (jt == 4 * tig + 1) {
+            ck1[0] += pk[0][jt]; ck1[2] += pk[1][jt]; cq1[0] += pq[0][jt]; cq1[2] += pq[1][jt];
+          } else if (jt == 4 * tig + 3) {
+            ck1[1] += pk[0][jt]; ck1[3] += pk[1][jt]; cq1[1] += pq[0][jt]; cq1[3] += pq[1][jt];
+          }
+        }
+        continue;
+      }
     }
     float eA[8];   // 2^a with the anchor a = G_C / 2 (anchored), else 2^G_C
 #pragma unroll

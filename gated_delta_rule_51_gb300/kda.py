@@ -164,10 +164,8 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
     the kernel; off means the caller did them: g is then the natural-log decay, at
     most 0 (A_log and dt_bias may be None), beta is beta itself, q and k are used
     without L2 norms.  safe_gate=False selects the gate without a lower bound,
-    ghat = -exp(A_log) softplus(g + dt_bias) (lower_bound is then not read).  With
-    either of those two gates, a 16-token chunk whose decay leaves the range the
-    chunked form factors exactly (a sum of ghat below -173 on some channel) sets
-    the gate-range bit of the workspace's error word (check_device_error).
+    ghat = -exp(A_log) softplus(g + dt_bias) (lower_bound is then not read).  Any
+    decay is computed exactly: chunks past 2^-250 take a direct route in the kernel.
     precise_state=True reads the carried state as a bf16 pair (KDA_PRECISE_STATE); the
     library already does so for lower_bound > -0.25 and for the two gates without a bound.
     """

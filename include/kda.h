@@ -60,7 +60,7 @@ typedef enum {
     KDA_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
     KDA_ERR_TIMEOUT = 6,            /* a device-side wait ran out of time (error word) */
     KDA_ERR_BAD_SEQLENS = 7,        /* cu_seqlens not monotone or not ending at T (error word) */
-    KDA_ERR_GATE_RANGE = 8          /* a 16-token chunk decayed past 2^-250 on some channel (error word) */
+    KDA_ERR_GATE_RANGE = 8          /* reserved: no longer raised (chunks past 2^-250 are computed) */
 } kda_status;
 
 /* State dtype for initial_state / final_state (README: absent, bf16 or fp32). */
@@ -84,10 +84,13 @@ typedef enum { KDA_STATE_NONE = 0, KDA_STATE_BF16 = 1, KDA_STATE_FP32 = 2 } kda_
  * The chunked form of kda_fwd_ex factors the decay inside each 16-token chunk
  * about half the chunk's total, which is exact while that total stays within
  * 2^-250 (a sum of ghat above -173 over the chunk's 16 tokens on every
- * channel).  The in-kernel safe gate never leaves this range (16 x 5 < 173); a
- * preactivated or softplus gate that does sets KDA_ERR_GATE_RANGE in the error
- * word, and the outputs of that call are then unspecified.  kda_decode runs the
- * token recurrence itself and takes any gate values.
+ * channel).  The in-kernel safe gate never leaves this range (16 x 5 < 173).
+ * With a preactivated or softplus gate, the 32 channels of a chunk that leave
+ * it take a direct route instead (every factor 2^G, 2^(G_C - G) and, per token
+ * pair, 2^(G_i - G_j), all at most 1), so any decay is computed exactly;
+ * KDA_ERR_GATE_RANGE is kept in the status list but kda_fwd_ex no longer
+ * raises it.  kda_decode runs the token recurrence itself and takes any gate
+ * values.
  *
  * One more flag is not a step of the method but a precision request:
  *   KDA_PRECISE_STATE     : the chunked form reads the carried state as a bf16 pair
@@ -183,9 +186,9 @@ KDA_API kda_status kda_fwd_ex(const kda_shape *shape, const void *q, const void 
 /*
  * Synchronises `stream`, reads the error word that the last kda_fwd on this
  * workspace left behind, stores it in *flags (0 = none; bit 0 = a device wait
- * timed out; bit 1 = malformed cu_seqlens; bit 2 = a chunk's decay out of the
- * gate range above) and returns KDA_OK, KDA_ERR_TIMEOUT, KDA_ERR_BAD_SEQLENS or
- * KDA_ERR_GATE_RANGE accordingly.
+ * timed out; bit 1 = malformed cu_seqlens; bit 2 = reserved for
+ * KDA_ERR_GATE_RANGE, no longer set) and returns KDA_OK, KDA_ERR_TIMEOUT or
+ * KDA_ERR_BAD_SEQLENS accordingly.
  */
 KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t stream, int *flags);
 

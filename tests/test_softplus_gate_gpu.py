@@ -94,16 +94,60 @@ def test_strong_decay_inside_the_anchored_range():
     check_state(fin, ref_fin, label="softplus strong decay")
 
 
-def test_out_of_range_decay_is_flagged_not_trapped():
+@pytest.mark.parametrize("shift,lo,hi", [(20.0, 300, 1000), (30.0, 400, 1600), (90.0, 2000, 6000)])
+def test_decay_past_the_anchored_range_is_computed(shift, lo, hi):
+    """Chunks that decay by more than 2^-250 (A_log 0 and g + dt_bias near 20, 30 and 90:
+    about 2^-460, 2^-690 and 2^-2080 a chunk) leave the range the anchored factors cover.
+    Those passes take the direct route (factors 2^G, 2^(G_C - G) and 2^(G_i - G_j), all at
+    most 1), so they match the oracle and the error word stays clear."""
     from gated_delta_rule_51_gb300 import kda
 
-    x = _shift_g(random_case(1, 64, 1, seed=1204), 20.0, a_log=0.0)     # about 2^-460 a chunk
-    ws = torch.empty(kda.workspace_size(kda.make_shape(1, 64, 1, 1)), dtype=torch.uint8, device="cuda")
-    _gpu(x, workspace=ws)
-    assert kda.check_device_error(ws) & 4
-    # a call within range on the same workspace clears the word
-    _gpu(random_case(1, 64, 1, seed=1205), workspace=ws)
+    x = _shift_g(random_case(1, 200, 2, seed=1204 + int(shift)), shift, a_log=0.0)
+    gsum = torch.nn.functional.softplus(x["g"].float() + x["dt_bias"].view(1, 1, 2, 128)).cpu().numpy()
+    chunk = gsum[0, :192].reshape(12, 16, 2, 128).sum(axis=1) / np.log(2.0)
+    assert chunk.min() > lo and chunk.max() < hi
+    ws = torch.empty(kda.workspace_size(kda.make_shape(1, 200, 2, 1)), dtype=torch.uint8, device="cuda")
+    ref_out, ref_fin = _oracle(x)
+    out, fin = _gpu(x, workspace=ws)
     assert kda.check_device_error(ws) == 0
+    check_out(out, ref_out.reshape(200, 2, 128), label=f"softplus decay shift {shift}")
+    check_state(fin, ref_fin, label=f"softplus decay shift {shift}")
+
+
+def test_mixed_chunks_in_and_out_of_range(monkeypatch):
+    """One head decays strongly (out of range, direct route), the other gently (anchored
+    route), in the same call, through the segment scan and with a partial last chunk."""
+    monkeypatch.setenv("KDA_SEG_TOKENS", "64")
+    x = random_case(1, 333, 2, seed=1230)
+    x["g"][:, :, 0] = (x["g"][:, :, 0].float() + 25.0).to(torch.bfloat16)
+    x["A_log"][0] = 0.0
+    ref_out, ref_fin = _oracle(x)
+    out, fin = _gpu(x)
+    check_out(out, ref_out.reshape(333, 2, 128), label="softplus mixed range")
+    check_state(fin, ref_fin, label="softplus mixed range")
+
+
+def test_preactivated_gate_far_past_the_range():
+    """A preactivated g in [-60, -20] (chunks decaying by 2^-460 .. 2^-1380): direct route."""
+    from gated_delta_rule_51_gb300 import kda
+    import oracle
+
+    x = random_case(1, 150, 2, seed=1240)
+    gen = torch.Generator(device="cuda").manual_seed(1241)
+    x["g"] = (-20.0 - 40.0 * torch.rand(x["g"].shape, generator=gen, device="cuda")).to(torch.bfloat16)
+    xc = to_cpu(x)
+    ref_out, ref_fin = oracle.kda_forward(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], xc["scale"], xc["A_log"],
+                                          xc["dt_bias"], xc["lower_bound"], xc["initial_state"],
+                                          use_gate_in_kernel=False)
+    out = torch.full_like(x["v"], float("nan"))
+    fin = torch.full_like(x["initial_state"], float("nan"))
+    ws = torch.empty(kda.workspace_size(kda.make_shape(1, 150, 2, 1)), dtype=torch.uint8, device="cuda")
+    kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], out, None, None, 0.0,
+            initial_state=x["initial_state"], final_state=fin, workspace=ws, use_gate_in_kernel=False)
+    torch.cuda.synchronize()
+    assert kda.check_device_error(ws) == 0
+    check_out(out, ref_out.reshape(150, 2, 128), label="preactivated [-60, -20]")
+    check_state(fin, ref_fin, label="preactivated [-60, -20]")
 
 
 def test_preactivated_gate_beyond_the_safe_range():
