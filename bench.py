@@ -93,7 +93,8 @@ def load_peaks():
 # the parameter structs): a committed DRAM count stands while none of them has changed
 KERNEL_FILES = {"chain": ("kda_chain.cuh", "kda_chain.cu", "kda_device.cuh", "kda_internal.h"),
                 "decode": ("kda_decode.cu", "kda_device.cuh", "kda_internal.h"),
-                "bwd": ("kda_bwd.cu", "kda_device.cuh", "kda_internal.h")}
+                "bwd": ("kda_bwd.cu", "kda_device.cuh", "kda_internal.h"),
+                "chain_bwd": ("kda_chain.cuh", "kda_chain_bwd.cu", "kda_device.cuh", "kda_internal.h")}
 
 
 def strip_comments(src: str) -> str:
@@ -455,8 +456,8 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
     barrier()
-    # launch phases: schedule, forward runs (every segment's forward and the transitions),
-    # carry composition, corrections of the split segments
+    # launch phases: schedule, forward runs (every segment's forward, overlapping the
+    # transition runs), carry composition, corrections of the split segments
     step_ms = [e[0].elapsed_time(e[4]) for e in ev]
     sch_ms = [e[0].elapsed_time(e[1]) for e in ev]
     fwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
@@ -743,7 +744,8 @@ def run_decode(args, w):
 def run_bwd(args, w):
     """The backward pass (kda_bwd) on workload w, with random bf16 dout and fp32 dfinal:
     every step reads the forward's inputs and writes every gradient; CUDA events around
-    each phase (prep, stored-state forward, reverse, chain rule)."""
+    each phase (chunked form: the runs' list, the two chains, the state products, the chunk
+    gradients; recurrent form: prep, stored-state forward, reverse, chain rule)."""
     import torch
 
     from gated_delta_rule_51_gb300 import inputs as I
@@ -771,10 +773,12 @@ def run_bwd(args, w):
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    recurrent = args.bwd_form == "recurrent"
+
     def step():
         kda.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["A_log"], x["dt_bias"],
                 x["lower_bound"], dout, initial_state=x["initial_state"], dfinal=dfinal,
-                cu_seqlens=x["cu_seqlens"], workspace=ws, out=outs)
+                cu_seqlens=x["cu_seqlens"], workspace=ws, out=outs, recurrent=recurrent)
 
     for _ in range(args.warmup):
         step()
@@ -796,8 +800,10 @@ def run_bwd(args, w):
         kda.set_profile_events(None)
         torch.cuda.synchronize(dev)
     step_ms = [e[0].elapsed_time(e[4]) for e in ev]
-    ph = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
-          for j, name in enumerate(("prep", "stored_state_forward", "reverse", "chain_rule"))}
+    names = (("prep", "stored_state_forward", "reverse", "chain_rule") if recurrent
+             else ("runs", "chains", "state_products", "chunk_gradients"))
+    ph = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, name in enumerate(names)}
+    dominant = "reverse" if recurrent else "chains"
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms = total_ms / args.steps
     tokens = w.B * w.T
@@ -805,9 +811,10 @@ def run_bwd(args, w):
     state_bytes = w.N * w.H * 128 * 128 * 4 * (int(w.has_initial_state) + 2)   # h0 and dfinal in, dh0 out
     nbytes = w.token_heads * BWD_BYTES_PER_TOKEN_HEAD + state_bytes + 2 * w.H * (4 + 128 * 4)
     hbm_gbs, _, peak_kind = load_peaks()
-    achieved = nbytes / (ph["reverse"] / 1000.0) / 1e9
+    achieved = nbytes / (ph[dominant] / 1000.0) / 1e9
+    kernel = "kda_bwd_reverse_kernel" if recurrent else "kda_chain_kernel<64> (forward and reverse chains)"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                "traffic": measured_traffic("bwd_" + w.name), "kernel": "kda_bwd_reverse_kernel",
+                "traffic": measured_traffic(("bwd_" if recurrent else "bwd_chunked_") + w.name), "kernel": kernel,
                 "peak_source": "measured, MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": nbytes,
@@ -820,8 +827,9 @@ def run_bwd(args, w):
     if rank == 0:
         line = {"metric": BWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": config_dict(w, {"pass": "backward", "dout": "bf16 N(0,1)", "dfinal": "fp32 0.1 N(0,1)",
+                "vs_baseline": None, "dtype": "f32" if recurrent else "bf16", "data": "synthetic",
+                "config": config_dict(w, {"pass": "backward", "form": args.bwd_form,
+                                          "dout": "bf16 N(0,1)", "dfinal": "fp32 0.1 N(0,1)",
                                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                                           "l2": "flushed between timed steps (252 MB write)",
                                           "launch": "direct calls"}),
@@ -843,6 +851,9 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd-form", choices=("chunked", "recurrent"), default="chunked",
+                    help="backward configs: the chunked tensor-core form (the library's default for the "
+                         "gate with a lower bound) or the fp32 recurrent one")
     args = ap.parse_args()
     if args.config.startswith("bwd"):
         # the backward pass on a forward workload: "bwd" is the fixed batch, "bwd_<name>" any other

@@ -15,8 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkda.so")
-SOURCES = ["kda_api.cu", "kda_chain.cu", "kda_chain_precise.cu", "kda_aux.cu", "kda_static_ws.cu", "kda_decode.cu",
-           "kda_bwd.cu"]
+SOURCES = ["kda_api.cu", "kda_chain.cu", "kda_chain_precise.cu", "kda_chain_aux.cu", "kda_chain_bwd.cu", "kda_aux.cu",
+           "kda_static_ws.cu", "kda_decode.cu", "kda_bwd.cu"]
 HEADERS = ["kda_device.cuh", "kda_internal.h", "kda_chain.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -81,9 +81,9 @@ int64_t choose_seg_tokens(const kda_shape& s, int sms) {
 
 struct Layout {
   int64_t seg_tokens = 0;
-  int64_t cap_forward = 0, cap_correct = 0, cap_compose = 0, cap_slots = 0, cap_ranks = 0;
-  size_t off_hdr = 0, off_forward = 0, off_correct = 0, off_compose = 0, off_slots = 0, off_ranks = 0, off_sm = 0,
-         off_zero = 0;
+  int64_t cap_forward = 0, cap_transition = 0, cap_correct = 0, cap_compose = 0, cap_slots = 0, cap_ranks = 0;
+  size_t off_hdr = 0, off_forward = 0, off_transition = 0, off_correct = 0, off_compose = 0, off_slots = 0,
+         off_ranks = 0, off_sm = 0, off_zero = 0;
   size_t total = 0;
 };
 
@@ -92,9 +92,10 @@ Layout make_layout(const kda_shape& s, int sms) {
   const int64_t rows = s.B * s.T;
   L.seg_tokens = choose_seg_tokens(s, sms);
   const int64_t splits = rows / L.seg_tokens;   // bound on sum over sequences of (nseg - 1)
-  // runs of the first launch: nseg forward + (nseg - 2) transition runs per sequence
+  // nseg forward and (nseg - 2) transition runs per sequence (the ranks are indexed over both)
   L.cap_ranks = s.N + 2 * splits;
-  L.cap_forward = s.H * L.cap_ranks;
+  L.cap_forward = s.H * (s.N + splits);
+  L.cap_transition = s.H * splits;
   L.cap_correct = s.H * splits;                 // nseg - 1 per sequence
   L.cap_slots = 2 * s.H * splits;               // 2 (nseg - 1) per split sequence
   L.cap_compose = s.H * std::min<int64_t>(s.N, splits);
@@ -103,6 +104,8 @@ Layout make_layout(const kda_shape& s, int sms) {
   off = align_up(off + sizeof(WorkHeader));
   L.off_forward = off;
   off = align_up(off + (size_t)L.cap_forward * sizeof(WorkItem));
+  L.off_transition = off;
+  off = align_up(off + (size_t)L.cap_transition * sizeof(WorkItem));
   L.off_correct = off;
   off = align_up(off + (size_t)L.cap_correct * sizeof(WorkItem));
   L.off_compose = off;
@@ -141,6 +144,47 @@ BwdLayout make_bwd_layout(const kda_shape& s) {
   off = align_up(off + nslot * (size_t)s.H * kSlotBytes);
   L.off_part = off;
   off = align_up(off + (size_t)kBwdSlices * TH * kBwdRowStride * sizeof(float));
+  L.off_dA = off;
+  off = align_up(off + TH * sizeof(float));
+  L.off_ppart = off;
+  off = align_up(off + (size_t)L.nblk * (size_t)s.H * kBwdParamStride * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+// The chunked backward's workspace: header, the chains' runs, per (chunk slot, head) the stored
+// states (bf16), Vn and dVn (fp32), the state products, then the per-token dA_log terms and the
+// parameter-reduction blocks.  Slots: n + row0(n) / 16 + c is below N + B T / 16 + 1.
+struct BwdChunkedLayout {
+  size_t off_hdr = 0, off_items = 0, off_s0 = 0, off_ds1 = 0, off_vn = 0, off_dvn = 0, off_xp = 0, off_zs = 0,
+         off_dA = 0, off_ppart = 0, total = 0;
+  int64_t nslots = 0;
+  int nblk = 0;
+};
+
+BwdChunkedLayout make_bwd_chunked_layout(const kda_shape& s) {
+  BwdChunkedLayout L;
+  const size_t BT = (size_t)(s.B * s.T), TH = BT * (size_t)s.H;
+  L.nslots = (int64_t)(BT / 16) + s.N + 1;
+  const size_t SH = (size_t)L.nslots * (size_t)s.H;
+  L.nblk = (int)((BT + kBwdParamTokens - 1) / kBwdParamTokens);
+  size_t off = 0;
+  L.off_hdr = off;
+  off = align_up(off + sizeof(WorkHeader));
+  L.off_items = off;
+  off = align_up(off + 2 * (size_t)s.N * (size_t)s.H * sizeof(WorkItem));
+  L.off_s0 = off;
+  off = align_up(off + SH * 16384 * sizeof(uint16_t));
+  L.off_ds1 = off;
+  off = align_up(off + SH * 16384 * sizeof(uint16_t));
+  L.off_vn = off;
+  off = align_up(off + SH * 2048 * sizeof(float));
+  L.off_dvn = off;
+  off = align_up(off + SH * 2048 * sizeof(float));
+  L.off_xp = off;
+  off = align_up(off + SH * 6144 * sizeof(float));
+  L.off_zs = off;
+  off = align_up(off + SH * 128 * sizeof(float));
   L.off_dA = off;
   off = align_up(off + TH * sizeof(float));
   L.off_ppart = off;
@@ -404,6 +448,8 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   sp.hdr = hdr;
   sp.correct = reinterpret_cast<WorkItem*>(ws + L.off_correct);
   sp.forward = reinterpret_cast<WorkItem*>(ws + L.off_forward);
+  sp.transition = reinterpret_cast<WorkItem*>(ws + L.off_transition);
+  sp.cap_transition = L.cap_transition;
   sp.compose = reinterpret_cast<ComposeItem*>(ws + L.off_compose);
   sp.cap_correct = L.cap_correct;
   sp.cap_forward = L.cap_forward;
@@ -455,13 +501,23 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
   cp.take = nullptr;
   cp.sm_arrivals = nullptr;
 
-  // first launch: every segment's forward run (outputs, local carries) and the transition
-  // runs, longest first, two CTAs per SM paired long with short
+  // the transition runs of the split sequences' middle segments (a kernel of their own: the
+  // forward runs' kernel carries none of their code); they usually stop after a few chunks
+  // they usually stop after a few chunks: the forward launch overlaps them
+  const bool transitions = L.cap_transition > 0;
+  if (transitions) {
+    cp.items = sp.transition;
+    cp.item_count = &hdr->n_transition;
+    if (launch_chain_aux(cp, (int)L.cap_transition, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    ++launches;
+  }
+  // every segment's forward run (outputs, local carries), longest first, two CTAs per SM
+  // paired long with short
   cp.items = sp.forward;
   cp.item_count = &hdr->n_forward;
   cp.take = hdr->take;
   cp.sm_arrivals = sp.sm_arrivals;
-  if (launch_chain(cp, (int)L.cap_forward, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  if (launch_chain(cp, (int)L.cap_forward, stream, transitions) != cudaSuccess) return KDA_ERR_CUDA;
   ++launches;
   mark(1, stream);
   if (L.cap_correct > 0) {
@@ -478,7 +534,7 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
     cp.item_count = &hdr->n_correct;
     cp.take = nullptr;
     cp.sm_arrivals = nullptr;
-    if (launch_chain(cp, (int)L.cap_correct, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_chain_aux(cp, (int)L.cap_correct, stream) != cudaSuccess) return KDA_ERR_CUDA;
     ++launches;
   } else {
     mark(2, stream);
@@ -521,7 +577,7 @@ kda_status kda_bwd_workspace_size(const kda_shape* shape, size_t* bytes) {
   kda_status st = check_shape(shape);
   if (st != KDA_OK) return st;
   if (shape->K != 128 || shape->V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
-  *bytes = make_bwd_layout(*shape).total;
+  *bytes = std::max(make_bwd_layout(*shape).total, make_bwd_chunked_layout(*shape).total);
   return KDA_OK;
 }
 
@@ -538,12 +594,12 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
   if (cu_seqlens != nullptr && s.B != 1) return KDA_ERR_INVALID_ARGUMENT;
   if (cu_seqlens == nullptr && s.N != s.B) return KDA_ERR_INVALID_ARGUMENT;
   if ((long long)s.N * s.H * kBwdSlices > 0x7fffffffLL) return KDA_ERR_INVALID_ARGUMENT;
-  if (!valid_flags(flags)) return KDA_ERR_INVALID_ARGUMENT;
+  if (!valid_flags(flags & ~(unsigned)KDA_BWD_RECURRENT)) return KDA_ERR_INVALID_ARGUMENT;
   const bool gate_here = !(flags & KDA_GATE_PREACTIVATED);
   if (uses_lower_bound(flags) && !(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_INVALID_ARGUMENT;
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
   auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
-  // token tensors are read and written four channels at a time
+  // token tensors are read and written four (chunked form: eight) channels at a time
   if (s.B * s.T > 0) {
     const void* tok16[] = {q, k, v, g, dout, dq, dk, dv, dg};
     for (const void* p : tok16)
@@ -560,15 +616,19 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
   if ((dfinal != nullptr && !aligned16(dfinal)) || (dh0 != nullptr && !aligned16(dh0)) ||
       (dA_log != nullptr && !aligned(dA_log, 4)) || (ddt_bias != nullptr && !aligned(ddt_bias, 4)))
     return KDA_ERR_INVALID_ARGUMENT;
+  // the gate with a lower bound takes the chunked form unless the recurrent one is asked for
+  const bool chunked = uses_lower_bound(flags) && !(flags & KDA_BWD_RECURRENT);
   const BwdLayout L = make_bwd_layout(s);
+  const BwdChunkedLayout C = make_bwd_chunked_layout(s);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
     return KDA_ERR_INVALID_ARGUMENT;
-  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < (chunked ? C.total : L.total)) return KDA_ERR_WORKSPACE_TOO_SMALL;
   DeviceInfo d;
   if (device_info(&d) != KDA_OK) return KDA_ERR_CUDA;
   if (d.major != 10 || d.minor != 3) return KDA_ERR_UNSUPPORTED_DEVICE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdParams p;
+  std::memset(&p, 0, sizeof(p));
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);
   p.v = static_cast<const uint16_t*>(v);
@@ -589,21 +649,81 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
   p.dh0 = dh0;
   p.dA_log = dA_log;
   p.ddt_bias = ddt_bias;
+  p.T = s.T;
+  p.BT = s.B * s.T;
+  p.N = (int)s.N;
+  p.H = (int)s.H;
+  p.flags = (int)(flags & kValidFlags);
+  p.scale = scale;
+  p.lower_bound = lower_bound;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (chunked) {
+    p.err = &reinterpret_cast<WorkHeader*>(ws + C.off_hdr)->err;
+    p.items = reinterpret_cast<WorkItem*>(ws + C.off_items);
+    p.item_count = &reinterpret_cast<WorkHeader*>(ws + C.off_hdr)->n_forward;
+    p.s0 = reinterpret_cast<const uint16_t*>(ws + C.off_s0);
+    p.ds1 = reinterpret_cast<const uint16_t*>(ws + C.off_ds1);
+    p.vn = reinterpret_cast<const float*>(ws + C.off_vn);
+    p.dvn = reinterpret_cast<const float*>(ws + C.off_dvn);
+    p.xp = reinterpret_cast<float*>(ws + C.off_xp);
+    p.zs = reinterpret_cast<float*>(ws + C.off_zs);
+    p.dA_tok = reinterpret_cast<float*>(ws + C.off_dA);
+    p.ppart = reinterpret_cast<float*>(ws + C.off_ppart);
+    p.nblk = C.nblk;
+    p.nslots = C.nslots;
+    // the chains: N H forward runs storing S0 and Vn, N H reverse runs storing dS1 and dVn
+    ChainParams cp;
+    std::memset(&cp, 0, sizeof(cp));
+    const int64_t rows = s.B * s.T;
+    if (rows > 0) {
+      if (!encode_tile_map(&cp.tm_q, q, rows, s.H) || !encode_halves_map(&cp.tm_k, k, rows, s.H) ||
+          !encode_halves_map(&cp.tm_g, g, rows, s.H) || !encode_halves_map(&cp.tm_v, v, rows, s.H) ||
+          !encode_halves_map(&cp.tm_dout, dout, rows, s.H))
+        return KDA_ERR_CUDA;
+    }
+    cp.beta = p.beta;
+    cp.A_log = A_log;
+    cp.dt_bias = dt_bias;
+    cp.init_state = initial_state;
+    cp.init_dtype = p.init_dtype;
+    cp.dfinal = dfinal;
+    cp.dh0 = dh0;
+    cp.save_s0 = reinterpret_cast<uint16_t*>(ws + C.off_s0);
+    cp.save_ds1 = reinterpret_cast<uint16_t*>(ws + C.off_ds1);
+    cp.save_vn = reinterpret_cast<float*>(ws + C.off_vn);
+    cp.save_dvn = reinterpret_cast<float*>(ws + C.off_dvn);
+    cp.items = p.items;
+    cp.item_count = p.item_count;
+    cp.err = p.err;
+    cp.H = (int)s.H;
+    cp.vsplit = 1;
+    cp.kdim = 128;
+    cp.vrows = 128;
+    cp.scale = scale;
+    cp.lower_bound = lower_bound;
+    cp.flags = (int)(flags & kValidFlags);
+    cp.precise = 0;
+    // profile marks: the runs, the chains, the state products, the chunk gradients
+    if (launch_bwd_chunked(p, 0, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    mark(0, stream);
+    if (launch_chain_bwd(cp, (int)(2 * s.N * s.H), stream) != cudaSuccess) return KDA_ERR_CUDA;
+    mark(1, stream);
+    if (launch_bwd_chunked(p, 2, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    mark(2, stream);
+    if (launch_bwd_chunked(p, 3, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    mark(3, stream);
+    const bool work = p.BT > 0 && p.H > 0;
+    t_last_launches = 1 + (s.N > 0 ? 1 : 0) + (work ? 2 : 0) +
+                      ((dA_log == nullptr && ddt_bias == nullptr) ? 0 : (C.nblk > 0 ? 2 : 1));
+    return KDA_OK;
+  }
   p.prep = reinterpret_cast<float*>(ws + L.off_prep);
   p.ckpt = reinterpret_cast<float*>(ws + L.off_ckpt);
   p.part = reinterpret_cast<float*>(ws + L.off_part);
   p.dA_tok = reinterpret_cast<float*>(ws + L.off_dA);
   p.ppart = reinterpret_cast<float*>(ws + L.off_ppart);
   p.err = &reinterpret_cast<WorkHeader*>(ws + L.off_hdr)->err;
-  p.T = s.T;
-  p.BT = s.B * s.T;
-  p.N = (int)s.N;
-  p.H = (int)s.H;
-  p.flags = (int)(flags & kValidFlags);
   p.nblk = L.nblk;
-  p.scale = scale;
-  p.lower_bound = lower_bound;
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   // profile marks after each phase: prep, stored-state forward, reverse, chain rule
   for (int phase = 0; phase < 4; ++phase) {
     if (launch_bwd(p, phase, stream) != cudaSuccess) return KDA_ERR_CUDA;

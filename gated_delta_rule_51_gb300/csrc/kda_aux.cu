@@ -25,11 +25,12 @@ namespace kda {
 //
 // A sequence of len tokens is cut into nseg = ceil(len / L) segments of L tokens (the
 // last one shorter).  Per head, the lists get:
-//   first launch   F_s, s = 0 .. nseg-1: forward runs writing outputs; F_0 starts from
+//   transitions    T_s, s = 1 .. nseg-2: transition runs into slot P_s (with a zero flag);
+//                  a launch of their own, first (they usually stop after a few chunks).
+//   forward        F_s, s = 0 .. nseg-1: forward runs writing outputs; F_0 starts from
 //                  the caller's initial state, the others from zero.  F_s stores its final
 //                  state in slot Q_s (for s = nseg-1 only when there is a final state;
 //                  an unsplit sequence writes the caller's final state directly).
-//                  T_s, s = 1 .. nseg-2: transition runs into slot P_s (with a zero flag).
 //   compose        S_1 = Q_0; S_{s+1} = P_s S_s + Q_s into Q_s, s = 1 .. nseg-2.
 //   last launch    C_s, s = 1 .. nseg-1: correction runs from Q_{s-1} = S_s, adding to the
 //                  outputs of F_s; C_{nseg-1} writes the final state Q_{nseg-1} + D.
@@ -78,11 +79,10 @@ __device__ long long block_scan(long long x, long long* buf) {
   return r;
 }
 
-// The first launch's runs are listed longest first, so that the first wave puts the longest
-// runs one to an SM and the short ones fill the second CTA slots and finish early: the long
-// chains then run alone for most of their length.  Runs are ranked by a length bucket, four
-// buckets per octave of chunk count (ties in arbitrary order; every run computes the same
-// either way).  Transition runs usually stop after a few chunks and are ranked shortest.
+// The forward runs are listed longest first, so that the first wave puts the longest runs one
+// to an SM and the short ones fill the second CTA slots and finish early: the long chains then
+// run alone for most of their length.  Runs are ranked by a length bucket, four buckets per
+// octave of chunk count (ties in arbitrary order; every run computes the same either way).
 constexpr int kLenBuckets = 4 * 32;
 __device__ __forceinline__ int len_bucket(long long chunks) {
   if (chunks < 4) return (int)(chunks < 0 ? 0 : chunks);
@@ -93,9 +93,9 @@ __device__ __forceinline__ int len_bucket(long long chunks) {
 __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const ScheduleParams p) {
   __shared__ unsigned int s_hist[kLenBuckets];
   __shared__ long long s_buf[kSchedThreads];
-  __shared__ long long s_tot[4];   // runs, corrections, compose chains, slots (running totals)
+  __shared__ long long s_tot[6];   // runs, corrections, compose chains, slots, transitions, forward runs
   __shared__ int s_start[kSchedThreads], s_len[kSchedThreads], s_nseg[kSchedThreads], s_incl[kSchedThreads];
-  __shared__ long long s_run0[kSchedThreads], s_corr0[kSchedThreads], s_slot0[kSchedThreads];
+  __shared__ long long s_run0[kSchedThreads], s_corr0[kSchedThreads], s_slot0[kSchedThreads], s_tr0[kSchedThreads];
   __shared__ int s_comp0[kSchedThreads];
   __shared__ int s_err;
   __shared__ unsigned long long s_max_chunks, s_sum_chunks;
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
         start += c;
       }
     }
-    if (tid == 0) s_tot[0] = s_tot[1] = s_tot[2] = s_tot[3] = 0;
+    if (tid == 0) s_tot[0] = s_tot[1] = s_tot[2] = s_tot[3] = s_tot[4] = s_tot[5] = 0;
     __syncthreads();
     for (long long base = 0; base < p.N; base += kSchedThreads) {
       const long long n = base + tid;
@@ -179,15 +179,17 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
       const long long nslot = nseg >= 2 ? 2 * (nseg - 1) : 0;
       const long long incl = block_scan(nruns, s_buf);
       const long long run0 = s_tot[0] + incl - nruns;
-      // pass 0: histogram of the runs' lengths; pass 1: each run's rank
+      // pass 0: histogram of the forward runs' lengths; pass 1: each forward run's rank
       if (n < p.N) {
-        for (long long r = 0; r < nruns; ++r) {
-          const long long flen = r < nseg ? (len <= 0 ? 0 : (len - r * L < L ? len - r * L : L)) : 0;
-          const int bk = r < nseg ? len_bucket((flen + 15) / 16) : 0;
+        for (long long r = 0; r < nseg; ++r) {
+          const long long flen = len <= 0 ? 0 : (len - r * L < L ? len - r * L : L);
+          const int bk = len_bucket((flen + 15) / 16);
           if (pass == 0) atomicAdd(&s_hist[bk], 1u);
           else if (run0 + r < p.cap_ranks) p.seg_rank[run0 + r] = (int)atomicAdd(&s_hist[bk], 1u);
         }
       }
+      const long long tr0 = s_tot[4] + block_scan(ntr, s_buf) - ntr;
+      const long long fw0 = s_tot[5] + block_scan(nseg, s_buf) - nseg;
       const long long corr0 = s_tot[1] + block_scan(ncorr, s_buf) - ncorr;
       const long long comp0 = s_tot[2] + block_scan(ncomp, s_buf) - ncomp;
       const long long slot0 = s_tot[3] + block_scan(nslot, s_buf) - nslot;
@@ -201,6 +203,7 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
         s_corr0[tid] = corr0;
         s_comp0[tid] = (int)comp0;
         s_slot0[tid] = slot0;
+        s_tr0[tid] = tr0;
         __syncthreads();
         // every (head, run) of this tile's sequences, spread over all threads
         const long long tile_runs = s_incl[count - 1];
@@ -252,8 +255,9 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
             }
           } else {
             const long long s = r - ns + 1;   // transition of segment s, 1 <= s <= ns - 2
-            if (fi < p.cap_forward && slots_ok)
-              p.forward[fi] = make_item(st0 + s * L, L, h, kModeTransition, nn, kInIdentity, qb + ns + s - 1, -1);
+            const long long ti = (s_tr0[nl] + s - 1) * H + h;
+            if (ti < p.cap_transition && slots_ok)
+              p.transition[ti] = make_item(st0 + s * L, L, h, kModeTransition, nn, kInIdentity, qb + ns + s - 1, -1);
           }
         }
       }
@@ -263,15 +267,19 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
         s_tot[1] = corr0 + ncorr;
         s_tot[2] = comp0 + ncomp;
         s_tot[3] = slot0 + nslot;
+        s_tot[4] = tr0 + ntr;
+        s_tot[5] = fw0 + nseg;
       }
       __syncthreads();
     }
   }
   if (tid == 0) {
-    const long long nf = s_tot[0] * H;
+    const long long nf = s_tot[5] * H;
+    const long long nt = s_tot[4] * H;
     const long long nc = s_tot[1] * H;
     const long long ncm = s_tot[2] * H;
     p.hdr->n_forward = (int)(nf < p.cap_forward ? nf : p.cap_forward);
+    p.hdr->n_transition = (int)(nt < p.cap_transition ? nt : p.cap_transition);
     p.hdr->n_correct = (int)(nc < p.cap_correct ? nc : p.cap_correct);
     p.hdr->n_compose = (int)(ncm < p.cap_compose ? ncm : p.cap_compose);
     p.hdr->err = s_err ? kErrBadSeqlens : 0;

@@ -168,6 +168,13 @@ __device__ __forceinline__ void mul2(uint32_t& x0, uint32_t& x1, float b0, float
   asm("mov.b64 {%0, %1}, %2;" : "=r"(x0), "=r"(x1) : "l"(c));
 }
 
+// 32 bf16 values (16 packed words) to global memory, 16 bytes at a time
+__device__ __forceinline__ void store_packed16(uint16_t* dst, const uint32_t (&pk)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) d[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+}
+
 // Named barrier of one prologue pair (64 threads; ids 1 and 2).
 __device__ __forceinline__ void pair_bar(int pair) { named_bar(1 + pair, 64); }
 
@@ -178,12 +185,14 @@ __device__ __forceinline__ void pair_bar(int pair) { named_bar(1 + pair, 64); }
 // 2 gid / 2 gid + 1 play the fragment rows gid / gid + 8, and the channel pair
 // (8 tig + 2 s, + 1) the k positions (tig, tig + 4) of k-step s; the partial
 // Grams of the two warps are summed through shared memory.
-template <int kFlags, bool kPrecise>
+// A reverse run of the backward (kBwd, rev) scales qh*2^G by qscale and writes Aqk transposed
+// and scaled: the B operands of its update (dO^T scale Q_p) and of its S-side GEMM (dO^T scale P).
+template <int kFlags, bool kPrecise, bool kBwd>
 __device__ __forceinline__ void prologue_pair_chunk(Stage& st, uint8_t* wl, StageSmall& sm, PairScratch& sc, int pair,
                                                     int w, int nv,
                                                     int* err, const float nr, const float lbl2,
                                                     const float* __restrict__ dtb, float beta_a, float beta_b,
-                                                    int lane, bool v_used) {
+                                                    int lane, bool v_used, bool rev, float qscale) {
   constexpr bool gate_pre = kFlags & kGatePreactivated;
   constexpr bool gate_sp = kFlags & kGateSoftplus;   // then nr = log2(e), lbl2 = -exp(A_log)
   // the safe gate keeps |G_C| <= 16 * 5 * log2(e) < 126, where the Gram factors 2^+-G are
@@ -488,6 +497,7 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, uint8_t* wl, Stag
         for (int u = 0; u < 4; ++u) {
           float a0 = qg[hr][2 * u], a1 = qg[hr][2 * u + 1];
           if (anchored) fmul2(a0, a1, eA[2 * u], eA[2 * u + 1]);
+          if (kBwd && rev) fmul2(a0, a1, qscale, qscale);
           qw[u] = pack_bf16x2(a0, a1);
         }
         *reinterpret_cast<uint4*>(qb + o) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
@@ -595,12 +605,24 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, uint8_t* wl, Stag
       float m4[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) m4[u] = (4 * tig + u <= i) ? v[u] : 0.f;
-      uint32_t h0, l0, h1, l1;
-      split_bf16x2(m4[0], m4[1], h0, l0);
-      split_bf16x2(m4[2], m4[3], h1, l1);
-      const uint32_t o = ns_off(i, 4 * tig);
-      *reinterpret_cast<uint2*>(sm.AQhi + o) = make_uint2(h0, h1);
-      *reinterpret_cast<uint2*>(sm.AQlo + o) = make_uint2(l0, l1);
+      if (kBwd && rev) {
+        // row j holds column j of qscale * Aqk (the K-major B of dO^T P)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint16_t hi, lo;
+          split_bf16(m4[u] * qscale, hi, lo);
+          const uint32_t o = ns_off(4 * tig + u, i);
+          *reinterpret_cast<uint16_t*>(sm.AQhi + o) = hi;
+          *reinterpret_cast<uint16_t*>(sm.AQlo + o) = lo;
+        }
+      } else {
+        uint32_t h0, l0, h1, l1;
+        split_bf16x2(m4[0], m4[1], h0, l0);
+        split_bf16x2(m4[2], m4[3], h1, l1);
+        const uint32_t o = ns_off(i, 4 * tig);
+        *reinterpret_cast<uint2*>(sm.AQhi + o) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(sm.AQlo + o) = make_uint2(l0, l1);
+      }
     }
     // rows of the v tile past the end of the sequence: zero
     if (partial && v_used) {
@@ -660,46 +682,24 @@ __device__ __forceinline__ void prologue_pair_chunk(Stage& st, uint8_t* wl, Stag
   __syncwarp();
 }
 
-// kFlags (steps the caller already did) is a template parameter: the prologue's inner
-// loops then carry no per-element tests of it
-// Two CTAs per SM (128 registers a thread); the precise-state kernels run one per SM.
-template <int kFlags>
-__global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
-    kda_chain_kernel(const __grid_constant__ ChainParams p) {
+// The body of one CTA's run.  kAux: the correction and transition runs (outputs added to the
+// ones already written; the run stops once its state is exactly zero); forward and reverse runs
+// take the body without that code.
+template <int kFlags, bool kAux>
+__device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& it) {
   // K = V = 128 is a compile-time shape; the kChainPadded variant reads K = 64 or V = 64 from p
   constexpr bool kPadded = kFlags & kChainPadded;
   constexpr bool kPrecise = kFlags & kChainPrecise;
+  constexpr bool kBwd = kFlags & kChainBwd;   // the backward's storing forward runs and reverse runs
   using SmemLayout = SmemLayoutT<kPrecise>;
   using StageT = typename std::conditional<kPrecise, StagePrecise, Stage>::type;
   constexpr uint32_t kCols = kPrecise ? kTmemColsPrecise : kTmemCols;
   const int kdim = kPadded ? p.kdim : 128;    // key channels the caller's tensors hold
   const int vrows = kPadded ? p.vrows : 128;  // state rows of a chain the caller's tensors hold
-  // Item of this CTA.  The forward launch pairs runs by SM: the list is longest first, the
-  // first CTA to start on an SM takes the longest run left and the second the shortest, so
-  // a long chain shares its SM with a short one and then runs alone.
-  int item = blockIdx.x;
-  if (p.take != nullptr) {
-    __shared__ int s_item;
-    if (threadIdx.x == 0) {
-      const int n_items = *p.item_count;
-      int pick = -1;
-      if (atomicAdd(&p.take[0], 1) < n_items) {   // at most n_items picks: head and tail never meet
-        unsigned smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        const int arrival = atomicAdd(&p.sm_arrivals[smid % kMaxSmIds], 1);
-        pick = (arrival & 1) == 0 ? atomicAdd(&p.take[1], 1) : n_items - 1 - atomicAdd(&p.take[2], 1);
-      }
-      s_item = pick;
-    }
-    __syncthreads();
-    item = s_item;
-    if (item < 0) return;
-  } else if (item >= *p.item_count) {
-    return;
-  }
-  const WorkItem it = p.items[item];
-  if (it.len < 0) return;   // placeholder entry of a work list
   const int nchunks = (it.len + kChunk - 1) / kChunk;
+  // a reverse run walks the chunks last first: iteration c handles chunk dchunk(c) of the run
+  const bool rev = kBwd && it.mode == kModeReverse;
+  auto dchunk = [&](int c) { return rev ? nchunks - 1 - c : c; };
   // work items count heads x value blocks: V = 128 * vsplit columns are independent
   // chains of 128 state rows each, sharing the head's q, k, g and beta
   const int head = it.head / p.vsplit, vblk = it.head - head * p.vsplit;
@@ -783,8 +783,8 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
       const float lbl2 = kpad ? 0.f : (gate_sp ? -rate : p.lower_bound * kLog2e);
       const int gid = lane >> 2;
       auto load_beta = [&](int c, float& b0, float& b1) {
-        const int base = it.row0 + c * kChunk;
-        const int nv = min(kChunk, it.len - c * kChunk);
+        const int base = it.row0 + dchunk(c) * kChunk;
+        const int nv = min(kChunk, it.len - dchunk(c) * kChunk);
         b0 = (c < nchunks && 2 * gid < nv) ? bf16_bits_to_f32(p.beta[(size_t)(base + 2 * gid) * H + h]) : 0.f;
         b1 = (c < nchunks && 2 * gid + 1 < nv) ? bf16_bits_to_f32(p.beta[(size_t)(base + 2 * gid + 1) * H + h])
                                                : 0.f;
@@ -794,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
       int iter = 0;
       for (int c = pair; c < nchunks; c += 2, ++iter) {
         const int s = c % kStages;
-        const int nv = min(kChunk, it.len - c * kChunk);
+        const int nv = min(kChunk, it.len - dchunk(c) * kChunk);
         const float cb0 = bl0, cb1 = bl1;
         load_beta(c + 2, bl0, bl1);
         // both warps of the pair agree on going on (the pair shares named barriers)
@@ -804,8 +804,9 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
         if (!(sc.okf[iter & 1][0] && sc.okf[iter & 1][1])) break;
         uint8_t* wl = nullptr;
         if constexpr (kPrecise) wl = &S.st[s].WL[0][0];
-        prologue_pair_chunk<kFlags & kValidFlags, kPrecise>(S.st[s], wl, S.sm[s], sc, pair, w, nv, p.err, nr, lbl2,
-                                                            dtb, cb0, cb1, lane, it.mode == kModeForward);
+        prologue_pair_chunk<kFlags & kValidFlags, kPrecise, kBwd>(S.st[s], wl, S.sm[s], sc, pair, w, nv, p.err, nr,
+                                                                  lbl2, dtb, cb0, cb1, lane,
+                                                                  it.mode == kModeForward || rev, rev, p.scale);
         if (lane == 0) mbar_arrive(&bar_op_full[s]);
       }
     } else {
@@ -825,17 +826,26 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
       const int h = head;
       const size_t srow = ((size_t)it.seq * p.H + h) * vstride + (size_t)kDimV * vblk + vrow;   // state row (n, h, v)
       // the correction and transition runs take v as zero (no U); the transition writes no outputs
-      const bool with_u = it.mode == kModeForward;
-      const bool with_o = it.mode != kModeTransition;
-      const bool correct = it.mode == kModeCorrect;
+      const bool with_u = !kAux && it.mode == kModeForward;
+      const bool with_o = !kBwd && it.mode != kModeTransition;   // the backward's runs store no outputs
+      const bool correct = kAux && it.mode == kModeCorrect;
       // both v-free runs stop once their state is exactly zero (it then stays zero)
-      const bool track_zero = it.mode != kModeForward;
+      constexpr bool track_zero = kAux;
+      // the backward's runs store, per chunk slot, the state copy and the Vn read-out
+      uint16_t* const save_state = rev ? p.save_ds1 : p.save_s0;
+      float* const save_vec = rev ? p.save_dvn : p.save_vn;
+      const size_t slot0 = (size_t)it.seq + (size_t)(it.row0 >> 4);   // slot of the run's chunk 0
       // instruction and shared-memory descriptors (stage s adds s * sizeof(Stage))
       const uint32_t id_u = idesc_bf16_f32(128, 32, 1, 0);
       const uint32_t id_x = idesc_bf16_f32(128, 32, 0, 0);
       const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1);   // kfac is an MN-major B
       const uint32_t id_o = idesc_bf16_f32(128, 16, 0, 0);
       const uint32_t id_w = idesc_bf16_f32(128, 16, 0, 0);   // precise: -W's remainder, Vn columns only
+      // reverse runs: dO^T (MN-major A) against P^T (K-major B, N = 16); the dS^T copy against
+      // K_d (K-major B, N = 16); dO^T against scale Q_p (MN-major B, N = 128)
+      const uint32_t id_r1 = idesc_bf16_f32(128, 16, 1, 0);
+      const uint32_t id_r2 = idesc_bf16_f32(128, 16, 0, 0);
+      const uint32_t id_r3 = idesc_bf16_f32(128, 128, 1, 1);
       constexpr uint64_t kStageStep = sizeof(StageT) >> 4;
       constexpr uint64_t kSmallStep = sizeof(StageSmall) >> 4;
       const StageT& s0 = S.st[0];
@@ -853,6 +863,20 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
       auto issue_gemm1 = [&](int c) {
         const uint64_t so = (uint64_t)(c % kStages) * kStageStep;
         const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
+        if (kBwd && rev) {
+          // dVn^T = dO^T (scale P) + dS^T K_d^T into D1[c & 1] columns 0-15
+          const uint64_t sso = (uint64_t)(c % kStages) * kSmallStep;
+          const uint64_t d_o = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
+          mma_ss(d1, d_o, smem_desc(smem_u32(m0.AQhi), 128, 256, kSwizzleNone) + sso, id_r1, 0);
+          mma_ss(d1, d_o, smem_desc(smem_u32(m0.AQlo), 128, 256, kSwizzleNone) + sso, id_r1, 1);
+          const uint64_t d_k0 = smem_desc(smem_u32(s0.K), 16, 1024, kSwizzle128B) + so;
+          const uint64_t d_k1 = smem_desc(smem_u32(s0.K) + 2048, 16, 1024, kSwizzle128B) + so;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(d1, tmem + kColSbf + 8u * k, (k < 4 ? d_k0 : d_k1) + (uint64_t)((k & 3) * 2), id_r2, 1u);
+          tc_commit(&bar_d1_full[c & 1]);
+          return;
+        }
         if (with_u) issue_u(c);
         const uint64_t d_x0 = smem_desc(smem_u32(s0.X[0]), 16, 1024, kSwizzle128B) + so;
         const uint64_t d_x1 = smem_desc(smem_u32(s0.X[1]), 16, 1024, kSwizzle128B) + so;
@@ -876,6 +900,18 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
         const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
         const uint64_t a_hi = smem_desc(smem_u32(S.vn_hi), 128, 256, kSwizzleNone);
         const uint64_t a_lo = smem_desc(smem_u32(S.vn_lo), 128, 256, kSwizzleNone);
+        if (kBwd && rev) {
+          // dS^T += dO^T (scale Q_p) + dVn^T (-W): Q_p and -W are rows 16-31 and 0-15 of the two
+          // 64-channel X tiles, 4096 bytes apart
+          const uint64_t d_o = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
+          const uint64_t d_q = smem_desc(smem_u32(s0.X[0]) + 2048, 4096, 1024, kSwizzle128B) + so;
+          const uint64_t d_w = smem_desc(smem_u32(s0.X[0]), 4096, 1024, kSwizzle128B) + so;
+          mma_ss(tmem + kColState, d_o, d_q, id_r3, 1);
+          mma_ss(tmem + kColState, a_hi, d_w, id_s, 1);
+          mma_ss(tmem + kColState, a_lo, d_w, id_s, 1);
+          tc_commit(&bar_d2_full);
+          return;
+        }
         const uint64_t kf_hi = smem_desc(smem_u32(s0.K), 2048, 1024, kSwizzle128B) + so;
         const uint64_t kf_lo = smem_desc(smem_u32(s0.G), 2048, 1024, kSwizzle128B) + so;
         mma_ss(tmem + kColState, a_hi, kf_hi, id_s, 1);
@@ -892,11 +928,11 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
       };
       // TMA loads of chunk c into stage c % kStages (lane 0 of warp kWarpTma only)
       const bool tma_thread = (warp == kWarpTma) && (lane == 0);
-      const bool load_v = with_u;
+      const bool load_v = with_u || rev;   // a reverse run loads dout where v goes
       int tma_issued = 0;
       auto issue_tma = [&](int c) {
         const int s = c % kStages;
-        const int row = it.row0 + c * kChunk;
+        const int row = it.row0 + dchunk(c) * kChunk;
         Stage& st = S.st[s];
         const uint32_t qkg_bytes = kdim == 64 ? 6144u : 12288u;
         mbar_arrive_expect_tx(&bar_full[s], qkg_bytes + (load_v ? (vrows == 64 ? 2048u : 4096u) : 0u));
@@ -913,6 +949,7 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
         }
         if (load_v) {
           if (vrows == 64) tma_load_3d(st.V, &p.tm_v, &bar_full[s], 0, head, row);   // V = 64: one tile
+          else if (kBwd && rev) tma_load_4d(st.V, &p.tm_dout, &bar_full[s], 0, head, row, 0);
           else tma_load_4d(st.V, &p.tm_v, &bar_full[s], 0, head, row, 2 * vblk);
         }
         ++tma_issued;
@@ -921,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_g);
-        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(kBwd && rev ? &p.tm_dout : &p.tm_v);
         for (int c = 0; c < kStages && c < nchunks; ++c) issue_tma(c);
       }
       __syncwarp();
@@ -929,7 +966,10 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
       // every epilogue warp runs every named barrier below, also after an abort,
       // so that the group never waits on a warp that left early
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_op_full[0], 0, ab));
-      // ---- initial state row v of S^T -> bf16 copy + decayed fp32 accumulator
+      // ---- initial state row v of S^T -> bf16 copy + decayed fp32 accumulator (a reverse run
+      //      starts from dL/d final_state, fp32)
+      const void* const init_ptr = rev ? static_cast<const void*>(p.dfinal) : p.init_state;
+      const int init_dt = rev ? 2 : p.init_dtype;
       if (ok) {
         const StageSmall& st0 = S.sm[0];
 #pragma unroll 1
@@ -946,18 +986,18 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
               const float4 x = src[t];
               s[4 * t] = x.x; s[4 * t + 1] = x.y; s[4 * t + 2] = x.z; s[4 * t + 3] = x.w;
             }
-          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 2 && vrow < vrows &&
+          } else if (it.in_slot == kInUser && init_ptr != nullptr && init_dt == 2 && vrow < vrows &&
                      32 * j < kdim) {
-            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) +
+            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(init_ptr) +
                                                                 srow * kdim + 32 * j);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const float4 x = src[t];
               s[4 * t] = x.x; s[4 * t + 1] = x.y; s[4 * t + 2] = x.z; s[4 * t + 3] = x.w;
             }
-          } else if (it.in_slot == kInUser && p.init_state != nullptr && p.init_dtype == 1 && vrow < vrows &&
+          } else if (it.in_slot == kInUser && init_ptr != nullptr && init_dt == 1 && vrow < vrows &&
                      32 * j < kdim) {
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.init_state) +
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(init_ptr) +
                                                               srow * kdim + 32 * j);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -984,6 +1024,8 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
             for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(s[2 * t], s[2 * t + 1]);
           }
           tmem_st16(tSb + 16u * j, pk);
+          if constexpr (kBwd)
+            store_packed16(save_state + ((slot0 + dchunk(0)) * p.H + h) * 16384 + (size_t)vrow * 128 + 32 * j, pk);
           uint32_t sv[32];
 #pragma unroll
           for (int t = 0; t < 32; ++t) sv[t] = __float_as_uint(s[t] * st0.gamC[32 * j + t]);
@@ -1004,6 +1046,16 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
       // Final state of the run's last chunk, column group j of row vrow: a workspace slot, or the
       // caller's tensor in its dtype.  A correction run adds its local final state (aux slot).
       auto write_final = [&](int j, uint32_t (&r)[32]) {
+        if constexpr (kBwd) {   // a reverse run's dS_0 -> dL/d initial_state (fp32)
+          if (rev && it.out_slot == kOutUser && p.dh0 != nullptr) {
+            float4* dst = reinterpret_cast<float4*>(p.dh0 + srow * 128 + 32 * j);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
+                                   __uint_as_float(r[4 * t + 2]), __uint_as_float(r[4 * t + 3]));
+          }
+          return;
+        }
         if (correct && it.aux_slot >= 0) {
           const float4* a = reinterpret_cast<const float4*>(p.ws_states + (size_t)it.aux_slot * 16384 +
                                                             (size_t)vrow * 128 + 32 * j);
@@ -1053,6 +1105,11 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
           uint32_t r[16];
           tmem_ld16(tD1 + 32u * b, r);
           tmem_ld_wait();
+          if constexpr (kBwd) {   // Vn (dVn) of this chunk, [16 tokens][128 v]
+            float* vd = save_vec + ((slot0 + dchunk(c)) * p.H + h) * 2048 + vrow;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) vd[128 * t] = __uint_as_float(r[t]);
+          }
           uint32_t hw[8], lw[8];
 #pragma unroll
           for (int t = 0; t < 8; ++t)
@@ -1103,6 +1160,9 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
                   pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
               }
               tmem_st16(tSb + 16u * j, pk);
+              if constexpr (kBwd)   // the state entering the next chunk handled (S_0, or dS_1 in reverse)
+                store_packed16(save_state + ((slot0 + dchunk(c + 1)) * p.H + h) * 16384 + (size_t)vrow * 128 + 32 * j,
+                               pk);
 #pragma unroll
               for (int t = 0; t < 8; ++t) {
                 const float4 gm = *reinterpret_cast<const float4*>(&stn.gamC[32 * j + 4 * t]);
@@ -1152,11 +1212,18 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
           const size_t row_elems = (size_t)p.H * vstride;
           uint16_t* obase = p.out + ((size_t)(it.row0 + c * kChunk) * p.H + h) * vstride + (size_t)kDimV * vblk;
           if (correct) {
-            if (vrow < vrows)
-              for (int i = 0; i < nv; ++i) {
-                uint16_t* o = obase + (size_t)i * row_elems + vrow;
-                *o = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_f32(*o) + p.scale * __uint_as_float(r[i])));
+            // (unrolled with a guard: a loop bound of nv would index r at run time and put it
+            // in local memory for every mode)
+            if (vrow < vrows) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                if (i < nv) {
+                  uint16_t* o = obase + (size_t)i * row_elems + vrow;
+                  *o = __bfloat16_as_ushort(
+                      __float2bfloat16_rn(bf16_bits_to_f32(*o) + p.scale * __uint_as_float(r[i])));
+                }
               }
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -1210,25 +1277,33 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
     }
   } else if (warp >= kWarpEpi0) {
     // zero-length run: the final state equals the initial state
-    if (it.mode == kModeTransition && threadIdx.x == kWarpEpi0 * 32 && it.out_slot >= 0)
-      p.zero_flags[it.out_slot] = 0;   // the identity
     const int q4 = warp & 3;
     const int vrow = q4 * 32 + lane;
-    const size_t srow = ((size_t)it.seq * p.H + head) * vstride + (size_t)kDimV * vblk + vrow;
-    for (int t = 0; t < 128; ++t) {
-      float x = 0.f;
-      if (it.in_slot == kInIdentity) x = (t == vrow) ? 1.f : 0.f;
-      else if (it.in_slot >= 0) x = p.ws_states[(size_t)it.in_slot * 16384 + (size_t)vrow * 128 + t];
-      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 2 && vrow < vrows && t < kdim)
-        x = static_cast<const float*>(p.init_state)[srow * kdim + t];
-      else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1 && vrow < vrows && t < kdim)
-        x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.init_state)[srow * kdim + t]);
-      if (it.mode == kModeCorrect && it.aux_slot >= 0) x += p.ws_states[(size_t)it.aux_slot * 16384 + (size_t)vrow * 128 + t];
-      if (it.out_slot >= 0) p.ws_states[(size_t)it.out_slot * 16384 + (size_t)vrow * 128 + t] = x;
-      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2 && vrow < vrows && t < kdim)
-        static_cast<float*>(p.final_state)[srow * kdim + t] = x;
-      else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 1 && vrow < vrows && t < kdim)
-        static_cast<uint16_t*>(p.final_state)[srow * kdim + t] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    if constexpr (kBwd) {   // a reverse run: dL/d initial_state = dL/d final_state
+      if (rev && it.out_slot == kOutUser && p.dh0 != nullptr) {
+        const size_t srow = ((size_t)it.seq * p.H + head) * 128 + vrow;
+        for (int t = 0; t < 128; ++t)
+          p.dh0[srow * 128 + t] = (it.in_slot == kInUser && p.dfinal != nullptr) ? p.dfinal[srow * 128 + t] : 0.f;
+      }
+    } else {
+      if (it.mode == kModeTransition && threadIdx.x == kWarpEpi0 * 32 && it.out_slot >= 0)
+        p.zero_flags[it.out_slot] = 0;   // the identity
+      const size_t srow = ((size_t)it.seq * p.H + head) * vstride + (size_t)kDimV * vblk + vrow;
+      for (int t = 0; t < 128; ++t) {
+        float x = 0.f;
+        if (it.in_slot == kInIdentity) x = (t == vrow) ? 1.f : 0.f;
+        else if (it.in_slot >= 0) x = p.ws_states[(size_t)it.in_slot * 16384 + (size_t)vrow * 128 + t];
+        else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 2 && vrow < vrows && t < kdim)
+          x = static_cast<const float*>(p.init_state)[srow * kdim + t];
+        else if (it.in_slot == kInUser && p.init_state && p.init_dtype == 1 && vrow < vrows && t < kdim)
+          x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.init_state)[srow * kdim + t]);
+        if (it.mode == kModeCorrect && it.aux_slot >= 0) x += p.ws_states[(size_t)it.aux_slot * 16384 + (size_t)vrow * 128 + t];
+        if (it.out_slot >= 0) p.ws_states[(size_t)it.out_slot * 16384 + (size_t)vrow * 128 + t] = x;
+        else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 2 && vrow < vrows && t < kdim)
+          static_cast<float*>(p.final_state)[srow * kdim + t] = x;
+        else if (it.out_slot == kOutUser && p.final_state && p.final_dtype == 1 && vrow < vrows && t < kdim)
+          static_cast<uint16_t*>(p.final_state)[srow * kdim + t] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      }
     }
   }
 
@@ -1238,11 +1313,51 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
   if (warp == kWarpEpi0) tmem_dealloc(tmem, kCols);
 }
 
-// Launch of one family of kernel variants: kBase is 0 (the usual kernels) or kChainPrecise.
+// kFlags (steps the caller already did) is a template parameter: the prologue's inner
+// loops then carry no per-element tests of it
+// Two CTAs per SM (128 registers a thread); the precise-state kernels run one per SM.
+template <int kFlags>
+__global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
+    kda_chain_kernel(const __grid_constant__ ChainParams p) {
+  // Item of this CTA.  The forward launch pairs runs by SM: the list is longest first, the
+  // first CTA to start on an SM takes the longest run left and the second the shortest, so
+  // a long chain shares its SM with a short one and then runs alone.
+  // the segment scan's transition runs let the forward runs' launch start beside them
+  if constexpr ((kFlags & kChainAux) != 0) griddep_launch_dependents();
+  int item = blockIdx.x;
+  if (p.take != nullptr) {
+    __shared__ int s_item;
+    if (threadIdx.x == 0) {
+      const int n_items = *p.item_count;
+      int pick = -1;
+      if (atomicAdd(&p.take[0], 1) < n_items) {   // at most n_items picks: head and tail never meet
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        const int arrival = atomicAdd(&p.sm_arrivals[smid % kMaxSmIds], 1);
+        pick = (arrival & 1) == 0 ? atomicAdd(&p.take[1], 1) : n_items - 1 - atomicAdd(&p.take[2], 1);
+      }
+      s_item = pick;
+    }
+    __syncthreads();
+    item = s_item;
+  } else if (item >= *p.item_count) {
+    item = -1;
+  }
+  // a launch that overlapped the transition runs completes only after them: every CTA waits
+  // for the previous kernel before it exits (the composition after this launch reads both)
+  if (item >= 0) {
+    const WorkItem it = p.items[item];
+    if (it.len >= 0) chain_run<kFlags, (kFlags & kChainAux) != 0>(p, it);   // len < 0: a placeholder
+  }
+  griddep_wait();
+}
+
+// Launch of one family of kernel variants: kBase is 0 (the usual kernels) or kChainPrecise, each
+// with or without kChainAux (the correction and transition runs' kernels).
 // Entries: the caller-side flags (the preactivated and softplus gates exclude each other: no
 // kernel for both), then the same for K = 64 or V = 64 (kChainPadded).
 template <int kBase>
-cudaError_t launch_chain_table(const ChainParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_chain_table(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev = false) {
   using Kernel = void (*)(ChainParams);
   static constexpr Kernel kernels[32] = {
       kda_chain_kernel<kBase + 0>, kda_chain_kernel<kBase + 1>, kda_chain_kernel<kBase + 2>,
@@ -1274,8 +1389,21 @@ cudaError_t launch_chain_table(const ChainParams& p, int grid, cudaStream_t s) {
   const bool padded = p.kdim != 128 || p.vrows != 128;
   const Kernel k = kernels[(p.flags & kValidFlags) | (padded ? kChainPadded : 0)];
   if (k == nullptr) return cudaErrorInvalidValue;
-  k<<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  if (!overlap_prev) {
+    k<<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
 }
 
 }  // namespace kda

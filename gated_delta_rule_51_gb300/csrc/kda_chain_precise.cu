@@ -6,8 +6,8 @@
 
 namespace kda {
 
-cudaError_t launch_chain_precise(const ChainParams& p, int grid, cudaStream_t s) {
-  return launch_chain_table<kChainPrecise>(p, grid, s);
+cudaError_t launch_chain_precise(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev) {
+  return launch_chain_table<kChainPrecise>(p, grid, s, overlap_prev);
 }
 
 }  // namespace kda

@@ -19,7 +19,9 @@ constexpr int kDimV = 128;
 //                    zero in fp32 (it then stays zero)
 //   kModeTransition  v taken as zero from the identity: the segment's transition matrix,
 //                    stopped (and flagged zero) once it is exactly zero in fp32
-enum : int { kModeForward = 0, kModeCorrect = 1, kModeTransition = 2 };
+//   kModeReverse     (backward chains only) the state gradient dS carried from the sequence's
+//                    end to its start: dout in place of v, chunks last first, dS_0 written out
+enum : int { kModeForward = 0, kModeCorrect = 1, kModeTransition = 2, kModeReverse = 3 };
 // in_slot values below zero:
 enum : int { kInZero = -1, kInIdentity = -2, kInUser = -3 };
 // out_slot values below zero:
@@ -41,10 +43,10 @@ struct WorkItem {
 struct WorkHeader {
   int err;             // error word (bit flags, see kda_device.cuh)
   int n_correct;       // number of correction items (the last phase)
-  int n_forward;       // number of items of the first phase (forward and transition runs)
+  int n_forward;       // number of forward runs (the first chain launch)
   int n_compose;       // number of (sequence, head) carry chains to compose
   int take[3];         // forward runs handed out: total, from the head, from the tail
-  int pad;
+  int n_transition;    // number of transition runs (their own launch, before the forward runs)
 };
 constexpr int kMaxSmIds = 256;   // per-SM arrival counters of the forward launch
 
@@ -85,6 +87,17 @@ struct ChainParams {
   int vrows;                           // value rows a chain carries to the caller: 128, or 64 for V = 64
                                        // (rows 64-127 then stay zero: v's second 64 columns read as 0)
   int precise;                         // 1: the precise-state kernels (state, W read as bf16 hi + lo)
+  // Backward chains (kChainBwd kernels) only.  Per (chunk slot, head), slot = seq + row0 / 16 +
+  // chunk (unique across sequences): the forward runs store each chunk's entering state (the
+  // bf16 copy of S^T, [128 v][128 k]) and Vn ([16 tokens][128 v] fp32); the reverse runs the
+  // gradient dS_1 at each chunk's end and dVn, in the same layouts.
+  CUtensorMap tm_dout;                 // 4-D map over dout, as tm_v
+  uint16_t* save_s0;
+  float* save_vn;
+  uint16_t* save_ds1;
+  float* save_dvn;
+  const float* dfinal;                 // reverse runs: dS at the sequence's end, fp32 [N, H, 128, 128], or null
+  float* dh0;                          // reverse runs: dS at its start (fp32), or null
 };
 
 struct ComposeParams {
@@ -105,8 +118,9 @@ struct ScheduleParams {
   WorkHeader* hdr;
   WorkItem* correct;
   WorkItem* forward;
+  WorkItem* transition;
   ComposeItem* compose;
-  long long cap_correct, cap_forward, cap_compose, cap_slots;
+  long long cap_correct, cap_forward, cap_transition, cap_compose, cap_slots;
   int* seg_rank;              // scratch: position of each forward run's segment in the list
   long long cap_ranks;
   int* sm_arrivals;           // [kMaxSmIds], zeroed here for the forward launch
@@ -122,6 +136,8 @@ constexpr unsigned kValidFlags = 15;
 // precise-state kernels (one CTA per SM)
 constexpr int kChainPadded = 16;
 constexpr int kChainPrecise = 32;
+constexpr int kChainBwd = 64;   // the backward's chains: storing forward runs and reverse runs
+constexpr int kChainAux = 128;  // the correction and transition runs' kernels (the others carry none of their code)
 
 struct DecodeParams {
   const uint16_t *q, *k, *v, *g, *beta;  // bf16 [B, T, H, K] (v [B, T, H, V]; beta [B, T, H], logits)
@@ -160,6 +176,17 @@ struct BwdParams {
   int64_t BT;                             // B * T
   int N, H, flags, nblk;
   float scale, lower_bound;
+  // The chunked path (kda_bwd.cu, kBwdChunked*): per (chunk slot, head), slot = n + row0(n) / 16 + c,
+  // what the backward chains stored, and the state products of the chunk.
+  const uint16_t* s0;                     // [slot][H][128 v][128 k] bf16: S entering the chunk
+  const float* vn;                        // [slot][H][16][128]: Vn
+  const uint16_t* ds1;                    // dS at the chunk's end, as s0
+  const float* dvn;                       // dVn, as vn
+  float* xp;                              // [slot][H][3][16][128]: dO S0^T, Vn dS1^T, dVn S0^T
+  float* zs;                              // [slot][H][128]: sum over v of dS1 * S0
+  WorkItem* items;                        // the chains' runs: N H forward, then N H reverse
+  int* item_count;
+  int64_t nslots;
 };
 
 // Backward workspace regions, in floats per unit.
@@ -171,11 +198,18 @@ constexpr int kBwdParamStride = 132;      // floats per (block, head): 128 ddt_b
 
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
-cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s);
-cudaError_t launch_chain_precise(const ChainParams& p, int grid, cudaStream_t s);
+// overlap_prev: the launch may start while the stream's previous kernel still runs (programmatic
+// dependent launch); its CTAs wait for that kernel's completion before they exit
+cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev = false);
+cudaError_t launch_chain_precise(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev = false);
+cudaError_t launch_chain_bwd(const ChainParams& p, int grid, cudaStream_t s);
+cudaError_t launch_chain_aux(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_compose(const ComposeParams& p, int grid, int sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 // phases 0-3: prep, stored-state forward, reverse, chain rule and parameter sums
 cudaError_t launch_bwd(const BwdParams& p, int phase, cudaStream_t s);
+// the chunked path around the chains' launch (launch_chain_bwd): phase 0 the error word and the
+// runs; 2 the state products; 3 the chunk gradients and the parameter sums
+cudaError_t launch_bwd_chunked(const BwdParams& p, int phase, cudaStream_t s);
 
 }  // namespace kda

@@ -29,6 +29,7 @@ EXPORTED_SYMBOLS = ("kda_status_string", "kda_workspace_size", "kda_fwd", "kda_c
                     "kda_decode", "kda_fwd_ex", "kda_bwd_workspace_size", "kda_bwd")
 KDA_GATE_PREACTIVATED, KDA_BETA_PREACTIVATED, KDA_NO_QK_L2NORM, KDA_GATE_SOFTPLUS = 1, 2, 4, 8
 KDA_PRECISE_STATE = 16
+KDA_BWD_RECURRENT = 32
 
 
 class kda_shape(ctypes.Structure):
@@ -304,12 +305,15 @@ def bwd_workspace_size(shape: kda_shape) -> int:
 def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None, dfinal=None,
         cu_seqlens=None, workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
         use_gate_in_kernel: bool = True, use_beta_sigmoid_in_kernel: bool = True,
-        use_qk_l2norm_in_kernel: bool = True, safe_gate: bool = True, out: Optional[dict] = None) -> dict:
+        use_qk_l2norm_in_kernel: bool = True, safe_gate: bool = True, out: Optional[dict] = None,
+        recurrent: bool = False) -> dict:
     """Gradients of sum(dout * out) + sum(dfinal * final_state) for the forward fwd() computes
     with the same arguments (K = V = 128).  dout: bf16 [B,T,H,128]; dfinal: fp32 [N,H,128,128]
     or None.  Returns fp32 tensors dq, dk, dg [B,T,H,128], dv [B,T,H,128], dbeta [B,T,H],
     dh0 [N,H,128,128], dA_log [H] and ddt_bias [H,128] (allocated here unless ``out`` holds
-    them).  dg is the gradient for the raw g passed in; dbeta for the beta logits."""
+    them).  dg is the gradient for the raw g passed in; dbeta for the beta logits.
+    recurrent=True asks for the fp32 token recurrence (KDA_BWD_RECURRENT) instead of the
+    chunked tensor-core form the gate with a lower bound takes by default."""
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
     B, T, H, K = q.shape
@@ -319,6 +323,8 @@ def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_stat
     N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
     V = v.shape[-1]
     flags = _flags(use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate)
+    if recurrent:
+        flags |= KDA_BWD_RECURRENT
     for name, t, dt, shp in (("q", q, torch.bfloat16, (B, T, H, K)), ("k", k, torch.bfloat16, (B, T, H, K)),
                              ("g", g, torch.bfloat16, (B, T, H, K)), ("v", v, torch.bfloat16, (B, T, H, V)),
                              ("beta", beta, torch.bfloat16, (B, T, H)), ("dout", dout, torch.bfloat16, (B, T, H, V))):
@@ -368,7 +374,7 @@ class KDAFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, scale, lower_bound,
                 use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate,
-                check_errors=False):
+                check_errors=False, recurrent_backward=False):
         B, T, H, K = q.shape
         N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
         V = v.shape[-1]
@@ -391,6 +397,7 @@ class KDAFunction(torch.autograd.Function):
         ctx.scalars = (scale, lower_bound)
         ctx.switches = sw
         ctx.check_errors = check_errors
+        ctx.recurrent = recurrent_backward
         return out, final_state
 
     @staticmethod
@@ -408,7 +415,7 @@ class KDAFunction(torch.autograd.Function):
         r = bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout.to(torch.bfloat16).contiguous(),
                 initial_state=initial_state,
                 dfinal=None if dfinal is None else dfinal.to(torch.float32).contiguous(),
-                cu_seqlens=cu_seqlens, workspace=ws, **ctx.switches)
+                cu_seqlens=cu_seqlens, workspace=ws, recurrent=ctx.recurrent, **ctx.switches)
         if ctx.check_errors:
             raise_on_device_error(check_device_error(workspace=ws, device=q.device), "kda_bwd")
         gate = ctx.switches["use_gate_in_kernel"]
@@ -418,12 +425,13 @@ class KDAFunction(torch.autograd.Function):
 
         return (cast(r["dq"], q), cast(r["dk"], k), cast(r["dv"], v), cast(r["dg"], g), cast(r["dbeta"], beta),
                 cast(r["dA_log"], A_log) if gate else None, cast(r["ddt_bias"], dt_bias) if gate else None,
-                cast(r["dh0"], initial_state), None, None, None, None, None, None, None, None)
+                cast(r["dh0"], initial_state), None, None, None, None, None, None, None, None, None)
 
 
 def kda_attention(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None, cu_seqlens=None,
                   use_gate_in_kernel: bool = True, use_beta_sigmoid_in_kernel: bool = True,
-                  use_qk_l2norm_in_kernel: bool = True, safe_gate: bool = True, check_errors: bool = False):
+                  use_qk_l2norm_in_kernel: bool = True, safe_gate: bool = True, check_errors: bool = False,
+                  recurrent_backward: bool = False):
     """The forward with autograd: returns (out, final_state); gradients flow to q, k, v, g,
     beta, A_log, dt_bias and initial_state through the CUDA backward (K = V = 128; other
     head dimensions are refused when an input requires grad).
@@ -432,7 +440,9 @@ def kda_attention(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_
     range and timed-out waits through an error word, not an exception.  With
     check_errors=True the forward and the backward each synchronise and raise KDAError when
     that word is set; otherwise the caller validates cu_seqlens (and, for the gates without a
-    lower bound, the decay range) itself."""
+    lower bound, the decay range) itself.  The backward takes the chunked tensor-core form for
+    the gate with a lower bound (gradients within 1e-2 relative Frobenius of the exact ones);
+    recurrent_backward=True asks for the fp32 token recurrence instead."""
     return KDAFunction.apply(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, scale, lower_bound,
                              use_gate_in_kernel, use_beta_sigmoid_in_kernel, use_qk_l2norm_in_kernel, safe_gate,
-                             check_errors)
+                             check_errors, recurrent_backward)

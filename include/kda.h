@@ -102,14 +102,21 @@ typedef enum { KDA_STATE_NONE = 0, KDA_STATE_BF16 = 1, KDA_STATE_FP32 = 2 } kda_
  *                           the preactivated and softplus gates, whose decay it cannot
  *                           bound; with a decaying gate the single copy's error fades
  *                           within a few chunks and the flag changes little.
- *                           kda_decode and kda_bwd compute in fp32 and ignore it.
+ *                           kda_decode and kda_bwd ignore it.
+ * And one selects the backward's form (kda_bwd only):
+ *   KDA_BWD_RECURRENT     : the token-by-token fp32 recurrence (gradients exact to fp32
+ *                           rounding) instead of the chunked tensor-core form, whose
+ *                           bf16 operands put the gradients within 1e-2 relative
+ *                           Frobenius of the exact ones.  The preactivated and softplus
+ *                           gates always take the recurrent form.
  */
 typedef enum {
     KDA_GATE_PREACTIVATED = 1,
     KDA_BETA_PREACTIVATED = 2,
     KDA_NO_QK_L2NORM = 4,
     KDA_GATE_SOFTPLUS = 8,
-    KDA_PRECISE_STATE = 16
+    KDA_PRECISE_STATE = 16,
+    KDA_BWD_RECURRENT = 32
 } kda_flags;
 
 /*
@@ -195,9 +202,10 @@ KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t st
 /*
  * Measurement aid (no counterpart in flash_kda): while `events` is non-NULL,
  * every kda_fwd records events[i] (cudaEvent_t handles owned by the caller) on
- * its stream right after its i-th launch -- 0: work-list scheduling, 1: the
- * forward runs (with the segment transition runs), 2: carry composition, 3: the
- * segment corrections -- so each phase can be timed with cudaEventElapsedTime
+ * its stream right after its i-th phase -- 0: work-list scheduling, 1: the
+ * segment transition runs and the forward runs (two launches, the second
+ * overlapping the first), 2: carry composition, 3: the segment corrections -- so
+ * each phase can be timed with cudaEventElapsedTime
  * (phases a call does not need are recorded empty).  n_events must be 4.
  * Pass NULL to stop.  The setting is process-wide and not thread-safe.
  */
@@ -284,11 +292,18 @@ KDA_API kda_status kda_decode(const kda_shape *shape, const void *q, const void 
  *                      sequence; zero with KDA_GATE_PREACTIVATED.
  *   workspace        : device scratch of at least kda_bwd_workspace_size bytes, 256-byte
  *                      aligned; it begins with the error word kda_check_device_error reads
- *                      (malformed cu_seqlens are clamped and flagged, as in kda_fwd).  It
- *                      holds the state at every 8th token: (B T / 8 + N + 1) x H x 64 KiB.
- * The result is deterministic (fixed-order sums, no atomics on values).  Returns KDA_OK
- * once the kernels are enqueued; argument errors as for kda_fwd (K or V other than 128:
- * KDA_ERR_UNSUPPORTED_SHAPE).
+ *                      (malformed cu_seqlens are clamped and flagged, as in kda_fwd).
+ * Two forms compute it.  The gate with a lower bound takes the chunked one unless flags
+ * has KDA_BWD_RECURRENT: two chains per (sequence, head) run side by side on tcgen05 (the
+ * forward storing each 16-token chunk's entering state, and the state gradient carried from
+ * the end to the start), then every chunk's gradients are computed independently; bf16
+ * operands, gradients within 1e-2 relative Frobenius of the exact ones (dA_log within 1e-3
+ * of the sum of its terms' magnitudes).  It stores about 106 KiB per 16 tokens and head.
+ * The recurrent form (the other gates, or KDA_BWD_RECURRENT) runs the token recurrence in
+ * fp32 and stores the state at every 8th token: (B T / 8 + N + 1) x H x 64 KiB.
+ * kda_bwd_workspace_size covers both.  The result is deterministic (fixed-order sums, no
+ * atomics on values).  Returns KDA_OK once the kernels are enqueued; argument errors as for
+ * kda_fwd (K or V other than 128: KDA_ERR_UNSUPPORTED_SHAPE).
  */
 KDA_API kda_status kda_bwd_workspace_size(const kda_shape *shape, size_t *bytes);
 KDA_API kda_status kda_bwd(const kda_shape *shape, const void *q, const void *k, const void *v, const void *g,

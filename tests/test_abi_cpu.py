@@ -219,6 +219,19 @@ def test_bwd_host_side_argument_errors(case, expected):
 def test_bwd_valid_arguments_reach_the_device_query():
     assert _bwd_call(kda.make_shape(1, 64, 2, 1)) in (4, 5)
     assert _bwd_call(kda.make_shape(1, 64, 2, 1), dh0=0, lb=9.0, flags=1, dt_bias=0) in (4, 5)
+    # KDA_BWD_RECURRENT selects the backward's form; kda_fwd_ex does not know it, and no
+    # higher bit is a flag
+    assert _bwd_call(kda.make_shape(1, 64, 2, 1), flags=kda.KDA_BWD_RECURRENT) in (4, 5)
+    assert _bwd_call(kda.make_shape(1, 64, 2, 1), flags=64) == 1
+    assert _fwd_ex_call(kda.KDA_BWD_RECURRENT) == 1
+
+
+def test_bwd_workspace_covers_the_chunked_form():
+    # the chunked form stores, per 16 tokens and head, S0 and dS1 (bf16, 32 KiB each), Vn and
+    # dVn (fp32, 8 KiB each), three 16 x 128 fp32 state products and a 128-float column sum
+    for shape in (kda.make_shape(1, 4096, 2, 1), kda.make_shape(3, 100, 4, 3), kda.make_shape(1, 16, 1, 1)):
+        slots = shape.B * shape.T // 16 + shape.N + 1
+        assert kda.bwd_workspace_size(shape) >= slots * shape.H * (2 * 32768 + 2 * 8192 + 3 * 8192 + 512)
 
 
 def test_bwd_workspace_holds_a_state_every_eighth_token():

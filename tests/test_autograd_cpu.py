@@ -25,9 +25,9 @@ CALLS = []
 
 
 def _fake_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None, dfinal=None,
-              cu_seqlens=None, workspace=None, **sw):
+              cu_seqlens=None, workspace=None, recurrent=False, **sw):
     CALLS.append(dict(dout_dtype=dout.dtype, dfinal_dtype=None if dfinal is None else dfinal.dtype,
-                      workspace=workspace is not None))
+                      workspace=workspace is not None, recurrent=recurrent))
     d = lambda t: None if t is None else t.detach().double().numpy()
     r = oracle.kda_backward(d(q), d(k), d(v), d(g), d(beta), float(np.float32(scale)), d(A_log), d(dt_bias),
                             float(np.float32(lower_bound)), d(dout), d(initial_state), d(dfinal),
@@ -64,7 +64,7 @@ def test_gradients_reach_every_input_in_its_dtype(init_dtype, lens):
     wo = torch.randn(out.shape, generator=gen).to(torch.bfloat16)
     wf = torch.randn(fin.shape, generator=gen)
     ((out.float() * wo.float()).sum() + (fin.float() * wf).sum()).backward()
-    assert CALLS == [dict(dout_dtype=torch.bfloat16, dfinal_dtype=torch.float32, workspace=False)]
+    assert CALLS == [dict(dout_dtype=torch.bfloat16, dfinal_dtype=torch.float32, workspace=False, recurrent=False)]
     ref = _fake_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], 0.088, x["A_log"], x["dt_bias"], -3.0, wo,
                     init, wf.to(fin.dtype).float(), cu)
     for n, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"), ("A_log", "dA_log"),

@@ -1,4 +1,5 @@
-"""GPU parity of the backward pass (kda_bwd through the C ABI) with the fp64 oracle's gradient.
+"""GPU parity of the recurrent backward (kda_bwd with KDA_BWD_RECURRENT, through the C ABI) with
+the fp64 oracle's gradient; the chunked form is tested in test_bwd_chunked_gpu.py.
 
 The oracle (oracle/kda_oracle_bwd.c, pinned by finite differences in
 test_oracle_backward_pins.py) receives exactly the GPU's inputs: the bf16 tensors, fp32
@@ -66,12 +67,12 @@ def _oracle(x, dout, dfinal, heads=None, **kw):
         None if cu is None else cu.cpu().numpy(), **kw)
 
 
-def _gpu(x, dout, dfinal, workspace=None, **kw):
+def _gpu(x, dout, dfinal, workspace=None, recurrent=True, **kw):
     from gated_delta_rule_51_gb300 import kda
 
     r = kda.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["A_log"], x["dt_bias"],
                 x["lower_bound"], dout, initial_state=x.get("initial_state"), dfinal=dfinal,
-                cu_seqlens=x.get("cu_seqlens"), workspace=workspace, **kw)
+                cu_seqlens=x.get("cu_seqlens"), workspace=workspace, recurrent=recurrent, **kw)
     torch.cuda.synchronize()
     return r
 
@@ -185,7 +186,8 @@ def test_autograd_function_matches_the_oracle_gradient():
               for n in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state")}
     out, fin = kda.kda_attention(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"], x["scale"],
                                  leaves["A_log"], leaves["dt_bias"], x["lower_bound"],
-                                 initial_state=leaves["initial_state"], cu_seqlens=x["cu_seqlens"])
+                                 initial_state=leaves["initial_state"], cu_seqlens=x["cu_seqlens"],
+                                 recurrent_backward=True)
     gen = torch.Generator().manual_seed(976)
     wo = torch.randn(out.shape, generator=gen).to(torch.bfloat16).cuda()
     wf = (0.1 * torch.randn(fin.shape, generator=gen)).cuda()
