@@ -671,6 +671,7 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     p.ppart = reinterpret_cast<float*>(ws + C.off_ppart);
     p.nblk = C.nblk;
     p.nslots = C.nslots;
+    p.sms = std::max(d.sms, 1);
     // the chains: N H forward runs storing S0 and Vn, N H reverse runs storing dS1 and dVn
     ChainParams cp;
     std::memset(&cp, 0, sizeof(cp));

@@ -20,7 +20,16 @@
 // Each chunk's per-token vectors, v and dout are staged in shared memory once, so the
 // per-token steps read no global memory.
 //
-// Kernels, in launch order:
+// Two forms.  The chunked one (the default for the gate with a lower bound; "chunked path"
+// below) runs the chunk recurrence on tensor cores in the chain kernels and every chunk's
+// gradients in parallel:
+//   items    the chains' runs (a forward and a reverse run per (sequence, head));
+//   (chains: kda_chain_kernel, kChainBwd, launched from kda_api.cu)
+//   xprod    per chunk: dO S0^T, Vn dS1^T, dVn S0^T on bf16 warp MMA, sum_v dS1 S0;
+//   chunk    per chunk: the 16 x 16 and 16 x 128 products on tf32 warp MMA (fp32-accurate
+//            split), then every token's gradients and the dA_log terms;
+//   param    dA_log and dt_bias summed over tokens, as below.
+// The recurrent one (the other gates, or KDA_BWD_RECURRENT), in launch order:
 //   prep     per token-head: alpha = exp(ghat), beta, qh, kh and the norms' scales;
 //   ckpt     the forward recurrence, storing the state at every kBwdChunk-th token;
 //   reverse  per chunk, last first: for each token (last first) the state before it is
@@ -29,8 +38,8 @@
 //            per-token column partials of dqh, dkh, dalpha, dbeta go to the workspace;
 //   finish   per token-head: the partials summed, then the norms, the sigmoid and the gate;
 //   param    dA_log and dt_bias summed over tokens in blocks, then over blocks.
-// Memory: the stored states take (B T / kBwdChunk + N + 1) x H x 64 KiB.  No kernel waits
-// on another CTA; the only barriers are __syncthreads.
+// Memory: the stored states take (B T / kBwdChunk + N + 1) x H x 64 KiB.  No kernel of either
+// form waits on another CTA; the only barriers are __syncthreads.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -421,9 +430,27 @@ __global__ void __launch_bounds__(128) kda_bwd_finish_kernel(const BwdParams p) 
 __global__ void __launch_bounds__(128) kda_bwd_param_kernel(const BwdParams p) {
   const int blk = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
   const int64_t t0 = (int64_t)blk * kBwdParamTokens, t1 = min(p.BT, t0 + kBwdParamTokens);
-  float acc = 0.f, accA = 0.f;
-  for (int64_t t = t0; t < t1; ++t) acc += p.dg[(t * p.H + h) * 128 + c];
-  for (int64_t t = t0 + c; t < t1; t += 128) accA += p.dA_tok[t * p.H + h];
+  // sixteen partial sums (token t into sum t mod 16) so that sixteen loads are in flight at once;
+  // they are combined in a fixed order, so the result is the same on every run
+  float a16[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) a16[u] = 0.f;
+  int64_t t = t0;
+  for (; t + 16 <= t1; t += 16) {
+    float x[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) x[u] = p.dg[((t + u) * p.H + h) * 128 + c];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) a16[u] += x[u];
+  }
+  for (; t < t1; ++t) a16[0] += p.dg[(t * p.H + h) * 128 + c];   // the tail, in order
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int u = 0; u < w; ++u) a16[u] += a16[u + w];
+  const float acc = a16[0];
+  float accA = 0.f;
+  for (int64_t ta = t0 + c; ta < t1; ta += 128) accA += p.dA_tok[ta * p.H + h];
   __shared__ float sA[128];
   sA[c] = accA;
   __syncthreads();
@@ -438,12 +465,32 @@ __global__ void __launch_bounds__(128) kda_bwd_param_kernel(const BwdParams p) {
 
 __global__ void __launch_bounds__(128) kda_bwd_param_sum_kernel(const BwdParams p) {
   const int h = blockIdx.x, c = threadIdx.x;
-  float acc = 0.f, accA = 0.f;
-  for (int b = 0; b < p.nblk; ++b) {
-    const float* src = p.ppart + ((size_t)b * p.H + h) * kBwdParamStride;
-    acc += src[c];
-    if (c == 0) accA += src[128];
+  // as above: sixteen partial sums over the blocks, combined in a fixed order
+  float a16[16], b16[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) a16[u] = b16[u] = 0.f;
+  int b = 0;
+  for (; b + 16 <= p.nblk; b += 16) {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float* src = p.ppart + ((size_t)(b + u) * p.H + h) * kBwdParamStride;
+      a16[u] += src[c];
+      if (c == 0) b16[u] += src[128];
+    }
   }
+  for (; b < p.nblk; ++b) {   // the tail, in order
+    const float* src = p.ppart + ((size_t)b * p.H + h) * kBwdParamStride;
+    a16[0] += src[c];
+    if (c == 0) b16[0] += src[128];
+  }
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int u = 0; u < w; ++u) {
+      a16[u] += a16[u + w];
+      b16[u] += b16[u + w];
+    }
+  const float acc = a16[0], accA = b16[0];
   if (p.ddt_bias != nullptr) p.ddt_bias[h * 128 + c] = acc;
   if (c == 0 && p.dA_log != nullptr) p.dA_log[h] = accA;
 }
@@ -462,7 +509,8 @@ __global__ void __launch_bounds__(128) kda_bwd_param_sum_kernel(const BwdParams 
 // with G the within-chunk cumsum of ghat, Gam = exp(G), Kp = kh Gam, Km = kh / Gam, Qp = qh Gam,
 // Kd = kh Gam_C / Gam, R = Kp Km^T, M = (I + Diag(beta) strict_lower(R))^-1, Tm = M Diag(beta).
 // Products of Gam and 1 / Gam are taken about the anchor a = G_C / 2 (exp(G - a), exp(a - G)),
-// so no factor leaves exp(|G_C| / 2); the gate with a lower bound keeps |G_C| <= 80.
+// so no factor leaves exp(|G_C| / 2); the gate with a lower bound keeps |G_C| <= 80.  The chunk
+// kernel keeps G in base 2 (G log2 e) and takes every factor as a power of two.
 // Then dghat = reverse cumsum of dG, and the norms, the beta sigmoid and the gate as in finish.
 
 constexpr int kXPad = 136;   // bf16 pitch of the state-product kernel's staged rows (272 bytes)
@@ -536,9 +584,11 @@ struct XprodSmem {
   float z[2][128];
 };
 
-__global__ void __launch_bounds__(256, 2) kda_bwd_xprod_kernel(const BwdParams p) {
-  const int64_t slot = blockIdx.x;
-  const int h = blockIdx.y;
+// One (chunk slot, head) unit; units are numbered with the heads fastest, so that the CTAs
+// working at once read every head of a few chunks and each token row is read whole from DRAM.
+__device__ __forceinline__ void xprod_unit(const BwdParams& p, int64_t unit) {
+  const int64_t slot = unit / p.H;
+  const int h = (int)(unit - slot * p.H);
   ChunkLoc cl;
   if (!chunk_of_slot(p, slot, cl)) return;
   extern __shared__ __align__(16) uint8_t xsm_raw[];
@@ -546,12 +596,20 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_xprod_kernel(const BwdParams p
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t sh = (size_t)slot * p.H + h;
   {
+    // all sixteen 16-byte loads of a thread in flight at once
     const uint4* a = reinterpret_cast<const uint4*>(p.s0 + sh * 16384);
     const uint4* b = reinterpret_cast<const uint4*>(p.ds1 + sh * 16384);
-    for (int i = tid; i < 2048; i += 256) {
-      const int v = i >> 4, c = (i & 15) * 8;
-      *reinterpret_cast<uint4*>(&sm.s0[v][c]) = a[i];
-      *reinterpret_cast<uint4*>(&sm.ds1[v][c]) = b[i];
+    uint4 ra[8], rb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      ra[u] = a[tid + 256 * u];
+      rb[u] = b[tid + 256 * u];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = tid + 256 * u, v = i & 127, c = (i >> 7) * 8;   // piece-major copies (kda_chain.cuh)
+      *reinterpret_cast<uint4*>(&sm.s0[v][c]) = ra[u];
+      *reinterpret_cast<uint4*>(&sm.ds1[v][c]) = rb[u];
     }
   }
   {
@@ -631,8 +689,18 @@ struct ChunkSmem {
   float qh[16][kGPad], kh[16][kGPad], G[16][kGPad];
   float Vn[16][kGPad], dVn[16][kGPad], X3[16][kGPad];
   float Kpa[16][kGPad], Kma[16][kGPad], Qpa[16][kGPad];   // kh exp(G - a), kh exp(a - G), qh exp(G - a)
-  uint16_t vb[16][kVPad], dob[16][kVPad];
-  float R[16][17], dP[16][17], dT[16][17], M[16][17], Tm[16][17], dM[16][17], Y[16][17], dA[16][17], dR[16][17];
+  union {
+    struct {   // v and dO rows (bf16), read by the first products only
+      uint16_t vb[16][kVPad], dob[16][kVPad];
+    } in;
+    struct {   // then the A operands of the second products as tf32 hi and lo parts:
+      uint32_t h[5][16][20], l[5][16][20];   // dP, dR, dP^T, dR^T, Tm^T
+    } a;
+  } u;
+  // 16 x 16 matrices, pitch 20 (the warp-MMA fragment reads of rows g, columns k + tq are then
+  // conflict-free)
+  float R[16][20], dP[16][20], dVnV[16][20], dWKp[16][20], dT[16][20], M[16][20], Tm[16][20], dM[16][20];
+  float Y[16][20], dA[16][20], dR[16][20];
   float beta[16], rq[16], rk[16], dbeta[16];
   float a[128], Ea[128], GC[128], Z[128];
 };
@@ -645,15 +713,60 @@ __device__ __forceinline__ void unpack8(const uint4 w, float (&x)[8]) {
     x[2 * u + 1] = bf16hi_to_f32(a[u]);
   }
 }
+// eight consecutive floats of shared memory as two 16-byte accesses (scalar accesses at the
+// 32-byte stride of the lanes' channel groups would conflict eight ways)
+__device__ __forceinline__ void ld8(const float* p, float (&x)[8]) {
+  const float4 a = ld4(p), b = ld4(p + 4);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void st8(float* p, const float (&x)[8]) {
+  st4(p, make_float4(x[0], x[1], x[2], x[3]));
+  st4(p + 4, make_float4(x[4], x[5], x[6], x[7]));
+}
 __device__ __forceinline__ float sum16(float x) {   // over the 16 lanes of a half-warp
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
 }
 
-__global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p) {
-  const int64_t slot = blockIdx.x;
-  const int h = blockIdx.y;
+// fp32-accurate products on tf32 warp MMA: x = hi + lo with both parts tf32 (relative 2^-22),
+// and A B = Ah Bh + Ah Bl + Al Bh (the Al Bl term is below fp32 rounding)
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+  hi = f32_to_tf32(x);
+  lo = f32_to_tf32(x - __uint_as_float(hi));
+}
+struct Frag4 {   // an A fragment (16 x 8) as hi and lo parts
+  uint32_t h[4], l[4];
+};
+struct Frag2 {   // a B fragment (8 x 8)
+  uint32_t h[2], l[2];
+};
+__device__ __forceinline__ Frag4 split4(float a0, float a1, float a2, float a3) {
+  Frag4 f;
+  tf32_split(a0, f.h[0], f.l[0]);
+  tf32_split(a1, f.h[1], f.l[1]);
+  tf32_split(a2, f.h[2], f.l[2]);
+  tf32_split(a3, f.h[3], f.l[3]);
+  return f;
+}
+__device__ __forceinline__ Frag2 split2f(float b0, float b1) {
+  Frag2 f;
+  tf32_split(b0, f.h[0], f.l[0]);
+  tf32_split(b1, f.h[1], f.l[1]);
+  return f;
+}
+__device__ __forceinline__ void mma3x(float (&d)[4], const Frag4& a, const Frag2& b) {
+  mma_tf32_16x8x8(d, a.l, b.h);
+  mma_tf32_16x8x8(d, a.h, b.l);
+  mma_tf32_16x8x8(d, a.h, b.h);
+}
+
+// the hardware base-2 exponential (relative error about 2^-22) and reciprocal
+__device__ __forceinline__ float sigm_fast(float x) { return rcp_approx(1.f + ex2_approx(-1.4426950408889634f * x)); }
+
+__device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
+  const int64_t slot = unit / p.H;
+  const int h = (int)(unit - slot * p.H);
   ChunkLoc cl;
   if (!chunk_of_slot(p, slot, cl)) return;
   extern __shared__ __align__(16) uint8_t csm_raw[];
@@ -682,10 +795,10 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p
       wv = *reinterpret_cast<const uint4*>(p.v + th * 128 + c0);
       wo = *reinterpret_cast<const uint4*>(p.dout + th * 128 + c0);
     }
-    *reinterpret_cast<uint2*>(&sm.vb[ti][c0]) = make_uint2(wv.x, wv.y);
-    *reinterpret_cast<uint2*>(&sm.vb[ti][c0 + 4]) = make_uint2(wv.z, wv.w);
-    *reinterpret_cast<uint2*>(&sm.dob[ti][c0]) = make_uint2(wo.x, wo.y);
-    *reinterpret_cast<uint2*>(&sm.dob[ti][c0 + 4]) = make_uint2(wo.z, wo.w);
+    *reinterpret_cast<uint2*>(&sm.u.in.vb[ti][c0]) = make_uint2(wv.x, wv.y);
+    *reinterpret_cast<uint2*>(&sm.u.in.vb[ti][c0 + 4]) = make_uint2(wv.z, wv.w);
+    *reinterpret_cast<uint2*>(&sm.u.in.dob[ti][c0]) = make_uint2(wo.x, wo.y);
+    *reinterpret_cast<uint2*>(&sm.u.in.dob[ti][c0 + 4]) = make_uint2(wo.z, wo.w);
     float q[8], k[8], gg[8];
     unpack8(wq, q);
     unpack8(wk, k);
@@ -700,17 +813,22 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p
     sk = sum16(sk);
     const float rq = tv ? (norm ? 1.f / sqrtf(sq + 1e-6f) : 1.f) : 0.f;
     const float rk = tv ? (norm ? 1.f / sqrtf(sk + 1e-6f) : 1.f) : 0.f;
+    float gh[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      sm.qh[ti][c0 + j] = q[j] * rq;
-      sm.kh[ti][c0 + j] = k[j] * rk;
-      sm.G[ti][c0 + j] = tv ? lb * sigm(rate * (gg[j] + dtb[j])) : 0.f;
+      q[j] *= rq;
+      k[j] *= rk;
+      // base-2 log-decay (the cumsum and every factor below are powers of two)
+      gh[j] = tv ? lb * 1.4426950408889634f * sigm_fast(rate * (gg[j] + dtb[j])) : 0.f;
     }
+    st8(&sm.qh[ti][c0], q);
+    st8(&sm.kh[ti][c0], k);
+    st8(&sm.G[ti][c0], gh);
     if ((tid & 15) == 0) {
       sm.rq[ti] = rq;
       sm.rk[ti] = rk;
       const float b = tv ? bfv(p.beta[th]) : 0.f;
-      sm.beta[ti] = tv ? (beta_pre ? b : sigm(b)) : 0.f;
+      sm.beta[ti] = tv ? (beta_pre ? b : sigm_fast(b)) : 0.f;
     }
     const float* vn = p.vn + sh * 2048 + ti * 128 + c0;
     const float* dvn = p.dvn + sh * 2048 + ti * 128 + c0;
@@ -734,38 +852,83 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p
     }
     sm.GC[tid] = acc;
     sm.a[tid] = 0.5f * acc;
-    sm.Ea[tid] = expf(0.5f * acc);
+    sm.Ea[tid] = ex2_approx(0.5f * acc);
   }
   __syncthreads();
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int c = c0 + j;
-    const float d = sm.G[ti][c] - sm.a[c];
-    const float gp = expf(d), gm = expf(-d);
-    const float kh = sm.kh[ti][c], qh = sm.qh[ti][c];
-    sm.Kpa[ti][c] = kh * gp;
-    sm.Kma[ti][c] = kh * gm;
-    sm.Qpa[ti][c] = qh * gp;
-  }
-  __syncthreads();
-  // ---- 16 x 16 products over 128 channels / value rows
   {
-    const int i = tid >> 4, j = tid & 15;
-    float r = 0.f, dp = 0.f, dvv = 0.f, dwk = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < 128; c += 4) {
-      const float4 kpi = ld4(&sm.Kpa[i][c]), kmj = ld4(&sm.Kma[j][c]), kpj = ld4(&sm.Kpa[j][c]);
-      const float4 x3i = ld4(&sm.X3[i][c]), ea = ld4(&sm.Ea[c]);
-      const float4 dvi = ld4(&sm.dVn[i][c]), vnj = ld4(&sm.Vn[j][c]);
-      const float4 vj = bf4(&sm.vb[j][c]), oi = bf4(&sm.dob[i][c]);
-      r += dot4(kpi, kmj);
-      dwk += x3i.x * kpj.x * ea.x + x3i.y * kpj.y * ea.y + x3i.z * kpj.z * ea.z + x3i.w * kpj.w * ea.w;
-      dvv += dot4(dvi, vj);
-      dp += dot4(oi, vnj);
+    float Gv[8], av[8], kh[8], qh[8], kpa[8], kma[8], qpa[8];
+    ld8(&sm.G[ti][c0], Gv);
+    ld8(&sm.a[c0], av);
+    ld8(&sm.kh[ti][c0], kh);
+    ld8(&sm.qh[ti][c0], qh);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float d = Gv[j] - av[j];
+      const float gp = ex2_approx(d), gm = ex2_approx(-d);
+      kpa[j] = kh[j] * gp;
+      kma[j] = kh[j] * gm;
+      qpa[j] = qh[j] * gp;
     }
-    sm.R[i][j] = r;
-    sm.dP[i][j] = j <= i ? p.scale * dp : 0.f;
-    sm.dT[i][j] = dvv - dwk;   // dVn V^T + dW Kp^T with dW = -X3
+    st8(&sm.Kpa[ti][c0], kpa);
+    st8(&sm.Kma[ti][c0], kma);
+    st8(&sm.Qpa[ti][c0], qpa);
+  }
+  __syncthreads();
+  // ---- 16 x 16 products over the 128 channels / value rows, on tf32 warp MMA: warp w computes
+  //      columns 8 (w & 1) .. + 7 of R = Kp' Km'^T, dP = scale dO Vn^T, dVnV = dVn V^T or
+  //      dWKp = X3 Kp^T (w >> 1); fragments: rows g, g + 8 and k columns tq, tq + 4
+  {
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
+    const int prod = warp >> 1, j0 = 8 * (warp & 1);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int c = 0; c < 128; c += 8) {
+      const int ca = c + tq, cb = c + tq + 4;
+      if (prod == 0) {
+        const Frag4 fa = split4(sm.Kpa[g][ca], sm.Kpa[g + 8][ca], sm.Kpa[g][cb], sm.Kpa[g + 8][cb]);
+        const Frag2 fb = split2f(sm.Kma[j0 + g][ca], sm.Kma[j0 + g][cb]);
+        mma3x(acc, fa, fb);
+      } else if (prod == 1) {   // dO is bf16: exact in tf32
+        const uint32_t ah[4] = {f32_to_tf32(bfv(sm.u.in.dob[g][ca])), f32_to_tf32(bfv(sm.u.in.dob[g + 8][ca])),
+                                f32_to_tf32(bfv(sm.u.in.dob[g][cb])), f32_to_tf32(bfv(sm.u.in.dob[g + 8][cb]))};
+        const Frag2 fb = split2f(sm.Vn[j0 + g][ca], sm.Vn[j0 + g][cb]);
+        mma_tf32_16x8x8(acc, ah, fb.l);
+        mma_tf32_16x8x8(acc, ah, fb.h);
+      } else if (prod == 2) {   // v is bf16: exact in tf32
+        const Frag4 fa = split4(sm.dVn[g][ca], sm.dVn[g + 8][ca], sm.dVn[g][cb], sm.dVn[g + 8][cb]);
+        const uint32_t bh[2] = {f32_to_tf32(bfv(sm.u.in.vb[j0 + g][ca])), f32_to_tf32(bfv(sm.u.in.vb[j0 + g][cb]))};
+        mma_tf32_16x8x8(acc, fa.l, bh);
+        mma_tf32_16x8x8(acc, fa.h, bh);
+      } else {
+        const Frag4 fa = split4(sm.X3[g][ca], sm.X3[g + 8][ca], sm.X3[g][cb], sm.X3[g + 8][cb]);
+        const Frag2 fb = split2f(sm.Kpa[j0 + g][ca] * sm.Ea[ca], sm.Kpa[j0 + g][cb] * sm.Ea[cb]);
+        mma3x(acc, fa, fb);
+      }
+    }
+    float (*dst)[20] = prod == 0 ? sm.R : prod == 1 ? sm.dP : prod == 2 ? sm.dVnV : sm.dWKp;
+    const int jc = j0 + 2 * tq;
+    float v0 = acc[0], v1 = acc[1], v2 = acc[2], v3 = acc[3];
+    if (prod == 1) {   // dP = scale dO Vn^T on and below the diagonal
+      v0 = jc <= g ? p.scale * v0 : 0.f;
+      v1 = jc + 1 <= g ? p.scale * v1 : 0.f;
+      v2 = jc <= g + 8 ? p.scale * v2 : 0.f;
+      v3 = jc + 1 <= g + 8 ? p.scale * v3 : 0.f;
+    }
+    dst[g][jc] = v0;
+    dst[g][jc + 1] = v1;
+    dst[g + 8][jc] = v2;
+    dst[g + 8][jc + 1] = v3;
+  }
+  __syncthreads();
+  {   // dT = dVn V^T + dW Kp^T with dW = -X3; dP and dP^T as tf32 parts (v and dO are read no more)
+    const int i = tid >> 4, j = tid & 15;
+    sm.dT[i][j] = sm.dVnV[i][j] - sm.dWKp[i][j];
+    uint32_t hi, lo;
+    tf32_split(sm.dP[i][j], hi, lo);
+    sm.u.a.h[0][i][j] = hi;
+    sm.u.a.l[0][i][j] = lo;
+    sm.u.a.h[2][j][i] = hi;
+    sm.u.a.l[2][j][i] = lo;
   }
   __syncthreads();
   // ---- M = (I + Diag(beta) strict_lower(R))^-1, one column per thread (forward substitution)
@@ -788,7 +951,9 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p
   __syncthreads();
   {
     const int i = tid >> 4, j = tid & 15;
-    sm.Tm[i][j] = sm.M[i][j] * sm.beta[j];
+    const float tm = sm.M[i][j] * sm.beta[j];
+    sm.Tm[i][j] = tm;
+    tf32_split(tm, sm.u.a.h[4][j][i], sm.u.a.l[4][j][i]);
     sm.dM[i][j] = sm.dT[i][j] * sm.beta[j];
   }
   __syncthreads();
@@ -809,6 +974,12 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p
     }
     sm.dA[i][j] = d;
     sm.dR[i][j] = sm.beta[i] * d;
+    uint32_t hi, lo;
+    tf32_split(sm.beta[i] * d, hi, lo);
+    sm.u.a.h[1][i][j] = hi;
+    sm.u.a.l[1][i][j] = lo;
+    sm.u.a.h[3][j][i] = hi;
+    sm.u.a.l[3][j][i] = lo;
   }
   __syncthreads();
   if (tid < 16) {
@@ -820,68 +991,112 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p
     for (int s2 = 0; s2 < 16; ++s2) db = fmaf(sm.dA[s][s2], sm.R[s][s2], db);
     sm.dbeta[s] = db;
   }
-  // ---- per element: dqh, dkh, dv, dG (before the cumsum) and dKd Kd
-  float dqh[8], dkh[8], dG[8], dkdkh[8];
+  __syncthreads();
+  // ---- [16 tokens] x [128 channels] products over the chunk's tokens, on tf32 warp MMA; warp w
+  //      owns channels 16 w .. + 15 (n-tiles nt = 0, 1):
+  //        sq = dP Km',  sp = dR Km',  smk = dP^T Qp' + dR^T Kp',  tw = Tm^T X3,  dv = Tm^T dVn
+  //      then, per element it holds (tokens g, g + 8; channels 16 w + 8 nt + 2 tq, + 1):
+  //      dqh, dkh, dv, dG (before the cumsum) and dKd Kd
   {
-    const float* xb = p.xp + sh * 6144 + ti * 128 + c0;
-    float x1[8], x2[8];
-    {
-      const float4 a0 = ld4(xb), a1 = ld4(xb + 4), b0 = ld4(xb + 2048), b1 = ld4(xb + 2048 + 4);
-      x1[0] = a0.x; x1[1] = a0.y; x1[2] = a0.z; x1[3] = a0.w; x1[4] = a1.x; x1[5] = a1.y; x1[6] = a1.z; x1[7] = a1.w;
-      x2[0] = b0.x; x2[1] = b0.y; x2[2] = b0.z; x2[3] = b0.w; x2[4] = b1.x; x2[5] = b1.y; x2[6] = b1.z; x2[7] = b1.w;
-    }
-    float sq[8] = {}, sp[8] = {}, smk[8] = {}, tw[8] = {}, dv[8] = {};
-#pragma unroll 2
-    for (int j = 0; j < 16; ++j) {
-      const float dpij = sm.dP[ti][j], drij = sm.dR[ti][j], dpji = sm.dP[j][ti], drji = sm.dR[j][ti];
-      const float tmji = sm.Tm[j][ti];
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
+    const float* xb = p.xp + sh * 6144;
+#pragma unroll 1
+    for (int nt = 0; nt < 2; ++nt) {
+      // this n-tile's X1 and X2 elements, loaded before its MMAs so that their latency is hidden
+      const int c = 16 * warp + 8 * nt + 2 * tq;
+      float2 x1v[2], x2v[2];
 #pragma unroll
-      for (int h4 = 0; h4 < 8; h4 += 4) {
-        const float4 km = ld4(&sm.Kma[j][c0 + h4]), qp = ld4(&sm.Qpa[j][c0 + h4]), kp = ld4(&sm.Kpa[j][c0 + h4]);
-        const float4 x3 = ld4(&sm.X3[j][c0 + h4]), dn = ld4(&sm.dVn[j][c0 + h4]);
-        const float kmv[4] = {km.x, km.y, km.z, km.w}, qpv[4] = {qp.x, qp.y, qp.z, qp.w};
-        const float kpv[4] = {kp.x, kp.y, kp.z, kp.w}, x3v[4] = {x3.x, x3.y, x3.z, x3.w};
-        const float dnv[4] = {dn.x, dn.y, dn.z, dn.w};
+      for (int hr = 0; hr < 2; ++hr) {
+        x1v[hr] = *reinterpret_cast<const float2*>(xb + (g + 8 * hr) * 128 + c);
+        x2v[hr] = *reinterpret_cast<const float2*>(xb + 2048 + (g + 8 * hr) * 128 + c);
+      }
+      float sq[4] = {}, sp[4] = {}, smk[4] = {}, tw[4] = {}, dv[4] = {};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          sq[h4 + u] = fmaf(dpij, kmv[u], sq[h4 + u]);
-          sp[h4 + u] = fmaf(drij, kmv[u], sp[h4 + u]);
-          smk[h4 + u] = fmaf(dpji, qpv[u], fmaf(drji, kpv[u], smk[h4 + u]));
-          tw[h4 + u] = fmaf(tmji, x3v[u], tw[h4 + u]);
-          dv[h4 + u] = fmaf(tmji, dnv[u], dv[h4 + u]);
+      for (int kk = 0; kk < 16; kk += 8) {
+        const int ka = kk + tq, kb = kk + tq + 4;
+        auto frag = [&](int m) {
+          Frag4 f;
+          f.h[0] = sm.u.a.h[m][g][ka]; f.h[1] = sm.u.a.h[m][g + 8][ka];
+          f.h[2] = sm.u.a.h[m][g][kb]; f.h[3] = sm.u.a.h[m][g + 8][kb];
+          f.l[0] = sm.u.a.l[m][g][ka]; f.l[1] = sm.u.a.l[m][g + 8][ka];
+          f.l[2] = sm.u.a.l[m][g][kb]; f.l[3] = sm.u.a.l[m][g + 8][kb];
+          return f;
+        };
+        const int cb = 16 * warp + 8 * nt + g;
+        const Frag2 bKm = split2f(sm.Kma[ka][cb], sm.Kma[kb][cb]);
+        const Frag2 bQp = split2f(sm.Qpa[ka][cb], sm.Qpa[kb][cb]);
+        const Frag2 bKp = split2f(sm.Kpa[ka][cb], sm.Kpa[kb][cb]);
+        const Frag2 bX3 = split2f(sm.X3[ka][cb], sm.X3[kb][cb]);
+        const Frag2 bdV = split2f(sm.dVn[ka][cb], sm.dVn[kb][cb]);
+        {
+          const Frag4 fP = frag(0);
+          mma3x(sq, fP, bKm);
+        }
+        {
+          const Frag4 fR = frag(1);
+          mma3x(sp, fR, bKm);
+        }
+        {
+          const Frag4 fPt = frag(2);
+          mma3x(smk, fPt, bQp);
+        }
+        {
+          const Frag4 fRt = frag(3);
+          mma3x(smk, fRt, bKp);
+        }
+        {
+          const Frag4 fTt = frag(4);
+          mma3x(tw, fTt, bX3);
+          mma3x(dv, fTt, bdV);
+        }
+      }
+      __syncwarp();   // every lane has read columns 16 w + 8 nt .. + 7 of Kpa, Qpa and X3: rewritten below
+      const float2 av = *reinterpret_cast<const float2*>(&sm.a[c]);
+      const float2 gcv = *reinterpret_cast<const float2*>(&sm.GC[c]);
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = g + 8 * hr;
+        const float2 Gv = *reinterpret_cast<const float2*>(&sm.G[i][c]);
+        const float2 khv = *reinterpret_cast<const float2*>(&sm.kh[i][c]);
+        const float2 qhv = *reinterpret_cast<const float2*>(&sm.qh[i][c]);
+        const float2 x1 = x1v[hr], x2 = x2v[hr];
+        const float Ge[2] = {Gv.x, Gv.y}, ae[2] = {av.x, av.y}, gce[2] = {gcv.x, gcv.y};
+        const float khe[2] = {khv.x, khv.y}, qhe[2] = {qhv.x, qhv.y}, x1e[2] = {x1.x, x1.y}, x2e[2] = {x2.x, x2.y};
+        float dqh[2], dkh[2], dG[2], dkdkh[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = 2 * hr + e;   // accumulator element: (row g + 8 hr, column 2 tq + e)
+          const float d = Ge[e] - ae[e];
+          const float gam = ex2_approx(Ge[e]), gp = ex2_approx(d), gm = ex2_approx(-d);
+          const float dk = ex2_approx(gce[e] - Ge[e]);
+          dqh[e] = p.scale * x1e[e] * gam + gp * sq[r];
+          const float dkp = -tw[r] * gam + gp * sp[r];
+          const float dkm = gm * smk[r];
+          const float dkd = x2e[e] * dk;
+          dkh[e] = dkp + dkm + dkd;
+          dG[e] = (dkp - dkm - dkd) * khe[e] + dqh[e] * qhe[e];
+          dkdkh[e] = dkd * khe[e];
+        }
+        *reinterpret_cast<float2*>(&sm.Kpa[i][c]) = make_float2(dqh[0], dqh[1]);
+        *reinterpret_cast<float2*>(&sm.Qpa[i][c]) = make_float2(dkh[0], dkh[1]);
+        *reinterpret_cast<float2*>(&sm.Vn[i][c]) = make_float2(dG[0], dG[1]);
+        *reinterpret_cast<float2*>(&sm.X3[i][c]) = make_float2(dkdkh[0], dkdkh[1]);
+        if (i < cl.nv) {
+          const int64_t thi = (cl.row + i) * p.H + h;
+          *reinterpret_cast<float2*>(p.dv + thi * 128 + c) = make_float2(dv[2 * hr], dv[2 * hr + 1]);
         }
       }
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = c0 + j;
-      const float Gv = sm.G[ti][c], d = Gv - sm.a[c];
-      const float gam = expf(Gv), gp = expf(d), gm = expf(-d), dk = expf(sm.GC[c] - Gv);
-      const float kh = sm.kh[ti][c], qh = sm.qh[ti][c];
-      dqh[j] = p.scale * x1[j] * gam + gp * sq[j];
-      const float dkp = -tw[j] * gam + gp * sp[j];
-      const float dkm = gm * smk[j];
-      const float dkd = x2[j] * dk;
-      dkh[j] = dkp + dkm + dkd;
-      dG[j] = (dkp - dkm - dkd) * kh + dqh[j] * qh;
-      dkdkh[j] = dkd * kh;
-    }
-    if (tv) {
-      st4(p.dv + th * 128 + c0, make_float4(dv[0], dv[1], dv[2], dv[3]));
-      st4(p.dv + th * 128 + c0 + 4, make_float4(dv[4], dv[5], dv[6], dv[7]));
-    }
-  }
-  __syncthreads();   // every read of Vn and X3 is done: they now hold dG and dKd Kd
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    sm.Vn[ti][c0 + j] = dG[j];
-    sm.X3[ti][c0 + j] = dkdkh[j];
   }
   __syncthreads();
+  // g of this thread's token and channels, for the gate's chain rule at the end (loaded now, so
+  // that its latency passes during the per-channel step)
+  uint4 wg = make_uint4(0u, 0u, 0u, 0u);
+  if (tv) wg = *reinterpret_cast<const uint4*>(p.g + th * 128 + c0);
   // ---- per channel: the last token's terms, then the reverse cumsum (dghat)
   if (tid < 128) {
     const int c = tid, last = cl.nv - 1;
-    float sl = expf(sm.GC[c]) * sm.Z[c];
+    float sl = ex2_approx(sm.GC[c]) * sm.Z[c];
     for (int i = 0; i <= last; ++i) sl += sm.X3[i][c];
     float acc = 0.f;
     for (int i = last; i >= 0; --i) {
@@ -892,30 +1107,31 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p
   __syncthreads();
   // ---- per token: the norms, the beta sigmoid and the gate
   {
+    float qh[8], kh[8], dgh[8], dqh[8], dkh[8];
+    ld8(&sm.qh[ti][c0], qh);
+    ld8(&sm.kh[ti][c0], kh);
+    ld8(&sm.Vn[ti][c0], dgh);
+    ld8(&sm.Kpa[ti][c0], dqh);
+    ld8(&sm.Qpa[ti][c0], dkh);
     float qd = 0.f, kd = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      qd = fmaf(sm.qh[ti][c0 + j], dqh[j], qd);
-      kd = fmaf(sm.kh[ti][c0 + j], dkh[j], kd);
+      qd = fmaf(qh[j], dqh[j], qd);
+      kd = fmaf(kh[j], dkh[j], kd);
     }
     qd = sum16(qd);
     kd = sum16(kd);
     const float rq = sm.rq[ti], rk = sm.rk[ti];
     float dq[8], dk[8], dg[8], wa = 0.f;
     float gg[8];
-    {
-      uint4 wg = make_uint4(0u, 0u, 0u, 0u);
-      if (tv) wg = *reinterpret_cast<const uint4*>(p.g + th * 128 + c0);
-      unpack8(wg, gg);
-    }
+    unpack8(wg, gg);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int c = c0 + j;
-      dq[j] = norm ? rq * (dqh[j] - sm.qh[ti][c] * qd) : dqh[j];
-      dk[j] = norm ? rk * (dkh[j] - sm.kh[ti][c] * kd) : dkh[j];
+      dq[j] = norm ? rq * (dqh[j] - qh[j] * qd) : dqh[j];
+      dk[j] = norm ? rk * (dkh[j] - kh[j] * kd) : dkh[j];
       // ghat = lb sigmoid(z), z = rate x: d/dx = rate lb s (1 - s); d/dA_log = x d/dx
-      const float x = gg[j] + dtb[j], sg = sigm(rate * x);
-      dg[j] = sm.Vn[ti][c] * lb * sg * (1.f - sg) * rate;
+      const float x = gg[j] + dtb[j], sg = sigm_fast(rate * x);
+      dg[j] = dgh[j] * lb * sg * (1.f - sg) * rate;
       wa = fmaf(dg[j], x, wa);
     }
     wa = sum16(wa);
@@ -932,6 +1148,22 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p
         p.dA_tok[th] = wa;
       }
     }
+  }
+}
+
+// Persistent CTAs (two per SM) walk the units: no CTA is launched per chunk.
+__global__ void __launch_bounds__(256, 2) kda_bwd_xprod_kernel(const BwdParams p) {
+  const int64_t units = p.nslots * p.H;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    xprod_unit(p, u);
+    __syncthreads();   // the unit's shared memory is reused by the next
+  }
+}
+__global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p) {
+  const int64_t units = p.nslots * p.H;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    chunk_unit(p, u);
+    __syncthreads();
   }
 }
 
@@ -995,7 +1227,7 @@ cudaError_t launch_bwd_chunked(const BwdParams& p, int phase, cudaStream_t s) {
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
   const int64_t NH = (int64_t)p.N * p.H;
-  const dim3 slots_grid((unsigned)std::max<int64_t>(p.nslots, 1), (unsigned)p.H);
+  const unsigned slots_grid = (unsigned)std::max<int64_t>(std::min<int64_t>(p.nslots * p.H, 2 * (int64_t)p.sms), 1);
   switch (phase) {
     case 0: {   // error word, the chains' runs
       if ((e = cudaMemsetAsync(p.err, 0, sizeof(int), s)) != cudaSuccess) return e;

@@ -168,11 +168,14 @@ __device__ __forceinline__ void mul2(uint32_t& x0, uint32_t& x1, float b0, float
   asm("mov.b64 {%0, %1}, %2;" : "=r"(x0), "=r"(x1) : "l"(c));
 }
 
-// 32 bf16 values (16 packed words) to global memory, 16 bytes at a time
-__device__ __forceinline__ void store_packed16(uint16_t* dst, const uint32_t (&pk)[16]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// Column group j (32 bf16 values, 16 packed words) of row `row` of a stored 128 x 128 state copy.
+// The copy is kept piece-major: 16-byte piece q (columns 8 q .. 8 q + 7) of row r at piece
+// index q * 128 + r, so that the 32 lanes of a warp (consecutive rows) write 512 contiguous bytes.
+__device__ __forceinline__ void store_packed16(uint16_t* copy, int row, int j, const uint32_t (&pk)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(copy);
 #pragma unroll
-  for (int t = 0; t < 4; ++t) d[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+  for (int t = 0; t < 4; ++t)
+    d[(4 * j + t) * 128 + row] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
 }
 
 // Named barrier of one prologue pair (64 threads; ids 1 and 2).
@@ -1025,7 +1028,7 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
           }
           tmem_st16(tSb + 16u * j, pk);
           if constexpr (kBwd)
-            store_packed16(save_state + ((slot0 + dchunk(0)) * p.H + h) * 16384 + (size_t)vrow * 128 + 32 * j, pk);
+            store_packed16(save_state + ((slot0 + dchunk(0)) * p.H + h) * 16384, vrow, j, pk);
           uint32_t sv[32];
 #pragma unroll
           for (int t = 0; t < 32; ++t) sv[t] = __float_as_uint(s[t] * st0.gamC[32 * j + t]);
@@ -1161,8 +1164,7 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
               }
               tmem_st16(tSb + 16u * j, pk);
               if constexpr (kBwd)   // the state entering the next chunk handled (S_0, or dS_1 in reverse)
-                store_packed16(save_state + ((slot0 + dchunk(c + 1)) * p.H + h) * 16384 + (size_t)vrow * 128 + 32 * j,
-                               pk);
+                store_packed16(save_state + ((slot0 + dchunk(c + 1)) * p.H + h) * 16384, vrow, j, pk);
 #pragma unroll
               for (int t = 0; t < 8; ++t) {
                 const float4 gm = *reinterpret_cast<const float4*>(&stn.gamC[32 * j + 4 * t]);

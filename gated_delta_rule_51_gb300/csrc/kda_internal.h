@@ -89,8 +89,8 @@ struct ChainParams {
   int precise;                         // 1: the precise-state kernels (state, W read as bf16 hi + lo)
   // Backward chains (kChainBwd kernels) only.  Per (chunk slot, head), slot = seq + row0 / 16 +
   // chunk (unique across sequences): the forward runs store each chunk's entering state (the
-  // bf16 copy of S^T, [128 v][128 k]) and Vn ([16 tokens][128 v] fp32); the reverse runs the
-  // gradient dS_1 at each chunk's end and dVn, in the same layouts.
+  // bf16 copy of S^T, piece-major: 16-byte piece q of row v at [q][v]) and Vn ([16 tokens][128 v]
+  // fp32); the reverse runs the gradient dS_1 at each chunk's end and dVn, in the same layouts.
   CUtensorMap tm_dout;                 // 4-D map over dout, as tm_v
   uint16_t* save_s0;
   float* save_vn;
@@ -178,7 +178,8 @@ struct BwdParams {
   float scale, lower_bound;
   // The chunked path (kda_bwd.cu, kBwdChunked*): per (chunk slot, head), slot = n + row0(n) / 16 + c,
   // what the backward chains stored, and the state products of the chunk.
-  const uint16_t* s0;                     // [slot][H][128 v][128 k] bf16: S entering the chunk
+  const uint16_t* s0;                     // [slot][H] bf16 copies of S^T entering the chunk, piece-major:
+                                          // columns 8 q .. 8 q + 7 of row v at [q][v][8]
   const float* vn;                        // [slot][H][16][128]: Vn
   const uint16_t* ds1;                    // dS at the chunk's end, as s0
   const float* dvn;                       // dVn, as vn
@@ -187,6 +188,7 @@ struct BwdParams {
   WorkItem* items;                        // the chains' runs: N H forward, then N H reverse
   int* item_count;
   int64_t nslots;
+  int sms;                                // the device's SM count (persistent CTAs: two per SM)
 };
 
 // Backward workspace regions, in floats per unit.
