@@ -156,8 +156,8 @@ BwdLayout make_bwd_layout(const kda_shape& s) {
 // states (bf16), Vn and dVn (fp32), the state products, then the per-token dA_log terms and the
 // parameter-reduction blocks.  Slots: n + row0(n) / 16 + c is below N + B T / 16 + 1.
 struct BwdChunkedLayout {
-  size_t off_hdr = 0, off_items = 0, off_s0 = 0, off_ds1 = 0, off_vn = 0, off_dvn = 0, off_xp = 0, off_zs = 0,
-         off_dA = 0, off_ppart = 0, total = 0;
+  size_t off_hdr = 0, off_items = 0, off_citems = 0, off_bslots = 0, off_s0 = 0, off_ds1 = 0, off_vn = 0, off_dvn = 0,
+         off_xp = 0, off_zs = 0, off_dA = 0, off_ppart = 0, total = 0;
   int64_t nslots = 0;
   int nblk = 0;
 };
@@ -172,7 +172,11 @@ BwdChunkedLayout make_bwd_chunked_layout(const kda_shape& s) {
   L.off_hdr = off;
   off = align_up(off + sizeof(WorkHeader));
   L.off_items = off;
+  off = align_up(off + 4 * (size_t)s.N * (size_t)s.H * sizeof(WorkItem));
+  L.off_citems = off;
   off = align_up(off + 2 * (size_t)s.N * (size_t)s.H * sizeof(WorkItem));
+  L.off_bslots = off;
+  off = align_up(off + 3 * (size_t)s.N * (size_t)s.H * kSlotBytes);
   L.off_s0 = off;
   off = align_up(off + SH * 16384 * sizeof(uint16_t));
   L.off_ds1 = off;
@@ -661,6 +665,12 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     p.err = &reinterpret_cast<WorkHeader*>(ws + C.off_hdr)->err;
     p.items = reinterpret_cast<WorkItem*>(ws + C.off_items);
     p.item_count = &reinterpret_cast<WorkHeader*>(ws + C.off_hdr)->n_forward;
+    p.citems = reinterpret_cast<WorkItem*>(ws + C.off_citems);
+    p.citem_count = &reinterpret_cast<WorkHeader*>(ws + C.off_hdr)->n_correct;
+    p.bslots = reinterpret_cast<float*>(ws + C.off_bslots);
+    // split each sequence in two when the chains alone would leave most SMs idle (four runs per
+    // (sequence, head) still fit one wave of two CTAs per SM)
+    p.split = 4 * s.N * s.H <= 2 * (int64_t)std::max(d.sms, 1) ? 1 : 0;
     p.s0 = reinterpret_cast<const uint16_t*>(ws + C.off_s0);
     p.ds1 = reinterpret_cast<const uint16_t*>(ws + C.off_ds1);
     p.vn = reinterpret_cast<const float*>(ws + C.off_vn);
@@ -695,6 +705,7 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     cp.save_dvn = reinterpret_cast<float*>(ws + C.off_dvn);
     cp.items = p.items;
     cp.item_count = p.item_count;
+    cp.ws_states = p.bslots;
     cp.err = p.err;
     cp.H = (int)s.H;
     cp.vsplit = 1;
@@ -707,14 +718,20 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     // profile marks: the runs, the chains, the state products, the chunk gradients
     if (launch_bwd_chunked(p, 0, stream) != cudaSuccess) return KDA_ERR_CUDA;
     mark(0, stream);
-    if (launch_chain_bwd(cp, (int)(2 * s.N * s.H), stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_chain_bwd(cp, (int)(4 * s.N * s.H), stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (p.split) {   // the corrections of the split sequences
+      ChainParams cc = cp;
+      cc.items = p.citems;
+      cc.item_count = p.citem_count;
+      if (launch_chain_bwd(cc, (int)(2 * s.N * s.H), stream, true) != cudaSuccess) return KDA_ERR_CUDA;
+    }
     mark(1, stream);
     if (launch_bwd_chunked(p, 2, stream) != cudaSuccess) return KDA_ERR_CUDA;
     mark(2, stream);
     if (launch_bwd_chunked(p, 3, stream) != cudaSuccess) return KDA_ERR_CUDA;
     mark(3, stream);
     const bool work = p.BT > 0 && p.H > 0;
-    t_last_launches = 1 + (s.N > 0 ? 1 : 0) + (work ? 2 : 0) +
+    t_last_launches = 1 + (s.N > 0 ? 1 + p.split : 0) + (work ? 2 : 0) +
                       ((dA_log == nullptr && ddt_bias == nullptr) ? 0 : (C.nblk > 0 ? 2 : 1));
     return KDA_OK;
   }

@@ -543,28 +543,66 @@ __device__ __forceinline__ bool chunk_of_slot(const BwdParams& p, int64_t slot, 
   return true;
 }
 
-// The chains' runs: per (sequence, head) a forward run storing S0 and Vn, then the same count
-// of reverse runs carrying dS from dfinal (or zero) to dh0.
+__device__ __forceinline__ WorkItem bwd_item(int64_t row0, int64_t len, int h, int mode, int n, int in_slot,
+                                             int out_slot, int aux_slot) {
+  WorkItem it;
+  it.row0 = (int)row0;
+  it.len = (int)len;
+  it.head = h;
+  it.mode = mode;
+  it.seq = n;
+  it.in_slot = in_slot;
+  it.out_slot = out_slot;
+  it.aux_slot = aux_slot;
+  return it;
+}
+
+// The chains' runs.  First launch, four per (sequence, head): forward runs storing S0 and Vn, and
+// reverse runs carrying dS from dfinal (or zero) to dh0 and storing dS1 and dVn.  With p.split, a
+// sequence of two or more chunks is cut at chunk m = ceil(chunks / 2), and the four runs are the
+// forward runs of its two halves (the second from zero) and the reverse runs of its two halves (the
+// first from zero); the second launch then runs, per (sequence, head), the forward correction of
+// the second half from the true state at the cut (slot A, left by the first half's forward run)
+// and the reverse correction of the first half from the true dS at the cut (slot B), which adds
+// the first half's own reverse run's final dS (slot C) to give dh0.  Both corrections take v
+// (dout) as zero and add their part to what the halves' runs stored; by linearity the sums are
+// the unsplit runs' values.  Unused entries are placeholders (len < 0).
 __global__ void __launch_bounds__(256) kda_bwd_items_kernel(const BwdParams p) {
   const int64_t NH = (int64_t)p.N * p.H;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * NH; i += stride) {
-    const bool rev = i >= NH;
-    const int64_t r = rev ? i - NH : i;
-    const int n = (int)(r / p.H), h = (int)(r - (int64_t)n * p.H);
-    const SeqRange sr = seq_range(p, n, !rev && h == 0);
-    WorkItem it;
-    it.row0 = (int)sr.t0;
-    it.len = (int)sr.len;
-    it.head = h;
-    it.mode = rev ? kModeReverse : kModeForward;
-    it.seq = n;
-    it.in_slot = (rev ? p.dfinal != nullptr : p.init_state != nullptr) ? kInUser : kInZero;
-    it.out_slot = (rev && p.dh0 != nullptr) ? kOutUser : kOutNone;
-    it.aux_slot = -1;
-    p.items[i] = it;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < NH; i += stride) {
+    const int n = (int)(i / p.H), h = (int)(i - (int64_t)n * p.H);
+    const SeqRange sr = seq_range(p, n, h == 0);
+    const int64_t chunks = (sr.len + 15) / 16;
+    const bool sp = p.split && chunks >= 2;
+    const int64_t len0 = sp ? 16 * ((chunks + 1) / 2) : sr.len, len1 = sr.len - len0;
+    const int sA = (int)(3 * i), sB = sA + 1, sC = sA + 2;
+    const int in_f = p.init_state != nullptr ? kInUser : kInZero;
+    const int in_r = p.dfinal != nullptr ? kInUser : kInZero;
+    const int dh = p.dh0 != nullptr ? kOutUser : kOutNone;
+    const WorkItem none = bwd_item(0, -1, h, kModeForward, n, kInZero, kOutNone, -1);
+    WorkItem* L = p.items + 4 * i;
+    WorkItem* C = p.citems + 2 * i;
+    if (!sp) {
+      L[0] = bwd_item(sr.t0, sr.len, h, kModeForward, n, in_f, kOutNone, -1);
+      L[1] = none;
+      L[2] = bwd_item(sr.t0, sr.len, h, kModeReverse, n, in_r, dh, -1);
+      L[3] = none;
+      C[0] = none;
+      C[1] = none;
+    } else {
+      L[0] = bwd_item(sr.t0, len0, h, kModeForward, n, in_f, sA, -1);
+      L[1] = bwd_item(sr.t0 + len0, len1, h, kModeForward, n, kInZero, kOutNone, -1);
+      L[2] = bwd_item(sr.t0 + len0, len1, h, kModeReverse, n, in_r, sB, -1);
+      L[3] = bwd_item(sr.t0, len0, h, kModeReverse, n, kInZero, dh == kOutUser ? sC : kOutNone, -1);
+      C[0] = bwd_item(sr.t0 + len0, len1, h, kModeCorrect, n, sA, kOutNone, -1);
+      C[1] = bwd_item(sr.t0, len0, h, kModeReverseCorrect, n, sB, dh, dh == kOutUser ? sC : -1);
+    }
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.item_count = (int)(2 * NH);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *p.item_count = (int)(4 * NH);
+    *p.citem_count = (int)(2 * NH);
+  }
 }
 
 __device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
@@ -1231,7 +1269,7 @@ cudaError_t launch_bwd_chunked(const BwdParams& p, int phase, cudaStream_t s) {
   switch (phase) {
     case 0: {   // error word, the chains' runs
       if ((e = cudaMemsetAsync(p.err, 0, sizeof(int), s)) != cudaSuccess) return e;
-      const int grid = (int)std::min<int64_t>(std::max<int64_t>((2 * NH + 255) / 256, 1), 1024);
+      const int grid = (int)std::min<int64_t>(std::max<int64_t>((NH + 255) / 256, 1), 1024);
       kda_bwd_items_kernel<<<grid, 256, 0, s>>>(p);
       return cudaGetLastError();
     }

@@ -178,6 +178,24 @@ __device__ __forceinline__ void store_packed16(uint16_t* copy, int row, int j, c
     d[(4 * j + t) * 128 + row] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
 }
 
+// Column group j of a stored copy (as store_packed16) plus 32 fp32 values, rounded to bf16 again:
+// a correction run's part added to what its segment's run stored.
+__device__ __forceinline__ void add_to_copy(uint16_t* copy, int row, int j, const float (&x)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(copy);
+  uint4 w[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) w[t] = d[(4 * j + t) * 128 + row];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t a[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      o[u] = pack_bf16x2(bf16lo_to_f32(a[u]) + x[8 * t + 2 * u], bf16hi_to_f32(a[u]) + x[8 * t + 2 * u + 1]);
+    d[(4 * j + t) * 128 + row] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // Named barrier of one prologue pair (64 threads; ids 1 and 2).
 __device__ __forceinline__ void pair_bar(int pair) { named_bar(1 + pair, 64); }
 
@@ -701,7 +719,7 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
   const int vrows = kPadded ? p.vrows : 128;  // state rows of a chain the caller's tensors hold
   const int nchunks = (it.len + kChunk - 1) / kChunk;
   // a reverse run walks the chunks last first: iteration c handles chunk dchunk(c) of the run
-  const bool rev = kBwd && it.mode == kModeReverse;
+  const bool rev = kBwd && (it.mode == kModeReverse || it.mode == kModeReverseCorrect);
   auto dchunk = [&](int c) { return rev ? nchunks - 1 - c : c; };
   // work items count heads x value blocks: V = 128 * vsplit columns are independent
   // chains of 128 state rows each, sharing the head's q, k, g and beta
@@ -831,7 +849,8 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
       // the correction and transition runs take v as zero (no U); the transition writes no outputs
       const bool with_u = !kAux && it.mode == kModeForward;
       const bool with_o = !kBwd && it.mode != kModeTransition;   // the backward's runs store no outputs
-      const bool correct = kAux && it.mode == kModeCorrect;
+      // (the backward's correction runs: kModeCorrect forward, kModeReverseCorrect reverse)
+      const bool correct = kAux && (it.mode == kModeCorrect || it.mode == kModeReverseCorrect);
       // both v-free runs stop once their state is exactly zero (it then stays zero)
       constexpr bool track_zero = kAux;
       // the backward's runs store, per chunk slot, the state copy and the Vn read-out
@@ -868,15 +887,18 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
         const uint32_t d1 = tmem + kColD1 + 32u * (c & 1);
         if (kBwd && rev) {
           // dVn^T = dO^T (scale P) + dS^T K_d^T into D1[c & 1] columns 0-15
-          const uint64_t sso = (uint64_t)(c % kStages) * kSmallStep;
-          const uint64_t d_o = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
-          mma_ss(d1, d_o, smem_desc(smem_u32(m0.AQhi), 128, 256, kSwizzleNone) + sso, id_r1, 0);
-          mma_ss(d1, d_o, smem_desc(smem_u32(m0.AQlo), 128, 256, kSwizzleNone) + sso, id_r1, 1);
+          if constexpr (!kAux) {   // a correction run takes dout as zero
+            const uint64_t sso = (uint64_t)(c % kStages) * kSmallStep;
+            const uint64_t d_o = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
+            mma_ss(d1, d_o, smem_desc(smem_u32(m0.AQhi), 128, 256, kSwizzleNone) + sso, id_r1, 0);
+            mma_ss(d1, d_o, smem_desc(smem_u32(m0.AQlo), 128, 256, kSwizzleNone) + sso, id_r1, 1);
+          }
           const uint64_t d_k0 = smem_desc(smem_u32(s0.K), 16, 1024, kSwizzle128B) + so;
           const uint64_t d_k1 = smem_desc(smem_u32(s0.K) + 2048, 16, 1024, kSwizzle128B) + so;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ts(d1, tmem + kColSbf + 8u * k, (k < 4 ? d_k0 : d_k1) + (uint64_t)((k & 3) * 2), id_r2, 1u);
+            mma_ts(d1, tmem + kColSbf + 8u * k, (k < 4 ? d_k0 : d_k1) + (uint64_t)((k & 3) * 2), id_r2,
+                   (kAux && k == 0) ? 0u : 1u);
           tc_commit(&bar_d1_full[c & 1]);
           return;
         }
@@ -906,10 +928,12 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
         if (kBwd && rev) {
           // dS^T += dO^T (scale Q_p) + dVn^T (-W): Q_p and -W are rows 16-31 and 0-15 of the two
           // 64-channel X tiles, 4096 bytes apart
-          const uint64_t d_o = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
-          const uint64_t d_q = smem_desc(smem_u32(s0.X[0]) + 2048, 4096, 1024, kSwizzle128B) + so;
           const uint64_t d_w = smem_desc(smem_u32(s0.X[0]), 4096, 1024, kSwizzle128B) + so;
-          mma_ss(tmem + kColState, d_o, d_q, id_r3, 1);
+          if constexpr (!kAux) {
+            const uint64_t d_o = smem_desc(smem_u32(s0.V), 2048, 1024, kSwizzle128B) + so;
+            const uint64_t d_q = smem_desc(smem_u32(s0.X[0]) + 2048, 4096, 1024, kSwizzle128B) + so;
+            mma_ss(tmem + kColState, d_o, d_q, id_r3, 1);
+          }
           mma_ss(tmem + kColState, a_hi, d_w, id_s, 1);
           mma_ss(tmem + kColState, a_lo, d_w, id_s, 1);
           tc_commit(&bar_d2_full);
@@ -931,7 +955,7 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
       };
       // TMA loads of chunk c into stage c % kStages (lane 0 of warp kWarpTma only)
       const bool tma_thread = (warp == kWarpTma) && (lane == 0);
-      const bool load_v = with_u || rev;   // a reverse run loads dout where v goes
+      const bool load_v = with_u || (rev && !kAux);   // a reverse run loads dout where v goes
       int tma_issued = 0;
       auto issue_tma = [&](int c) {
         const int s = c % kStages;
@@ -1027,8 +1051,11 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
             for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(s[2 * t], s[2 * t + 1]);
           }
           tmem_st16(tSb + 16u * j, pk);
-          if constexpr (kBwd)
-            store_packed16(save_state + ((slot0 + dchunk(0)) * p.H + h) * 16384, vrow, j, pk);
+          if constexpr (kBwd) {
+            uint16_t* cp = save_state + ((slot0 + dchunk(0)) * p.H + h) * 16384;
+            if constexpr (kAux) add_to_copy(cp, vrow, j, s);
+            else store_packed16(cp, vrow, j, pk);
+          }
           uint32_t sv[32];
 #pragma unroll
           for (int t = 0; t < 32; ++t) sv[t] = __float_as_uint(s[t] * st0.gamC[32 * j + t]);
@@ -1049,9 +1076,28 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
       // Final state of the run's last chunk, column group j of row vrow: a workspace slot, or the
       // caller's tensor in its dtype.  A correction run adds its local final state (aux slot).
       auto write_final = [&](int j, uint32_t (&r)[32]) {
-        if constexpr (kBwd) {   // a reverse run's dS_0 -> dL/d initial_state (fp32)
-          if (rev && it.out_slot == kOutUser && p.dh0 != nullptr) {
-            float4* dst = reinterpret_cast<float4*>(p.dh0 + srow * 128 + 32 * j);
+        if constexpr (kBwd) {
+          // a reverse correction adds the segment's own reverse run's final dS (aux slot); a run
+          // ending at a segment boundary leaves its state in a workspace slot; a reverse run that
+          // reaches the sequence's start writes dL/d initial_state (fp32)
+          if (correct && it.aux_slot >= 0) {
+            const float4* a = reinterpret_cast<const float4*>(p.ws_states + (size_t)it.aux_slot * 16384 +
+                                                              (size_t)vrow * 128 + 32 * j);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float4 x = a[t];
+              r[4 * t] = __float_as_uint(__uint_as_float(r[4 * t]) + x.x);
+              r[4 * t + 1] = __float_as_uint(__uint_as_float(r[4 * t + 1]) + x.y);
+              r[4 * t + 2] = __float_as_uint(__uint_as_float(r[4 * t + 2]) + x.z);
+              r[4 * t + 3] = __float_as_uint(__uint_as_float(r[4 * t + 3]) + x.w);
+            }
+          }
+          float4* dst = nullptr;
+          if (it.out_slot >= 0)
+            dst = reinterpret_cast<float4*>(p.ws_states + (size_t)it.out_slot * 16384 + (size_t)vrow * 128 + 32 * j);
+          else if (rev && it.out_slot == kOutUser && p.dh0 != nullptr)
+            dst = reinterpret_cast<float4*>(p.dh0 + srow * 128 + 32 * j);
+          if (dst != nullptr) {
 #pragma unroll
             for (int t = 0; t < 8; ++t)
               dst[t] = make_float4(__uint_as_float(r[4 * t]), __uint_as_float(r[4 * t + 1]),
@@ -1108,10 +1154,18 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
           uint32_t r[16];
           tmem_ld16(tD1 + 32u * b, r);
           tmem_ld_wait();
-          if constexpr (kBwd) {   // Vn (dVn) of this chunk, [16 tokens][128 v]
+          if constexpr (kBwd) {   // Vn (dVn) of this chunk, [16 tokens][128 v]; a correction adds its part
             float* vd = save_vec + ((slot0 + dchunk(c)) * p.H + h) * 2048 + vrow;
+            if constexpr (kAux) {
+              float old[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) vd[128 * t] = __uint_as_float(r[t]);
+              for (int t = 0; t < 16; ++t) old[t] = vd[128 * t];
+#pragma unroll
+              for (int t = 0; t < 16; ++t) vd[128 * t] = old[t] + __uint_as_float(r[t]);
+            } else {
+#pragma unroll
+              for (int t = 0; t < 16; ++t) vd[128 * t] = __uint_as_float(r[t]);
+            }
           }
           uint32_t hw[8], lw[8];
 #pragma unroll
@@ -1163,8 +1217,17 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
                   pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
               }
               tmem_st16(tSb + 16u * j, pk);
-              if constexpr (kBwd)   // the state entering the next chunk handled (S_0, or dS_1 in reverse)
-                store_packed16(save_state + ((slot0 + dchunk(c + 1)) * p.H + h) * 16384, vrow, j, pk);
+              if constexpr (kBwd) {   // the state entering the next chunk handled (S_0, or dS_1 in reverse)
+                uint16_t* cp = save_state + ((slot0 + dchunk(c + 1)) * p.H + h) * 16384;
+                if constexpr (kAux) {
+                  float sv[32];
+#pragma unroll
+                  for (int t = 0; t < 32; ++t) sv[t] = __uint_as_float(r[t]);
+                  add_to_copy(cp, vrow, j, sv);
+                } else {
+                  store_packed16(cp, vrow, j, pk);
+                }
+              }
 #pragma unroll
               for (int t = 0; t < 8; ++t) {
                 const float4 gm = *reinterpret_cast<const float4*>(&stn.gamC[32 * j + 4 * t]);

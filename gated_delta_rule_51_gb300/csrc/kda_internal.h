@@ -21,7 +21,10 @@ constexpr int kDimV = 128;
 //                    stopped (and flagged zero) once it is exactly zero in fp32
 //   kModeReverse     (backward chains only) the state gradient dS carried from the sequence's
 //                    end to its start: dout in place of v, chunks last first, dS_0 written out
-enum : int { kModeForward = 0, kModeCorrect = 1, kModeTransition = 2, kModeReverse = 3 };
+//   kModeReverseCorrect (backward, split sequences) the reverse run with dout taken as zero from
+//                    the true dS at a segment's end, adding to what the segment's reverse run
+//                    stored; kModeCorrect does the same for the forward runs (v taken as zero)
+enum : int { kModeForward = 0, kModeCorrect = 1, kModeTransition = 2, kModeReverse = 3, kModeReverseCorrect = 4 };
 // in_slot values below zero:
 enum : int { kInZero = -1, kInIdentity = -2, kInUser = -3 };
 // out_slot values below zero:
@@ -185,8 +188,12 @@ struct BwdParams {
   const float* dvn;                       // dVn, as vn
   float* xp;                              // [slot][H][3][16][128]: dO S0^T, Vn dS1^T, dVn S0^T
   float* zs;                              // [slot][H][128]: sum over v of dS1 * S0
-  WorkItem* items;                        // the chains' runs: N H forward, then N H reverse
+  WorkItem* items;                        // the chains' runs: four per (sequence, head)
   int* item_count;
+  WorkItem* citems;                       // the correction runs of split sequences: two per (sequence, head)
+  int* citem_count;
+  float* bslots;                          // three 128 x 128 fp32 states per (sequence, head) (split sequences)
+  int split;                              // split sequences of two or more chunks in two
   int64_t nslots;
   int sms;                                // the device's SM count (persistent CTAs: two per SM)
 };
@@ -204,7 +211,7 @@ cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
 // dependent launch); its CTAs wait for that kernel's completion before they exit
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev = false);
 cudaError_t launch_chain_precise(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev = false);
-cudaError_t launch_chain_bwd(const ChainParams& p, int grid, cudaStream_t s);
+cudaError_t launch_chain_bwd(const ChainParams& p, int grid, cudaStream_t s, bool corrections = false);
 cudaError_t launch_chain_aux(const ChainParams& p, int grid, cudaStream_t s);
 cudaError_t launch_compose(const ComposeParams& p, int grid, int sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);

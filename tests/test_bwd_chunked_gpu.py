@@ -114,6 +114,16 @@ def test_chunked_backward_fixed_workload_sampled_heads():
     _compare(r, _oracle(x, dout, dfinal, heads=heads), x, "bwd chunked fixed workload heads 0,7,15", heads=heads)
 
 
+def test_chunked_backward_many_chains_unsplit():
+    """With many (sequence, head) chains kda_bwd keeps every sequence whole (the other cases here
+    split each sequence of two or more chunks in two and correct across the cut)."""
+    gen = np.random.default_rng(1977)
+    lens = [int(x) for x in gen.integers(1, 70, size=40)]
+    x = random_case(1, sum(lens), 2, seed=1978, lens=lens)   # 80 chains: more than the split allows
+    dout, dfinal = _grads_in(x, 1979)
+    _compare(_gpu(x, dout, dfinal, recurrent=False), _oracle(x, dout, dfinal), x, "bwd chunked 80 chains")
+
+
 def test_chunked_backward_without_dh0_or_parameter_gradients():
     from gated_delta_rule_51_gb300 import kda
 
