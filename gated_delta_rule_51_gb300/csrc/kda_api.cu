@@ -152,19 +152,20 @@ BwdLayout make_bwd_layout(const kda_shape& s) {
   return L;
 }
 
-// The chunked backward's workspace: header, the chains' runs, per (chunk slot, head) the stored
-// states (bf16), Vn and dVn (fp32), the state products, then the per-token dA_log terms and the
-// parameter-reduction blocks.  Slots: n + row0(n) / 16 + c is below N + B T / 16 + 1.
+// The chunked backward's workspace: header, the chains' runs and correction runs, three state
+// slots per (sequence, head) for split sequences, per (chunk slot, head) the stored states (bf16),
+// Vn and dVn (fp32), the state products and the parameter partials, then the partials of blocks of
+// 64 slots.  Slots: n + row0(n) / 16 + c is below N + B T / 16 + 1.
 struct BwdChunkedLayout {
   size_t off_hdr = 0, off_items = 0, off_citems = 0, off_bslots = 0, off_s0 = 0, off_ds1 = 0, off_vn = 0, off_dvn = 0,
-         off_xp = 0, off_zs = 0, off_dA = 0, off_ppart = 0, total = 0;
+         off_xp = 0, off_zs = 0, off_ppart = 0, total = 0;
   int64_t nslots = 0;
   int nblk = 0;
 };
 
 BwdChunkedLayout make_bwd_chunked_layout(const kda_shape& s) {
   BwdChunkedLayout L;
-  const size_t BT = (size_t)(s.B * s.T), TH = BT * (size_t)s.H;
+  const size_t BT = (size_t)(s.B * s.T);
   L.nslots = (int64_t)(BT / 16) + s.N + 1;
   const size_t SH = (size_t)L.nslots * (size_t)s.H;
   L.nblk = (int)((BT + kBwdParamTokens - 1) / kBwdParamTokens);
@@ -189,10 +190,9 @@ BwdChunkedLayout make_bwd_chunked_layout(const kda_shape& s) {
   off = align_up(off + SH * 6144 * sizeof(float));
   L.off_zs = off;
   off = align_up(off + SH * 128 * sizeof(float));
-  L.off_dA = off;
-  off = align_up(off + TH * sizeof(float));
-  L.off_ppart = off;
-  off = align_up(off + (size_t)L.nblk * (size_t)s.H * kBwdParamStride * sizeof(float));
+  L.off_ppart = off;   // per (chunk slot, head) parameter partials, then per block of 64 slots
+  off = align_up(off + ((size_t)std::max<int64_t>(L.nslots, 1) + (size_t)(L.nslots + 63) / 64) * (size_t)s.H *
+                           kBwdParamStride * sizeof(float));
   L.total = off;
   return L;
 }
@@ -677,7 +677,6 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     p.dvn = reinterpret_cast<const float*>(ws + C.off_dvn);
     p.xp = reinterpret_cast<float*>(ws + C.off_xp);
     p.zs = reinterpret_cast<float*>(ws + C.off_zs);
-    p.dA_tok = reinterpret_cast<float*>(ws + C.off_dA);
     p.ppart = reinterpret_cast<float*>(ws + C.off_ppart);
     p.nblk = C.nblk;
     p.nslots = C.nslots;

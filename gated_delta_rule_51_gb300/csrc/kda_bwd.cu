@@ -806,7 +806,10 @@ __device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
   const int64_t slot = unit / p.H;
   const int h = (int)(unit - slot * p.H);
   ChunkLoc cl;
-  if (!chunk_of_slot(p, slot, cl)) return;
+  if (!chunk_of_slot(p, slot, cl)) {   // a slot without a chunk adds nothing to the parameter sums
+    if (threadIdx.x <= 128) p.ppart[unit * kBwdParamStride + threadIdx.x] = 0.f;
+    return;
+  }
   extern __shared__ __align__(16) uint8_t csm_raw[];
   ChunkSmem& sm = *reinterpret_cast<ChunkSmem*>(csm_raw);
   const int tid = threadIdx.x;
@@ -1183,10 +1186,62 @@ __device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
       if ((tid & 15) == 0) {
         const float b = sm.beta[ti];
         p.dbeta[th] = beta_pre ? sm.dbeta[ti] : sm.dbeta[ti] * b * (1.f - b);
-        p.dA_tok[th] = wa;
       }
     }
+    // this unit's parameter partials: d dt_bias summed over the chunk's tokens (per channel) and
+    // the dA_log terms summed; the units are summed in a fixed order afterwards
+    __syncthreads();   // Kma and Y are read no more
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dg[j] = tv ? dg[j] : 0.f;
+    st8(&sm.Kma[ti][c0], dg);
+    if ((tid & 15) == 0) sm.Y[0][ti] = tv ? wa : 0.f;
+    __syncthreads();
+    if (tid < 128) {
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc += sm.Kma[i][tid];
+      p.ppart[unit * kBwdParamStride + tid] = acc;
+    } else if (tid == 128) {
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc += sm.Y[0][i];
+      p.ppart[unit * kBwdParamStride + 128] = acc;
+    }
   }
+}
+
+// Grid (ceil(nslots / 64), H): block b sums the partials of the 64 units (slots 64 b .. 64 b + 63,
+// head h) in slot order, sixteen loads in flight; kda_bwd_param_sum_kernel then sums the blocks.
+__global__ void __launch_bounds__(128) kda_bwd_unit_sum_kernel(const BwdParams p, float* out) {
+  const int blk = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const int64_t s0 = (int64_t)blk * 64, s1 = min(p.nslots, s0 + 64);
+  float a16[16], b16[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) a16[u] = b16[u] = 0.f;
+  int64_t sl = s0;
+  for (; sl + 16 <= s1; sl += 16) {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float* src = p.ppart + ((sl + u) * p.H + h) * kBwdParamStride;
+      a16[u] += src[c];
+      if (c == 0) b16[u] += src[128];
+    }
+  }
+  for (; sl < s1; ++sl) {   // the tail, in order
+    const float* src = p.ppart + (sl * p.H + h) * kBwdParamStride;
+    a16[0] += src[c];
+    if (c == 0) b16[0] += src[128];
+  }
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int u = 0; u < w; ++u) {
+      a16[u] += a16[u + w];
+      b16[u] += b16[u + w];
+    }
+  float* dst = out + ((size_t)blk * p.H + h) * kBwdParamStride;
+  dst[c] = a16[0];
+  if (c == 0) dst[128] = b16[0];
 }
 
 // Persistent CTAs (two per SM) walk the units: no CTA is launched per chunk.
@@ -1282,11 +1337,17 @@ cudaError_t launch_bwd_chunked(const BwdParams& p, int phase, cudaStream_t s) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }
       if (p.dA_log != nullptr || p.ddt_bias != nullptr) {
-        if (p.nblk > 0) {
-          kda_bwd_param_kernel<<<dim3(p.nblk, p.H), 128, 0, s>>>(p);
+        // the units' partials, summed in slot blocks of 64, then over the blocks
+        const int nb = (int)((p.nslots + 63) / 64);
+        float* blocks = p.ppart + (size_t)std::max<int64_t>(p.nslots, 1) * p.H * kBwdParamStride;
+        if (nb > 0) {
+          kda_bwd_unit_sum_kernel<<<dim3(nb, p.H), 128, 0, s>>>(p, blocks);
           if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        kda_bwd_param_sum_kernel<<<p.H, 128, 0, s>>>(p);
+        BwdParams q = p;
+        q.ppart = blocks;
+        q.nblk = nb;
+        kda_bwd_param_sum_kernel<<<p.H, 128, 0, s>>>(q);
       }
       return cudaGetLastError();
     }
