@@ -613,114 +613,130 @@ __device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t&
 // ---------------------------------------------------------------------------- state products
 // Per (chunk, head): X1 = dO S0^T, X2 = Vn dS1^T, X3 = dVn S0^T ([16 tokens][128 channels],
 // contractions over the 128 value rows) on bf16 warp MMA with fp32 accumulation (Vn and dVn
-// split into bf16 hi + lo), and Z = sum over v of dS1 * S0 per channel.  Warp w owns channels
-// 16 w .. 16 w + 15.
+// split into bf16 hi + lo), and Z = sum over v of dS1 * S0 per channel, the diagonal of
+// S0^T dS1.  Warp w owns channels 16 w .. 16 w + 15.
 struct XprodSmem {
-  uint16_t s0[128][kXPad];    // [v][k]
-  uint16_t ds1[128][kXPad];
+  // S0 and dS1 as stored (piece-major, [k / 8][v][k % 8]: 2 KB per eight channels), brought
+  // in by one bulk copy each; eight consecutive v of a piece are 128 contiguous bytes, so the
+  // transposed fragment loads below are conflict-free
+  uint16_t s0[16 * 1024];
+  uint16_t ds1[16 * 1024];
   uint16_t a[5][16][kXPad];   // dO, Vn hi, Vn lo, dVn hi, dVn lo: [token][v]
-  float z[2][128];
+  uint64_t bar;               // the copies' completion (one phase per unit)
+  int abort;
 };
 
-// One (chunk slot, head) unit; units are numbered with the heads fastest, so that the CTAs
-// working at once read every head of a few chunks and each token row is read whole from DRAM.
-__device__ __forceinline__ void xprod_unit(const BwdParams& p, int64_t unit) {
-  const int64_t slot = unit / p.H;
-  const int h = (int)(unit - slot * p.H);
-  ChunkLoc cl;
-  if (!chunk_of_slot(p, slot, cl)) return;
-  extern __shared__ __align__(16) uint8_t xsm_raw[];
-  XprodSmem& sm = *reinterpret_cast<XprodSmem*>(xsm_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const size_t sh = (size_t)slot * p.H + h;
-  {
-    // all sixteen 16-byte loads of a thread in flight at once
-    const uint4* a = reinterpret_cast<const uint4*>(p.s0 + sh * 16384);
-    const uint4* b = reinterpret_cast<const uint4*>(p.ds1 + sh * 16384);
-    uint4 ra[8], rb[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      ra[u] = a[tid + 256 * u];
-      rb[u] = b[tid + 256 * u];
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = tid + 256 * u, v = i & 127, c = (i >> 7) * 8;   // piece-major copies (kda_chain.cuh)
-      *reinterpret_cast<uint4*>(&sm.s0[v][c]) = ra[u];
-      *reinterpret_cast<uint4*>(&sm.ds1[v][c]) = rb[u];
-    }
-  }
-  {
-    const int t = tid >> 4, c = (tid & 15) * 8;
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (t < cl.nv) x = *reinterpret_cast<const uint4*>(p.dout + ((cl.row + t) * p.H + h) * 128 + c);
-    *reinterpret_cast<uint4*>(&sm.a[0][t][c]) = x;
-    const float* vn = p.vn + sh * 2048 + t * 128 + c;
-    const float* dvn = p.dvn + sh * 2048 + t * 128 + c;
-    const float4 v0 = ld4(vn), v1 = ld4(vn + 4), d0 = ld4(dvn), d1 = ld4(dvn + 4);
-    uint32_t vh[4], vl[4], dh[4], dl[4];
-    split2(v0.x, v0.y, vh[0], vl[0]);
-    split2(v0.z, v0.w, vh[1], vl[1]);
-    split2(v1.x, v1.y, vh[2], vl[2]);
-    split2(v1.z, v1.w, vh[3], vl[3]);
-    split2(d0.x, d0.y, dh[0], dl[0]);
-    split2(d0.z, d0.w, dh[1], dl[1]);
-    split2(d1.x, d1.y, dh[2], dl[2]);
-    split2(d1.z, d1.w, dh[3], dl[3]);
-    *reinterpret_cast<uint4*>(&sm.a[1][t][c]) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
-    *reinterpret_cast<uint4*>(&sm.a[2][t][c]) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
-    *reinterpret_cast<uint4*>(&sm.a[3][t][c]) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-    *reinterpret_cast<uint4*>(&sm.a[4][t][c]) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
-  }
-  __syncthreads();
-  // fragments: A rows = tokens (ldmatrix row r of matrix lane >> 3), B = the state's [v][k]
-  // rows read transposed (column-major 16 v x 8 k per n-tile)
+// The unit's rows of dO, Vn and dVn as the A operands (thread: token tid / 16, values
+// 8 (tid % 16) .. + 7): loaded into registers first, stored to shared memory later.
+struct XprodRows {
+  uint4 x;
+  float4 v0, v1, d0, d1;
+};
+__device__ __forceinline__ XprodRows xprod_load_a(const BwdParams& p, const ChunkLoc& cl, size_t sh, int h) {
+  const int tid = threadIdx.x, t = tid >> 4, c = (tid & 15) * 8;
+  XprodRows r;
+  r.x = make_uint4(0u, 0u, 0u, 0u);
+  if (t < cl.nv) r.x = *reinterpret_cast<const uint4*>(p.dout + ((cl.row + t) * p.H + h) * 128 + c);
+  const float* vn = p.vn + sh * 2048 + t * 128 + c;
+  const float* dvn = p.dvn + sh * 2048 + t * 128 + c;
+  r.v0 = ld4(vn);
+  r.v1 = ld4(vn + 4);
+  r.d0 = ld4(dvn);
+  r.d1 = ld4(dvn + 4);
+  return r;
+}
+__device__ __forceinline__ void xprod_store_a(XprodSmem& sm, const XprodRows& r) {
+  const int tid = threadIdx.x, t = tid >> 4, c = (tid & 15) * 8;
+  *reinterpret_cast<uint4*>(&sm.a[0][t][c]) = r.x;
+  uint32_t vh[4], vl[4], dh[4], dl[4];
+  split2(r.v0.x, r.v0.y, vh[0], vl[0]);
+  split2(r.v0.z, r.v0.w, vh[1], vl[1]);
+  split2(r.v1.x, r.v1.y, vh[2], vl[2]);
+  split2(r.v1.z, r.v1.w, vh[3], vl[3]);
+  split2(r.d0.x, r.d0.y, dh[0], dl[0]);
+  split2(r.d0.z, r.d0.w, dh[1], dl[1]);
+  split2(r.d1.x, r.d1.y, dh[2], dl[2]);
+  split2(r.d1.z, r.d1.w, dh[3], dl[3]);
+  *reinterpret_cast<uint4*>(&sm.a[1][t][c]) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+  *reinterpret_cast<uint4*>(&sm.a[2][t][c]) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+  *reinterpret_cast<uint4*>(&sm.a[3][t][c]) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
+  *reinterpret_cast<uint4*>(&sm.a[4][t][c]) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
+}
+
+// the bulk copies of a unit's S0 and dS1 (one thread)
+__device__ __forceinline__ void xprod_issue(const BwdParams& p, XprodSmem& sm, size_t sh) {
+  mbar_arrive_expect_tx(&sm.bar, 2 * 32768);
+  bulk_load(sm.s0, p.s0 + sh * 16384, 32768, &sm.bar);
+  bulk_load(sm.ds1, p.ds1 + sh * 16384, 32768, &sm.bar);
+}
+
+struct XprodAcc {
+  float x1[2][4], x2[2][4], x3[2][4], z[2][4];
+};
+
+__device__ __forceinline__ void xprod_mma(const XprodSmem& sm, XprodAcc& r) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k0 = 16 * warp;
-  const int r = lane & 15, cofs = (lane >> 4) * 8;
-  float x1[2][4] = {}, x2[2][4] = {}, x3[2][4] = {};
+  const int rr = lane & 15, cofs = (lane >> 4) * 8;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) r.x1[nt][e] = r.x2[nt][e] = r.x3[nt][e] = r.z[nt][e] = 0.f;
+  // the fragment rows of lane: value row v0 + rr, channels k0 + cofs .. + 7 (piece (k0 + cofs) / 8)
+  const uint32_t s_base = smem_u32(sm.s0) + (uint32_t)((((k0 + cofs) >> 3) * 1024 + rr * 8) * 2);
+  const uint32_t d_base = smem_u32(sm.ds1) + (uint32_t)((((k0 + cofs) >> 3) * 1024 + rr * 8) * 2);
 #pragma unroll 2
   for (int ks = 0; ks < 8; ++ks) {
     const int v0 = 16 * ks;
     uint32_t a[5][4];
 #pragma unroll
-    for (int m = 0; m < 5; ++m) ldmatrix_x4(a[m], smem_u32(&sm.a[m][r][v0 + cofs]));
+    for (int m = 0; m < 5; ++m) ldmatrix_x4(a[m], smem_u32(&sm.a[m][rr][v0 + cofs]));
+    // B fragments (the state's [v][k] rows read transposed): registers 2 nt, 2 nt + 1 are n-tile
+    // nt (channels k0 + 8 nt ..); the same registers in the order 0, 2, 1, 3 are the A fragment
+    // of S0^T (rows = channels k0 .. k0 + 15, columns = v)
     uint32_t bs[4], bd[4];
-    ldmatrix_x4_trans(bs, smem_u32(&sm.s0[v0 + r][k0 + cofs]));
-    ldmatrix_x4_trans(bd, smem_u32(&sm.ds1[v0 + r][k0 + cofs]));
+    ldmatrix_x4_trans(bs, s_base + v0 * 16);
+    ldmatrix_x4_trans(bd, d_base + v0 * 16);
+    const uint32_t s0t[4] = {bs[0], bs[2], bs[1], bs[3]};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const uint32_t b_s[2] = {bs[2 * nt], bs[2 * nt + 1]};
       const uint32_t b_d[2] = {bd[2 * nt], bd[2 * nt + 1]};
-      mma_bf16_16x8x16(x1[nt], a[0], b_s);
-      mma_bf16_16x8x16(x3[nt], a[3], b_s);
-      mma_bf16_16x8x16(x3[nt], a[4], b_s);
-      mma_bf16_16x8x16(x2[nt], a[1], b_d);
-      mma_bf16_16x8x16(x2[nt], a[2], b_d);
+      mma_bf16_16x8x16(r.x1[nt], a[0], b_s);
+      mma_bf16_16x8x16(r.x3[nt], a[3], b_s);
+      mma_bf16_16x8x16(r.x3[nt], a[4], b_s);
+      mma_bf16_16x8x16(r.x2[nt], a[1], b_d);
+      mma_bf16_16x8x16(r.x2[nt], a[2], b_d);
+      mma_bf16_16x8x16(r.z[nt], s0t, b_d);
     }
   }
-  {
-    const int k = tid & 127, half = tid >> 7;
-    float z = 0.f;
-    for (int v = 64 * half; v < 64 * half + 64; ++v) z = fmaf(bfv(sm.s0[v][k]), bfv(sm.ds1[v][k]), z);
-    sm.z[half][k] = z;
-  }
+}
+
+__device__ __forceinline__ void xprod_store(const BwdParams& p, size_t sh, const XprodAcc& r) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k0 = 16 * warp, g = lane >> 2, tq = lane & 3;
   float* xb = p.xp + sh * 6144;
-  const int g = lane >> 2, tq = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     const int col = k0 + 8 * nt + 2 * tq;
-    *reinterpret_cast<float2*>(xb + g * 128 + col) = make_float2(x1[nt][0], x1[nt][1]);
-    *reinterpret_cast<float2*>(xb + (g + 8) * 128 + col) = make_float2(x1[nt][2], x1[nt][3]);
-    *reinterpret_cast<float2*>(xb + 2048 + g * 128 + col) = make_float2(x2[nt][0], x2[nt][1]);
-    *reinterpret_cast<float2*>(xb + 2048 + (g + 8) * 128 + col) = make_float2(x2[nt][2], x2[nt][3]);
-    *reinterpret_cast<float2*>(xb + 4096 + g * 128 + col) = make_float2(x3[nt][0], x3[nt][1]);
-    *reinterpret_cast<float2*>(xb + 4096 + (g + 8) * 128 + col) = make_float2(x3[nt][2], x3[nt][3]);
+    *reinterpret_cast<float2*>(xb + g * 128 + col) = make_float2(r.x1[nt][0], r.x1[nt][1]);
+    *reinterpret_cast<float2*>(xb + (g + 8) * 128 + col) = make_float2(r.x1[nt][2], r.x1[nt][3]);
+    *reinterpret_cast<float2*>(xb + 2048 + g * 128 + col) = make_float2(r.x2[nt][0], r.x2[nt][1]);
+    *reinterpret_cast<float2*>(xb + 2048 + (g + 8) * 128 + col) = make_float2(r.x2[nt][2], r.x2[nt][3]);
+    *reinterpret_cast<float2*>(xb + 4096 + g * 128 + col) = make_float2(r.x3[nt][0], r.x3[nt][1]);
+    *reinterpret_cast<float2*>(xb + 4096 + (g + 8) * 128 + col) = make_float2(r.x3[nt][2], r.x3[nt][3]);
   }
-  __syncthreads();
-  if (tid < 128) p.zs[sh * 128 + tid] = sm.z[0][tid] + sm.z[1][tid];
+  // the diagonal of S0^T dS1: channel k0 + g (n-tile 0, row g, column 2 tq + e) and channel
+  // k0 + 8 + g (n-tile 1, row g + 8) sit in lane 4 g + g / 2, element e = g % 2
+  if ((g >> 1) == tq) {
+    const bool odd = g & 1;   // selects, not a runtime index: the accumulators stay in registers
+    p.zs[sh * 128 + k0 + g] = odd ? r.z[0][1] : r.z[0][0];
+    p.zs[sh * 128 + k0 + 8 + g] = odd ? r.z[1][3] : r.z[1][2];
+  }
 }
 
 // ---------------------------------------------------------------------------- chunk gradients
+
 // Per (chunk, head), 256 threads: thread (i = tid / 16, channels 8 (tid % 16) .. + 7) for the
 // per-element steps, thread (i, j) = (tid / 16, tid % 16) for the 16 x 16 ones.
 struct ChunkSmem {
@@ -1244,13 +1260,72 @@ __global__ void __launch_bounds__(128) kda_bwd_unit_sum_kernel(const BwdParams p
   if (c == 0) dst[128] = b16[0];
 }
 
-// Persistent CTAs (two per SM) walk the units: no CTA is launched per chunk.
+// Persistent CTAs (two per SM) walk the units, heads fastest (the CTAs working at once read
+// every head of a few chunks, so each token row is read whole from DRAM).  The next unit's S0
+// and dS1 copies are requested as soon as this unit's products have read the buffers, and its
+// A operands staged while they arrive; the wait on them is bounded (timeout: the error word's
+// timeout bit, and the CTA stops after its copies in flight have landed).
 __global__ void __launch_bounds__(256, 2) kda_bwd_xprod_kernel(const BwdParams p) {
+  extern __shared__ __align__(128) uint8_t xsm_raw[];
+  XprodSmem& sm = *reinterpret_cast<XprodSmem*>(xsm_raw);
   const int64_t units = p.nslots * p.H;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    xprod_unit(p, u);
-    __syncthreads();   // the unit's shared memory is reused by the next
+  const int tid = threadIdx.x;
+  auto locate = [&](int64_t u, ChunkLoc& cl, size_t& sh, int& h) {
+    const int64_t slot = u / p.H;
+    h = (int)(u - slot * p.H);
+    sh = (size_t)slot * p.H + h;
+    return u < units && chunk_of_slot(p, slot, cl);
+  };
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    sm.abort = 0;
+    mbar_fence_init();
   }
+  __syncthreads();
+  const AbortState ab{&sm.abort, p.err};
+  int64_t u = blockIdx.x;
+  ChunkLoc cl;
+  size_t sh;
+  int h;
+  bool valid = locate(u, cl, sh, h);
+  if (valid) {
+    if (tid == 0) xprod_issue(p, sm, sh);
+    xprod_store_a(sm, xprod_load_a(p, cl, sh, h));
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  bool pending = valid;   // a copy of this CTA is in flight
+  for (; u < units; u += gridDim.x) {
+    XprodAcc r;
+    if (valid) {
+      const bool ok = mbar_wait(&sm.bar, phase, ab);
+      phase ^= 1u;
+      pending = !ok;
+      if (ok) xprod_mma(sm, r);
+    }
+    __syncthreads();   // every warp is done with the buffers (or the CTA is stopping)
+    if (sm.abort) break;
+    ChunkLoc ncl;
+    size_t nsh;
+    int nh;
+    const bool nvalid = locate(u + gridDim.x, ncl, nsh, nh);
+    if (nvalid && tid == 0) {
+      fence_proxy_async_smem();
+      xprod_issue(p, sm, nsh);
+    }
+    pending = pending || nvalid;
+    // the next unit's rows are requested before this unit's products are written out
+    XprodRows rows;
+    if (nvalid) rows = xprod_load_a(p, ncl, nsh, nh);
+    if (valid) xprod_store(p, sh, r);
+    if (nvalid) xprod_store_a(sm, rows);
+    __syncthreads();
+    valid = nvalid;
+    cl = ncl;
+    sh = nsh;
+    h = nh;
+  }
+  if (pending) mbar_wait_drain(&sm.bar, phase);
 }
 __global__ void __launch_bounds__(256, 2) kda_bwd_chunk_kernel(const BwdParams p) {
   const int64_t units = p.nslots * p.H;
