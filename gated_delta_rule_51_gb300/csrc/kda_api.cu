@@ -152,8 +152,9 @@ BwdLayout make_bwd_layout(const kda_shape& s) {
   return L;
 }
 
-// The chunked backward's workspace: header, the chains' runs and correction runs, three state
-// slots per (sequence, head) for split sequences, per (chunk slot, head) the stored states (bf16),
+// The chunked backward's workspace: header, the chains' runs and correction runs, the state
+// slots of cut sequences (2 kBwdMaxParts - 1 per (sequence, head), for at most
+// kBwdMaxSplitChains chains: more chains are never cut), per (chunk slot, head) the stored states (bf16),
 // Vn and dVn (fp32), the state products and the parameter partials, then the partials of blocks of
 // 64 slots.  Slots: n + row0(n) / 16 + c is below N + B T / 16 + 1.
 struct BwdChunkedLayout {
@@ -173,11 +174,12 @@ BwdChunkedLayout make_bwd_chunked_layout(const kda_shape& s) {
   L.off_hdr = off;
   off = align_up(off + sizeof(WorkHeader));
   L.off_items = off;
-  off = align_up(off + 4 * (size_t)s.N * (size_t)s.H * sizeof(WorkItem));
+  const size_t NH = (size_t)s.N * (size_t)s.H;
+  off = align_up(off + 2 * kBwdMaxParts * NH * sizeof(WorkItem));
   L.off_citems = off;
-  off = align_up(off + 2 * (size_t)s.N * (size_t)s.H * sizeof(WorkItem));
+  off = align_up(off + 2 * (kBwdMaxParts - 1) * NH * sizeof(WorkItem));
   L.off_bslots = off;
-  off = align_up(off + 3 * (size_t)s.N * (size_t)s.H * kSlotBytes);
+  off = align_up(off + (2 * kBwdMaxParts - 1) * std::min<size_t>(NH, kBwdMaxSplitChains) * kSlotBytes);
   L.off_s0 = off;
   off = align_up(off + SH * 16384 * sizeof(uint16_t));
   L.off_ds1 = off;
@@ -668,9 +670,17 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     p.citems = reinterpret_cast<WorkItem*>(ws + C.off_citems);
     p.citem_count = &reinterpret_cast<WorkHeader*>(ws + C.off_hdr)->n_correct;
     p.bslots = reinterpret_cast<float*>(ws + C.off_bslots);
-    // split each sequence in two when the chains alone would leave most SMs idle (four runs per
-    // (sequence, head) still fit one wave of two CTAs per SM)
-    p.split = 4 * s.N * s.H <= 2 * (int64_t)std::max(d.sms, 1) ? 1 : 0;
+    // cut each sequence into parts when the chains alone would leave most SMs idle: the most parts
+    // (kBwdMaxParts, halving) that keep the 2 parts runs per (sequence, head) within one wave of
+    // two CTAs per SM
+    const int64_t NH = s.N * s.H, wave = 2 * (int64_t)std::max(d.sms, 1);
+    p.parts = 1;
+    if (NH <= kBwdMaxSplitChains)
+      for (int P = kBwdMaxParts; P > 1; P /= 2)
+        if (2 * P * NH <= wave) {
+          p.parts = P;
+          break;
+        }
     p.s0 = reinterpret_cast<const uint16_t*>(ws + C.off_s0);
     p.ds1 = reinterpret_cast<const uint16_t*>(ws + C.off_ds1);
     p.vn = reinterpret_cast<const float*>(ws + C.off_vn);
@@ -681,7 +691,8 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     p.nblk = C.nblk;
     p.nslots = C.nslots;
     p.sms = std::max(d.sms, 1);
-    // the chains: N H forward runs storing S0 and Vn, N H reverse runs storing dS1 and dVn
+    // the chains: per part of each (sequence, head) a forward run storing S0 and Vn and a reverse
+    // run storing dS1 and dVn
     ChainParams cp;
     std::memset(&cp, 0, sizeof(cp));
     const int64_t rows = s.B * s.T;
@@ -717,12 +728,12 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     // profile marks: the runs, the chains, the state products, the chunk gradients
     if (launch_bwd_chunked(p, 0, stream) != cudaSuccess) return KDA_ERR_CUDA;
     mark(0, stream);
-    if (launch_chain_bwd(cp, (int)(4 * s.N * s.H), stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (p.split) {   // the corrections of the split sequences
+    if (launch_chain_bwd(cp, (int)(2 * p.parts * NH), stream) != cudaSuccess) return KDA_ERR_CUDA;
+    for (int l = 1; l < p.parts; ++l) {   // the corrections of the cut sequences, cut by cut
       ChainParams cc = cp;
-      cc.items = p.citems;
+      cc.items = p.citems + (size_t)(l - 1) * 2 * NH;
       cc.item_count = p.citem_count;
-      if (launch_chain_bwd(cc, (int)(2 * s.N * s.H), stream, true) != cudaSuccess) return KDA_ERR_CUDA;
+      if (launch_chain_bwd(cc, (int)(2 * NH), stream, true) != cudaSuccess) return KDA_ERR_CUDA;
     }
     mark(1, stream);
     if (launch_bwd_chunked(p, 2, stream) != cudaSuccess) return KDA_ERR_CUDA;
@@ -730,7 +741,7 @@ kda_status kda_bwd(const kda_shape* shape, const void* q, const void* k, const v
     if (launch_bwd_chunked(p, 3, stream) != cudaSuccess) return KDA_ERR_CUDA;
     mark(3, stream);
     const bool work = p.BT > 0 && p.H > 0;
-    t_last_launches = 1 + (s.N > 0 ? 1 + p.split : 0) + (work ? 2 : 0) +
+    t_last_launches = 1 + (s.N > 0 ? p.parts : 0) + (work ? 2 : 0) +
                       ((dA_log == nullptr && ddt_bias == nullptr) ? 0 : (C.nblk > 0 ? 2 : 1));
     return KDA_OK;
   }

@@ -23,7 +23,7 @@
 // Two forms.  The chunked one (the default for the gate with a lower bound; "chunked path"
 // below) runs the chunk recurrence on tensor cores in the chain kernels and every chunk's
 // gradients in parallel:
-//   items    the chains' runs (a forward and a reverse run per (sequence, head));
+//   items    the chains' runs (a forward and a reverse run per part of each (sequence, head));
 //   (chains: kda_chain_kernel, kChainBwd, launched from kda_api.cu)
 //   xprod    per chunk: dO S0^T, Vn dS1^T, dVn S0^T on bf16 warp MMA, sum_v dS1 S0;
 //   chunk    per chunk: the 16 x 16 and 16 x 128 products on tf32 warp MMA (fp32-accurate
@@ -557,50 +557,71 @@ __device__ __forceinline__ WorkItem bwd_item(int64_t row0, int64_t len, int h, i
   return it;
 }
 
-// The chains' runs.  First launch, four per (sequence, head): forward runs storing S0 and Vn, and
-// reverse runs carrying dS from dfinal (or zero) to dh0 and storing dS1 and dVn.  With p.split, a
-// sequence of two or more chunks is cut at chunk m = ceil(chunks / 2), and the four runs are the
-// forward runs of its two halves (the second from zero) and the reverse runs of its two halves (the
-// first from zero); the second launch then runs, per (sequence, head), the forward correction of
-// the second half from the true state at the cut (slot A, left by the first half's forward run)
-// and the reverse correction of the first half from the true dS at the cut (slot B), which adds
-// the first half's own reverse run's final dS (slot C) to give dh0.  Both corrections take v
-// (dout) as zero and add their part to what the halves' runs stored; by linearity the sums are
-// the unsplit runs' values.  Unused entries are placeholders (len < 0).
+// The chains' runs.  A sequence of c chunks is cut into P = min(parts, c) parts at chunk
+// boundaries (P = 1 when parts = 1 or c <= 1).  The first launch runs, per (sequence, head) and
+// part j, the part's forward run (the first from the true initial state, the others from zero)
+// and its reverse run (the last from dfinal or zero, the others from zero); these store S0 and
+// Vn, or dS1 and dVn, and leave their final states in slots: forward part j < P - 1 in E_j,
+// reverse part j in F_j (F_0 only when dh0 is wanted; with P = 1 the reverse run writes dh0).
+// Correction launch l = 1 .. parts - 1 then runs, for each sequence with l < P, the forward
+// correction of part l from the true state E_{l-1} and the reverse correction of part
+// r = P - 1 - l from the true dS F_{r+1}.  Corrections take v (dout) as zero and add their
+// part to what the parts' runs stored; each adds its final state to the slot its part's run
+// left there (E_l, F_r), which then holds the true state at that cut, or gives dh0 with F_0
+// added.  By linearity the sums are the uncut runs' values.  Slots of chain i: E_j at
+// (2 parts - 1) i + j, F_j at (2 parts - 1) i + parts - 1 + j.  Unused entries are placeholders
+// (len < 0).
 __global__ void __launch_bounds__(256) kda_bwd_items_kernel(const BwdParams p) {
   const int64_t NH = (int64_t)p.N * p.H;
+  const int P = p.parts;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < NH; i += stride) {
     const int n = (int)(i / p.H), h = (int)(i - (int64_t)n * p.H);
     const SeqRange sr = seq_range(p, n, h == 0);
     const int64_t chunks = (sr.len + 15) / 16;
-    const bool sp = p.split && chunks >= 2;
-    const int64_t len0 = sp ? 16 * ((chunks + 1) / 2) : sr.len, len1 = sr.len - len0;
-    const int sA = (int)(3 * i), sB = sA + 1, sC = sA + 2;
+    const int Pn = (int)(chunks < (int64_t)P ? (chunks > 1 ? chunks : 1) : P);
+    auto part_row = [&](int j) {   // first row of part j (j = Pn: the sequence's end)
+      return j >= Pn ? sr.t0 + sr.len : sr.t0 + 16 * ((chunks * j) / Pn);
+    };
+    const int base = (int)((2 * P - 1) * i);
+    auto E = [&](int j) { return base + j; };
+    auto F = [&](int j) { return base + P - 1 + j; };
     const int in_f = p.init_state != nullptr ? kInUser : kInZero;
     const int in_r = p.dfinal != nullptr ? kInUser : kInZero;
     const int dh = p.dh0 != nullptr ? kOutUser : kOutNone;
     const WorkItem none = bwd_item(0, -1, h, kModeForward, n, kInZero, kOutNone, -1);
-    WorkItem* L = p.items + 4 * i;
-    WorkItem* C = p.citems + 2 * i;
-    if (!sp) {
-      L[0] = bwd_item(sr.t0, sr.len, h, kModeForward, n, in_f, kOutNone, -1);
-      L[1] = none;
-      L[2] = bwd_item(sr.t0, sr.len, h, kModeReverse, n, in_r, dh, -1);
-      L[3] = none;
-      C[0] = none;
-      C[1] = none;
-    } else {
-      L[0] = bwd_item(sr.t0, len0, h, kModeForward, n, in_f, sA, -1);
-      L[1] = bwd_item(sr.t0 + len0, len1, h, kModeForward, n, kInZero, kOutNone, -1);
-      L[2] = bwd_item(sr.t0 + len0, len1, h, kModeReverse, n, in_r, sB, -1);
-      L[3] = bwd_item(sr.t0, len0, h, kModeReverse, n, kInZero, dh == kOutUser ? sC : kOutNone, -1);
-      C[0] = bwd_item(sr.t0 + len0, len1, h, kModeCorrect, n, sA, kOutNone, -1);
-      C[1] = bwd_item(sr.t0, len0, h, kModeReverseCorrect, n, sB, dh, dh == kOutUser ? sC : -1);
+    WorkItem* L = p.items + 2 * P * i;
+    for (int j = 0; j < P; ++j) {
+      if (j >= Pn) {
+        L[j] = none;
+        L[P + j] = none;
+        continue;
+      }
+      const int64_t r0 = part_row(j), len = part_row(j + 1) - r0;
+      L[j] = bwd_item(r0, len, h, kModeForward, n, j == 0 ? in_f : kInZero, j < Pn - 1 ? E(j) : kOutNone, -1);
+      const int rout = Pn == 1 ? dh : (j > 0 ? F(j) : (dh == kOutUser ? F(0) : kOutNone));
+      L[P + j] = bwd_item(r0, len, h, kModeReverse, n, j == Pn - 1 ? in_r : kInZero, rout, -1);
+    }
+    for (int l = 1; l < P; ++l) {
+      WorkItem* C = p.citems + (int64_t)(l - 1) * 2 * NH + 2 * i;
+      if (l >= Pn) {
+        C[0] = none;
+        C[1] = none;
+        continue;
+      }
+      const int64_t f0 = part_row(l), r = Pn - 1 - l, q0 = part_row((int)r);
+      const bool fout = l < Pn - 1;
+      C[0] = bwd_item(f0, part_row(l + 1) - f0, h, kModeCorrect, n, E(l - 1), fout ? E(l) : kOutNone,
+                      fout ? E(l) : -1);
+      if (r > 0)
+        C[1] = bwd_item(q0, part_row((int)r + 1) - q0, h, kModeReverseCorrect, n, F((int)r + 1), F((int)r),
+                        F((int)r));
+      else
+        C[1] = bwd_item(q0, part_row(1) - q0, h, kModeReverseCorrect, n, F(1), dh, dh == kOutUser ? F(0) : -1);
     }
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *p.item_count = (int)(4 * NH);
+    *p.item_count = (int)(2 * P * NH);
     *p.citem_count = (int)(2 * NH);
   }
 }
@@ -747,13 +768,14 @@ struct ChunkSmem {
     struct {   // v and dO rows (bf16), read by the first products only
       uint16_t vb[16][kVPad], dob[16][kVPad];
     } in;
-    struct {   // then the A operands of the second products as tf32 hi and lo parts:
-      uint32_t h[5][16][20], l[5][16][20];   // dP, dR, dP^T, dR^T, Tm^T
-    } a;
+    // then the A operands of the second products as tf32 {hi, lo} pairs: dP, dR, dP^T, dR^T,
+    // Tm^T (pitch 20 pairs: the 64-bit fragment reads of rows g, columns k + tq are conflict-free)
+    uint2 a[5][16][20];
   } u;
   // 16 x 16 matrices, pitch 20 (the warp-MMA fragment reads of rows g, columns k + tq are then
-  // conflict-free)
+  // conflict-free); the first products' second halves (channels 64 .. 127) land in P2
   float R[16][20], dP[16][20], dVnV[16][20], dWKp[16][20], dT[16][20], M[16][20], Tm[16][20], dM[16][20];
+  float P2[4][16][20];
   float Y[16][20], dA[16][20], dR[16][20];
   float beta[16], rq[16], rk[16], dbeta[16];
   float a[128], Ea[128], GC[128], Z[128];
@@ -931,61 +953,68 @@ __device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
     st8(&sm.Qpa[ti][c0], qpa);
   }
   __syncthreads();
-  // ---- 16 x 16 products over the 128 channels / value rows, on tf32 warp MMA: warp w computes
-  //      columns 8 (w & 1) .. + 7 of R = Kp' Km'^T, dP = scale dO Vn^T, dVnV = dVn V^T or
-  //      dWKp = X3 Kp^T (w >> 1); fragments: rows g, g + 8 and k columns tq, tq + 4
+  // ---- 16 x 16 products over the 128 channels / value rows, on tf32 warp MMA: warps 2 p and
+  //      2 p + 1 compute product p (R = Kp' Km'^T, dP = dO Vn^T, dVnV = dVn V^T, dWKp = X3 Kp^T)
+  //      over channels 0 .. 63 and 64 .. 127, both column tiles (each operand is split once);
+  //      fragments: rows g, g + 8 and k columns tq, tq + 4
   {
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
-    const int prod = warp >> 1, j0 = 8 * (warp & 1);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int c = 0; c < 128; c += 8) {
+    const int prod = warp >> 1, half = warp & 1;
+    float acc[2][4] = {};
+#pragma unroll 2
+    for (int c = 64 * half; c < 64 * half + 64; c += 8) {
       const int ca = c + tq, cb = c + tq + 4;
       if (prod == 0) {
         const Frag4 fa = split4(sm.Kpa[g][ca], sm.Kpa[g + 8][ca], sm.Kpa[g][cb], sm.Kpa[g + 8][cb]);
-        const Frag2 fb = split2f(sm.Kma[j0 + g][ca], sm.Kma[j0 + g][cb]);
-        mma3x(acc, fa, fb);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) mma3x(acc[nt], fa, split2f(sm.Kma[8 * nt + g][ca], sm.Kma[8 * nt + g][cb]));
       } else if (prod == 1) {   // dO is bf16: exact in tf32
         const uint32_t ah[4] = {f32_to_tf32(bfv(sm.u.in.dob[g][ca])), f32_to_tf32(bfv(sm.u.in.dob[g + 8][ca])),
                                 f32_to_tf32(bfv(sm.u.in.dob[g][cb])), f32_to_tf32(bfv(sm.u.in.dob[g + 8][cb]))};
-        const Frag2 fb = split2f(sm.Vn[j0 + g][ca], sm.Vn[j0 + g][cb]);
-        mma_tf32_16x8x8(acc, ah, fb.l);
-        mma_tf32_16x8x8(acc, ah, fb.h);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const Frag2 fb = split2f(sm.Vn[8 * nt + g][ca], sm.Vn[8 * nt + g][cb]);
+          mma_tf32_16x8x8(acc[nt], ah, fb.l);
+          mma_tf32_16x8x8(acc[nt], ah, fb.h);
+        }
       } else if (prod == 2) {   // v is bf16: exact in tf32
         const Frag4 fa = split4(sm.dVn[g][ca], sm.dVn[g + 8][ca], sm.dVn[g][cb], sm.dVn[g + 8][cb]);
-        const uint32_t bh[2] = {f32_to_tf32(bfv(sm.u.in.vb[j0 + g][ca])), f32_to_tf32(bfv(sm.u.in.vb[j0 + g][cb]))};
-        mma_tf32_16x8x8(acc, fa.l, bh);
-        mma_tf32_16x8x8(acc, fa.h, bh);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint32_t bh[2] = {f32_to_tf32(bfv(sm.u.in.vb[8 * nt + g][ca])),
+                                  f32_to_tf32(bfv(sm.u.in.vb[8 * nt + g][cb]))};
+          mma_tf32_16x8x8(acc[nt], fa.l, bh);
+          mma_tf32_16x8x8(acc[nt], fa.h, bh);
+        }
       } else {
         const Frag4 fa = split4(sm.X3[g][ca], sm.X3[g + 8][ca], sm.X3[g][cb], sm.X3[g + 8][cb]);
-        const Frag2 fb = split2f(sm.Kpa[j0 + g][ca] * sm.Ea[ca], sm.Kpa[j0 + g][cb] * sm.Ea[cb]);
-        mma3x(acc, fa, fb);
+        const float ea = sm.Ea[ca], eb = sm.Ea[cb];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          mma3x(acc[nt], fa, split2f(sm.Kpa[8 * nt + g][ca] * ea, sm.Kpa[8 * nt + g][cb] * eb));
       }
     }
-    float (*dst)[20] = prod == 0 ? sm.R : prod == 1 ? sm.dP : prod == 2 ? sm.dVnV : sm.dWKp;
-    const int jc = j0 + 2 * tq;
-    float v0 = acc[0], v1 = acc[1], v2 = acc[2], v3 = acc[3];
-    if (prod == 1) {   // dP = scale dO Vn^T on and below the diagonal
-      v0 = jc <= g ? p.scale * v0 : 0.f;
-      v1 = jc + 1 <= g ? p.scale * v1 : 0.f;
-      v2 = jc <= g + 8 ? p.scale * v2 : 0.f;
-      v3 = jc + 1 <= g + 8 ? p.scale * v3 : 0.f;
+    float (*dst)[20] = half ? sm.P2[prod] : prod == 0 ? sm.R : prod == 1 ? sm.dP : prod == 2 ? sm.dVnV : sm.dWKp;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int jc = 8 * nt + 2 * tq;
+      dst[g][jc] = acc[nt][0];
+      dst[g][jc + 1] = acc[nt][1];
+      dst[g + 8][jc] = acc[nt][2];
+      dst[g + 8][jc + 1] = acc[nt][3];
     }
-    dst[g][jc] = v0;
-    dst[g][jc + 1] = v1;
-    dst[g + 8][jc] = v2;
-    dst[g + 8][jc + 1] = v3;
   }
   __syncthreads();
-  {   // dT = dVn V^T + dW Kp^T with dW = -X3; dP and dP^T as tf32 parts (v and dO are read no more)
+  {   // the two halves added; dT = dVn V^T + dW Kp^T with dW = -X3; dP = scale dO Vn^T on and
+      // below the diagonal, and dP, dP^T as tf32 pairs (v and dO are read no more)
     const int i = tid >> 4, j = tid & 15;
-    sm.dT[i][j] = sm.dVnV[i][j] - sm.dWKp[i][j];
-    uint32_t hi, lo;
-    tf32_split(sm.dP[i][j], hi, lo);
-    sm.u.a.h[0][i][j] = hi;
-    sm.u.a.l[0][i][j] = lo;
-    sm.u.a.h[2][j][i] = hi;
-    sm.u.a.l[2][j][i] = lo;
+    sm.R[i][j] += sm.P2[0][i][j];
+    sm.dT[i][j] = (sm.dVnV[i][j] + sm.P2[2][i][j]) - (sm.dWKp[i][j] + sm.P2[3][i][j]);
+    const float dp = j <= i ? p.scale * (sm.dP[i][j] + sm.P2[1][i][j]) : 0.f;
+    uint2 hl;
+    tf32_split(dp, hl.x, hl.y);
+    sm.u.a[0][i][j] = hl;
+    sm.u.a[2][j][i] = hl;
   }
   __syncthreads();
   // ---- M = (I + Diag(beta) strict_lower(R))^-1, one column per thread (forward substitution)
@@ -1010,7 +1039,9 @@ __device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
     const int i = tid >> 4, j = tid & 15;
     const float tm = sm.M[i][j] * sm.beta[j];
     sm.Tm[i][j] = tm;
-    tf32_split(tm, sm.u.a.h[4][j][i], sm.u.a.l[4][j][i]);
+    uint2 hl;
+    tf32_split(tm, hl.x, hl.y);
+    sm.u.a[4][j][i] = hl;
     sm.dM[i][j] = sm.dT[i][j] * sm.beta[j];
   }
   __syncthreads();
@@ -1031,12 +1062,10 @@ __device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
     }
     sm.dA[i][j] = d;
     sm.dR[i][j] = sm.beta[i] * d;
-    uint32_t hi, lo;
-    tf32_split(sm.beta[i] * d, hi, lo);
-    sm.u.a.h[1][i][j] = hi;
-    sm.u.a.l[1][i][j] = lo;
-    sm.u.a.h[3][j][i] = hi;
-    sm.u.a.l[3][j][i] = lo;
+    uint2 hl;
+    tf32_split(sm.beta[i] * d, hl.x, hl.y);
+    sm.u.a[1][i][j] = hl;
+    sm.u.a[3][j][i] = hl;
   }
   __syncthreads();
   if (tid < 16) {
@@ -1072,11 +1101,11 @@ __device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
       for (int kk = 0; kk < 16; kk += 8) {
         const int ka = kk + tq, kb = kk + tq + 4;
         auto frag = [&](int m) {
+          const uint2 a0 = sm.u.a[m][g][ka], a1 = sm.u.a[m][g + 8][ka];
+          const uint2 a2 = sm.u.a[m][g][kb], a3 = sm.u.a[m][g + 8][kb];
           Frag4 f;
-          f.h[0] = sm.u.a.h[m][g][ka]; f.h[1] = sm.u.a.h[m][g + 8][ka];
-          f.h[2] = sm.u.a.h[m][g][kb]; f.h[3] = sm.u.a.h[m][g + 8][kb];
-          f.l[0] = sm.u.a.l[m][g][ka]; f.l[1] = sm.u.a.l[m][g + 8][ka];
-          f.l[2] = sm.u.a.l[m][g][kb]; f.l[3] = sm.u.a.l[m][g + 8][kb];
+          f.h[0] = a0.x; f.h[1] = a1.x; f.h[2] = a2.x; f.h[3] = a3.x;
+          f.l[0] = a0.y; f.l[1] = a1.y; f.l[2] = a2.y; f.l[3] = a3.y;
           return f;
         };
         const int cb = 16 * warp + 8 * nt + g;
@@ -1109,7 +1138,7 @@ __device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
       }
       __syncwarp();   // every lane has read columns 16 w + 8 nt .. + 7 of Kpa, Qpa and X3: rewritten below
       const float2 av = *reinterpret_cast<const float2*>(&sm.a[c]);
-      const float2 gcv = *reinterpret_cast<const float2*>(&sm.GC[c]);
+      const float2 eav = *reinterpret_cast<const float2*>(&sm.Ea[c]);
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int i = g + 8 * hr;
@@ -1117,15 +1146,16 @@ __device__ __forceinline__ void chunk_unit(const BwdParams& p, int64_t unit) {
         const float2 khv = *reinterpret_cast<const float2*>(&sm.kh[i][c]);
         const float2 qhv = *reinterpret_cast<const float2*>(&sm.qh[i][c]);
         const float2 x1 = x1v[hr], x2 = x2v[hr];
-        const float Ge[2] = {Gv.x, Gv.y}, ae[2] = {av.x, av.y}, gce[2] = {gcv.x, gcv.y};
+        const float Ge[2] = {Gv.x, Gv.y}, ae[2] = {av.x, av.y}, eae[2] = {eav.x, eav.y};
         const float khe[2] = {khv.x, khv.y}, qhe[2] = {qhv.x, qhv.y}, x1e[2] = {x1.x, x1.y}, x2e[2] = {x2.x, x2.y};
         float dqh[2], dkh[2], dG[2], dkdkh[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int r = 2 * hr + e;   // accumulator element: (row g + 8 hr, column 2 tq + e)
+          // with the anchor a = G_C / 2: 2^G = 2^(G - a) 2^a and 2^(G_C - G) = 2^(a - G) 2^a
           const float d = Ge[e] - ae[e];
-          const float gam = ex2_approx(Ge[e]), gp = ex2_approx(d), gm = ex2_approx(-d);
-          const float dk = ex2_approx(gce[e] - Ge[e]);
+          const float gp = ex2_approx(d), gm = ex2_approx(-d);
+          const float gam = gp * eae[e], dk = gm * eae[e];
           dqh[e] = p.scale * x1e[e] * gam + gp * sq[r];
           const float dkp = -tw[r] * gam + gp * sp[r];
           const float dkm = gm * smk[r];

@@ -188,12 +188,13 @@ struct BwdParams {
   const float* dvn;                       // dVn, as vn
   float* xp;                              // [slot][H][3][16][128]: dO S0^T, Vn dS1^T, dVn S0^T
   float* zs;                              // [slot][H][128]: sum over v of dS1 * S0
-  WorkItem* items;                        // the chains' runs: four per (sequence, head)
+  WorkItem* items;                        // the chains' runs: 2 parts per (sequence, head)
   int* item_count;
-  WorkItem* citems;                       // the correction runs of split sequences: two per (sequence, head)
+  WorkItem* citems;                       // the correction runs of split sequences: parts - 1 launches,
+                                          // two per (sequence, head) each
   int* citem_count;
-  float* bslots;                          // three 128 x 128 fp32 states per (sequence, head) (split sequences)
-  int split;                              // split sequences of two or more chunks in two
+  float* bslots;                          // 2 parts - 1 128 x 128 fp32 states per (sequence, head)
+  int parts;                              // cut each sequence into up to this many parts (1 or 2)
   int64_t nslots;
   int sms;                                // the device's SM count (persistent CTAs: two per SM)
 };
@@ -203,6 +204,11 @@ constexpr int kBwdChunk = 8;              // tokens between two stored states
 constexpr int kBwdRowStride = 388;        // floats per token-head in prep and part (128 x 3 + 4)
 constexpr int kBwdSlices = 4;             // row slices (CTAs) per head in the recurrences
 constexpr int kBwdParamTokens = 256;      // tokens per block of the parameter reduction
+// The chunked backward's chains: parts per sequence at most.  Four parts measured slower than two
+// on the fixed batch (chains 0.48 against 0.39 ms): their three correction launches run one after
+// another, each for the tens of chunks its state takes to decay to exactly zero.
+constexpr int kBwdMaxParts = 2;
+constexpr int kBwdMaxSplitChains = 256;  // (sequence, head) chains beyond which no sequence is cut
 constexpr int kBwdParamStride = 132;      // floats per (block, head): 128 ddt_bias + dA_log + pad
 
 // Host-side launchers (defined in the .cu files).

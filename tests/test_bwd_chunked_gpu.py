@@ -114,12 +114,24 @@ def test_chunked_backward_fixed_workload_sampled_heads():
     _compare(r, _oracle(x, dout, dfinal, heads=heads), x, "bwd chunked fixed workload heads 0,7,15", heads=heads)
 
 
+def test_chunked_backward_two_parts_at_the_limit():
+    """kda_bwd cuts each sequence of two or more chunks in two while the four runs per (sequence,
+    head) fit one wave of two CTAs per SM; this case sits at that limit (SMs / 2 chains)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_seq = sms // 4   # chains = 2 n_seq <= SMs / 2
+    assert 4 * 2 * n_seq <= 2 * sms
+    gen = np.random.default_rng(1980)
+    lens = [int(x) for x in gen.integers(20, 120, size=n_seq)]
+    x = random_case(1, sum(lens), 2, seed=1981, lens=lens)
+    dout, dfinal = _grads_in(x, 1982)
+    _compare(_gpu(x, dout, dfinal, recurrent=False), _oracle(x, dout, dfinal), x, f"bwd chunked {2 * n_seq} chains")
+
+
 def test_chunked_backward_many_chains_unsplit():
-    """With many (sequence, head) chains kda_bwd keeps every sequence whole (the other cases here
-    split each sequence of two or more chunks in two and correct across the cut)."""
+    """With many (sequence, head) chains kda_bwd keeps every sequence whole."""
     gen = np.random.default_rng(1977)
     lens = [int(x) for x in gen.integers(1, 70, size=40)]
-    x = random_case(1, sum(lens), 2, seed=1978, lens=lens)   # 80 chains: more than the split allows
+    x = random_case(1, sum(lens), 2, seed=1978, lens=lens)   # 80 chains: more than SMs / 2
     dout, dfinal = _grads_in(x, 1979)
     _compare(_gpu(x, dout, dfinal, recurrent=False), _oracle(x, dout, dfinal), x, "bwd chunked 80 chains")
 
