@@ -534,17 +534,18 @@ kda_status kda_fwd_ex(const kda_shape* shape, const void* q, const void* k, cons
     cmp.item_count = &hdr->n_compose;
     if (launch_compose(cmp, (int)L.cap_compose, d.sms, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (L.cap_compose > 0) ++launches;
-    mark(2, stream);
-    // last launch: the corrections of segments 1 .. n-1 from their true entering states
+    // last launch: the corrections of segments 1 .. n-1 from their true entering states.  It
+    // starts beside the composition: its runs set up and prepare their first chunks' operands
+    // from the inputs, then wait for the composed states (so no profile mark between the two:
+    // an event recorded there would order the launch after the composition)
     cp.items = sp.correct;
     cp.item_count = &hdr->n_correct;
     cp.take = nullptr;
     cp.sm_arrivals = nullptr;
-    if (launch_chain_aux(cp, (int)L.cap_correct, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_chain_aux(cp, (int)L.cap_correct, stream, true) != cudaSuccess) return KDA_ERR_CUDA;
     ++launches;
-  } else {
-    mark(2, stream);
   }
+  mark(2, stream);
   mark(3, stream);
   t_last_launches = launches;
   return KDA_OK;

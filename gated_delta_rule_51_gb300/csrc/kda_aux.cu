@@ -324,6 +324,9 @@ __device__ __forceinline__ void bulk_load_g2s(void* smem_dst, const void* gmem_s
 
 template <int kRows>
 __global__ void __launch_bounds__(kComposeThreads) kda_compose_kernel(const ComposeParams p) {
+  // the correction launch after this one may start beside it: its runs read the composed
+  // states only after waiting for this grid
+  griddep_launch_dependents();
   constexpr int kRowsPerThread = kRows / 4;
   constexpr uint32_t kQBytes = kRows * 128 * 4;
   const int item = blockIdx.x / (128 / kRows);

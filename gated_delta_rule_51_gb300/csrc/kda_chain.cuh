@@ -989,6 +989,11 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
         for (int c = 0; c < kStages && c < nchunks; ++c) issue_tma(c);
       }
       __syncwarp();
+      // A correction launch may have started beside the kernel that writes its entering states
+      // (and after the one that wrote the outputs it adds to).  The loads above read inputs
+      // only; the epilogue warps, the only ones that read a state slot or touch the outputs,
+      // wait for that kernel here (a no-op in a launch that did not overlap its predecessor).
+      if constexpr (kAux) griddep_wait();
       bool issued_any = false;
       // every epilogue warp runs every named barrier below, also after an abort,
       // so that the group never waits on a warp that left early
@@ -1143,10 +1148,30 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
         }
       };
       bool stopped = false;   // a correction or transition run whose state became exactly zero
+      // A backward correction run reads back, per chunk, the Vn rows and the state copy its
+      // part's run stored (read-modify-writes on the chain's critical path): this thread's rows
+      // of them are requested into L2 a chunk ahead (Vn of chunk c, the copy entering chunk c + 1,
+      // at the top of chunk c - 1)
+      auto prefetch_rows = [&](int c) {
+        if constexpr (kBwd && kAux) {
+          if (c < nchunks) {
+            const float* vd = save_vec + ((slot0 + dchunk(c)) * p.H + h) * 2048 + vrow;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) prefetch_l2(vd + 128 * t);
+          }
+          if (c + 1 < nchunks) {
+            const uint16_t* cp = save_state + ((slot0 + dchunk(c + 1)) * p.H + h) * 16384;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) prefetch_l2(cp + ((size_t)q * 128 + vrow) * 8);
+          }
+        }
+      };
+      prefetch_rows(0);
       for (int c = 0; c < nchunks; ++c) {
         const int b = c & 1;
         const int nv = min(kChunk, it.len - c * kChunk);
         const bool last = (c == nchunks - 1);
+        prefetch_rows(c + 1);
         // ---- E1: Vn^T row v (16 tokens) -> split bf16 operand; then the update MMAs
         ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar_d1_full[b], (c >> 1) & 1, ab));
         if (ok) {
@@ -1278,16 +1303,18 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
           uint16_t* obase = p.out + ((size_t)(it.row0 + c * kChunk) * p.H + h) * vstride + (size_t)kDimV * vblk;
           if (correct) {
             // (unrolled with a guard: a loop bound of nv would index r at run time and put it
-            // in local memory for every mode)
+            // in local memory for every mode).  Every output is read before any is written:
+            // the compiler cannot tell that the stores do not alias the later loads, and would
+            // otherwise wait for each load in turn.
             if (vrow < vrows) {
+              uint16_t old[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                if (i < nv) {
-                  uint16_t* o = obase + (size_t)i * row_elems + vrow;
-                  *o = __bfloat16_as_ushort(
-                      __float2bfloat16_rn(bf16_bits_to_f32(*o) + p.scale * __uint_as_float(r[i])));
-                }
-              }
+              for (int i = 0; i < 16; ++i) old[i] = i < nv ? obase[(size_t)i * row_elems + vrow] : (uint16_t)0;
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (i < nv)
+                  obase[(size_t)i * row_elems + vrow] = __bfloat16_as_ushort(
+                      __float2bfloat16_rn(bf16_bits_to_f32(old[i]) + p.scale * __uint_as_float(r[i])));
             }
           } else {
 #pragma unroll
@@ -1342,6 +1369,7 @@ __device__ __forceinline__ void chain_run(const ChainParams& p, const WorkItem& 
     }
   } else if (warp >= kWarpEpi0) {
     // zero-length run: the final state equals the initial state
+    if constexpr (kAux) griddep_wait();
     const int q4 = warp & 3;
     const int vrow = q4 * 32 + lane;
     if constexpr (kBwd) {   // a reverse run: dL/d initial_state = dL/d final_state
@@ -1388,7 +1416,8 @@ __global__ void __launch_bounds__(kThreads, (kFlags & kChainPrecise) ? 1 : 2)
   // first CTA to start on an SM takes the longest run left and the second the shortest, so
   // a long chain shares its SM with a short one and then runs alone.
   // the segment scan's transition runs let the forward runs' launch start beside them
-  if constexpr ((kFlags & kChainAux) != 0) griddep_launch_dependents();
+  // and the backward's runs let its correction launch start beside them
+  if constexpr ((kFlags & (kChainAux | kChainBwd)) != 0) griddep_launch_dependents();
   int item = blockIdx.x;
   if (p.take != nullptr) {
     __shared__ int s_item;

@@ -6,9 +6,9 @@
 
 namespace kda {
 
-cudaError_t launch_chain_aux(const ChainParams& p, int grid, cudaStream_t s) {
-  if (p.precise) return launch_chain_table<kChainAux | kChainPrecise>(p, grid, s);
-  return launch_chain_table<kChainAux>(p, grid, s);
+cudaError_t launch_chain_aux(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev) {
+  if (p.precise) return launch_chain_table<kChainAux | kChainPrecise>(p, grid, s, overlap_prev);
+  return launch_chain_table<kChainAux>(p, grid, s, overlap_prev);
 }
 
 }  // namespace kda

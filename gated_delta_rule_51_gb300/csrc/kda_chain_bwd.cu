@@ -34,8 +34,24 @@ cudaError_t launch_chain_bwd(const ChainParams& p, int grid, cudaStream_t s, boo
   if ((p.flags & (kGatePreactivated | kGateSoftplus)) != 0 || p.kdim != 128 || p.vrows != 128 || p.precise)
     return cudaErrorInvalidValue;
   const Kernel k = kernels[((p.flags & (kBetaPreactivated | kNoQkL2Norm)) >> 1) + (corrections ? 4 : 0)];
-  k<<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  if (!corrections) {
+    k<<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  // the corrections start beside the runs (programmatic dependent launch): they load their
+  // first chunks' inputs and prepare their operands, and wait for the runs before they read a
+  // slot or a stored copy
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
 }
 
 }  // namespace kda

@@ -218,7 +218,9 @@ cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev = false);
 cudaError_t launch_chain_precise(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev = false);
 cudaError_t launch_chain_bwd(const ChainParams& p, int grid, cudaStream_t s, bool corrections = false);
-cudaError_t launch_chain_aux(const ChainParams& p, int grid, cudaStream_t s);
+// overlap_prev: launched to start beside the previous kernel of the stream (programmatic
+// dependent launch); the runs wait for it before they read a state slot or touch the outputs
+cudaError_t launch_chain_aux(const ChainParams& p, int grid, cudaStream_t s, bool overlap_prev = false);
 cudaError_t launch_compose(const ComposeParams& p, int grid, int sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 // phases 0-3: prep, stored-state forward, reverse, chain rule and parameter sums

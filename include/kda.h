@@ -204,8 +204,9 @@ KDA_API kda_status kda_check_device_error(const void *workspace, kda_stream_t st
  * every kda_fwd records events[i] (cudaEvent_t handles owned by the caller) on
  * its stream right after its i-th phase -- 0: work-list scheduling, 1: the
  * segment transition runs and the forward runs (two launches, the second
- * overlapping the first), 2: carry composition, 3: the segment corrections -- so
- * each phase can be timed with cudaEventElapsedTime
+ * overlapping the first), 2: carry composition and the segment corrections (two
+ * launches, the second starting beside the first: no event between them), 3:
+ * recorded with 2 -- so each phase can be timed with cudaEventElapsedTime
  * (phases a call does not need are recorded empty).  n_events must be 4.
  * Pass NULL to stop.  The setting is process-wide and not thread-safe.
  */
