@@ -158,6 +158,35 @@ def test_chunked_backward_is_deterministic():
         assert torch.equal(a[n], b[n]), n
 
 
+def test_chunked_backward_captured_in_a_cuda_graph_replays_identically():
+    """A few chains: each sequence is cut in two and the correction launch starts beside the
+    runs (a programmatic dependency, a graph edge once captured); each replay of the captured
+    call gives the direct call's gradients bit for bit."""
+    from gated_delta_rule_51_gb300 import kda
+
+    x = random_case(1, 400, 2, seed=1983, lens=[150, 250])
+    dout, dfinal = _grads_in(x, 1984)
+    ref = _gpu(x, dout, dfinal, recurrent=False)
+    ws = torch.empty(kda.bwd_workspace_size(kda.make_shape(1, 400, 2, 2)), dtype=torch.uint8, device="cuda")
+    r = {n: torch.full_like(ref[n], float("nan")) for n in NAMES}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            kda.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["A_log"], x["dt_bias"],
+                    x["lower_bound"], dout, initial_state=x["initial_state"], dfinal=dfinal,
+                    cu_seqlens=x["cu_seqlens"], workspace=ws, out=r)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        for n in NAMES:
+            r[n].fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for n in NAMES:
+            assert torch.equal(r[n], ref[n]), n
+
+
 def test_chunked_backward_malformed_cu_seqlens_is_flagged():
     from gated_delta_rule_51_gb300 import kda
 

@@ -258,6 +258,40 @@ def test_forward_captured_in_a_cuda_graph_replays_identically():
         assert torch.equal(fin, fin_ref)
 
 
+def test_segment_scan_captured_in_a_cuda_graph_replays_identically(monkeypatch):
+    # with segments forced, a call runs the transition launch, the forward launch overlapping
+    # it, the composition and the correction launch starting beside the composition; captured
+    # in a graph (programmatic dependencies become graph edges), each replay still gives the
+    # direct call's result bit for bit, and that result matches the oracle
+    from gated_delta_rule_51_gb300 import kda
+
+    monkeypatch.setenv("KDA_SEG_TOKENS", "96")
+    x = random_case(1, 700, 3, seed=952, lens=[300, 17, 383])
+    out_ref, fin_ref = run_gpu(x)
+    o_or, f_or = run_oracle(x)
+    check_out(out_ref, o_or.reshape(700, 3, 128), label="graph, segments of 96")
+    check_state(fin_ref, f_or, label="graph, segments of 96")
+    ws = torch.empty(kda.workspace_size(kda.make_shape(1, 700, 3, 3)), dtype=torch.uint8, device="cuda")
+    out = torch.full_like(out_ref, float("nan"))
+    fin = torch.full_like(fin_ref, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], out, x["A_log"], x["dt_bias"],
+                    x["lower_bound"], initial_state=x["initial_state"], final_state=fin,
+                    cu_seqlens=x["cu_seqlens"], workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        fin.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, out_ref)
+        assert torch.equal(fin, fin_ref)
+
+
 @pytest.mark.parametrize("total,H", [(32768, 64), (131072, 32), (131072, 64), (262144, 32), (262144, 64)])
 def test_sweep_workloads_large_cells_sampled(total, H):
     """The sweep cells past the three small ones (up to 16.8M token-heads at H = 64): every
