@@ -84,6 +84,7 @@ __device__ long long block_scan(long long x, long long* buf) {
 // run alone for most of their length.  Runs are ranked by a length bucket, four buckets per
 // octave of chunk count (ties in arbitrary order; every run computes the same either way).
 constexpr int kLenBuckets = 4 * 32;
+constexpr int kSegCandidates = 64;   // segment lengths the schedule weighs against one wave
 __device__ __forceinline__ int len_bucket(long long chunks) {
   if (chunks < 4) return (int)(chunks < 0 ? 0 : chunks);
   const int msb = 63 - __clzll(chunks);
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
   __shared__ int s_comp0[kSchedThreads];
   __shared__ int s_err;
   __shared__ unsigned long long s_max_chunks, s_sum_chunks;
+  __shared__ unsigned long long s_runs[kSegCandidates];
   __shared__ long long s_L;
   const int tid = threadIdx.x;
   const long long H = p.H;
@@ -143,6 +145,46 @@ __global__ void __launch_bounds__(kSchedThreads) kda_schedule_kernel(const Sched
     s_L = Lx;
   }
   __syncthreads();
+  // A split whose forward runs only just exceed one wave of resident CTAs (by at most a quarter)
+  // leaves the excess runs for a second wave, each after a whole run of the first: take instead
+  // the shortest longer segment, at most a quarter longer, whose runs fit one wave.  Candidates
+  // L0 + c * step (kSegCandidates of them) are counted side by side.  Longer segments only mean
+  // fewer runs, so the work lists sized from the host's length still suffice.
+  if (!p.seg_forced && s_L < total_rows) {
+    const long long L0 = s_L;
+    long long step = ((L0 / 4) / kSegCandidates + 15) / 16 * 16;
+    if (step < 16) step = 16;
+    for (int i = tid; i < kSegCandidates; i += kSchedThreads) s_runs[i] = 0;
+    __syncthreads();
+    for (long long idx = tid; idx < (long long)p.N * kSegCandidates; idx += kSchedThreads) {
+      const long long n = idx / kSegCandidates;
+      const int c = (int)(idx - n * kSegCandidates);
+      long long len = p.T;
+      if (p.cu_seqlens) {
+        long long a = p.cu_seqlens[n], b = p.cu_seqlens[n + 1];
+        a = a < 0 ? 0 : (a > total_rows ? total_rows : a);
+        b = b < a ? a : (b > total_rows ? total_rows : b);
+        len = b - a;
+      }
+      const long long Lc = L0 + c * step;
+      atomicAdd(&s_runs[c], (unsigned long long)(len <= 0 ? 1 : (len + Lc - 1) / Lc));
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const long long runs0 = (long long)s_runs[0] * H;
+      if (runs0 > p.resident && 4 * runs0 <= 5 * p.resident) {
+        for (int c = 1; c < kSegCandidates; ++c) {
+          const long long Lc = L0 + c * step;
+          if (4 * Lc > 5 * L0) break;
+          if ((long long)s_runs[c] * H <= p.resident) {
+            s_L = Lc;
+            break;
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
   const long long L = s_L;
   for (int pass = 0; pass < 2; ++pass) {
     if (pass == 1 && tid == 0) {   // bucket counts -> first rank of each bucket, longest first
