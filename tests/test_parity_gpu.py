@@ -152,6 +152,15 @@ def test_sweep_workloads_small_cells(total, H):
     _compare(x, torch.float32, w.name)
 
 
+def test_segment_length_refined_to_fit_one_wave():
+    """One sequence of 4096 tokens with 40 heads: on a GPU of 152 SMs (304 resident chain CTAs)
+    the host's segment length cuts it into 8 segments, 320 forward runs, a few more than one
+    wave, and the schedule kernel takes a longer segment (7 segments, 280 runs).  Whatever the
+    SM count, the result must match the oracle."""
+    x = random_case(1, 4096, 40, seed=1990, lens=[4096])
+    _compare(x, torch.float32, "one sequence, 40 heads")
+
+
 def test_determinism_bitwise():
     x = random_case(1, 3000, 4, seed=14, lens=[1000, 2000])
     o1, f1 = run_gpu(x)
