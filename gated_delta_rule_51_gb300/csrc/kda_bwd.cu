@@ -1329,9 +1329,11 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_xprod_kernel(const BwdParams p
     XprodAcc r;
     if (valid) {
       const bool ok = mbar_wait(&sm.bar, phase, ab);
-      phase ^= 1u;
-      pending = !ok;
-      if (ok) xprod_mma(sm, r);
+      if (ok) {
+        phase ^= 1u;   // a copy that did not land keeps its phase for the drain below
+        pending = false;
+        xprod_mma(sm, r);
+      }
     }
     __syncthreads();   // every warp is done with the buffers (or the CTA is stopping)
     if (sm.abort) break;
